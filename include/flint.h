@@ -1,0 +1,194 @@
+/*
+ * flint.h -- C ABI of the Flint NVFP4 MoE feed-forward / output-head library for
+ * one NVIDIA B300 (sm_103a).
+ *
+ * What it computes.  The token-generation step of the Flint-40B-A2B MoE body and
+ * head, as described in "Flint: 125 tokens a second is what 2.5B active parameters
+ * buy at 273 GB/s" (section "The shape, read from the headers": hidden 2,048; 256
+ * routed SwiGLU experts of width 512 with 6 selected per token; one shared expert
+ * of width 1,024; an untied 150,144-entry output head) and "Recursive Releases
+ * Flint, a 40B MoE Coding Model That Runs Locally at 125 Tokens per Second"
+ * (section "How does Flint's architecture work?": a router selects 6 experts per
+ * token, plus 1 always-active shared expert).  Weights are NVFP4 ("Flint: 125
+ * tokens a second ...", sections "Why active parameters set the speed" -- the output
+ * head is 4-bit too -- and "Checking 125 tokens a second" -- 4-bit values with an
+ * 8-bit scale per 16, 4.5 bits per weight).  Prompt processing ("Flint-40B-A2B:
+ * AI-Built MoE Coding Model Hits 125 tok/s on MacBook Pro", section "Custom
+ * Inference Kernels") is the same layer over many tokens at once.
+ *
+ * NVFP4 matrix [rows, cols] (blocks of 16 along cols):
+ *   codes  uint8 [rows, cols/2]  E2M1 codes; element 2j in bits 0-3 of byte j,
+ *                                element 2j+1 in bits 4-7 (bit 3 of a code = sign)
+ *   scales uint8 [rows, cols/16] E4M3 (OCP "e4m3fn") block scales, row-major
+ *   tensor_scale fp32            one per matrix
+ *   value(r, c) = fp32(fp32(e2m1(code) * e4m3(scale)) * tensor_scale)
+ * A stack of n_mat matrices is stored matrix after matrix.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers unless stated.  Structs passed by
+ *    pointer (flint_nvfp4, flint_moe_layer) live in HOST memory and are read
+ *    during the call only.
+ *  - Nothing allocates, frees or synchronises, except flint_last_device_status
+ *    (which synchronises the stream).  All work is enqueued on `stream` (a
+ *    cudaStream_t; NULL = the legacy default stream).  Scratch memory is the
+ *    caller's workspace `ws` of `ws_bytes` bytes (see flint_workspace_bytes),
+ *    256-byte aligned; two calls in flight at once need distinct workspaces.
+ *  - Weight pointers (codes, scales, router_w) and activation inputs (x_bf16)
+ *    must be 16-byte aligned (128-bit loads) with rows of a multiple of 32
+ *    elements; outputs and per-token vectors (out, residual, logits, topk_*)
+ *    need only their element's natural alignment.  Argument checks run on the
+ *    host before any launch and return an error code without enqueuing
+ *    anything.
+ *  - Conditions found on the device (non-finite weights, a bounded wait that
+ *    expired) set a device status word that flint_last_device_status reads and
+ *    clears.  Kernels never trap.
+ */
+#ifndef FLINT_H
+#define FLINT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FLINT_OK = 0,
+  FLINT_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, k > E, ... */
+  FLINT_ERR_ALIGNMENT = 2,     /* a pointer is not 16-byte aligned */
+  FLINT_ERR_SHAPE = 3,         /* cols not a multiple of 32, mismatched shapes */
+  FLINT_ERR_WORKSPACE = 4,     /* ws too small or not 256-byte aligned */
+  FLINT_ERR_NONFINITE = 5,     /* (device) a NaN/Inf weight was quantised */
+  FLINT_ERR_TIMEOUT = 6,       /* (device) a bounded wait gave up */
+  FLINT_ERR_CUDA = 7,          /* a CUDA runtime call or launch failed */
+  FLINT_ERR_UNSUPPORTED = 8    /* a size beyond what this build supports */
+} flint_status;
+
+typedef void* flint_stream; /* a cudaStream_t */
+
+/* One NVFP4 matrix or stack of matrices (device pointers; struct in host memory). */
+typedef struct {
+  const uint8_t* codes;       /* [n_mat, rows, cols/2] */
+  const uint8_t* scales;      /* [n_mat, rows, cols/16] */
+  const float* tensor_scale;  /* [n_mat] */
+  int n_mat, rows, cols;
+} flint_nvfp4;
+
+/* One MoE layer.  Routed experts are stacks of n_experts matrices:
+ *   gate, up : [E, F, H]      down : [E, H, F]
+ *   sh_gate, sh_up : [1, Fs, H]   sh_down : [1, H, Fs]
+ * router_w is bf16 [E, H]; router_bias fp32 [E] or NULL (added to the logits). */
+typedef struct {
+  int hidden, n_experts, top_k, expert_width, shared_width;
+  const void* router_w;
+  const float* router_bias;
+  flint_nvfp4 gate, up, down;
+  flint_nvfp4 sh_gate, sh_up, sh_down;
+} flint_moe_layer;
+
+/* Limits of this build. */
+#define FLINT_MAX_DECODE_TOKENS 8     /* B of flint_moe_decode / flint_lm_head */
+#define FLINT_MAX_HIDDEN 4096
+#define FLINT_MAX_EXPERTS 512
+#define FLINT_MAX_TOP_K 16
+
+/* ----------------------------------------------------------------------------
+ * flint_quantize_nvfp4 -- bf16 weights -> NVFP4.
+ * Follows the 4.5-bit format of "Flint: 125 tokens a second ...", section
+ * "Checking 125 tokens a second".  The pages do not give the recipe; this one is
+ * the two-level NVFP4 scheme, all in fp32 with IEEE division:
+ *   tsc   = amax(|W_m|) / 2688        (2688 = 6 * 448; 1.0 if amax == 0)
+ *   s_b   = E4M3_rne_satfinite((amax_b / 6) / tsc)   per 16-element block
+ *   eff_b = e4m3(s_b) * tsc
+ *   q     = E2M1_rne_satfinite(w / eff_b)            (0 when eff_b == 0)
+ * w_bf16: [n_mat, rows, cols] bf16, device.  codes/scales/tensor_scale: outputs
+ * (device, caller-owned).  ws: flint_workspace_bytes(FLINT_OP_QUANTIZE, ...).
+ * A NaN/Inf weight sets FLINT_ERR_NONFINITE in the device status word (the
+ * matrix's outputs are then unspecified).  cols % 32 == 0.
+ * -------------------------------------------------------------------------- */
+flint_status flint_quantize_nvfp4(const void* w_bf16, int n_mat, int rows, int cols,
+                                  uint8_t* codes, uint8_t* scales, float* tensor_scale,
+                                  void* ws, size_t ws_bytes, flint_stream stream);
+
+/* Dequantise an NVFP4 stack to fp32 [n_mat, rows, cols] (the value formula above).
+ * A check and debugging aid; no workspace. */
+flint_status flint_dequantize_nvfp4(const flint_nvfp4* m, float* out, flint_stream stream);
+
+/* ----------------------------------------------------------------------------
+ * flint_moe_decode -- one MoE layer for B <= FLINT_MAX_DECODE_TOKENS tokens.
+ * Router: logits = Wr x + b (bf16 x bf16, fp32 accumulate); softmax over the E
+ * experts; the top_k experts by logit (ties to the lower index) in descending
+ * order; weights = p_i / sum of the selected p ("Recursive Releases Flint ...",
+ * "How does Flint's architecture work?").  Experts are SwiGLU:
+ *   h_e = silu(Wg_e x) * (Wu_e x),  y_e = Wd_e h_e
+ * and the shared expert is always added with weight 1:
+ *   out = residual + sum_i w_i y_{e_i} + y_shared
+ * x_bf16: [B, H] bf16.  residual: fp32 [B, H], or NULL to use x itself.
+ * out: fp32 [B, H].  x_next_bf16: NULL, or bf16 [B, H] receiving
+ *   RMSNorm(out) = bf16(out / sqrt(mean(out^2) + rms_eps)) (gain 1) for chaining
+ *   layers.  topk_idx int32 [B, k] / topk_w fp32 [B, k]: optional outputs.
+ * out may alias residual.  ws: flint_workspace_bytes(FLINT_OP_MOE_DECODE, ...).
+ * -------------------------------------------------------------------------- */
+flint_status flint_moe_decode(const flint_moe_layer* layer, const void* x_bf16,
+                              const float* residual, float* out, void* x_next_bf16,
+                              float rms_eps, int32_t* topk_idx, float* topk_w, int B,
+                              void* ws, size_t ws_bytes, flint_stream stream);
+
+/* ----------------------------------------------------------------------------
+ * flint_moe_prefill -- the same layer over T prompt tokens, as a token-permuted
+ * grouped GEMM on block-scaled FP4 tensor cores.  Both operands of the FP4
+ * products are NVFP4: x rows and the SwiGLU outputs h are quantised with the
+ * recipe above and a unit tensor scale before their products.
+ *   out[t] = x[t] + sum_j w_tj * y_{e_tj}(t) + y_shared(t)      (fp32 [T, H])
+ * topk_idx / topk_w: optional [T, k] outputs.  expert_counts: optional int32 [E]
+ * output (tokens routed to each expert); pair_order: optional int32 [T*k] output,
+ * the (t*k + j) pair ids in expert-major order, ascending t within an expert.
+ * ws: flint_workspace_bytes(FLINT_OP_MOE_PREFILL, ...).
+ * -------------------------------------------------------------------------- */
+flint_status flint_moe_prefill(const flint_moe_layer* layer, const void* x_bf16, float* out,
+                               int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+                               int32_t* pair_order, int T, void* ws, size_t ws_bytes,
+                               flint_stream stream);
+
+/* ----------------------------------------------------------------------------
+ * flint_lm_head -- NVFP4 output head ("Flint: 125 tokens a second ...", sections
+ * "The shape, read from the headers" and "Why active parameters set the speed").
+ * logits[b, v] = sum_k value(W[v, k]) x[b, k]  (fp32 [B, V]); argmax[b] = the
+ * largest logit's index, ties to the lower index (int32 [B]).  Either output may
+ * be NULL.  W: one matrix [1, V, H].  B <= FLINT_MAX_DECODE_TOKENS.
+ * ws: flint_workspace_bytes(FLINT_OP_LM_HEAD, ...).
+ * -------------------------------------------------------------------------- */
+flint_status flint_lm_head(const flint_nvfp4* W, const void* x_bf16, float* logits,
+                           int32_t* argmax, int B, void* ws, size_t ws_bytes,
+                           flint_stream stream);
+
+enum {
+  FLINT_OP_QUANTIZE = 0,
+  FLINT_OP_MOE_DECODE = 1,
+  FLINT_OP_MOE_PREFILL = 2,
+  FLINT_OP_LM_HEAD = 3
+};
+
+/* Workspace bytes for an op.  Arguments that an op does not use are ignored:
+ *   QUANTIZE:    n_tokens = n_mat
+ *   MOE_DECODE:  hidden, n_experts, top_k, width, shared_width, n_tokens = B
+ *   MOE_PREFILL: hidden, n_experts, top_k, width, shared_width, n_tokens = T
+ *   LM_HEAD:     hidden, vocab, n_tokens = B                                  */
+size_t flint_workspace_bytes(int op, int hidden, int n_experts, int top_k, int width,
+                             int shared_width, int vocab, int n_tokens);
+
+/* Synchronises `stream`, returns the device status word (FLINT_OK if no device
+ * condition was raised since the last read) and clears it. */
+flint_status flint_last_device_status(flint_stream stream);
+
+/* A static description of a status code. */
+const char* flint_status_string(flint_status status);
+
+/* Library version string. */
+const char* flint_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FLINT_H */

@@ -1,0 +1,103 @@
+"""CPU checks of the C-ABI library: it loads, exports every function include/flint.h
+declares, and rejects bad arguments on the host before anything is enqueued (these
+calls never reach the GPU, so they run without one)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_moe_decode_02_b300 import build, flint
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flint.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return flint.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(flint_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_north_star_calls():
+    names = declared_functions()
+    for n in ("flint_quantize_nvfp4", "flint_moe_decode", "flint_moe_prefill", "flint_lm_head"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_host_only_helpers(L):
+    assert b"sm_103a" in L.flint_version()
+    for s in range(9):
+        assert len(L.flint_status_string(s)) > 0
+    nb = flint.workspace_bytes(flint.OP_MOE_DECODE, 2048, 256, 6, 512, 1024, 0, 1)
+    assert nb > 0 and nb % 256 == 0
+    assert flint.workspace_bytes(flint.OP_LM_HEAD, 2048, 0, 0, 0, 0, 150144, 8) > 0
+    assert flint.workspace_bytes(flint.OP_MOE_PREFILL, 2048, 256, 6, 512, 1024, 0, 4096) > 0
+
+
+FAKE = 0x10000000        # aligned, never dereferenced: the checks fail first
+FAKE_MIS = 0x10000008    # 8-byte aligned only
+
+
+def _nv(n, r, c, codes=FAKE):
+    return flint._NVFP4C(codes, FAKE, FAKE, n, r, c)
+
+
+def _layer(H=256, E=16, k=2, F=64, Fs=128, router=FAKE, gate_cols=None):
+    return flint._LayerC(H, E, k, F, Fs, router, None, _nv(E, F, gate_cols or H), _nv(E, F, H),
+                         _nv(E, H, F), _nv(1, Fs, H), _nv(1, Fs, H), _nv(1, H, Fs))
+
+
+def test_quantize_argument_checks(L):
+    q = L.flint_quantize_nvfp4
+    assert q(None, 1, 8, 32, FAKE, FAKE, FAKE, FAKE, 256, None) == 1
+    assert q(FAKE, 1, 8, 48, FAKE, FAKE, FAKE, FAKE, 256, None) == 3       # cols % 32
+    assert q(FAKE, 0, 8, 32, FAKE, FAKE, FAKE, FAKE, 256, None) == 1
+    assert q(FAKE_MIS, 1, 8, 32, FAKE, FAKE, FAKE, FAKE, 256, None) == 2
+    assert q(FAKE, 1, 8, 32, FAKE, FAKE, FAKE, FAKE + 16, 256, None) == 4  # ws alignment
+    assert q(FAKE, 1000, 8, 32, FAKE, FAKE, FAKE, FAKE, 256, None) == 4    # ws size
+
+
+def test_decode_argument_checks(L):
+    d = L.flint_moe_decode
+    lay = _layer()
+    ws = flint.workspace_bytes(flint.OP_MOE_DECODE, 256, 16, 2, 64, 128, 0, 1)
+    args = lambda **kw: dict(dict(x=FAKE, res=None, out=FAKE, xn=None, eps=1e-6, idx=None,
+                                  w=None, B=1, ws=FAKE, wsb=ws), **kw)
+    call = lambda lay, a: d(ctypes.byref(lay), a["x"], a["res"], a["out"], a["xn"], a["eps"],
+                            a["idx"], a["w"], a["B"], a["ws"], a["wsb"], None)
+    assert d(None, FAKE, None, FAKE, None, 1e-6, None, None, 1, FAKE, ws, None) == 1
+    assert call(lay, args(B=0)) == 1
+    assert call(lay, args(B=9)) == 8                                    # > FLINT_MAX_DECODE_TOKENS
+    assert call(lay, args(x=FAKE_MIS)) == 2
+    assert call(lay, args(wsb=ws - 1)) == 4
+    assert call(_layer(k=17, E=32), args()) == 8                        # top_k > MAX
+    assert call(_layer(k=20, E=16), args()) == 1                        # k > E
+    assert call(_layer(H=96), args()) == 8                              # not a power of two
+    assert call(_layer(H=250), args()) == 3                             # not a multiple of 32
+    assert call(_layer(gate_cols=512), args()) == 3                     # stack shape mismatch
+    assert call(_layer(router=FAKE_MIS), args()) == 2
+
+
+def test_lm_head_argument_checks(L):
+    h = L.flint_lm_head
+    W = _nv(1, 4096, 256)
+    ws = flint.workspace_bytes(flint.OP_LM_HEAD, 256, 0, 0, 0, 0, 4096, 1)
+    assert h(ctypes.byref(W), FAKE, None, None, 1, FAKE, ws, None) == 1   # no output at all
+    assert h(ctypes.byref(W), FAKE, FAKE, None, 0, FAKE, ws, None) == 1
+    assert h(ctypes.byref(W), FAKE, FAKE, None, 9, FAKE, ws, None) == 8
+    W2 = _nv(2, 4096, 256)
+    assert h(ctypes.byref(W2), FAKE, FAKE, None, 1, FAKE, ws, None) == 3
+    assert h(ctypes.byref(W), FAKE_MIS, FAKE, None, 1, FAKE, ws, None) == 2
+    assert h(ctypes.byref(W), FAKE, FAKE, None, 1, FAKE, 16, None) == 4
