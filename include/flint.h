@@ -75,16 +75,31 @@ typedef struct {
   int n_mat, rows, cols;
 } flint_nvfp4;
 
+/* Column-chunk copy of an NVFP4 stack: the same bytes reordered so that each
+ * 32-column chunk of every row of a matrix is contiguous across rows:
+ *   codes  [n_mat][cols/32][rows][16]     scales [n_mat][cols/32][rows][2]
+ * The decode kernels read the down projections in this layout (a slice of 32
+ * SwiGLU outputs then multiplies one contiguous block).  Build it once with
+ * flint_nvfp4_column_chunks; the tensor scales are those of the row-major stack. */
+typedef struct {
+  const uint8_t* codes;
+  const uint8_t* scales;
+} flint_nvfp4_cc;
+
 /* One MoE layer.  Routed experts are stacks of n_experts matrices:
  *   gate, up : [E, F, H]      down : [E, H, F]
  *   sh_gate, sh_up : [1, Fs, H]   sh_down : [1, H, Fs]
- * router_w is bf16 [E, H]; router_bias fp32 [E] or NULL (added to the logits). */
+ * router_w is bf16 [E, H]; router_bias fp32 [E] or NULL (added to the logits).
+ * down_cc / sh_down_cc: column-chunk copies of down / sh_down, required by the
+ * decode entry points (flint_moe_decode, flint_decode_tokens); the prefill path
+ * reads the row-major stacks. */
 typedef struct {
   int hidden, n_experts, top_k, expert_width, shared_width;
   const void* router_w;
   const float* router_bias;
   flint_nvfp4 gate, up, down;
   flint_nvfp4 sh_gate, sh_up, sh_down;
+  flint_nvfp4_cc down_cc, sh_down_cc;
 } flint_moe_layer;
 
 /* Limits of this build. */
@@ -92,6 +107,7 @@ typedef struct {
 #define FLINT_MAX_HIDDEN 4096
 #define FLINT_MAX_EXPERTS 512
 #define FLINT_MAX_TOP_K 16
+#define FLINT_MAX_LAYERS 64           /* n_layers of flint_decode_tokens */
 
 /* ----------------------------------------------------------------------------
  * flint_quantize_nvfp4 -- bf16 weights -> NVFP4.
@@ -111,12 +127,20 @@ flint_status flint_quantize_nvfp4(const void* w_bf16, int n_mat, int rows, int c
                                   uint8_t* codes, uint8_t* scales, float* tensor_scale,
                                   void* ws, size_t ws_bytes, flint_stream stream);
 
+/* Reorder an NVFP4 stack (row-major) into its column-chunk copy (see
+ * flint_nvfp4_cc).  codes_cc / scales_cc: device outputs of the same sizes as
+ * m->codes / m->scales.  Weight preparation, like quantisation. */
+flint_status flint_nvfp4_column_chunks(const flint_nvfp4* m, uint8_t* codes_cc,
+                                       uint8_t* scales_cc, flint_stream stream);
+
 /* Dequantise an NVFP4 stack to fp32 [n_mat, rows, cols] (the value formula above).
  * A check and debugging aid; no workspace. */
 flint_status flint_dequantize_nvfp4(const flint_nvfp4* m, float* out, flint_stream stream);
 
 /* ----------------------------------------------------------------------------
- * flint_moe_decode -- one MoE layer for B <= FLINT_MAX_DECODE_TOKENS tokens.
+ * flint_moe_decode -- one MoE layer for B <= FLINT_MAX_DECODE_TOKENS tokens
+ * (flint_decode_tokens with one layer and no head; the tokens run one after
+ * another).
  * Router: logits = Wr x + b (bf16 x bf16, fp32 accumulate); softmax over the E
  * experts; the top_k experts by logit (ties to the lower index) in descending
  * order; weights = p_i / sum of the selected p ("Recursive Releases Flint ...",
@@ -134,6 +158,35 @@ flint_status flint_moe_decode(const flint_moe_layer* layer, const void* x_bf16,
                               const float* residual, float* out, void* x_next_bf16,
                               float rms_eps, int32_t* topk_idx, float* topk_w, int B,
                               void* ws, size_t ws_bytes, flint_stream stream);
+
+/* ----------------------------------------------------------------------------
+ * flint_decode_tokens -- T tokens, one after another, each through n_layers chained
+ * MoE layers and (optionally) the output head, in ONE persistent kernel launch.
+ * For token t:   h_0 = residual[t] (or x[t] if residual is NULL), x_0 = x[t]
+ *                h_{l+1} = h_l + MoE_l(x_l)      (MoE_l as in flint_moe_decode)
+ *                x_{l+1} = bf16(RMSNorm(h_{l+1}))  (eps rms_eps, gain 1)
+ * and the head, when given, reads x_{n_layers}:  logits[t] = W x, argmax[t].
+ * This is the per-token FFN weight stream of "Flint: 125 tokens a second ...",
+ * section "Why active parameters set the speed" (every active weight read once
+ * per token), and the CUDA counterpart of the single fused decode kernel of
+ * "Flint-40B-A2B: AI-Built MoE Coding Model Hits 125 tok/s on MacBook Pro",
+ * section "Custom Inference Kernels".
+ * layers: host array of n_layers (<= FLINT_MAX_LAYERS) layers of equal shape.
+ * head: one NVFP4 matrix [1, V, H], or NULL.  x_bf16: [T, H].  residual: fp32
+ * [T, H] or NULL.  Outputs, each optional: out fp32 [T, H] = h_{n_layers};
+ * x_out_bf16 [T, H] = x_{n_layers}; logits fp32 [T, V]; argmax int32 [T];
+ * topk_idx int32 / topk_w fp32 [T, n_layers, k].
+ * The kernel is cooperative: one CTA per SM, grid-wide barriers whose waits are
+ * bounded (FLINT_ERR_TIMEOUT in the device status word if one expires).  Down
+ * projections are summed with fp32 atomics, so outputs may differ in the last
+ * bits from run to run.  ws: flint_workspace_bytes(FLINT_OP_MOE_DECODE, ...).
+ * -------------------------------------------------------------------------- */
+flint_status flint_decode_tokens(const flint_moe_layer* layers, int n_layers,
+                                 const flint_nvfp4* head, const void* x_bf16,
+                                 const float* residual, int T, float rms_eps, float* out,
+                                 void* x_out_bf16, float* logits, int32_t* argmax,
+                                 int32_t* topk_idx, float* topk_w, void* ws,
+                                 size_t ws_bytes, flint_stream stream);
 
 /* ----------------------------------------------------------------------------
  * flint_moe_prefill -- the same layer over T prompt tokens, as a token-permuted
@@ -172,7 +225,8 @@ enum {
 
 /* Workspace bytes for an op.  Arguments that an op does not use are ignored:
  *   QUANTIZE:    n_tokens = n_mat
- *   MOE_DECODE:  hidden, n_experts, top_k, width, shared_width, n_tokens = B
+ *   MOE_DECODE:  hidden, n_experts, top_k, width, shared_width (also for
+ *                flint_decode_tokens; any number of tokens and layers)
  *   MOE_PREFILL: hidden, n_experts, top_k, width, shared_width, n_tokens = T
  *   LM_HEAD:     hidden, vocab, n_tokens = B                                  */
 size_t flint_workspace_bytes(int op, int hidden, int n_experts, int top_k, int width,

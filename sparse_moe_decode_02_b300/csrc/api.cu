@@ -55,6 +55,30 @@ flint_status check_layer(const flint_moe_layer* L) {
 
 NVPtr nv(const flint_nvfp4& m) { return NVPtr{m.codes, m.scales, m.tensor_scale}; }
 
+// The decode path also reads the column-chunk copies of the down projections.
+flint_status check_decode_layer(const flint_moe_layer* L) {
+  flint_status s = check_layer(L);
+  if (s != FLINT_OK) return s;
+  if (!L->down_cc.codes || !L->down_cc.scales || !L->sh_down_cc.codes || !L->sh_down_cc.scales)
+    return FLINT_ERR_INVALID_ARG;
+  if (!aligned16(L->down_cc.codes) || !aligned16(L->down_cc.scales) ||
+      !aligned16(L->sh_down_cc.codes) || !aligned16(L->sh_down_cc.scales))
+    return FLINT_ERR_ALIGNMENT;
+  return FLINT_OK;
+}
+
+flint::LayerPtrs layer_ptrs(const flint_moe_layer& L) {
+  flint::LayerPtrs p;
+  p.router_w = static_cast<const uint16_t*>(L.router_w);
+  p.router_bias = L.router_bias;
+  p.gate = nv(L.gate); p.up = nv(L.up); p.sh_gate = nv(L.sh_gate); p.sh_up = nv(L.sh_up);
+  p.dcc_codes = L.down_cc.codes; p.dcc_scales = L.down_cc.scales;
+  p.down_tsc = L.down.tensor_scale;
+  p.sh_dcc_codes = L.sh_down_cc.codes; p.sh_dcc_scales = L.sh_down_cc.scales;
+  p.sh_down_tsc = L.sh_down.tensor_scale;
+  return p;
+}
+
 flint_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FLINT_OK : FLINT_ERR_CUDA; }
 
 }  // namespace
@@ -84,8 +108,8 @@ size_t flint_workspace_bytes(int op, int hidden, int n_experts, int top_k, int w
     case FLINT_OP_QUANTIZE:
       return ((size_t)(n_tokens > 0 ? n_tokens : 1) * sizeof(unsigned int) + 255) & ~(size_t)255;
     case FLINT_OP_MOE_DECODE:
-      return flint::decode_workspace_bytes(hidden, n_experts, top_k, width, shared_width,
-                                           n_tokens);
+      (void)top_k; (void)width; (void)shared_width;
+      return flint::decode_workspace_bytes(hidden, n_experts);
     case FLINT_OP_LM_HEAD:
       return flint::lm_head_workspace_bytes(hidden, vocab, n_tokens);
     case FLINT_OP_MOE_PREFILL:
@@ -123,44 +147,95 @@ flint_status flint_dequantize_nvfp4(const flint_nvfp4* m, float* out, flint_stre
                                             static_cast<cudaStream_t>(stream)));
 }
 
+static flint_status decode_tokens_impl(const flint_moe_layer* layers, int n_layers,
+                                       const flint_nvfp4* head, const void* x_bf16,
+                                       const float* residual, int T, float rms_eps, float* out,
+                                       void* x_out_bf16, float* logits, int32_t* argmax,
+                                       int32_t* topk_idx, float* topk_w, void* ws,
+                                       size_t ws_bytes, flint_stream stream) {
+  if (!layers || !x_bf16 || !ws) return FLINT_ERR_INVALID_ARG;
+  if (n_layers <= 0 || T <= 0) return FLINT_ERR_INVALID_ARG;
+  if (n_layers > FLINT_MAX_LAYERS) return FLINT_ERR_UNSUPPORTED;
+  if (!(rms_eps >= 0.f)) return FLINT_ERR_INVALID_ARG;
+  const flint_moe_layer& L0 = layers[0];
+  for (int l = 0; l < n_layers; ++l) {
+    flint_status s = check_decode_layer(&layers[l]);
+    if (s != FLINT_OK) return s;
+    const flint_moe_layer& L = layers[l];
+    if (L.hidden != L0.hidden || L.n_experts != L0.n_experts || L.top_k != L0.top_k ||
+        L.expert_width != L0.expert_width || L.shared_width != L0.shared_width)
+      return FLINT_ERR_SHAPE;
+  }
+  if (L0.hidden < 64) return FLINT_ERR_UNSUPPORTED;
+  if (head) {
+    if (head->n_mat != 1 || head->cols != L0.hidden || head->rows <= 0) return FLINT_ERR_SHAPE;
+    flint_status s = check_nvfp4(*head, 1, head->rows, head->cols);
+    if (s != FLINT_OK) return s;
+  } else if (logits || argmax) {
+    return FLINT_ERR_INVALID_ARG;
+  }
+  if (!aligned16(x_bf16) || (residual && !aligned4(residual)) || (out && !aligned4(out)) ||
+      (x_out_bf16 && !aligned16(x_out_bf16)) || (logits && !aligned4(logits)) ||
+      (argmax && !aligned4(argmax)) || (topk_idx && !aligned4(topk_idx)) ||
+      (topk_w && !aligned4(topk_w)))
+    return FLINT_ERR_ALIGNMENT;
+  if (!aligned256(ws) ||
+      ws_bytes < flint_workspace_bytes(FLINT_OP_MOE_DECODE, L0.hidden, L0.n_experts, L0.top_k,
+                                       L0.expert_width, L0.shared_width, 0, T))
+    return FLINT_ERR_WORKSPACE;
+  static flint::PersistArgs a;   // large (layer table): keep it off the stack
+  std::memset(&a, 0, sizeof(a));
+  a.H = L0.hidden; a.E = L0.n_experts; a.K = L0.top_k; a.F = L0.expert_width;
+  a.Fs = L0.shared_width; a.L = n_layers; a.T = T; a.eps = rms_eps;
+  a.x = static_cast<const uint16_t*>(x_bf16);
+  a.residual = residual;
+  a.out = out;
+  a.x_out = static_cast<uint16_t*>(x_out_bf16);
+  if (head) {
+    a.head = nv(*head);
+    a.V = head->rows;
+  }
+  a.logits = logits;
+  a.argmax = argmax;
+  a.idx_out = topk_idx;
+  a.w_out = topk_w;
+  for (int l = 0; l < n_layers; ++l) a.layer[l] = layer_ptrs(layers[l]);
+  flint::decode_carve(a, ws);
+  return from_cuda(flint::launch_persistent(a, static_cast<cudaStream_t>(stream)));
+}
+
+flint_status flint_decode_tokens(const flint_moe_layer* layers, int n_layers,
+                                 const flint_nvfp4* head, const void* x_bf16,
+                                 const float* residual, int T, float rms_eps, float* out,
+                                 void* x_out_bf16, float* logits, int32_t* argmax,
+                                 int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
+                                 flint_stream stream) {
+  return decode_tokens_impl(layers, n_layers, head, x_bf16, residual, T, rms_eps, out,
+                            x_out_bf16, logits, argmax, topk_idx, topk_w, ws, ws_bytes, stream);
+}
+
 flint_status flint_moe_decode(const flint_moe_layer* L, const void* x_bf16, const float* residual,
                               float* out, void* x_next_bf16, float rms_eps, int32_t* topk_idx,
                               float* topk_w, int B, void* ws, size_t ws_bytes,
                               flint_stream stream) {
-  flint_status s = check_layer(L);
-  if (s != FLINT_OK) return s;
-  if (!x_bf16 || !out || !ws) return FLINT_ERR_INVALID_ARG;
+  if (!L || !out) return FLINT_ERR_INVALID_ARG;
   if (B <= 0) return FLINT_ERR_INVALID_ARG;
   if (B > FLINT_MAX_DECODE_TOKENS) return FLINT_ERR_UNSUPPORTED;
-  if (!(rms_eps >= 0.f)) return FLINT_ERR_INVALID_ARG;
-  if (!aligned16(x_bf16) || !aligned4(out) || (residual && !aligned4(residual)) ||
-      (x_next_bf16 && !aligned2(x_next_bf16)) || (topk_idx && !aligned4(topk_idx)) ||
-      (topk_w && !aligned4(topk_w)))
-    return FLINT_ERR_ALIGNMENT;
-  if (!aligned256(ws) ||
-      ws_bytes < flint_workspace_bytes(FLINT_OP_MOE_DECODE, L->hidden, L->n_experts, L->top_k,
-                                       L->expert_width, L->shared_width, 0, B))
-    return FLINT_ERR_WORKSPACE;
-  flint::DecodeArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.H = L->hidden; a.E = L->n_experts; a.K = L->top_k; a.F = L->expert_width;
-  a.Fs = L->shared_width; a.B = B;
-  a.router_w = static_cast<const uint16_t*>(L->router_w);
-  a.router_bias = L->router_bias;
-  a.gate = nv(L->gate); a.up = nv(L->up); a.down = nv(L->down);
-  a.sh_gate = nv(L->sh_gate); a.sh_up = nv(L->sh_up); a.sh_down = nv(L->sh_down);
-  a.x = static_cast<const uint16_t*>(x_bf16);
-  a.residual = residual;
-  a.out = out;
-  a.x_next = static_cast<uint16_t*>(x_next_bf16);
-  a.eps = rms_eps;
-  a.idx_out = topk_idx;
-  a.w_out = topk_w;
-  flint::decode_carve(a, ws);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(a.counters, 0, 4 * sizeof(unsigned int), st);
-  if (e != cudaSuccess) return FLINT_ERR_CUDA;
-  return from_cuda(flint::launch_decode(a, st));
+  return decode_tokens_impl(L, 1, nullptr, x_bf16, residual, B, rms_eps, out, x_next_bf16,
+                            nullptr, nullptr, topk_idx, topk_w, ws, ws_bytes, stream);
+}
+
+flint_status flint_nvfp4_column_chunks(const flint_nvfp4* m, uint8_t* codes_cc,
+                                       uint8_t* scales_cc, flint_stream stream) {
+  if (!m || !codes_cc || !scales_cc) return FLINT_ERR_INVALID_ARG;
+  if (m->n_mat <= 0 || m->rows <= 0 || m->cols <= 0) return FLINT_ERR_INVALID_ARG;
+  if (m->cols % 32) return FLINT_ERR_SHAPE;
+  flint_status s = check_nvfp4(*m, m->n_mat, m->rows, m->cols);
+  if (s != FLINT_OK) return s;
+  if (!aligned16(codes_cc) || !aligned16(scales_cc)) return FLINT_ERR_ALIGNMENT;
+  return from_cuda(flint::launch_column_chunks(m->codes, m->scales, m->n_mat, m->rows, m->cols,
+                                               codes_cc, scales_cc,
+                                               static_cast<cudaStream_t>(stream)));
 }
 
 flint_status flint_lm_head(const flint_nvfp4* W, const void* x_bf16, float* logits,

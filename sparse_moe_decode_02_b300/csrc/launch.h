@@ -11,30 +11,46 @@ struct NVPtr {
   const float* tsc;
 };
 
-struct DecodeArgs {
-  int H, E, K, F, Fs, B;
+struct LayerPtrs {
   const uint16_t* router_w;
   const float* router_bias;
-  NVPtr gate, up, down, sh_gate, sh_up, sh_down;
-  const uint16_t* x;
-  const float* residual;
-  float* out;
-  uint16_t* x_next;
-  float eps;
-  int32_t* idx_out;
-  float* w_out;
-  // workspace
-  float* logits;       // [B][E]
-  int32_t* sel_idx;    // [B][K]
-  float* sel_w;        // [B][K]
-  float* h_routed;     // [B][K][F]
-  float* h_shared;     // [B][Fs]
-  unsigned int* counters;  // [4], zero between launches
+  NVPtr gate, up, sh_gate, sh_up;
+  const uint8_t* dcc_codes;       // column-chunk copy of down [E][F/32][H][16]
+  const uint8_t* dcc_scales;      // [E][F/32][H][2]
+  const float* down_tsc;          // [E]
+  const uint8_t* sh_dcc_codes;    // column-chunk copy of sh_down [1][Fs/32][H][16]
+  const uint8_t* sh_dcc_scales;
+  const float* sh_down_tsc;       // [1]
 };
 
-size_t decode_workspace_bytes(int H, int E, int K, int F, int Fs, int B);
-void decode_carve(DecodeArgs& a, void* ws);
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
+constexpr int kMaxLayers = 64;
+
+struct PersistArgs {
+  int H, E, K, F, Fs, L, T, V;
+  float eps;
+  const uint16_t* x;       // [T, H] bf16
+  const float* residual;   // [T, H] or null
+  float* out;              // [T, H] or null
+  uint16_t* x_out;         // [T, H] or null
+  NVPtr head;              // codes null: no head
+  float* logits;           // [T, V] or null
+  int32_t* argmax;         // [T] or null
+  int32_t* idx_out;        // [T, L, K] or null
+  float* w_out;            // [T, L, K] or null
+  // workspace
+  unsigned* bar;           // grid barrier {arrivals, generation, abort}
+  float* logits_ws;        // [E]
+  float* acc;              // [2][H] residual ping-pong
+  float* best_v;           // [grid]
+  int* best_i;             // [grid]
+  LayerPtrs layer[kMaxLayers];
+};
+
+size_t decode_workspace_bytes(int H, int E);
+void decode_carve(PersistArgs& a, void* ws);
+cudaError_t launch_persistent(const PersistArgs& a, cudaStream_t st);
+cudaError_t launch_column_chunks(const uint8_t* codes, const uint8_t* scales, int n_mat, int rows,
+                                 int cols, uint8_t* codes_cc, uint8_t* scales_cc, cudaStream_t st);
 
 struct PrefillArgs {
   int H, E, K, F, Fs, T;

@@ -37,19 +37,25 @@ class _NVFP4C(ctypes.Structure):
                 ("rows", ctypes.c_int), ("cols", ctypes.c_int)]
 
 
+class _CCC(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+
+
 class _LayerC(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
                 ("expert_width", ctypes.c_int), ("shared_width", ctypes.c_int),
                 ("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
                 ("gate", _NVFP4C), ("up", _NVFP4C), ("down", _NVFP4C),
-                ("sh_gate", _NVFP4C), ("sh_up", _NVFP4C), ("sh_down", _NVFP4C)]
+                ("sh_gate", _NVFP4C), ("sh_up", _NVFP4C), ("sh_down", _NVFP4C),
+                ("down_cc", _CCC), ("sh_down_cc", _CCC)]
 
 
 _lib = None
 
-_SYMBOLS = ["flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_moe_decode",
-            "flint_moe_prefill", "flint_lm_head", "flint_workspace_bytes",
-            "flint_last_device_status", "flint_status_string", "flint_version"]
+_SYMBOLS = ["flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_nvfp4_column_chunks",
+            "flint_moe_decode", "flint_decode_tokens", "flint_moe_prefill", "flint_lm_head",
+            "flint_workspace_bytes", "flint_last_device_status", "flint_status_string",
+            "flint_version"]
 
 
 def lib() -> ctypes.CDLL:
@@ -64,6 +70,9 @@ def lib() -> ctypes.CDLL:
     vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     L.flint_quantize_nvfp4.argtypes = [vp, i, i, i, vp, vp, vp, vp, sz, vp]
     L.flint_dequantize_nvfp4.argtypes = [ctypes.POINTER(_NVFP4C), vp, vp]
+    L.flint_nvfp4_column_chunks.argtypes = [ctypes.POINTER(_NVFP4C), vp, vp, vp]
+    L.flint_decode_tokens.argtypes = [ctypes.POINTER(_LayerC), i, ctypes.POINTER(_NVFP4C), vp, vp,
+                                      i, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.flint_moe_decode.argtypes = [ctypes.POINTER(_LayerC), vp, vp, vp, vp, ctypes.c_float, vp,
                                    vp, i, vp, sz, vp]
     L.flint_moe_prefill.argtypes = [ctypes.POINTER(_LayerC), vp, vp, vp, vp, vp, vp, i, vp, sz,
@@ -75,8 +84,9 @@ def lib() -> ctypes.CDLL:
     L.flint_status_string.argtypes = [i]
     L.flint_status_string.restype = ctypes.c_char_p
     L.flint_version.restype = ctypes.c_char_p
-    for name in ("flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_moe_decode",
-                 "flint_moe_prefill", "flint_lm_head", "flint_last_device_status"):
+    for name in ("flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_nvfp4_column_chunks",
+                 "flint_moe_decode", "flint_decode_tokens", "flint_moe_prefill",
+                 "flint_lm_head", "flint_last_device_status"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -140,6 +150,8 @@ class MoELayer:
     sh_up: NVFP4
     sh_down: NVFP4
     top_k: int
+    down_cc: tuple | None = None      # (codes, scales) column-chunk copy of down
+    sh_down_cc: tuple | None = None   # (codes, scales) column-chunk copy of sh_down
 
     @property
     def dims(self):
@@ -148,10 +160,11 @@ class MoELayer:
 
     def c(self) -> _LayerC:
         H, E, k, F, Fs = self.dims
+        cc = lambda t: _CCC(None, None) if t is None else _CCC(t[0].data_ptr(), t[1].data_ptr())
         return _LayerC(H, E, k, F, Fs, self.router_w.data_ptr(),
                        None if self.router_bias is None else self.router_bias.data_ptr(),
                        self.gate.c(), self.up.c(), self.down.c(), self.sh_gate.c(),
-                       self.sh_up.c(), self.sh_down.c())
+                       self.sh_up.c(), self.sh_down.c(), cc(self.down_cc), cc(self.sh_down_cc))
 
     def nbytes(self) -> int:
         return (self.router_w.numel() * 2 + sum(m.nbytes() for m in (
@@ -175,6 +188,16 @@ def quantize_nvfp4(w: torch.Tensor, stream=None, ws=None) -> NVFP4:
                                       _ptr(q.tsc), _ptr(ws), ws.numel(), _stream(stream)),
            "flint_quantize_nvfp4")
     return q
+
+
+def nvfp4_column_chunks(m: NVFP4, stream=None):
+    """Column-chunk copy (codes, scales) of an NVFP4 stack (see flint.h)."""
+    codes = torch.empty_like(m.codes)
+    scales = torch.empty_like(m.scales)
+    mc = m.c()
+    _check(lib().flint_nvfp4_column_chunks(ctypes.byref(mc), _ptr(codes), _ptr(scales),
+                                           _stream(stream)), "flint_nvfp4_column_chunks")
+    return codes, scales
 
 
 def dequantize_nvfp4(m: NVFP4, stream=None) -> torch.Tensor:
@@ -205,6 +228,25 @@ def moe_decode(layer: MoELayer, x: torch.Tensor, residual: torch.Tensor | None =
                                   _ptr(x_next), float(rms_eps), _ptr(topk_idx), _ptr(topk_w), B,
                                   _ptr(ws), ws.numel(), _stream(stream)), "flint_moe_decode")
     return out
+
+
+def decode_tokens(layers, x: torch.Tensor, head: NVFP4 | None = None,
+                  residual: torch.Tensor | None = None, rms_eps: float = 1e-6, out=None,
+                  x_out=None, logits=None, argmax=None, topk_idx=None, topk_w=None, ws=None,
+                  stream=None):
+    """T tokens through len(layers) chained layers (+ head) in one launch."""
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    T = x.shape[0]
+    H, E, k, F, Fs = layers[0].dims
+    arr = (_LayerC * len(layers))(*[l.c() for l in layers])
+    hc = head.c() if head is not None else None
+    nb = workspace_bytes(OP_MOE_DECODE, H, E, k, F, Fs, 0, T)
+    ws = _workspace(nb, x.device, ws)
+    _check(lib().flint_decode_tokens(arr, len(layers), ctypes.byref(hc) if hc else None, _ptr(x),
+                                     _ptr(residual), T, float(rms_eps), _ptr(out), _ptr(x_out),
+                                     _ptr(logits), _ptr(argmax), _ptr(topk_idx), _ptr(topk_w),
+                                     _ptr(ws), ws.numel(), _stream(stream)), "flint_decode_tokens")
 
 
 def moe_prefill(layer: MoELayer, x: torch.Tensor, out: torch.Tensor | None = None,

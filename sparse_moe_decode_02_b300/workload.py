@@ -23,9 +23,11 @@ def build_layer(spec: synth.LayerSpec, device="cuda", stream=None) -> flint.MoEL
     router = spec.weights_bf16(synth.KIND_ROUTER, device=device)[0].contiguous()
     bias = spec.bias()
     bias_t = None if bias is None else torch.from_numpy(bias).to(device)
-    return flint.MoELayer(router, bias_t, q(synth.KIND_GATE), q(synth.KIND_UP),
-                          q(synth.KIND_DOWN), q(synth.KIND_SH_GATE), q(synth.KIND_SH_UP),
-                          q(synth.KIND_SH_DOWN), s.top_k)
+    down, sh_down = q(synth.KIND_DOWN), q(synth.KIND_SH_DOWN)
+    return flint.MoELayer(router, bias_t, q(synth.KIND_GATE), q(synth.KIND_UP), down,
+                          q(synth.KIND_SH_GATE), q(synth.KIND_SH_UP), sh_down, s.top_k,
+                          down_cc=flint.nvfp4_column_chunks(down, stream=stream),
+                          sh_down_cc=flint.nvfp4_column_chunks(sh_down, stream=stream))
 
 
 def build_head(seed: int, vocab: int, hidden: int, device="cuda", stream=None) -> flint.NVFP4:

@@ -54,9 +54,10 @@ def _nv(n, r, c, codes=FAKE):
     return flint._NVFP4C(codes, FAKE, FAKE, n, r, c)
 
 
-def _layer(H=256, E=16, k=2, F=64, Fs=128, router=FAKE, gate_cols=None):
+def _layer(H=256, E=16, k=2, F=64, Fs=128, router=FAKE, gate_cols=None, cc=FAKE):
     return flint._LayerC(H, E, k, F, Fs, router, None, _nv(E, F, gate_cols or H), _nv(E, F, H),
-                         _nv(E, H, F), _nv(1, Fs, H), _nv(1, Fs, H), _nv(1, H, Fs))
+                         _nv(E, H, F), _nv(1, Fs, H), _nv(1, Fs, H), _nv(1, H, Fs),
+                         flint._CCC(cc, cc), flint._CCC(cc, cc))
 
 
 def test_quantize_argument_checks(L):
@@ -88,6 +89,40 @@ def test_decode_argument_checks(L):
     assert call(_layer(H=250), args()) == 3                             # not a multiple of 32
     assert call(_layer(gate_cols=512), args()) == 3                     # stack shape mismatch
     assert call(_layer(router=FAKE_MIS), args()) == 2
+    assert call(_layer(cc=None), args()) == 1                           # no column-chunk copy
+    assert call(_layer(cc=FAKE_MIS), args()) == 2
+
+
+def test_decode_tokens_argument_checks(L):
+    dt = L.flint_decode_tokens
+    ws = flint.workspace_bytes(flint.OP_MOE_DECODE, 256, 16, 2, 64, 128, 0, 4)
+    arr = (flint._LayerC * 3)(_layer(), _layer(), _layer())
+    head = _nv(1, 4096, 256)
+    ok = lambda **kw: dict(dict(layers=arr, n=3, head=ctypes.byref(head), x=FAKE, res=None, T=4,
+                                eps=1e-6, out=None, xo=None, lg=None, am=FAKE, ti=None, tw=None,
+                                ws=FAKE, wsb=ws), **kw)
+    call = lambda a: dt(a["layers"], a["n"], a["head"], a["x"], a["res"], a["T"], a["eps"],
+                        a["out"], a["xo"], a["lg"], a["am"], a["ti"], a["tw"], a["ws"], a["wsb"],
+                        None)
+    assert call(ok(n=0)) == 1
+    assert call(ok(n=65)) == 8                                          # > FLINT_MAX_LAYERS
+    assert call(ok(T=0)) == 1
+    assert call(ok(head=None)) == 1                                     # argmax without a head
+    bad_head = _nv(1, 4096, 512)
+    assert call(ok(head=ctypes.byref(bad_head))) == 3                   # head cols != hidden
+    mixed = (flint._LayerC * 2)(_layer(), _layer(F=128))
+    assert call(ok(layers=mixed, n=2)) == 3                             # layers of unequal shape
+    assert call(ok(eps=-1.0)) == 1
+    assert call(ok(wsb=16)) == 4
+
+
+def test_column_chunks_argument_checks(L):
+    cc = L.flint_nvfp4_column_chunks
+    m = _nv(2, 64, 80)
+    assert cc(ctypes.byref(m), None, FAKE, None) == 1
+    assert cc(ctypes.byref(m), FAKE, FAKE, None) == 3                   # cols % 32
+    m2 = _nv(2, 64, 128)
+    assert cc(ctypes.byref(m2), FAKE_MIS, FAKE, None) == 2
 
 
 def test_lm_head_argument_checks(L):
