@@ -166,7 +166,7 @@ static flint_status decode_tokens_impl(const flint_moe_layer* layers, int n_laye
         L.expert_width != L0.expert_width || L.shared_width != L0.shared_width)
       return FLINT_ERR_SHAPE;
   }
-  if (L0.hidden < 64) return FLINT_ERR_UNSUPPORTED;
+  if (L0.hidden < 64 || L0.hidden > 2048) return FLINT_ERR_UNSUPPORTED;
   if (head) {
     if (head->n_mat != 1 || head->cols != L0.hidden || head->rows <= 0) return FLINT_ERR_SHAPE;
     flint_status s = check_nvfp4(*head, 1, head->rows, head->cols);
@@ -183,6 +183,14 @@ static flint_status decode_tokens_impl(const flint_moe_layer* layers, int n_laye
       ws_bytes < flint_workspace_bytes(FLINT_OP_MOE_DECODE, L0.hidden, L0.n_experts, L0.top_k,
                                        L0.expert_width, L0.shared_width, 0, T))
     return FLINT_ERR_WORKSPACE;
+  {
+    // one CTA per unit (32-wide SwiGLU slice) plus at least one router CTA
+    const int grid = flint::decode_grid();
+    const int units = L0.shared_width / 32 + L0.top_k * (L0.expert_width / 32);
+    if (units + 1 > grid) return FLINT_ERR_UNSUPPORTED;
+    if (flint::decode_smem_bytes(L0.hidden, L0.n_experts, grid - units) > 200 * 1024)
+      return FLINT_ERR_UNSUPPORTED;
+  }
   static flint::PersistArgs a;   // large (layer table): keep it off the stack
   std::memset(&a, 0, sizeof(a));
   a.H = L0.hidden; a.E = L0.n_experts; a.K = L0.top_k; a.F = L0.expert_width;

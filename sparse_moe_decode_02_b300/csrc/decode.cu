@@ -4,29 +4,34 @@
 // The layer ("Flint: 125 tokens a second is what 2.5B active parameters buy at 273
 // GB/s", section "The shape, read from the headers"; "Recursive Releases Flint, a 40B
 // MoE Coding Model That Runs Locally at 125 Tokens per Second", section "How does
-// Flint's architecture work?") needs its weights once per token and has one data
-// dependency that no schedule can hide: which experts are read depends on the router.
-// Per layer the kernel runs two phases separated by grid-wide barriers:
+// Flint's architecture work?") needs every active weight once per token and has one
+// dependency no schedule can hide: which experts are read depends on the router.
 //
-//  A  every warp stages x_l (RMSNorm of the running residual h_l, computed redundantly
-//     per warp) in registers.  Router CTAs compute the bf16 router logits.  Shared
-//     CTAs each own a 32-wide slice of the shared expert: 32 gate/up row pairs ->
-//     32 SwiGLU outputs (shared memory) -> their split-K contribution to all H down
-//     rows (a contiguous column-chunk block of the down matrix), kept in shared memory.
-//     Every CTA also copies its share of h_l into the next residual buffer.
-//  -- barrier --
-//  B  every CTA computes the softmax top-k from the logits (one warp, redundantly).
-//     Routed CTAs each own (slot, 32-wide slice): they issue all loads of their unit
-//     at once (gate/up rows and the down block, ~110 KB per CTA for Flint), compute
-//     the slice's SwiGLU outputs, and red.add w_slot * (down block x h slice) into the
-//     next residual; shared CTAs red.add their contribution.
-//  -- barrier --
+// CTA roles (fixed for the launch).  With n_sh = Fs/32 shared-expert slices and
+// n_rt = k*F/32 routed slices ("units": 32 SwiGLU outputs and their down block):
+//   shared CTAs  [0, n_sh)              one shared-expert unit each
+//   routed CTAs  [n_sh, n_sh + n_rt)    one (slot, slice) unit of the selected experts
+//   router CTAs  the rest               router rows, and the copy of h_l into the next
+//                                       residual buffer
+// Step s = one layer of one token.  Two monotonic counters replace grid barriers:
+//   logits(s) -- bumped by each router CTA once its logits and its share of the
+//                residual copy are written;
+//   done(s)   -- bumped by each unit CTA once its down contribution is red.added.
+// Every CTA waits for done(s-1) (h_l complete) and stages x_l = bf16(RMSNorm(h_l)) in
+// registers from one CTA-wide read of h_l.  Router CTAs compute logits and signal.
+// Shared CTAs compute their unit right away (it needs only x_l), then wait for
+// logits(s) before red.adding.  Routed CTAs wait for logits(s), compute the softmax
+// top-k, then stream their unit.  Unit and router weights move global -> shared
+// memory by TMA bulk copies (cp.async.bulk + mbarrier); router rows and shared units
+// do not depend on the data, so the copies for step s+1 are issued as soon as step s
+// has consumed the buffer.  The down projection of a unit is a split-K contribution to
+// all H rows (a contiguous column-chunk block, see flint.h), summed into the next
+// residual with red.global.add.v4.f32.
 //
-// After the last layer the head GEMV (optional) runs over the whole grid, each CTA
-// keeps its best (logit, index), and CTA 0 reduces them after one more barrier.
-// Barrier waits are bounded by %globaltimer: on expiry the kernel records
-// FLINT_ERR_TIMEOUT, raises an abort flag that releases every other wait, and runs to
-// the end without hanging.
+// After the last layer of a token the head GEMV (optional) runs over all CTAs; each
+// CTA posts its best (logit, index) and CTA 0 reduces them.  Every wait is bounded by
+// %globaltimer: on expiry the kernel records FLINT_ERR_TIMEOUT, raises an abort flag
+// that releases all other waits, and runs to the end without hanging.
 #include "common.cuh"
 #include "gemv.cuh"
 #include "launch.h"
@@ -36,37 +41,34 @@ namespace flint {
 constexpr int kPWarps = 16;
 constexpr int kPThreads = 32 * kPWarps;
 constexpr int kSlice = 32;          // SwiGLU outputs per unit (one code chunk of down)
+constexpr int kMaxCtas = 1024;
+// Sync words, each on its own 128-byte line.
+constexpr int kSyncLogits = 0, kSyncDone = 32, kSyncHead = 64, kSyncAbort = 96;
+constexpr int kSyncWords = 128;
 
-// ---------------------------------------------------------------- grid barrier
+// ---------------------------------------------------------------- sync primitives
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-}
 
-// bar[0]: arrivals (monotonic), bar[1]: generation released, bar[2]: abort flag.
-__device__ __forceinline__ void grid_sync(unsigned* bar, unsigned& gen) {
-  __syncthreads();
+// Thread 0 spins (bounded) until *cnt >= target; the CTA then proceeds together.
+__device__ __forceinline__ void wait_count(unsigned* sync, int which, unsigned target) {
   if (threadIdx.x == 0) {
-    const unsigned target = ++gen;
-    __threadfence();
-    const unsigned arrived = atomicAdd(&bar[0], 1u) + 1u;
-    if (arrived == target * gridDim.x) {
-      st_release_gpu(&bar[1], target);
-    } else {
-      const unsigned long long t0 = globaltimer();
-      unsigned polls = 0;
-      while (ld_acquire_gpu(&bar[1]) < target) {
-        if ((++polls & 255u) == 0) {
-          if (ld_acquire_gpu(&bar[2])) break;
-          if (globaltimer() - t0 > kWaitLimitNs) {
-            raise_status(FLINT_ERR_TIMEOUT);
-            atomicExch(&bar[2], 1u);
-            break;
-          }
+    const unsigned* cnt = sync + which;
+    unsigned polls = 0;
+    unsigned long long t0 = 0;
+    while (ld_acquire_gpu(cnt) < target) {
+      if ((++polls & 127u) == 0) {
+        if (ld_acquire_gpu(sync + kSyncAbort)) break;
+        const unsigned long long now = globaltimer();
+        if (t0 == 0) {
+          t0 = now;
+        } else if (now - t0 > kWaitLimitNs) {
+          raise_status(FLINT_ERR_TIMEOUT);
+          atomicExch(sync + kSyncAbort, 1u);
+          break;
         }
       }
     }
@@ -74,51 +76,105 @@ __device__ __forceinline__ void grid_sync(unsigned* bar, unsigned& gen) {
   __syncthreads();
 }
 
-// ---------------------------------------------------------------- vector atomics
+// Publishes every write of this CTA made before the call, then bumps the counter.
+__device__ __forceinline__ void signal_count(unsigned* sync, int which) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(sync + which, 1u);
+  }
+}
+
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
                :: "l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
-// ---------------------------------------------------------------- activation staging
-// Warp-redundant RMSNorm: every warp reads the whole residual h (fp32, L2) in its
-// chunk order, sums squares (identical order in every warp), and returns the bf16
-// x = bf16(h / sqrt(mean(h^2) + eps)) as bf16x2 pairs of the lane's chunks.
-template <int CPL>
-__device__ __forceinline__ void rmsnorm_bf16_pairs(uint32_t (&xb)[CPL * 16], const float* h, int H,
-                                                   float eps, int sl, int LPR) {
-  float v[CPL * 32];
-#pragma unroll
-  for (int i = 0; i < CPL; ++i) {
-    const float4* src = reinterpret_cast<const float4*>(h + 32 * (sl + LPR * i));
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float4 f = __ldcg(src + j);
-      v[i * 32 + 4 * j] = f.x; v[i * 32 + 4 * j + 1] = f.y;
-      v[i * 32 + 4 * j + 2] = f.z; v[i * 32 + 4 * j + 3] = f.w;
+// ---------------------------------------------------------------- TMA bulk copies
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+               :: "r"(smem_addr(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
+               "selp.u32 %0, 1, 0, p; }"
+               : "=r"(ok) : "r"(smem_addr(b)), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded wait for a bulk-copy phase; on expiry records FLINT_ERR_TIMEOUT.
+__device__ __forceinline__ void mbar_wait(uint64_t* b, uint32_t parity, unsigned* sync) {
+  unsigned long long t0 = 0;
+  unsigned polls = 0;
+  while (!mbar_try(b, parity)) {
+    if ((++polls & 63u) == 0) {
+      const unsigned long long now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitNs) {
+        raise_status(FLINT_ERR_TIMEOUT);
+        atomicExch(sync + kSyncAbort, 1u);
+        break;
+      }
     }
   }
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
+// ---------------------------------------------------------------- activation staging
+// The CTA reads the residual h (fp32 [H], L2) once into shared memory, sums squares in
+// a fixed order (every CTA gets the same value), and leaves r = 1/sqrt(mean(h^2)+eps)
+// in *s_r.  Warps then build their bf16 x = bf16(h * r) pairs from shared memory.
+__device__ __forceinline__ void cta_load_rms(const float* h, float* s_h, float* s_red, int H,
+                                             float eps, float* s_r) {
   float ss = 0.f;
-#pragma unroll
-  for (int q = 0; q < CPL * 32; ++q) ss = fmaf(v[q], v[q], ss);
-  ss = sum_lanes_rt(ss, LPR);
-  const float r = 1.0f / sqrtf(ss / (float)H + eps);
-#pragma unroll
-  for (int q = 0; q < CPL * 16; ++q)
-    xb[q] = (uint32_t)f32_to_bf16_rn(v[2 * q] * r) | ((uint32_t)f32_to_bf16_rn(v[2 * q + 1] * r) << 16);
+  for (int n = 4 * threadIdx.x; n < H; n += 4 * kPThreads) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(h + n));
+    *reinterpret_cast<float4*>(s_h + n) = v;
+    ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
+  }
+  ss = sum_lanes<32>(ss);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int w = 0; w < kPWarps; ++w) tot += s_red[w];
+    *s_r = 1.0f / sqrtf(tot / (float)H + eps);
+  }
+  __syncthreads();
+}
+
+// The token's input row (bf16) into shared memory as fp32 (exact).
+__device__ __forceinline__ void cta_load_input(const uint16_t* x, float* s_h, int H) {
+  for (int n = 2 * threadIdx.x; n < H; n += 2 * kPThreads) {
+    const uint32_t two = __ldcg(reinterpret_cast<const unsigned int*>(x + n));
+    s_h[n] = bf16_bits_to_f32(two & 0xFFFFu);
+    s_h[n + 1] = bf16_bits_to_f32(two >> 16);
+  }
+  __syncthreads();
 }
 
 template <int CPL>
-__device__ __forceinline__ void load_bf16_pairs(uint32_t (&xb)[CPL * 16], const uint16_t* x, int sl,
-                                                int LPR) {
+__device__ __forceinline__ void rms_pairs_from_smem(uint32_t (&xb)[CPL * 16], const float* s_h,
+                                                    float r, int sl, int LPR) {
 #pragma unroll
   for (int i = 0; i < CPL; ++i) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + 32 * (sl + LPR * i));
+    const float4* src = reinterpret_cast<const float4*>(s_h + 32 * (sl + LPR * i));
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint4 q = __ldcg(src + j);
-      xb[i * 16 + 4 * j] = q.x; xb[i * 16 + 4 * j + 1] = q.y;
-      xb[i * 16 + 4 * j + 2] = q.z; xb[i * 16 + 4 * j + 3] = q.w;
+    for (int j = 0; j < 8; ++j) {
+      const float4 f = src[j];
+      xb[i * 16 + 2 * j] = (uint32_t)f32_to_bf16_rn(f.x * r) | ((uint32_t)f32_to_bf16_rn(f.y * r) << 16);
+      xb[i * 16 + 2 * j + 1] = (uint32_t)f32_to_bf16_rn(f.z * r) | ((uint32_t)f32_to_bf16_rn(f.w * r) << 16);
     }
   }
 }
@@ -161,108 +217,106 @@ __device__ __forceinline__ void stage_slice(XStage<1, 2>& hs, const float* s_h) 
   }
 }
 
-// ---------------------------------------------------------------- per-layer units
-struct UnitLoads {
-  RowRegs<1> dn[4];    // down block rows (4 consecutive rows per lane per pass)
+// ---------------------------------------------------------------- shared-memory rows
+template <int CPL>
+__device__ __forceinline__ void lds_row(RowRegs<CPL>& r, const uint8_t* codes_row,
+                                        const uint8_t* scales_row, int sl, int LPR) {
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = sl + LPR * i;
+    r.q[i] = *reinterpret_cast<const uint4*>(codes_row + 16 * c);
+    r.s[i] = *reinterpret_cast<const uint16_t*>(scales_row + 2 * c);
+  }
+}
+
+template <int CPL>
+__device__ __forceinline__ void lds_row_bf16(RowBF16<CPL>& r, const uint16_t* row, int sl, int LPR) {
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const uint4* src = reinterpret_cast<const uint4*>(row + 32 * (sl + LPR * i));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) r.q[i * 4 + j] = src[j];
+  }
+}
+
+// ---------------------------------------------------------------- units
+// Shared-memory image of one unit: 32 gate rows, 32 up rows (codes then scales) and
+// the down block (H rows x one 32-column chunk).
+struct UnitLayout {
+  uint32_t gc, gs, uc, us, dc, ds, bytes;
+  __host__ __device__ static UnitLayout of(int H) {
+    UnitLayout u;
+    u.gc = 0;
+    u.gs = u.gc + kSlice * (H / 2);
+    u.uc = u.gs + kSlice * (H / 16);
+    u.us = u.uc + kSlice * (H / 2);
+    u.dc = u.us + kSlice * (H / 16);
+    u.ds = u.dc + H * 16;
+    u.bytes = u.ds + H * 2;
+    return u;
+  }
 };
 
-// One 32-wide SwiGLU slice of one expert: gate/up rows [j0, j0+32) of (gate, up) stacks
-// (matrix `mat`), then the split-K contribution of the down column chunk j0/32 to all
-// H rows.  The contribution, times `wgt`, is either red.added into acc (direct) or
-// accumulated into the CTA's shared partial s_part[H].
+// Issues the bulk copies of one unit (thread 0 only): gate/up rows [row0, row0+32) of
+// the stacks and the down column-chunk block `chunk`.
+__device__ __forceinline__ void issue_unit_copy(uint8_t* buf, uint64_t* bar, int H, const NVPtr& gate,
+                                                const NVPtr& up, const uint8_t* dcc_codes,
+                                                const uint8_t* dcc_scales, size_t row0,
+                                                size_t chunk) {
+  const UnitLayout L = UnitLayout::of(H);
+  mbar_expect_tx(bar, L.bytes);
+  bulk_g2s(buf + L.gc, gate.codes + row0 * (H / 2), kSlice * (H / 2), bar);
+  bulk_g2s(buf + L.gs, gate.scales + row0 * (H / 16), kSlice * (H / 16), bar);
+  bulk_g2s(buf + L.uc, up.codes + row0 * (H / 2), kSlice * (H / 2), bar);
+  bulk_g2s(buf + L.us, up.scales + row0 * (H / 16), kSlice * (H / 16), bar);
+  bulk_g2s(buf + L.dc, dcc_codes + chunk * H * 16, H * 16, bar);
+  bulk_g2s(buf + L.ds, dcc_scales + chunk * H * 2, H * 2, bar);
+}
+
+// Computes one unit from shared memory: 32 SwiGLU outputs, then the down contribution
+// (times wgt) of all H rows, added into s_part[H].
 template <int CPL>
-__device__ __forceinline__ void swiglu_slice_unit(const PersistArgs& a, const NVPtr& gate,
-                                                  const NVPtr& up, const uint8_t* dcc_codes,
-                                                  const uint8_t* dcc_scales, float dtsc,
-                                                  size_t mat, int width, int j0, float wgt,
-                                                  const XStage<CPL, 1>& xs, float* s_h,
-                                                  float* acc, float* s_part) {
+__device__ __forceinline__ void unit_compute(const uint8_t* buf, int H, float gate_tsc,
+                                             float up_tsc, float down_tsc, float wgt,
+                                             const XStage<CPL, 1>& xs, float* s_h,
+                                             float* s_part) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int H = a.H;
   const int LPR = H / (32 * CPL), RPP = 32 / LPR;
   const int slice = lane / LPR, sl = lane % LPR;
-  const size_t cb = H / 2, sb = H / 16;
-  // --- issue all loads: gate/up pairs of this warp, then the down rows
-  constexpr int kPairs = 2;  // pair passes per warp (32 pairs / 16 warps for RPP = 1)
-  RowRegs<CPL> g[kPairs], u[kPairs];
-  int pj[kPairs];
-#pragma unroll
-  for (int i = 0; i < kPairs; ++i) {
-    int p = (warp * RPP + slice) + kPWarps * RPP * i;
-    pj[i] = p;
+  const UnitLayout U = UnitLayout::of(H);
+  const float gs = gate_tsc * xs.unscale, us = up_tsc * xs.unscale;
+  // SwiGLU outputs: pair p handled by (warp, slice)
+  for (int p0 = warp * RPP; p0 < kSlice; p0 += kPWarps * RPP) {
+    const int p = p0 + slice;
     const int pr = p < kSlice ? p : 0;
-    const size_t row = mat * width + j0 + pr;
-    load_row<CPL>(g[i], gate.codes + row * cb, gate.scales + row * sb, sl, LPR);
-    load_row<CPL>(u[i], up.codes + row * cb, up.scales + row * sb, sl, LPR);
-  }
-  // down block: chunk c = j0/32 of matrix `mat` -> rows [0, H) contiguous
-  const int rows_per_warp = H / kPWarps;
-  const size_t chunk = (size_t)mat * (width / 32) + j0 / 32;
-  const uint8_t* dc = dcc_codes + chunk * H * 16;
-  const uint8_t* ds = dcc_scales + chunk * H * 2;
-  const int nbase = warp * rows_per_warp;
-  // every lane owns 4 consecutive rows per 128-row group
-  UnitLoads L;
-  const int r0 = 4 * lane;
-  const bool have = r0 < rows_per_warp;   // rows_per_warp >= 4 always (H >= 64)
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int n = nbase + (have ? r0 + q : 0);
-    L.dn[q].q[0] = ldg_stream(dc + (size_t)n * 16);
-    L.dn[q].s[0] = ldg_stream_u16(ds + (size_t)n * 2);
-  }
-  // --- SwiGLU outputs of the slice
-  const float gs = gate.tsc[mat] * xs.unscale, us = up.tsc[mat] * xs.unscale;
-#pragma unroll
-  for (int i = 0; i < kPairs; ++i) {
-    const float vg = sum_lanes_rt(dot_row<CPL, 1>(g[i], xs), LPR);
-    const float vu = sum_lanes_rt(dot_row<CPL, 1>(u[i], xs), LPR);
-    if (sl == 0 && pj[i] < kSlice) s_h[pj[i]] = silu(vg * gs) * (vu * us);
+    RowRegs<CPL> g, u;
+    lds_row<CPL>(g, buf + U.gc + pr * (H / 2), buf + U.gs + pr * (H / 16), sl, LPR);
+    lds_row<CPL>(u, buf + U.uc + pr * (H / 2), buf + U.us + pr * (H / 16), sl, LPR);
+    const float vg = sum_lanes_rt(dot_row<CPL, 1>(g, xs), LPR);
+    const float vu = sum_lanes_rt(dot_row<CPL, 1>(u, xs), LPR);
+    if (sl == 0 && p < kSlice) s_h[p] = silu(vg * gs) * (vu * us);
   }
   __syncthreads();
   XStage<1, 2> hs;
   stage_slice(hs, s_h);
-  const float scale = dtsc * hs.unscale * wgt;
-  float part[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) part[q] = dot_row<1, 2>(L.dn[q], hs) * scale;
-  // remaining row groups (only when H / 16 > 128, i.e. H > 2048)
-  if (have) {
-    if (s_part) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) s_part[nbase + r0 + q] += part[q];
-    } else {
-      red_add_v4(acc + nbase + r0, part[0], part[1], part[2], part[3]);
-    }
+  const float scale = down_tsc * hs.unscale * wgt;
+  // down block: consecutive lanes take consecutive rows (conflict-free shared loads)
+  for (int n = warp * 32 + lane; n < H; n += kPWarps * 32) {
+    RowRegs<1> d;
+    d.q[0] = *reinterpret_cast<const uint4*>(buf + U.dc + n * 16);
+    d.s[0] = *reinterpret_cast<const uint16_t*>(buf + U.ds + n * 2);
+    s_part[n] += dot_row<1, 2>(d, hs) * scale;
   }
-  for (int rb = 128; rb < rows_per_warp; rb += 128) {
-    const int rr = rb + r0;
-    if (rr < rows_per_warp) {
-      RowRegs<1> d4[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        d4[q].q[0] = ldg_stream(dc + (size_t)(nbase + rr + q) * 16);
-        d4[q].s[0] = ldg_stream_u16(ds + (size_t)(nbase + rr + q) * 2);
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) part[q] = dot_row<1, 2>(d4[q], hs) * scale;
-      if (s_part) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) s_part[nbase + rr + q] += part[q];
-      } else {
-        red_add_v4(acc + nbase + rr, part[0], part[1], part[2], part[3]);
-      }
-    }
-  }
-  __syncthreads();   // s_h is reused by the next unit
+  __syncthreads();
 }
 
-// Softmax top-k by one warp (see flint.h): largest logit first, ties to the lower index.
+// ---------------------------------------------------------------- top-k
 __device__ __forceinline__ unsigned order_key(float v) {
   const unsigned u = __float_as_uint(v);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Softmax top-k by one warp (see flint.h): largest logit first, ties to the lower index.
 __device__ void topk_warp(const float* logits, int E, int K, int* s_sel, float* s_w) {
   const int lane = threadIdx.x & 31;
   constexpr int kMaxPerLane = FLINT_MAX_EXPERTS / 32;
@@ -271,15 +325,13 @@ __device__ void topk_warp(const float* logits, int E, int K, int* s_sel, float* 
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) {
     const int e = lane + 32 * i;
-    float l = (e < E) ? __ldcg(logits + e) : -INFINITY;
+    float l = (e < E) ? logits[e] : -INFINITY;
     l = (l == l) ? l : -INFINITY;
     val[i] = l;
-    key[i] = (e < E) ? order_key(l) : 0u;      // padding never beats a real expert
+    key[i] = (e < E) ? order_key(l) : 0u;      // every live key is >= 1
   }
   float top0 = 0.f, z = 0.f;
   for (int s = 0; s < K; ++s) {
-    // this lane's best candidate: largest key, then lowest index (retired keys are 0,
-    // every live key is >= 1, so a candidate always exists while s < K <= E)
     unsigned bk = 0u;
     int bi = 0x7FFFFFFF;
 #pragma unroll
@@ -304,9 +356,10 @@ __device__ void topk_warp(const float* logits, int E, int K, int* s_sel, float* 
   }
   __syncwarp();
   if (lane < K) s_w[lane] = s_w[lane] / z;
+  __syncwarp();
 }
 
-// ---------------------------------------------------------------- head phase
+// ---------------------------------------------------------------- head
 template <int CPL>
 __device__ __forceinline__ void head_rows(const PersistArgs& a, const XStage<CPL, 1>& xs, int t,
                                           float& bv, int& bi) {
@@ -350,6 +403,8 @@ __device__ __forceinline__ void best_reduce_warp(float& v, int& i) {
 }
 
 // ---------------------------------------------------------------- the kernel
+enum Role { kRoleShared = 0, kRoleRouted = 1, kRoleRouter = 2 };
+
 template <int CPL>
 __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid_constant__ PersistArgs a) {
   __shared__ float s_h[kSlice];
@@ -357,105 +412,150 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
   __shared__ float s_w[FLINT_MAX_TOP_K];
   __shared__ float s_bv[kPWarps];
   __shared__ int s_bi[kPWarps];
-  extern __shared__ float s_part[];            // [H]: shared-expert partials of this CTA
+  __shared__ float s_red[kPWarps];
+  __shared__ float s_r;
+  __shared__ float s_logits[FLINT_MAX_EXPERTS];
+  __shared__ __align__(8) uint64_t s_bar;
+  extern __shared__ __align__(128) uint8_t s_dyn[];
+  float* s_hx = reinterpret_cast<float*>(s_dyn);                       // [H] residual h
+  float* s_part = s_hx + a.H;                                          // [H] down partials
+  uint8_t* s_wbuf = reinterpret_cast<uint8_t*>(s_part + a.H);          // weight buffer
+
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nC = gridDim.x, c = blockIdx.x;
+  const int c = blockIdx.x, nC = gridDim.x;
   const int H = a.H;
   const int LPR = H / (32 * CPL), RPP = 32 / LPR;
   const int slice = lane / LPR, sl = lane % LPR;
   const int n_sh = a.Fs / kSlice;
-  const int n_rt = a.K * (a.F / kSlice);
-  const int router_per_cta = kPWarps * RPP;
-  const int n_rcta = (a.E + router_per_cta - 1) / router_per_cta;
-  unsigned* bar = a.bar;
-  unsigned gen = 0;
-  int cur = 0;                                  // acc buffer holding h after layer >= 1
+  const int per_slot = a.F / kSlice;
+  const int n_rt = a.K * per_slot;
+  const int n_units = n_sh + n_rt;
+  const int nR = nC - n_units;                       // router CTAs (host checks >= 1)
+  const Role role = c < n_sh ? kRoleShared : (c < n_units ? kRoleRouted : kRoleRouter);
+  const int ridx = c - n_units;                      // router CTA index
+  const int rows_per_router = (a.E + nR - 1) / nR;
+  const int r_lo = role == kRoleRouter ? min(a.E, ridx * rows_per_router) : 0;
+  const int r_hi = role == kRoleRouter ? min(a.E, r_lo + rows_per_router) : 0;
+  unsigned* sync = a.bar;
+  uint32_t phase = 0;                                // parity of the weight-buffer mbarrier
+  (void)lane;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&s_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  // Data-independent weight copies of a layer: router rows or this CTA's shared unit.
+  auto issue_static = [&](int l) {
+    if (threadIdx.x != 0) return;
+    const LayerPtrs& P = a.layer[l];
+    if (role == kRoleShared) {
+      issue_unit_copy(s_wbuf, &s_bar, H, P.sh_gate, P.sh_up, P.sh_dcc_codes, P.sh_dcc_scales,
+                      (size_t)c * kSlice, (size_t)c);
+    } else if (role == kRoleRouter && r_hi > r_lo) {
+      const uint32_t bytes = (uint32_t)(r_hi - r_lo) * H * 2;
+      mbar_expect_tx(&s_bar, bytes);
+      bulk_g2s(s_wbuf, P.router_w + (size_t)r_lo * H, bytes, &s_bar);
+    }
+  };
+  issue_static(0);
+
+  unsigned step = 0;                                 // global layer step
   for (int t = 0; t < a.T; ++t) {
-    for (int l = 0; l < a.L; ++l) {
+    for (int l = 0; l < a.L; ++l, ++step) {
       const LayerPtrs& P = a.layer[l];
-      float* acc_cur = a.acc + cur * H;
-      float* acc_next = a.acc + (cur ^ 1) * H;
-      // ---------------- A
-      // x_l as bf16 pairs (every warp)
+      float* acc_cur = a.acc + (step & 1) * H;
+      float* acc_next = a.acc + ((step + 1) & 1) * H;
+      const int l_next = (l + 1 < a.L) ? l + 1 : 0;
+      const bool more = (l + 1 < a.L) || (t + 1 < a.T);
+      // ---- h_l complete: stage x_l
+      if (step > 0) wait_count(sync, kSyncDone, (unsigned)n_units * step);
       uint32_t xb[CPL * 16];
-      if (l == 0) load_bf16_pairs<CPL>(xb, a.x + (size_t)t * H, sl, LPR);
-      else rmsnorm_bf16_pairs<CPL>(xb, acc_cur, H, a.eps, sl, LPR);
-      // next residual buffer <- h_l (this CTA's rows)
-      for (int n = c * kPThreads + threadIdx.x; n < H; n += nC * kPThreads) {
-        float hv;
-        if (l > 0) hv = __ldcg(acc_cur + n);
-        else if (a.residual) hv = a.residual[(size_t)t * H + n];
-        else hv = bf16_bits_to_f32(a.x[(size_t)t * H + n]);
-        acc_next[n] = hv;
+      if (l == 0) {
+        cta_load_input(a.x + (size_t)t * H, s_hx, H);
+        rms_pairs_from_smem<CPL>(xb, s_hx, 1.0f, sl, LPR);
+      } else {
+        cta_load_rms(acc_cur, s_hx, s_red, H, a.eps, &s_r);
+        rms_pairs_from_smem<CPL>(xb, s_hx, s_r, sl, LPR);
       }
-      bool has_shared = false;
-      for (int n = threadIdx.x; n < H; n += kPThreads) s_part[n] = 0.f;
-      __syncthreads();
-      // router rows
-      const int rc0 = ((c - (n_sh + n_rt)) % nC + nC) % nC;
-      for (int rc = rc0; rc < n_rcta; rc += nC) {
-        const int row = rc * router_per_cta + warp * RPP + slice;
-        XRawBF16<CPL> xr;
+
+      if (role == kRoleRouter) {
+        // next residual buffer <- h_l (router CTAs share the rows)
+        for (int n = ridx * kPThreads + threadIdx.x; n < H; n += nR * kPThreads)
+          acc_next[n] = (l == 0 && a.residual) ? a.residual[(size_t)t * H + n] : s_hx[n];
+        if (r_hi > r_lo) {
+          mbar_wait(&s_bar, phase, sync);
+          phase ^= 1;
+          XRawBF16<CPL> xr;
 #pragma unroll
-        for (int q = 0; q < CPL * 16; ++q) xr.p[q] = xb[q];
-        RowBF16<CPL> r;
-        load_row_bf16<CPL>(r, P.router_w + (size_t)(row < a.E ? row : 0) * H, sl, LPR);
-        const float v = sum_lanes_rt(dot_row_bf16<CPL>(r, xr), LPR);
-        if (row < a.E && sl == 0) a.logits_ws[row] = v + (P.router_bias ? P.router_bias[row] : 0.f);
-      }
-      // shared units
-      if (c < n_sh || n_sh > nC) {
-        XStage<CPL, 1> xs;
-        stage_from_pairs<CPL>(xs, xb, LPR);
-        for (int u = c; u < n_sh; u += nC) {
-          has_shared = true;
-          swiglu_slice_unit<CPL>(a, P.sh_gate, P.sh_up, P.sh_dcc_codes, P.sh_dcc_scales,
-                                 P.sh_down_tsc[0], 0, a.Fs, u * kSlice, 1.0f, xs, s_h, nullptr,
-                                 s_part);
-        }
-      }
-      grid_sync(bar, gen);
-      // ---------------- B
-      if (warp == 0) topk_warp(a.logits_ws, a.E, a.K, s_sel, s_w);
-      __syncthreads();
-      if (c == 0 && threadIdx.x < a.K) {
-        const size_t o = ((size_t)t * a.L + l) * a.K + threadIdx.x;
-        if (a.idx_out) a.idx_out[o] = s_sel[threadIdx.x];
-        if (a.w_out) a.w_out[o] = s_w[threadIdx.x];
-      }
-      if (has_shared) {
-        for (int n = 4 * threadIdx.x; n < H; n += 4 * kPThreads)
-          red_add_v4(acc_next + n, s_part[n], s_part[n + 1], s_part[n + 2], s_part[n + 3]);
-      }
-      {
-        int u0 = (c - n_sh) % nC;
-        if (u0 < 0) u0 += nC;
-        if (u0 < n_rt) {
-          XStage<CPL, 1> xs;
-          stage_from_pairs<CPL>(xs, xb, LPR);
-          const int per_slot = a.F / kSlice;
-          for (int u = u0; u < n_rt; u += nC) {
-            const int s = u / per_slot, j = u % per_slot;
-            int e = s_sel[s];
-            if (e < 0 || e >= a.E) { raise_status(FLINT_ERR_INVALID_ARG); e = 0; }
-            swiglu_slice_unit<CPL>(a, P.gate, P.up, P.dcc_codes, P.dcc_scales, P.down_tsc[e],
-                                   (size_t)e, a.F, j * kSlice, s_w[s], xs, s_h, acc_next,
-                                   nullptr);
+          for (int q = 0; q < CPL * 16; ++q) xr.p[q] = xb[q];
+          for (int r0 = r_lo + warp * RPP; r0 < r_hi; r0 += kPWarps * RPP) {
+            const int row = r0 + slice;
+            RowBF16<CPL> rw;
+            lds_row_bf16<CPL>(rw, reinterpret_cast<const uint16_t*>(s_wbuf) +
+                                      (size_t)((row < r_hi ? row : r_lo) - r_lo) * H, sl, LPR);
+            const float v = sum_lanes_rt(dot_row_bf16<CPL>(rw, xr), LPR);
+            if (row < r_hi && sl == 0) a.logits_ws[row] = v + (P.router_bias ? P.router_bias[row] : 0.f);
           }
         }
+        signal_count(sync, kSyncLogits);
+        __syncthreads();                       // buffer reads done before it is refilled
+        if (more) issue_static(l_next);
+      } else if (role == kRoleShared) {
+        XStage<CPL, 1> xs;
+        stage_from_pairs<CPL>(xs, xb, LPR);
+        for (int n = threadIdx.x; n < H; n += kPThreads) s_part[n] = 0.f;
+        mbar_wait(&s_bar, phase, sync);
+        phase ^= 1;
+        unit_compute<CPL>(s_wbuf, H, P.sh_gate.tsc[0], P.sh_up.tsc[0], P.sh_down_tsc[0], 1.0f, xs,
+                          s_h, s_part);
+        if (more) issue_static(l_next);         // unit_compute ended with a CTA barrier
+        wait_count(sync, kSyncLogits, (unsigned)nR * (step + 1));
+        for (int n = 4 * threadIdx.x; n < H; n += 4 * kPThreads)
+          red_add_v4(acc_next + n, s_part[n], s_part[n + 1], s_part[n + 2], s_part[n + 3]);
+        signal_count(sync, kSyncDone);
+      } else {  // routed
+        XStage<CPL, 1> xs;
+        stage_from_pairs<CPL>(xs, xb, LPR);
+        for (int n = threadIdx.x; n < H; n += kPThreads) s_part[n] = 0.f;
+        wait_count(sync, kSyncLogits, (unsigned)nR * (step + 1));
+        for (int e = threadIdx.x; e < a.E; e += kPThreads) s_logits[e] = __ldcg(a.logits_ws + e);
+        __syncthreads();
+        if (warp == 0) topk_warp(s_logits, a.E, a.K, s_sel, s_w);
+        __syncthreads();
+        const int u = c - n_sh;
+        const int sslot = u / per_slot, j = u % per_slot;
+        int e = s_sel[sslot];
+        if (e < 0 || e >= a.E) { raise_status(FLINT_ERR_INVALID_ARG); e = 0; }
+        if (threadIdx.x == 0)
+          issue_unit_copy(s_wbuf, &s_bar, H, P.gate, P.up, P.dcc_codes, P.dcc_scales,
+                          (size_t)e * a.F + (size_t)j * kSlice, (size_t)e * per_slot + j);
+        if (u == 0 && threadIdx.x < a.K) {
+          const size_t o = ((size_t)t * a.L + l) * a.K + threadIdx.x;
+          if (a.idx_out) a.idx_out[o] = s_sel[threadIdx.x];
+          if (a.w_out) a.w_out[o] = s_w[threadIdx.x];
+        }
+        mbar_wait(&s_bar, phase, sync);
+        phase ^= 1;
+        unit_compute<CPL>(s_wbuf, H, P.gate.tsc[e], P.up.tsc[e], P.down_tsc[e], s_w[sslot], xs, s_h,
+                          s_part);
+        for (int n = 4 * threadIdx.x; n < H; n += 4 * kPThreads)
+          red_add_v4(acc_next + n, s_part[n], s_part[n + 1], s_part[n + 2], s_part[n + 3]);
+        signal_count(sync, kSyncDone);
       }
-      grid_sync(bar, gen);
-      cur ^= 1;
     }
     // ---------------- outputs of token t
-    const float* hfin = a.acc + cur * H;
+    wait_count(sync, kSyncDone, (unsigned)n_units * step);
+    const float* hfin = a.acc + (step & 1) * H;
     if (a.out)
       for (int n = c * kPThreads + threadIdx.x; n < H; n += nC * kPThreads)
         a.out[(size_t)t * H + n] = __ldcg(hfin + n);
     if (a.x_out || a.head.codes) {
       uint32_t xb[CPL * 16];
-      rmsnorm_bf16_pairs<CPL>(xb, hfin, H, a.eps, sl, LPR);
-      if (a.x_out && c == 0 && warp == 0) {
+      cta_load_rms(hfin, s_hx, s_red, H, a.eps, &s_r);
+      rms_pairs_from_smem<CPL>(xb, s_hx, s_r, sl, LPR);
+      if (a.x_out && c == 0 && warp == 0 && slice == 0) {
         uint32_t* dst = reinterpret_cast<uint32_t*>(a.x_out + (size_t)t * H);
 #pragma unroll
         for (int i = 0; i < CPL; ++i)
@@ -469,29 +569,37 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         int bi = 0x7FFFFFFF;
         head_rows<CPL>(a, xs, t, bv, bi);
         best_reduce_warp(bv, bi);
-        if (lane == 0) { s_bv[warp] = bv; s_bi[warp] = bi; }
+        if ((threadIdx.x & 31) == 0) { s_bv[warp] = bv; s_bi[warp] = bi; }
         __syncthreads();
+        float* best_v = a.best_v + (t & 1) * kMaxCtas;
+        int* best_i = a.best_i + (t & 1) * kMaxCtas;
         if (threadIdx.x == 0) {
           for (int w = 1; w < kPWarps; ++w)
             if (s_bv[w] > bv || (s_bv[w] == bv && s_bi[w] < bi)) { bv = s_bv[w]; bi = s_bi[w]; }
-          a.best_v[c] = bv;
-          a.best_i[c] = bi;
+          best_v[c] = bv;
+          best_i[c] = bi;
         }
-        grid_sync(bar, gen);
-        if (c == 0 && warp == 0) {
-          float v = -INFINITY;
-          int i = 0x7FFFFFFF;
-          for (int k = lane; k < nC; k += 32) {
-            const float kv = __ldcg(a.best_v + k);
-            const int ki = __ldcg(a.best_i + k);
-            if (kv > v || (kv == v && ki < i)) { v = kv; i = ki; }
+        signal_count(sync, kSyncHead);
+        if (c == 0) {
+          wait_count(sync, kSyncHead, (unsigned)nC * (t + 1));
+          if (warp == 0) {
+            const int ln = threadIdx.x & 31;
+            float v = -INFINITY;
+            int i = 0x7FFFFFFF;
+            for (int k = ln; k < nC; k += 32) {
+              const float kv = __ldcg(best_v + k);
+              const int ki = __ldcg(best_i + k);
+              if (kv > v || (kv == v && ki < i)) { v = kv; i = ki; }
+            }
+            best_reduce_warp(v, i);
+            if (ln == 0 && a.argmax) a.argmax[t] = (i < a.V) ? i : 0;
           }
-          best_reduce_warp(v, i);
-          if (lane == 0 && a.argmax) a.argmax[t] = (i < a.V) ? i : 0;
         }
       }
     }
   }
+  // No bulk copy is in flight at exit: copies are issued only while `more` holds, and
+  // every issued copy is waited for in the step that follows.
 }
 
 // ---------------------------------------------------------------- column-chunk repack
@@ -526,40 +634,46 @@ cudaError_t launch_column_chunks(const uint8_t* codes, const uint8_t* scales, in
 
 // ---------------------------------------------------------------- host side
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
-constexpr int kMaxCtas = 1024;
 
 size_t decode_workspace_bytes(int H, int E) {
-  return align256(sizeof(float) * E) + align256(sizeof(float) * 2 * H) + 256 +
-         align256(kMaxCtas * (sizeof(float) + sizeof(int)));
+  return sizeof(unsigned) * kSyncWords + align256(sizeof(float) * E) +
+         align256(sizeof(float) * 2 * H) + 2 * align256(2 * kMaxCtas * sizeof(float));
 }
 
 void decode_carve(PersistArgs& a, void* ws) {
   char* p = static_cast<char*>(ws);
-  a.bar = reinterpret_cast<unsigned*>(p); p += 256;
+  a.bar = reinterpret_cast<unsigned*>(p); p += sizeof(unsigned) * kSyncWords;
   a.logits_ws = reinterpret_cast<float*>(p); p += align256(sizeof(float) * a.E);
   a.acc = reinterpret_cast<float*>(p); p += align256(sizeof(float) * 2 * a.H);
-  a.best_v = reinterpret_cast<float*>(p); p += align256(kMaxCtas * sizeof(float));
+  a.best_v = reinterpret_cast<float*>(p); p += align256(2 * kMaxCtas * sizeof(float));
   a.best_i = reinterpret_cast<int*>(p);
+}
+
+static int g_sms = 0;
+int decode_grid() {
+  if (g_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_sms > kMaxCtas) g_sms = kMaxCtas;
+  }
+  return g_sms;
+}
+
+size_t decode_smem_bytes(int H, int E, int nR) {
+  const size_t unit = UnitLayout::of(H).bytes;
+  const size_t router = (size_t)((E + nR - 1) / nR) * H * 2;
+  return 2 * sizeof(float) * H + (unit > router ? unit : router);
 }
 
 template <int CPL>
 static cudaError_t launch_persistent_cpl(const PersistArgs& a, cudaStream_t st) {
-  static int grid = 0;
-  const size_t smem = sizeof(float) * a.H;
-  if (grid == 0) {
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaError_t e = cudaFuncSetAttribute(k_decode_persistent<CPL>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(sizeof(float) * FLINT_MAX_HIDDEN));
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode_persistent<CPL>, kPThreads,
-                                                      sizeof(float) * FLINT_MAX_HIDDEN);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorLaunchOutOfResources;
-    grid = sms < kMaxCtas ? sms : kMaxCtas;   // one CTA per SM
-  }
+  const int grid = decode_grid();
+  const int nR = grid - (a.Fs / kSlice + a.K * (a.F / kSlice));
+  const size_t smem = decode_smem_bytes(a.H, a.E, nR);
+  cudaError_t e = cudaFuncSetAttribute(k_decode_persistent<CPL>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kPThreads);
@@ -574,11 +688,10 @@ static cudaError_t launch_persistent_cpl(const PersistArgs& a, cudaStream_t st) 
 }
 
 cudaError_t launch_persistent(const PersistArgs& a, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(a.bar, 0, 256, st);
+  cudaError_t e = cudaMemsetAsync(a.bar, 0, sizeof(unsigned) * kSyncWords, st);
   if (e != cudaSuccess) return e;
   if (a.H <= 1024) return launch_persistent_cpl<1>(a, st);
-  if (a.H <= 2048) return launch_persistent_cpl<2>(a, st);
-  return launch_persistent_cpl<4>(a, st);
+  return launch_persistent_cpl<2>(a, st);
 }
 
 }  // namespace flint

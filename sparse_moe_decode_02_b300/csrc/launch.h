@@ -47,6 +47,8 @@ struct PersistArgs {
 };
 
 size_t decode_workspace_bytes(int H, int E);
+int decode_grid();                                   // CTAs of the persistent kernel
+size_t decode_smem_bytes(int H, int E, int n_router_ctas);
 void decode_carve(PersistArgs& a, void* ws);
 cudaError_t launch_persistent(const PersistArgs& a, cudaStream_t st);
 cudaError_t launch_column_chunks(const uint8_t* codes, const uint8_t* scales, int n_mat, int rows,
