@@ -131,71 +131,77 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 }
 
 // ---------------------------------------------------------------- activation staging
-// The CTA reads the residual h (fp32 [H], L2) once into shared memory, sums squares in
-// a fixed order (every CTA gets the same value), and leaves r = 1/sqrt(mean(h^2)+eps)
-// in *s_r.  Warps then build their bf16 x = bf16(h * r) pairs from shared memory.
-__device__ __forceinline__ void cta_load_rms(const float* h, float* s_h, float* s_red, int H,
-                                             float eps, float* s_r) {
-  float ss = 0.f;
-  for (int n = 4 * threadIdx.x; n < H; n += 4 * kPThreads) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(h + n));
-    *reinterpret_cast<float4*>(s_h + n) = v;
-    ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss);
-    ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
+// x_l is built once per CTA (thread t owns elements [4t, 4t+4); H <= 4 * 512):
+//   h    fp32 residual (global, L2) -> s_hx (kept for the residual copy)
+//   x    bf16(h * r), r = 1/sqrt(mean(h^2) + eps)  (r = 1 for a layer-0 input, which
+//        is bf16 already)                            -> s_xb
+//   xf   f16(x * 2^k), the GEMV operand; 2^k puts max|x| in [2^14, 2^15) -> s_xf
+// Sum of squares and max|h| come from one fixed-order block reduction, so every CTA
+// derives the same r and k (max|bf16(h r)| = bf16(max|h| r): rounding is monotone).
+struct Staged {
+  float unscale;    // 2^-k
+};
+
+__device__ __forceinline__ Staged cta_stage(const float* h_f32, const uint16_t* x_bf16, int H,
+                                            float eps, float* s_hx, uint16_t* s_xb,
+                                            uint16_t* s_xf, float* s_red) {
+  const int n = 4 * threadIdx.x;
+  const bool own = n < H;
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  if (own) {
+    if (h_f32) {
+      const float4 f = __ldcg(reinterpret_cast<const float4*>(h_f32 + n));
+      v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    } else {
+      const uint2 b = __ldcg(reinterpret_cast<const uint2*>(x_bf16 + n));
+      v[0] = bf16_bits_to_f32(b.x & 0xFFFFu); v[1] = bf16_bits_to_f32(b.x >> 16);
+      v[2] = bf16_bits_to_f32(b.y & 0xFFFFu); v[3] = bf16_bits_to_f32(b.y >> 16);
+    }
+    *reinterpret_cast<float4*>(s_hx + n) = make_float4(v[0], v[1], v[2], v[3]);
   }
+  float ss = 0.f, am = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) { ss = fmaf(v[q], v[q], ss); am = fmaxf(am, fabsf(v[q])); }
   ss = sum_lanes<32>(ss);
-  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+  if ((threadIdx.x & 31) == 0) { s_red[threadIdx.x >> 5] = ss; s_red[kPWarps + (threadIdx.x >> 5)] = am; }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float tot = 0.f;
-    for (int w = 0; w < kPWarps; ++w) tot += s_red[w];
-    *s_r = 1.0f / sqrtf(tot / (float)H + eps);
+  float tot = 0.f, amax = 0.f;
+#pragma unroll
+  for (int w = 0; w < kPWarps; ++w) { tot += s_red[w]; amax = fmaxf(amax, s_red[kPWarps + w]); }
+  const float r = h_f32 ? 1.0f / sqrtf(tot / (float)H + eps) : 1.0f;
+  const float xmax = bf16_bits_to_f32(f32_to_bf16_rn(amax * r));
+  const int k = f16_stage_exponent(xmax);
+  const float s = exp2i(k);
+  if (own) {
+    uint16_t b[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) b[q] = f32_to_bf16_rn(v[q] * r);
+    *reinterpret_cast<uint2*>(s_xb + n) =
+        make_uint2((uint32_t)b[0] | ((uint32_t)b[1] << 16), (uint32_t)b[2] | ((uint32_t)b[3] << 16));
+    const uint32_t f01 = pack_f16x2_rn(bf16_bits_to_f32(b[0]) * s, bf16_bits_to_f32(b[1]) * s);
+    const uint32_t f23 = pack_f16x2_rn(bf16_bits_to_f32(b[2]) * s, bf16_bits_to_f32(b[3]) * s);
+    *reinterpret_cast<uint2*>(s_xf + n) = make_uint2(f01, f23);
   }
   __syncthreads();
+  return Staged{exp2i(-k)};
 }
 
-// The token's input row (bf16) into shared memory as fp32 (exact).
-__device__ __forceinline__ void cta_load_input(const uint16_t* x, float* s_h, int H) {
-  for (int n = 2 * threadIdx.x; n < H; n += 2 * kPThreads) {
-    const uint32_t two = __ldcg(reinterpret_cast<const unsigned int*>(x + n));
-    s_h[n] = bf16_bits_to_f32(two & 0xFFFFu);
-    s_h[n + 1] = bf16_bits_to_f32(two >> 16);
-  }
-  __syncthreads();
-}
-
+// The lane's chunk pairs from a staged 16-bit vector (bf16 or f16) in shared memory.
 template <int CPL>
-__device__ __forceinline__ void rms_pairs_from_smem(uint32_t (&xb)[CPL * 16], const float* s_h,
-                                                    float r, int sl, int LPR) {
+__device__ __forceinline__ void pairs_from_smem(uint32_t (&p)[CPL * 16], const uint16_t* s_v,
+                                                int sl, int LPR) {
 #pragma unroll
   for (int i = 0; i < CPL; ++i) {
-    const float4* src = reinterpret_cast<const float4*>(s_h + 32 * (sl + LPR * i));
+    const uint4* src = reinterpret_cast<const uint4*>(s_v + 32 * (sl + LPR * i));
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float4 f = src[j];
-      xb[i * 16 + 2 * j] = (uint32_t)f32_to_bf16_rn(f.x * r) | ((uint32_t)f32_to_bf16_rn(f.y * r) << 16);
-      xb[i * 16 + 2 * j + 1] = (uint32_t)f32_to_bf16_rn(f.z * r) | ((uint32_t)f32_to_bf16_rn(f.w * r) << 16);
+    for (int j = 0; j < 4; ++j) {
+      const uint4 q = src[j];
+      p[i * 16 + 4 * j] = q.x; p[i * 16 + 4 * j + 1] = q.y;
+      p[i * 16 + 4 * j + 2] = q.z; p[i * 16 + 4 * j + 3] = q.w;
     }
   }
-}
-
-// bf16 pairs -> f16 pairs scaled by 2^k (exact), amax over the slice
-template <int CPL>
-__device__ __forceinline__ void stage_from_pairs(XStage<CPL, 1>& xs, const uint32_t (&xb)[CPL * 16],
-                                                 int LPR) {
-  float amax = 0.f;
-#pragma unroll
-  for (int q = 0; q < CPL * 16; ++q) {
-    amax = fmaxf(amax, fabsf(bf16_bits_to_f32(xb[q] & 0xFFFFu)));
-    amax = fmaxf(amax, fabsf(bf16_bits_to_f32(xb[q] >> 16)));
-  }
-  amax = max_lanes_rt(amax, LPR);
-  const int k = f16_stage_exponent(amax);
-  const float s = exp2i(k);
-  xs.unscale = exp2i(-k);
-#pragma unroll
-  for (int q = 0; q < CPL * 16; ++q)
-    xs.p[0][q] = pack_f16x2_rn(bf16_bits_to_f32(xb[q] & 0xFFFFu) * s, bf16_bits_to_f32(xb[q] >> 16) * s);
 }
 
 // A 32-value slice (shared memory) staged as hi/lo f16 pairs: every lane holds all 32.
@@ -317,9 +323,9 @@ __device__ __forceinline__ unsigned order_key(float v) {
 }
 
 // Softmax top-k by one warp (see flint.h): largest logit first, ties to the lower index.
+template <int kMaxPerLane>
 __device__ void topk_warp(const float* logits, int E, int K, int* s_sel, float* s_w) {
   const int lane = threadIdx.x & 31;
-  constexpr int kMaxPerLane = FLINT_MAX_EXPERTS / 32;
   unsigned key[kMaxPerLane];
   float val[kMaxPerLane];
 #pragma unroll
@@ -357,6 +363,16 @@ __device__ void topk_warp(const float* logits, int E, int K, int* s_sel, float* 
   __syncwarp();
   if (lane < K) s_w[lane] = s_w[lane] / z;
   __syncwarp();
+}
+
+__device__ __forceinline__ void topk_dispatch(const float* logits, int E, int K, int* s_sel,
+                                              float* s_w) {
+  const int per_lane = (E + 31) / 32;
+  if (per_lane <= 1) topk_warp<1>(logits, E, K, s_sel, s_w);
+  else if (per_lane <= 2) topk_warp<2>(logits, E, K, s_sel, s_w);
+  else if (per_lane <= 4) topk_warp<4>(logits, E, K, s_sel, s_w);
+  else if (per_lane <= 8) topk_warp<8>(logits, E, K, s_sel, s_w);
+  else topk_warp<16>(logits, E, K, s_sel, s_w);
 }
 
 // ---------------------------------------------------------------- head
@@ -412,14 +428,15 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
   __shared__ float s_w[FLINT_MAX_TOP_K];
   __shared__ float s_bv[kPWarps];
   __shared__ int s_bi[kPWarps];
-  __shared__ float s_red[kPWarps];
-  __shared__ float s_r;
+  __shared__ float s_red[2 * kPWarps];
   __shared__ float s_logits[FLINT_MAX_EXPERTS];
   __shared__ __align__(8) uint64_t s_bar;
   extern __shared__ __align__(128) uint8_t s_dyn[];
   float* s_hx = reinterpret_cast<float*>(s_dyn);                       // [H] residual h
   float* s_part = s_hx + a.H;                                          // [H] down partials
-  uint8_t* s_wbuf = reinterpret_cast<uint8_t*>(s_part + a.H);          // weight buffer
+  uint16_t* s_xb = reinterpret_cast<uint16_t*>(s_part + a.H);          // [H] x, bf16
+  uint16_t* s_xf = s_xb + a.H;                                         // [H] x * 2^k, f16
+  uint8_t* s_wbuf = reinterpret_cast<uint8_t*>(s_xf + a.H);            // weight buffer
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = blockIdx.x, nC = gridDim.x;
@@ -471,14 +488,8 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
       const bool more = (l + 1 < a.L) || (t + 1 < a.T);
       // ---- h_l complete: stage x_l
       if (step > 0) wait_count(sync, kSyncDone, (unsigned)n_units * step);
-      uint32_t xb[CPL * 16];
-      if (l == 0) {
-        cta_load_input(a.x + (size_t)t * H, s_hx, H);
-        rms_pairs_from_smem<CPL>(xb, s_hx, 1.0f, sl, LPR);
-      } else {
-        cta_load_rms(acc_cur, s_hx, s_red, H, a.eps, &s_r);
-        rms_pairs_from_smem<CPL>(xb, s_hx, s_r, sl, LPR);
-      }
+      const Staged stg = cta_stage(l == 0 ? nullptr : acc_cur, a.x + (size_t)t * H, H, a.eps, s_hx,
+                                   s_xb, s_xf, s_red);
 
       if (role == kRoleRouter) {
         // next residual buffer <- h_l (router CTAs share the rows)
@@ -488,8 +499,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
           mbar_wait(&s_bar, phase, sync);
           phase ^= 1;
           XRawBF16<CPL> xr;
-#pragma unroll
-          for (int q = 0; q < CPL * 16; ++q) xr.p[q] = xb[q];
+          pairs_from_smem<CPL>(xr.p, s_xb, sl, LPR);
           for (int r0 = r_lo + warp * RPP; r0 < r_hi; r0 += kPWarps * RPP) {
             const int row = r0 + slice;
             RowBF16<CPL> rw;
@@ -504,7 +514,8 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         if (more) issue_static(l_next);
       } else if (role == kRoleShared) {
         XStage<CPL, 1> xs;
-        stage_from_pairs<CPL>(xs, xb, LPR);
+        pairs_from_smem<CPL>(xs.p[0], s_xf, sl, LPR);
+        xs.unscale = stg.unscale;
         for (int n = threadIdx.x; n < H; n += kPThreads) s_part[n] = 0.f;
         mbar_wait(&s_bar, phase, sync);
         phase ^= 1;
@@ -517,12 +528,13 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         signal_count(sync, kSyncDone);
       } else {  // routed
         XStage<CPL, 1> xs;
-        stage_from_pairs<CPL>(xs, xb, LPR);
+        pairs_from_smem<CPL>(xs.p[0], s_xf, sl, LPR);
+        xs.unscale = stg.unscale;
         for (int n = threadIdx.x; n < H; n += kPThreads) s_part[n] = 0.f;
         wait_count(sync, kSyncLogits, (unsigned)nR * (step + 1));
         for (int e = threadIdx.x; e < a.E; e += kPThreads) s_logits[e] = __ldcg(a.logits_ws + e);
         __syncthreads();
-        if (warp == 0) topk_warp(s_logits, a.E, a.K, s_sel, s_w);
+        if (warp == 0) topk_dispatch(s_logits, a.E, a.K, s_sel, s_w);
         __syncthreads();
         const int u = c - n_sh;
         const int sslot = u / per_slot, j = u % per_slot;
@@ -552,19 +564,14 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
       for (int n = c * kPThreads + threadIdx.x; n < H; n += nC * kPThreads)
         a.out[(size_t)t * H + n] = __ldcg(hfin + n);
     if (a.x_out || a.head.codes) {
-      uint32_t xb[CPL * 16];
-      cta_load_rms(hfin, s_hx, s_red, H, a.eps, &s_r);
-      rms_pairs_from_smem<CPL>(xb, s_hx, s_r, sl, LPR);
-      if (a.x_out && c == 0 && warp == 0 && slice == 0) {
-        uint32_t* dst = reinterpret_cast<uint32_t*>(a.x_out + (size_t)t * H);
-#pragma unroll
-        for (int i = 0; i < CPL; ++i)
-#pragma unroll
-          for (int q = 0; q < 16; ++q) dst[16 * (sl + LPR * i) + q] = xb[i * 16 + q];
-      }
+      const Staged stg = cta_stage(hfin, nullptr, H, a.eps, s_hx, s_xb, s_xf, s_red);
+      if (a.x_out && c == 0)
+        for (int n = 4 * threadIdx.x; n < H; n += 4 * kPThreads)
+          *reinterpret_cast<uint2*>(a.x_out + (size_t)t * H + n) = *reinterpret_cast<const uint2*>(s_xb + n);
       if (a.head.codes) {
         XStage<CPL, 1> xs;
-        stage_from_pairs<CPL>(xs, xb, LPR);
+        pairs_from_smem<CPL>(xs.p[0], s_xf, sl, LPR);
+        xs.unscale = stg.unscale;
         float bv = -INFINITY;
         int bi = 0x7FFFFFFF;
         head_rows<CPL>(a, xs, t, bv, bi);
@@ -663,7 +670,7 @@ int decode_grid() {
 size_t decode_smem_bytes(int H, int E, int nR) {
   const size_t unit = UnitLayout::of(H).bytes;
   const size_t router = (size_t)((E + nR - 1) / nR) * H * 2;
-  return 2 * sizeof(float) * H + (unit > router ? unit : router);
+  return (2 * sizeof(float) + 2 * sizeof(uint16_t)) * H + (unit > router ? unit : router);
 }
 
 template <int CPL>
