@@ -189,6 +189,33 @@ flint_status flint_decode_tokens(const flint_moe_layer* layers, int n_layers,
                                  size_t ws_bytes, flint_stream stream);
 
 /* ----------------------------------------------------------------------------
+ * flint_decode_tokens_noalloc -- flint_decode_tokens without a workspace argument.
+ * No counterpart on the Flint pages: this is a service to callers that cannot
+ * allocate device memory for scratch -- a host that reserves the whole GPU up front
+ * and gives its extensions no allocator, or a serving loop that must not call
+ * cudaMalloc (which can block and synchronise the device).  The scratch lives in a
+ * fixed device array of FLINT_NOALLOC_SCRATCH_BYTES inside the library, held on
+ * every GPU that loads the library until the process exits; this entry point calls
+ * no cudaMalloc/cudaFree or other allocating routine.
+ *  - The first call on a device looks up that array's device address
+ *    (cudaGetSymbolAddress) for the current device and caches it; make that first
+ *    call before any stream capture.
+ *  - All calls share the one array.  Calls whose kernels overlap on the GPU (other
+ *    streams, other host threads) race on it and must be serialised by the caller.
+ *    Each call clears what must start at zero; the rest is rewritten before use.
+ *  - A shape whose scratch would exceed FLINT_NOALLOC_SCRATCH_BYTES is rejected with
+ *    FLINT_ERR_UNSUPPORTED (every shape flint_decode_tokens supports fits).
+ * Arguments and results are those of flint_decode_tokens.
+ * -------------------------------------------------------------------------- */
+#define FLINT_NOALLOC_SCRATCH_BYTES (64 * 1024)
+flint_status flint_decode_tokens_noalloc(const flint_moe_layer* layers, int n_layers,
+                                         const flint_nvfp4* head, const void* x_bf16,
+                                         const float* residual, int T, float rms_eps,
+                                         float* out, void* x_out_bf16, float* logits,
+                                         int32_t* argmax, int32_t* topk_idx, float* topk_w,
+                                         flint_stream stream);
+
+/* ----------------------------------------------------------------------------
  * flint_moe_prefill -- the same layer over T prompt tokens, as a token-permuted
  * grouped GEMM on block-scaled FP4 tensor cores.  Both operands of the FP4
  * products are NVFP4: x rows and the SwiGLU outputs h are quantised with the

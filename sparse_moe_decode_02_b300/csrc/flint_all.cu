@@ -5,3 +5,4 @@
 #include "lm_head.cu"
 #include "prefill.cu"
 #include "api.cu"
+#include "noalloc.cu"

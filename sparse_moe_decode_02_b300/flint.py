@@ -73,6 +73,9 @@ def lib() -> ctypes.CDLL:
     L.flint_nvfp4_column_chunks.argtypes = [ctypes.POINTER(_NVFP4C), vp, vp, vp]
     L.flint_decode_tokens.argtypes = [ctypes.POINTER(_LayerC), i, ctypes.POINTER(_NVFP4C), vp, vp,
                                       i, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flint_decode_tokens_noalloc.argtypes = [ctypes.POINTER(_LayerC), i, ctypes.POINTER(_NVFP4C),
+                                              vp, vp, i, ctypes.c_float, vp, vp, vp, vp, vp, vp,
+                                              vp]
     L.flint_moe_decode.argtypes = [ctypes.POINTER(_LayerC), vp, vp, vp, vp, ctypes.c_float, vp,
                                    vp, i, vp, sz, vp]
     L.flint_moe_prefill.argtypes = [ctypes.POINTER(_LayerC), vp, vp, vp, vp, vp, vp, i, vp, sz,
@@ -85,8 +88,8 @@ def lib() -> ctypes.CDLL:
     L.flint_status_string.restype = ctypes.c_char_p
     L.flint_version.restype = ctypes.c_char_p
     for name in ("flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_nvfp4_column_chunks",
-                 "flint_moe_decode", "flint_decode_tokens", "flint_moe_prefill",
-                 "flint_lm_head", "flint_last_device_status"):
+                 "flint_moe_decode", "flint_decode_tokens", "flint_decode_tokens_noalloc",
+                 "flint_moe_prefill", "flint_lm_head", "flint_last_device_status"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -247,6 +250,23 @@ def decode_tokens(layers, x: torch.Tensor, head: NVFP4 | None = None,
                                      _ptr(residual), T, float(rms_eps), _ptr(out), _ptr(x_out),
                                      _ptr(logits), _ptr(argmax), _ptr(topk_idx), _ptr(topk_w),
                                      _ptr(ws), ws.numel(), _stream(stream)), "flint_decode_tokens")
+
+
+def decode_tokens_noalloc(layers, x: torch.Tensor, head: NVFP4 | None = None,
+                          residual: torch.Tensor | None = None, rms_eps: float = 1e-6, out=None,
+                          x_out=None, logits=None, argmax=None, topk_idx=None, topk_w=None,
+                          stream=None):
+    """decode_tokens with the library's fixed device scratch instead of a workspace (for
+    callers that cannot allocate; see flint_decode_tokens_noalloc in flint.h)."""
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    arr = (_LayerC * len(layers))(*[l.c() for l in layers])
+    hc = head.c() if head is not None else None
+    _check(lib().flint_decode_tokens_noalloc(arr, len(layers), ctypes.byref(hc) if hc else None,
+                                             _ptr(x), _ptr(residual), x.shape[0], float(rms_eps),
+                                             _ptr(out), _ptr(x_out), _ptr(logits), _ptr(argmax),
+                                             _ptr(topk_idx), _ptr(topk_w), _stream(stream)),
+           "flint_decode_tokens_noalloc")
 
 
 def moe_prefill(layer: MoELayer, x: torch.Tensor, out: torch.Tensor | None = None,
