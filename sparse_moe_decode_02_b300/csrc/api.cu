@@ -279,6 +279,8 @@ flint_status flint_moe_prefill(const flint_moe_layer* L, const void* x_bf16, flo
   if (s != FLINT_OK) return s;
   if (!x_bf16 || !out || !ws) return FLINT_ERR_INVALID_ARG;
   if (T <= 0) return FLINT_ERR_INVALID_ARG;
+  if (!flint::prefill_shape_ok(L->hidden, L->n_experts, L->top_k, L->expert_width, L->shared_width))
+    return FLINT_ERR_UNSUPPORTED;
   if (!aligned16(x_bf16) || !aligned16(out) || (topk_idx && !aligned4(topk_idx)) ||
       (topk_w && !aligned4(topk_w)) || (expert_counts && !aligned4(expert_counts)) ||
       (pair_order && !aligned4(pair_order)))

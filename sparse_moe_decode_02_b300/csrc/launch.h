@@ -68,6 +68,7 @@ struct PrefillArgs {
 };
 
 size_t prefill_workspace_bytes(int H, int E, int K, int F, int Fs, int T);
+bool prefill_shape_ok(int H, int E, int K, int F, int Fs);
 cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st);
 
 size_t lm_head_workspace_bytes(int H, int V, int B);
