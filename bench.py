@@ -32,14 +32,15 @@ N_TOKENS = 256
 EPS = 1e-6
 SEED = 0
 ZIPF = 1.1
+PREFILL_TOKENS = 4096
 
 
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return {"hbm_gbs": d.get("hbm_gbs"), "src": "measured"}
-    return {"hbm_gbs": 6400.0, "src": "fallback"}
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"), "src": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "src": "fallback"}
 
 
 class ClockSampler:
@@ -125,77 +126,33 @@ def run_flint(args):
     torch.cuda.synchronize()
     T = args.tokens
     x_tok = synth.tokens_bf16(SEED, H, T, stream=1 + rank, device=dev)
-    h = [torch.empty(1, H, dtype=torch.float32, device=dev) for _ in range(2)]
-    xb = [torch.empty(1, H, dtype=torch.bfloat16, device=dev) for _ in range(2)]
     argmax = torch.zeros(T, dtype=torch.int32, device=dev)
-    ws_dec = torch.empty(flint.workspace_bytes(flint.OP_MOE_DECODE, H, shape.n_experts,
-                                               shape.top_k, shape.expert_width,
-                                               shape.shared_width, 0, 1),
-                         dtype=torch.uint8, device=dev)
-    ws_head = torch.empty(flint.workspace_bytes(flint.OP_LM_HEAD, H, 0, 0, 0, 0, shape.vocab, 1),
-                          dtype=torch.uint8, device=dev)
-
-    def token_calls(t, stream):
-        """One decode token: 47 chained layers then the head (public C-ABI calls)."""
-        x_in = x_tok[t:t + 1]
-        for l, layer in enumerate(layers):
-            res = None if l == 0 else h[l % 2]
-            flint.moe_decode(layer, x_in, residual=res, out=h[(l + 1) % 2],
-                             x_next=xb[l % 2], rms_eps=EPS, ws=ws_dec, stream=stream)
-            x_in = xb[l % 2]
-        flint.lm_head(head, x_in, want_logits=False, argmax=argmax[t:t + 1], ws=ws_head,
-                      stream=stream)
-
-    def layer_only_calls(stream, reps):
-        for r in range(reps):
-            for l, layer in enumerate(layers):
-                res = None if l == 0 else h[l % 2]
-                flint.moe_decode(layer, xb[(l + 1) % 2] if l else x_tok[0:1], residual=res,
-                                 out=h[(l + 1) % 2], x_next=xb[l % 2], rms_eps=EPS, ws=ws_dec,
-                                 stream=stream)
-
-    # CUDA graphs: one per token position (the input row differs)
-    cap = torch.cuda.Stream()
-    graphs = []
-    torch.cuda.synchronize()
-    with torch.cuda.stream(cap):
-        token_calls(0, cap)     # eager warm-up outside capture
-    torch.cuda.synchronize()
-    for t in range(T):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cap):
-            token_calls(t, cap)
-        graphs.append(g)
-    g_layers = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_layers, stream=cap):
-        layer_only_calls(cap, 2)
-    g_head = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_head, stream=cap):
-        for r in range(8):
-            flint.lm_head(head, xb[0], want_logits=False, argmax=argmax[0:1], ws=ws_head,
-                          stream=cap)
-    torch.cuda.synchronize()
+    ws = torch.empty(flint.workspace_bytes(flint.OP_MOE_DECODE, H, shape.n_experts, shape.top_k,
+                                           shape.expert_width, shape.shared_width, 0, T),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
 
     def step():
-        for g in graphs:
-            g.replay()
+        """256 tokens x 47 layers + head: one persistent kernel launch (public C ABI)."""
+        flint.decode_tokens(layers, x_tok, head=head, rms_eps=EPS, argmax=argmax, ws=ws,
+                            stream=stream)
 
-    stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     assert flint.last_device_status() == 0, "device status after warm-up"
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        ev0.record(stream)
-        for _ in range(args.steps):
+        ev[0].record(stream)
+        for i in range(args.steps):
             step()
-        ev1.record(stream)
+            ev[i + 1].record(stream)
         torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1)
+    per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    ms = ev[0].elapsed_time(ev[-1])
     if world > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -204,24 +161,12 @@ def run_flint(args):
     tok_per_s = world * args.steps * T / (ms / 1e3)
     status = flint.last_device_status()
 
-    # per-unit timings for the roofline: the MoE layer call and the head, each replayed
-    # from a graph of back-to-back launches (weights far larger than L2 between reuses)
-    def time_graph(g, reps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g.replay()
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / reps
-
-    layer_ms = time_graph(g_layers, 10) / (2 * args.layers)
-    head_ms = time_graph(g_head, 10) / 8
     layer_bytes = workload.layer_bytes_per_token(shape)
     head_b = workload.head_bytes(shape.vocab, H)
     token_bytes = args.layers * layer_bytes + head_b
+    launch_bytes = T * token_bytes
+    launch_ms = statistics.mean(per_launch)
+    achieved = launch_bytes / (launch_ms * 1e-3) / 1e9
     peaks = _peaks()
 
     # end to end through the public API: host (pinned) inputs in, argmax out, per step
@@ -262,31 +207,93 @@ def run_flint(args):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "flint_moe_decode (one MoE layer call, B=1)",
-            "achieved": round(layer_bytes / (layer_ms * 1e-3) / 1e9, 1),
+            "kernel": "k_decode_persistent (flint_decode_tokens: %d tokens x %d layers + head)"
+                      % (T, args.layers),
+            "achieved": round(achieved, 1),
             "peak": peaks["hbm_gbs"],
             "peak_src": peaks["src"],
             "unit": "GB/s",
-            "frac": round(layer_bytes / (layer_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "frac": round(achieved / peaks["hbm_gbs"], 4),
             "traffic": None,
-            "algorithmic_bytes_per_launch": layer_bytes,
-            "launch_us": round(layer_ms * 1e3, 3),
-            "lm_head_us": round(head_ms * 1e3, 3),
-            "lm_head_GBs": round(head_b / (head_ms * 1e-3) / 1e9, 1),
-            "step_GBs": round(token_bytes * T * args.steps / (ms * 1e-3) / 1e9, 1),
+            "algorithmic_bytes_per_launch": launch_bytes,
+            "algorithmic_bytes_per_token": token_bytes,
+            "launch_ms": round(launch_ms, 4),
+            "us_per_token": round(launch_ms * 1e3 / T, 3),
+            "frac_of_8TBps": round(achieved / 8000.0, 4),
         },
         "e2e": {"value": round(e2e_tok_s, 1), "unit": "tok/s",
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * 4},
-        "gpu_launches": args.steps * T * (args.layers * 3 + 1),
+        "gpu_launches": args.steps,
         "clocks": clk.summary(),
         "device_status": status,
         "prefill": None,
     }
+    if not args.no_prefill:
+        del layers, head
+        torch.cuda.empty_cache()
+        result["prefill"] = measure_prefill(dev)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args)
     if world > 1:
         dist.destroy_process_group()
     return result if rank == 0 else None
+
+
+def measure_prefill(dev, reps: int = 10):
+    """Prompt processing on one Flint layer: 4096 tokens, Zipf(1.1) router bias."""
+    import torch
+
+    from sparse_moe_decode_02_b300 import flint, synth, workload
+
+    shape = synth.FLINT
+    T = PREFILL_TOKENS
+    layer = workload.build_layer(synth.LayerSpec(shape, seed=SEED, layer=0, zipf=ZIPF), dev)
+    x = synth.tokens_bf16(SEED, shape.hidden, T, stream=11, device=dev)
+    out = torch.empty(T, shape.hidden, dtype=torch.float32, device=dev)
+    idx = torch.empty(T, shape.top_k, dtype=torch.int32, device=dev)
+    counts = torch.empty(shape.n_experts, dtype=torch.int32, device=dev)
+    ws = torch.empty(flint.workspace_bytes(flint.OP_MOE_PREFILL, shape.hidden, shape.n_experts,
+                                           shape.top_k, shape.expert_width, shape.shared_width, 0,
+                                           T), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    # a buffer larger than L2, rewritten between timed runs
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        flint.moe_prefill(layer, x, out=out, expert_counts=counts, topk_idx=idx, ws=ws)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        flint.moe_prefill(layer, x, out=out, expert_counts=counts, topk_idx=idx, ws=ws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    cnt = counts.cpu().numpy()
+    H, F, Fs, k = shape.hidden, shape.expert_width, shape.shared_width, shape.top_k
+    flops = 2.0 * T * k * 3 * H * F + 2.0 * T * 3 * H * Fs          # FP4 products
+    router_flops = 2.0 * T * shape.n_experts * H
+    nv = lambda n: n // 2 + n // 16
+    touched = int((cnt > 0).sum())
+    weight_bytes = touched * 3 * nv(H * F) + 3 * nv(H * Fs) + shape.n_experts * H * 2
+    bytes_ = weight_bytes + T * H * 2 + T * H * 4
+    peaks = _peaks()
+    fp4_peak = peaks["bf16_tflops"] * 6.0                              # nominal fp4/bf16 = 6
+    tflops = flops / (ms * 1e-3) / 1e12
+    del layer, ws, flush
+    return {
+        "workload": "Flint prompt processing: one MoE layer, %d tokens, Zipf(1.1) bias" % T,
+        "value": round(T / (ms * 1e-3), 1), "unit": "tok/s", "ms": round(ms, 4),
+        "fp4_gflop": round(flops / 1e9, 1), "router_gflop": round(router_flops / 1e9, 2),
+        "tflops": round(tflops, 1), "fp4_peak_tflops": round(fp4_peak, 1),
+        "fp4_peak_src": "measured bf16 %s x 6 (nominal FP4/BF16 dense ratio)" % peaks["src"],
+        "frac_fp4_peak": round(tflops / fp4_peak, 4),
+        "experts_touched": touched, "bytes": bytes_,
+        "frac_hbm": round(bytes_ / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+        "l2_policy": "256 MB buffer rewritten before each timed run",
+    }
 
 
 # ------------------------------------------------------------------------------ oracle arm
@@ -380,6 +387,7 @@ def main():
     ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--cpu-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     res = run_reference(args) if args.impl == "reference" else run_flint(args)
     if res is not None:
