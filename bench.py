@@ -388,7 +388,16 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the prompt-processing layer (prints its object)")
     args = ap.parse_args()
+    if args.prefill_only and args.impl == "flint":
+        import torch
+        torch.cuda.set_device(0)
+        from sparse_moe_decode_02_b300 import flint
+        flint.lib()
+        print(json.dumps(measure_prefill(torch.device("cuda", 0), reps=args.steps)), flush=True)
+        return
     res = run_reference(args) if args.impl == "reference" else run_flint(args)
     if res is not None:
         print(json.dumps(res), flush=True)
