@@ -75,12 +75,14 @@ typedef struct {
   int n_mat, rows, cols;
 } flint_nvfp4;
 
-/* Column-chunk copy of an NVFP4 stack: the same bytes reordered so that each
- * 32-column chunk of every row of a matrix is contiguous across rows:
- *   codes  [n_mat][cols/32][rows][16]     scales [n_mat][cols/32][rows][2]
- * The decode kernels read the down projections in this layout (a slice of 32
- * SwiGLU outputs then multiplies one contiguous block).  Build it once with
- * flint_nvfp4_column_chunks; the tensor scales are those of the row-major stack. */
+/* Column-chunk copy of an NVFP4 stack: the same bytes reordered so that the codes of
+ * each 8-column chunk, and the scales of each 16-column block, of all rows of a
+ * matrix are contiguous:
+ *   codes  [n_mat][cols/8][rows][4]     scales [n_mat][cols/16][rows]
+ * The decode kernel reads the down projections in this layout (a unit of 8 SwiGLU
+ * outputs then multiplies one contiguous block of codes and one of scales).  Build it
+ * once with flint_nvfp4_column_chunks; the tensor scales are those of the row-major
+ * stack.  The buffers have the sizes of the row-major codes and scales. */
 typedef struct {
   const uint8_t* codes;
   const uint8_t* scales;

@@ -183,16 +183,14 @@ static flint_status decode_tokens_impl(const flint_moe_layer* layers, int n_laye
       ws_bytes < flint_workspace_bytes(FLINT_OP_MOE_DECODE, L0.hidden, L0.n_experts, L0.top_k,
                                        L0.expert_width, L0.shared_width, 0, T))
     return FLINT_ERR_WORKSPACE;
-  {
-    // one CTA per unit (32-wide SwiGLU slice) plus at least one router CTA
-    const int grid = flint::decode_grid();
-    const int units = L0.shared_width / 32 + L0.top_k * (L0.expert_width / 32);
-    if (units + 1 > grid) return FLINT_ERR_UNSUPPORTED;
-    if (flint::decode_smem_bytes(L0.hidden, L0.n_experts, grid - units) > 200 * 1024)
-      return FLINT_ERR_UNSUPPORTED;
-  }
+  const flint::DecodePlan plan =
+      flint::decode_plan(L0.hidden, L0.n_experts, L0.top_k, L0.expert_width, L0.shared_width,
+                         flint::decode_grid());
+  if (!plan.ok) return FLINT_ERR_UNSUPPORTED;
   static flint::PersistArgs a;   // large (layer table): keep it off the stack
   std::memset(&a, 0, sizeof(a));
+  a.max_router_rows = plan.router_rows;
+  a.max_shared_units = plan.shared_units;
   a.H = L0.hidden; a.E = L0.n_experts; a.K = L0.top_k; a.F = L0.expert_width;
   a.Fs = L0.shared_width; a.L = n_layers; a.T = T; a.eps = rms_eps;
   a.x = static_cast<const uint16_t*>(x_bf16);

@@ -40,11 +40,17 @@ namespace flint {
 
 constexpr int kPWarps = 16;
 constexpr int kPThreads = 32 * kPWarps;
-constexpr int kSlice = 32;          // SwiGLU outputs per unit (one code chunk of down)
+constexpr int kUnit = 8;            // SwiGLU outputs per unit (one 8-column chunk of down)
+constexpr int kMaxRouterRows = kPThreads / 64;   // router rows per CTA (64 threads each)
+constexpr int kMaxRoutedUnits = 6;  // routed units per CTA and step
+constexpr size_t kMaxDecodeSmem = 220 * 1024;
 constexpr int kMaxCtas = 1024;
 // Sync words, each on its own 128-byte line.
-constexpr int kSyncLogits = 0, kSyncDone = 32, kSyncHead = 64, kSyncAbort = 96;
+constexpr int kSyncDone = 32, kSyncHead = 64, kSyncAbort = 96;
 constexpr int kSyncWords = 128;
+// Copies of the residual accumulator: unit u adds into copy u % kAccCopies, which
+// spreads the atomic traffic; readers sum the copies in a fixed order.
+constexpr int kAccCopies = 2;
 
 // ---------------------------------------------------------------- sync primitives
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
@@ -82,6 +88,38 @@ __device__ __forceinline__ void signal_count(unsigned* sync, int which) {
   if (threadIdx.x == 0) {
     __threadfence();
     atomicAdd(sync + which, 1u);
+  }
+}
+
+// Router logits travel as tagged 64-bit words {value bits, step + 1}: the writer's
+// release store publishes everything the CTA wrote before (the residual copy); a
+// reader that sees its tag needs no counter.  The tags are cleared before each launch.
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+// Waits (bounded) until *p carries `tag` and returns its value.
+__device__ __forceinline__ float wait_tagged(const unsigned long long* p, unsigned tag, unsigned* sync) {
+  unsigned polls = 0;
+  unsigned long long t0 = 0;
+  for (;;) {
+    const unsigned long long v = ld_acquire_u64(p);
+    if ((unsigned)(v >> 32) == tag) return __uint_as_float((unsigned)v);
+    if ((++polls & 63u) == 0) {
+      if (ld_acquire_gpu(sync + kSyncAbort)) return 0.f;
+      const unsigned long long now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitNs) {
+        raise_status(FLINT_ERR_TIMEOUT);
+        atomicExch(sync + kSyncAbort, 1u);
+        return 0.f;
+      }
+    }
   }
 }
 
@@ -150,8 +188,13 @@ __device__ __forceinline__ Staged cta_stage(const float* h_f32, const uint16_t* 
   float v[4] = {0.f, 0.f, 0.f, 0.f};
   if (own) {
     if (h_f32) {
-      const float4 f = __ldcg(reinterpret_cast<const float4*>(h_f32 + n));
-      v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+      // h = copy 0 + copy 1 + ... (fixed order: every CTA gets the same bits)
+      float4 f[kAccCopies];
+#pragma unroll
+      for (int c = 0; c < kAccCopies; ++c) f[c] = __ldcg(reinterpret_cast<const float4*>(h_f32 + c * H + n));
+      v[0] = f[0].x; v[1] = f[0].y; v[2] = f[0].z; v[3] = f[0].w;
+#pragma unroll
+      for (int c = 1; c < kAccCopies; ++c) { v[0] += f[c].x; v[1] += f[c].y; v[2] += f[c].z; v[3] += f[c].w; }
     } else {
       const uint2 b = __ldcg(reinterpret_cast<const uint2*>(x_bf16 + n));
       v[0] = bf16_bits_to_f32(b.x & 0xFFFFu); v[1] = bf16_bits_to_f32(b.x >> 16);
@@ -204,25 +247,6 @@ __device__ __forceinline__ void pairs_from_smem(uint32_t (&p)[CPL * 16], const u
   }
 }
 
-// A 32-value slice (shared memory) staged as hi/lo f16 pairs: every lane holds all 32.
-__device__ __forceinline__ void stage_slice(XStage<1, 2>& hs, const float* s_h) {
-  float amax = 0.f;
-#pragma unroll
-  for (int q = 0; q < kSlice; ++q) amax = fmaxf(amax, fabsf(s_h[q]));
-  const int k = f16_stage_exponent(amax);
-  const float s = exp2i(k);
-  hs.unscale = exp2i(-k);
-#pragma unroll
-  for (int q = 0; q < 16; ++q) {
-    const float a = s_h[2 * q] * s, b = s_h[2 * q + 1] * s;
-    const uint32_t hi = pack_f16x2_rn(a, b);
-    float ha, hb;
-    f16x2_to_f32x2(hi, ha, hb);
-    hs.p[0][q] = hi;
-    hs.p[1][q] = pack_f16x2_rn(a - ha, b - hb);
-  }
-}
-
 // ---------------------------------------------------------------- shared-memory rows
 template <int CPL>
 __device__ __forceinline__ void lds_row(RowRegs<CPL>& r, const uint8_t* codes_row,
@@ -246,74 +270,113 @@ __device__ __forceinline__ void lds_row_bf16(RowBF16<CPL>& r, const uint16_t* ro
 }
 
 // ---------------------------------------------------------------- units
-// Shared-memory image of one unit: 32 gate rows, 32 up rows (codes then scales) and
-// the down block (H rows x one 32-column chunk).
+// A unit is kUnit = 8 consecutive SwiGLU outputs of one expert (routed or shared): 8
+// gate rows, 8 up rows, and the matching 8-column chunk of the down matrix (H rows x
+// 4 code bytes, plus the H scale bytes of the 16-column block that holds it), each
+// contiguous in HBM (see the column-chunk layout in flint.h).  Its shared-memory image:
 struct UnitLayout {
   uint32_t gc, gs, uc, us, dc, ds, bytes;
   __host__ __device__ static UnitLayout of(int H) {
     UnitLayout u;
     u.gc = 0;
-    u.gs = u.gc + kSlice * (H / 2);
-    u.uc = u.gs + kSlice * (H / 16);
-    u.us = u.uc + kSlice * (H / 2);
-    u.dc = u.us + kSlice * (H / 16);
-    u.ds = u.dc + H * 16;
-    u.bytes = u.ds + H * 2;
+    u.gs = u.gc + kUnit * (H / 2);
+    u.uc = u.gs + kUnit * (H / 16);
+    u.us = u.uc + kUnit * (H / 2);
+    u.dc = u.us + kUnit * (H / 16);
+    u.ds = u.dc + H * 4;
+    u.bytes = u.ds + H;
     return u;
   }
 };
 
-// Issues the bulk copies of one unit (thread 0 only): gate/up rows [row0, row0+32) of
-// the stacks and the down column-chunk block `chunk`.
-__device__ __forceinline__ void issue_unit_copy(uint8_t* buf, uint64_t* bar, int H, const NVPtr& gate,
-                                                const NVPtr& up, const uint8_t* dcc_codes,
-                                                const uint8_t* dcc_scales, size_t row0,
-                                                size_t chunk) {
+// One of the six bulk copies of a unit (piece 0-5: gate codes, gate scales, up codes,
+// up scales, down codes, down scales): gate/up rows [row0, row0 + 8) of the stacks,
+// down code chunk `chunk` and scale block chunk / 2 of matrix `m`.  The six pieces are
+// issued by six lanes at once; the mbarrier's expected bytes are set beforehand.
+__device__ __forceinline__ void unit_copy_piece(int piece, uint8_t* buf, uint64_t* bar, int H,
+                                                const NVPtr& gate, const NVPtr& up,
+                                                const uint8_t* dcc_codes, const uint8_t* dcc_scales,
+                                                size_t row0, size_t m, int chunks_per_mat, int chunk) {
   const UnitLayout L = UnitLayout::of(H);
-  mbar_expect_tx(bar, L.bytes);
-  bulk_g2s(buf + L.gc, gate.codes + row0 * (H / 2), kSlice * (H / 2), bar);
-  bulk_g2s(buf + L.gs, gate.scales + row0 * (H / 16), kSlice * (H / 16), bar);
-  bulk_g2s(buf + L.uc, up.codes + row0 * (H / 2), kSlice * (H / 2), bar);
-  bulk_g2s(buf + L.us, up.scales + row0 * (H / 16), kSlice * (H / 16), bar);
-  bulk_g2s(buf + L.dc, dcc_codes + chunk * H * 16, H * 16, bar);
-  bulk_g2s(buf + L.ds, dcc_scales + chunk * H * 2, H * 2, bar);
+  switch (piece) {
+    case 0: bulk_g2s(buf + L.gc, gate.codes + row0 * (H / 2), kUnit * (H / 2), bar); break;
+    case 1: bulk_g2s(buf + L.gs, gate.scales + row0 * (H / 16), kUnit * (H / 16), bar); break;
+    case 2: bulk_g2s(buf + L.uc, up.codes + row0 * (H / 2), kUnit * (H / 2), bar); break;
+    case 3: bulk_g2s(buf + L.us, up.scales + row0 * (H / 16), kUnit * (H / 16), bar); break;
+    case 4: bulk_g2s(buf + L.dc, dcc_codes + (m * chunks_per_mat + chunk) * H * 4, H * 4, bar); break;
+    default: bulk_g2s(buf + L.ds, dcc_scales + (m * (chunks_per_mat / 2) + chunk / 2) * H, H, bar); break;
+  }
 }
 
-// Computes one unit from shared memory: 32 SwiGLU outputs, then the down contribution
-// (times wgt) of all H rows, added into s_part[H].
+// One unit from shared memory: the 16 gate/up row dot products (a warp per row), the 8
+// SwiGLU values, then this thread's 4 down rows [4t, 4t + 4) times wgt, added into
+// part[].  The buffer stays in use until the caller's next CTA barrier; consecutive
+// calls must alternate the s_gu / s_hs scratch.
 template <int CPL>
 __device__ __forceinline__ void unit_compute(const uint8_t* buf, int H, float gate_tsc,
                                              float up_tsc, float down_tsc, float wgt,
-                                             const XStage<CPL, 1>& xs, float* s_h,
-                                             float* s_part) {
+                                             const XStage<CPL, 1>& xs, float* s_gu,
+                                             uint32_t* s_hs, float (&part)[4]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int LPR = H / (32 * CPL), RPP = 32 / LPR;
   const int slice = lane / LPR, sl = lane % LPR;
   const UnitLayout U = UnitLayout::of(H);
-  const float gs = gate_tsc * xs.unscale, us = up_tsc * xs.unscale;
-  // SwiGLU outputs: pair p handled by (warp, slice)
-  for (int p0 = warp * RPP; p0 < kSlice; p0 += kPWarps * RPP) {
-    const int p = p0 + slice;
-    const int pr = p < kSlice ? p : 0;
-    RowRegs<CPL> g, u;
-    lds_row<CPL>(g, buf + U.gc + pr * (H / 2), buf + U.gs + pr * (H / 16), sl, LPR);
-    lds_row<CPL>(u, buf + U.uc + pr * (H / 2), buf + U.us + pr * (H / 16), sl, LPR);
-    const float vg = sum_lanes_rt(dot_row<CPL, 1>(g, xs), LPR);
-    const float vu = sum_lanes_rt(dot_row<CPL, 1>(u, xs), LPR);
-    if (sl == 0 && p < kSlice) s_h[p] = silu(vg * gs) * (vu * us);
+  for (int r0 = warp * RPP; r0 < 2 * kUnit; r0 += kPWarps * RPP) {
+    const int r = r0 + slice;
+    const int rr = r < 2 * kUnit ? r : 0;
+    const bool is_up = rr >= kUnit;
+    const int row = is_up ? rr - kUnit : rr;
+    RowRegs<CPL> w;
+    lds_row<CPL>(w, buf + (is_up ? U.uc : U.gc) + row * (H / 2),
+                 buf + (is_up ? U.us : U.gs) + row * (H / 16), sl, LPR);
+    const float v = sum_lanes_rt(dot_row<CPL, 1>(w, xs), LPR);
+    if (sl == 0 && r < 2 * kUnit) s_gu[r] = v * (is_up ? up_tsc : gate_tsc) * xs.unscale;
   }
   __syncthreads();
-  XStage<1, 2> hs;
-  stage_slice(hs, s_h);
-  const float scale = down_tsc * hs.unscale * wgt;
-  // down block: consecutive lanes take consecutive rows (conflict-free shared loads)
-  for (int n = warp * 32 + lane; n < H; n += kPWarps * 32) {
-    RowRegs<1> d;
-    d.q[0] = *reinterpret_cast<const uint4*>(buf + U.dc + n * 16);
-    d.s[0] = *reinterpret_cast<const uint16_t*>(buf + U.ds + n * 2);
-    s_part[n] += dot_row<1, 2>(d, hs) * scale;
+  // SwiGLU values, computed once by lanes 0-7 of warp 0 and staged as hi/lo f16 pairs
+  // scaled by 2^k: s_hs[0..3] hi pairs, s_hs[4..7] lo pairs, s_hs[8] the down scale.
+  if (warp == 0) {
+    const float hj = lane < kUnit ? silu(s_gu[lane]) * s_gu[kUnit + (lane & (kUnit - 1))] : 0.f;
+    float amax = fabsf(hj);
+#pragma unroll
+    for (int o = kUnit / 2; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const int k = f16_stage_exponent(amax);
+    const float v = hj * exp2i(k);
+    const float w = __shfl_down_sync(0xffffffffu, v, 1);      // the odd partner
+    if (lane < kUnit && (lane & 1) == 0) {
+      const uint32_t hi = pack_f16x2_rn(v, w);
+      float ha, hb;
+      f16x2_to_f32x2(hi, ha, hb);
+      s_hs[lane / 2] = hi;
+      s_hs[kUnit / 2 + lane / 2] = pack_f16x2_rn(v - ha, w - hb);
+    }
+    if (lane == 0) s_hs[kUnit] = __float_as_uint(down_tsc * exp2i(-k) * wgt);
   }
   __syncthreads();
+  uint32_t hh[kUnit / 2], hl[kUnit / 2];
+#pragma unroll
+  for (int q = 0; q < kUnit / 2; ++q) { hh[q] = s_hs[q]; hl[q] = s_hs[kUnit / 2 + q]; }
+  const float scale = __uint_as_float(s_hs[kUnit]);
+  const int n0 = 4 * threadIdx.x;
+  if (n0 < H) {
+    const uint4 cw = *reinterpret_cast<const uint4*>(buf + U.dc + 4 * n0);
+    const uint32_t sw = *reinterpret_cast<const uint32_t*>(buf + U.ds + n0);
+    const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t f[4];
+      e2m1x8_to_f16x2x4(wv[q], f[0], f[1], f[2], f[3]);
+      float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        fma2_f16(a0, a1, f[i], hh[i]);
+        fma2_f16(b0, b1, f[i], hl[i]);
+      }
+      float s0, s1;
+      f16x2_to_f32x2(e4m3x2_to_f16x2((sw >> (8 * q)) & 0xFFu), s0, s1);
+      part[q] = fmaf((a0 + a1) + (b0 + b1), s0 * scale, part[q]);
+    }
+  }
 }
 
 // ---------------------------------------------------------------- top-k
@@ -321,58 +384,149 @@ __device__ __forceinline__ unsigned order_key(float v) {
   const unsigned u = __float_as_uint(v);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+__device__ __forceinline__ float key_value(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+// (key, index) a comes before b: larger key, or equal key and lower index.
+__device__ __forceinline__ bool before(unsigned ka, int ia, unsigned kb, int ib) {
+  return ka > kb || (ka == kb && ia < ib);
+}
 
-// Softmax top-k by one warp (see flint.h): largest logit first, ties to the lower index.
-template <int kMaxPerLane>
-__device__ void topk_warp(const float* logits, int E, int K, int* s_sel, float* s_w) {
-  const int lane = threadIdx.x & 31;
-  unsigned key[kMaxPerLane];
-  float val[kMaxPerLane];
+// Bitonic network over N register pairs, leaving them in `before` order.
+template <int N>
+__device__ __forceinline__ void sort_pairs(unsigned (&k)[N], int (&ix)[N]) {
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
-    const int e = lane + 32 * i;
-    float l = (e < E) ? logits[e] : -INFINITY;
-    l = (l == l) ? l : -INFINITY;
-    val[i] = l;
-    key[i] = (e < E) ? order_key(l) : 0u;      // every live key is >= 1
-  }
-  float top0 = 0.f, z = 0.f;
-  for (int s = 0; s < K; ++s) {
-    unsigned bk = 0u;
-    int bi = 0x7FFFFFFF;
+  for (int size = 2; size <= N; size <<= 1) {
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && key[i] != 0u && (key[i] > bk || (key[i] == bk && e < bi))) {
-        bk = key[i];
-        bi = e;
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool first_half = (i & size) == 0;
+          const bool swap = first_half ? before(k[j], ix[j], k[i], ix[i]) : before(k[i], ix[i], k[j], ix[j]);
+          const unsigned tk = swap ? k[j] : k[i];
+          const int ti = swap ? ix[j] : ix[i];
+          k[j] = swap ? k[i] : k[j];
+          ix[j] = swap ? ix[i] : ix[j];
+          k[i] = tk;
+          ix[i] = ti;
+        }
       }
     }
-    const unsigned wk = __reduce_max_sync(0xffffffffu, bk);
-    const int we = (int)__reduce_min_sync(0xffffffffu, (unsigned)(bk == wk ? bi : 0x7FFFFFFF));
-    float mine = 0.f;
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i)
-      if (lane + 32 * i == we) { mine = val[i]; key[i] = 0u; }
-    const float wl = __shfl_sync(0xffffffffu, mine, we & 31);
-    if (s == 0) top0 = wl;
-    const float p = expf(wl - top0);
-    z += p;
-    if (lane == 0) { s_sel[s] = we; s_w[s] = p; }
   }
+}
+
+// Exact softmax top-k by one warp (see flint.h): the K largest logits, ties to the
+// lower index, in that order; weights exp(l_i - l_0) / sum over the selected.  Lane l
+// holds logits [PER*l, PER*l + PER) sorted; each round the warp takes the best head
+// (one max-reduction; a second reduction only when heads tie) and its lane pops it.
+template <int PER>
+__device__ __noinline__ void topk_exact(const float* logits, int E, int K, int* s_sel, float* s_w) {
+  const int lane = threadIdx.x & 31;
+  unsigned key[PER];
+  int idx[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane * PER + i;
+    float l = (e < E) ? logits[e] : -INFINITY;
+    l = (l == l) ? l : -INFINITY;
+    key[i] = (e < E) ? order_key(l) : 0u;      // every live key is >= 1
+    idx[i] = e;
+  }
+  if (PER > 1) sort_pairs<PER>(key, idx);
+  unsigned my_key = 0u;
+  int my_sel = 0;
+  for (int s = 0; s < K; ++s) {
+    const unsigned wk = __reduce_max_sync(0xffffffffu, key[0]);
+    unsigned tie = __ballot_sync(0xffffffffu, key[0] == wk);
+    if (tie & (tie - 1u)) {
+      const unsigned wi = __reduce_min_sync(0xffffffffu, key[0] == wk ? (unsigned)idx[0] : 0xFFFFFFFFu);
+      tie = __ballot_sync(0xffffffffu, key[0] == wk && (unsigned)idx[0] == wi);
+    }
+    const int wl = __ffs(tie) - 1;
+    const int we = __shfl_sync(0xffffffffu, idx[0], wl);
+    if (lane == s) { my_key = wk; my_sel = we; }
+    if (lane == wl) {
+#pragma unroll
+      for (int i = 0; i + 1 < PER; ++i) { key[i] = key[i + 1]; idx[i] = idx[i + 1]; }
+      key[PER - 1] = 0u;
+      idx[PER - 1] = 0x7FFFFFFF;
+    }
+  }
+  const float l = key_value(my_key);
+  const float l0 = __shfl_sync(0xffffffffu, l, 0);
+  const float p = lane < K ? expf(l - l0) : 0.f;
+  float z = p;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  if (lane < K) { s_sel[lane] = my_sel; s_w[lane] = p / z; }
   __syncwarp();
-  if (lane < K) s_w[lane] = s_w[lane] / z;
+}
+
+// Fast path for E <= 256: one 32-bit key per logit = (upper 24 bits of the order key,
+// 255 - index), so a single max-reduction per round yields both the winner and its
+// index, and ties go to the lower index.  Dropping the low 8 bits of the order key can
+// only misorder logits that agree in their upper 24 bits; such a pair among the K + 1
+// best shows up as two consecutive winners with equal upper bits, and the exact path
+// then decides.  Returns false (warp-uniform) in that case.
+template <int PER>
+__device__ __forceinline__ bool topk_fast(const float* logits, int E, int K, int* s_sel, float* s_w) {
+  const int lane = threadIdx.x & 31;
+  unsigned pk[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane * PER + i;
+    float l = (e < E) ? logits[e] : -INFINITY;
+    l = (l == l) ? l : -INFINITY;
+    pk[i] = (e < E) ? ((order_key(l) & 0xFFFFFF00u) | (unsigned)(255 - e)) : 0u;
+  }
+  unsigned prev = 0u;
+  bool exact = true;
+  int my_sel = 0;
+  for (int s = 0; s <= K; ++s) {                    // round K only checks the boundary
+    unsigned m = pk[0];
+#pragma unroll
+    for (int i = 1; i < PER; ++i) m = max(m, pk[i]);
+    const unsigned w = __reduce_max_sync(0xffffffffu, m);
+    if (s > 0 && (w >> 8) == (prev >> 8) && w != 0u) exact = false;
+    prev = w;
+    if (s == K) break;
+    const int e = 255 - (int)(w & 255u);
+    if (lane == s) my_sel = e;
+    if (lane == e / PER) {
+#pragma unroll
+      for (int i = 0; i < PER; ++i)
+        if (i == e % PER) pk[i] = 0u;
+    }
+  }
+  if (!exact) return false;
+  float l = lane < K ? logits[my_sel] : 0.f;
+  l = (l == l) ? l : -INFINITY;
+  const float l0 = __shfl_sync(0xffffffffu, l, 0);
+  const float p = lane < K ? expf(l - l0) : 0.f;
+  float z = p;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  if (lane < K) { s_sel[lane] = my_sel; s_w[lane] = p / z; }
   __syncwarp();
+  return true;
+}
+
+template <int PER>
+__device__ __forceinline__ void topk_per(const float* logits, int E, int K, int* s_sel, float* s_w) {
+  if (PER <= 8 && E <= 256 && topk_fast<PER>(logits, E, K, s_sel, s_w)) return;
+  topk_exact<PER>(logits, E, K, s_sel, s_w);
 }
 
 __device__ __forceinline__ void topk_dispatch(const float* logits, int E, int K, int* s_sel,
                                               float* s_w) {
   const int per_lane = (E + 31) / 32;
-  if (per_lane <= 1) topk_warp<1>(logits, E, K, s_sel, s_w);
-  else if (per_lane <= 2) topk_warp<2>(logits, E, K, s_sel, s_w);
-  else if (per_lane <= 4) topk_warp<4>(logits, E, K, s_sel, s_w);
-  else if (per_lane <= 8) topk_warp<8>(logits, E, K, s_sel, s_w);
-  else topk_warp<16>(logits, E, K, s_sel, s_w);
+  if (per_lane <= 1) topk_per<1>(logits, E, K, s_sel, s_w);
+  else if (per_lane <= 2) topk_per<2>(logits, E, K, s_sel, s_w);
+  else if (per_lane <= 4) topk_per<4>(logits, E, K, s_sel, s_w);
+  else if (per_lane <= 8) topk_per<8>(logits, E, K, s_sel, s_w);
+  else topk_per<16>(logits, E, K, s_sel, s_w);
 }
 
 // ---------------------------------------------------------------- head
@@ -419,150 +573,208 @@ __device__ __forceinline__ void best_reduce_warp(float& v, int& i) {
 }
 
 // ---------------------------------------------------------------- the kernel
-enum Role { kRoleShared = 0, kRoleRouted = 1, kRoleRouter = 2 };
-
+// Work of CTA c (of G) in every layer step, all CTAs running the same code:
+//   router rows      e = c, c + G, ...                       (< E)
+//   shared units     s = G-1-c, G-1-c + G, ...               (< Fs/8)
+//   routed units     r = c, c + G, ...                       (< K*F/8)
+// Routed units fill CTAs from the front and shared units from the back, so the
+// busiest CTAs hold at most one unit more than the least busy.  Shared units and
+// router rows do not depend on the data: their copies for the next step are issued as
+// soon as this step has consumed them.
 template <int CPL>
 __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid_constant__ PersistArgs a) {
-  __shared__ float s_h[kSlice];
+  __shared__ float s_gu[2][2 * kUnit];              // alternating per unit
+  __shared__ uint32_t s_hs[2][kUnit + 1];
+  __shared__ float s_rp[kPWarps];
   __shared__ int s_sel[FLINT_MAX_TOP_K];
   __shared__ float s_w[FLINT_MAX_TOP_K];
   __shared__ float s_bv[kPWarps];
   __shared__ int s_bi[kPWarps];
   __shared__ float s_red[2 * kPWarps];
   __shared__ float s_logits[FLINT_MAX_EXPERTS];
-  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ float s_bias[kMaxRouterRows];
+  __shared__ __align__(8) uint64_t s_bar_st;
+  __shared__ __align__(8) uint64_t s_bar_rt[kMaxRoutedUnits];
   extern __shared__ __align__(128) uint8_t s_dyn[];
+  const int H = a.H;
+  const UnitLayout U = UnitLayout::of(H);
   float* s_hx = reinterpret_cast<float*>(s_dyn);                       // [H] residual h
-  float* s_part = s_hx + a.H;                                          // [H] down partials
-  uint16_t* s_xb = reinterpret_cast<uint16_t*>(s_part + a.H);          // [H] x, bf16
-  uint16_t* s_xf = s_xb + a.H;                                         // [H] x * 2^k, f16
-  uint8_t* s_wbuf = reinterpret_cast<uint8_t*>(s_xf + a.H);            // weight buffer
+  uint16_t* s_xb = reinterpret_cast<uint16_t*>(s_hx + H);              // [H] x, bf16
+  uint16_t* s_xf = s_xb + H;                                           // [H] x * 2^k, f16
+  uint8_t* s_router = reinterpret_cast<uint8_t*>(s_xf + H);            // [RR][H] bf16 rows
+  uint8_t* s_static = s_router + (size_t)a.max_router_rows * H * 2;   // shared units
+  uint8_t* s_routed = s_static + (size_t)a.max_shared_units * U.bytes; // routed units
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c = blockIdx.x, nC = gridDim.x;
-  const int H = a.H;
+  const int c = blockIdx.x, G = gridDim.x;
   const int LPR = H / (32 * CPL), RPP = 32 / LPR;
   const int slice = lane / LPR, sl = lane % LPR;
-  const int n_sh = a.Fs / kSlice;
-  const int per_slot = a.F / kSlice;
-  const int n_rt = a.K * per_slot;
-  const int n_units = n_sh + n_rt;
-  const int nR = nC - n_units;                       // router CTAs (host checks >= 1)
-  const Role role = c < n_sh ? kRoleShared : (c < n_units ? kRoleRouted : kRoleRouter);
-  const int ridx = c - n_units;                      // router CTA index
-  const int rows_per_router = (a.E + nR - 1) / nR;
-  const int r_lo = role == kRoleRouter ? min(a.E, ridx * rows_per_router) : 0;
-  const int r_hi = role == kRoleRouter ? min(a.E, r_lo + rows_per_router) : 0;
+  const int n_sh = a.Fs / kUnit;                    // shared units
+  const int per_slot = a.F / kUnit;                 // routed units per selected expert
+  const int n_rt = a.K * per_slot;                  // routed units
+  const int my_rows = c < a.E ? (a.E - 1 - c) / G + 1 : 0;
+  const int my_sh = (G - 1 - c) < n_sh ? (n_sh - 1 - (G - 1 - c)) / G + 1 : 0;
+  const int my_rt = c < n_rt ? (n_rt - 1 - c) / G + 1 : 0;
+  const int n_wait = a.E > G ? a.E : G;             // tags every CTA waits for (see below)
   unsigned* sync = a.bar;
-  uint32_t phase = 0;                                // parity of the weight-buffer mbarrier
-  (void)lane;
+  uint32_t ph_st = 0, ph_rt = 0;                    // mbarrier parities
 
   if (threadIdx.x == 0) {
-    mbar_init(&s_bar, 1);
+    mbar_init(&s_bar_st, 1);
+    for (int i = 0; i < kMaxRoutedUnits; ++i) mbar_init(&s_bar_rt[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  // Data-independent weight copies of a layer: router rows or this CTA's shared unit.
+  // Data-independent copies of layer l: this CTA's router rows and shared units, one
+  // copy per lane of warp 0 (the calling warp).
+  const uint32_t static_bytes = (uint32_t)my_rows * H * 2 + (uint32_t)my_sh * U.bytes;
   auto issue_static = [&](int l) {
-    if (threadIdx.x != 0) return;
+    if (static_bytes == 0) return;
     const LayerPtrs& P = a.layer[l];
-    if (role == kRoleShared) {
-      issue_unit_copy(s_wbuf, &s_bar, H, P.sh_gate, P.sh_up, P.sh_dcc_codes, P.sh_dcc_scales,
-                      (size_t)c * kSlice, (size_t)c);
-    } else if (role == kRoleRouter && r_hi > r_lo) {
-      const uint32_t bytes = (uint32_t)(r_hi - r_lo) * H * 2;
-      mbar_expect_tx(&s_bar, bytes);
-      bulk_g2s(s_wbuf, P.router_w + (size_t)r_lo * H, bytes, &s_bar);
+    if (lane == 0) mbar_expect_tx(&s_bar_st, static_bytes);
+    __syncwarp();
+    for (int q = lane; q < my_rows + 6 * my_sh; q += 32) {
+      if (q < my_rows) {
+        bulk_g2s(s_router + (size_t)q * H * 2, P.router_w + (size_t)(c + q * G) * H, H * 2, &s_bar_st);
+      } else {
+        const int i = (q - my_rows) / 6, piece = (q - my_rows) % 6;
+        const int su = (G - 1 - c) + i * G;
+        unit_copy_piece(piece, s_static + (size_t)i * U.bytes, &s_bar_st, H, P.sh_gate, P.sh_up,
+                        P.sh_dcc_codes, P.sh_dcc_scales, (size_t)su * kUnit, 0, n_sh, su);
+      }
     }
   };
-  issue_static(0);
+  if (warp == 0) issue_static(0);
 
   unsigned step = 0;                                 // global layer step
   for (int t = 0; t < a.T; ++t) {
     for (int l = 0; l < a.L; ++l, ++step) {
       const LayerPtrs& P = a.layer[l];
-      float* acc_cur = a.acc + (step & 1) * H;
-      float* acc_next = a.acc + ((step + 1) & 1) * H;
+      float* acc_cur = a.acc + (step & 1) * (kAccCopies * H);
+      float* acc_next = a.acc + ((step + 1) & 1) * (kAccCopies * H);
       const int l_next = (l + 1 < a.L) ? l + 1 : 0;
       const bool more = (l + 1 < a.L) || (t + 1 < a.T);
+      const unsigned tag = step + 1;
+      for (int i = threadIdx.x; i < my_rows; i += kPThreads)
+        s_bias[i] = P.router_bias ? __ldg(P.router_bias + c + i * G) : 0.f;
       // ---- h_l complete: stage x_l
-      if (step > 0) wait_count(sync, kSyncDone, (unsigned)n_units * step);
+      if (step > 0) wait_count(sync, kSyncDone, (unsigned)G * step);
       const Staged stg = cta_stage(l == 0 ? nullptr : acc_cur, a.x + (size_t)t * H, H, a.eps, s_hx,
                                    s_xb, s_xf, s_red);
-
-      if (role == kRoleRouter) {
-        // next residual buffer <- h_l (router CTAs share the rows)
-        for (int n = ridx * kPThreads + threadIdx.x; n < H; n += nR * kPThreads)
-          acc_next[n] = (l == 0 && a.residual) ? a.residual[(size_t)t * H + n] : s_hx[n];
-        if (r_hi > r_lo) {
-          mbar_wait(&s_bar, phase, sync);
-          phase ^= 1;
-          XRawBF16<CPL> xr;
-          pairs_from_smem<CPL>(xr.p, s_xb, sl, LPR);
-          for (int r0 = r_lo + warp * RPP; r0 < r_hi; r0 += kPWarps * RPP) {
-            const int row = r0 + slice;
-            RowBF16<CPL> rw;
-            lds_row_bf16<CPL>(rw, reinterpret_cast<const uint16_t*>(s_wbuf) +
-                                      (size_t)((row < r_hi ? row : r_lo) - r_lo) * H, sl, LPR);
-            const float v = sum_lanes_rt(dot_row_bf16<CPL>(rw, xr), LPR);
-            if (row < r_hi && sl == 0) a.logits_ws[row] = v + (P.router_bias ? P.router_bias[row] : 0.f);
-          }
+      // ---- next residual buffers <- (h_l, 0, ...): each CTA a share, published by its tags
+      for (int n = 4 * (c + G * threadIdx.x); n < H; n += 4 * G * kPThreads) {
+        float4 v;
+        if (l == 0 && a.residual) {
+          const float* rp = a.residual + (size_t)t * H + n;
+          v = make_float4(rp[0], rp[1], rp[2], rp[3]);
+        } else {
+          v = *reinterpret_cast<const float4*>(s_hx + n);
         }
-        signal_count(sync, kSyncLogits);
-        __syncthreads();                       // buffer reads done before it is refilled
-        if (more) issue_static(l_next);
-      } else if (role == kRoleShared) {
-        XStage<CPL, 1> xs;
-        pairs_from_smem<CPL>(xs.p[0], s_xf, sl, LPR);
-        xs.unscale = stg.unscale;
-        for (int n = threadIdx.x; n < H; n += kPThreads) s_part[n] = 0.f;
-        mbar_wait(&s_bar, phase, sync);
-        phase ^= 1;
-        unit_compute<CPL>(s_wbuf, H, P.sh_gate.tsc[0], P.sh_up.tsc[0], P.sh_down_tsc[0], 1.0f, xs,
-                          s_h, s_part);
-        if (more) issue_static(l_next);         // unit_compute ended with a CTA barrier
-        wait_count(sync, kSyncLogits, (unsigned)nR * (step + 1));
-        for (int n = 4 * threadIdx.x; n < H; n += 4 * kPThreads)
-          red_add_v4(acc_next + n, s_part[n], s_part[n + 1], s_part[n + 2], s_part[n + 3]);
-        signal_count(sync, kSyncDone);
-      } else {  // routed
-        XStage<CPL, 1> xs;
-        pairs_from_smem<CPL>(xs.p[0], s_xf, sl, LPR);
-        xs.unscale = stg.unscale;
-        for (int n = threadIdx.x; n < H; n += kPThreads) s_part[n] = 0.f;
-        wait_count(sync, kSyncLogits, (unsigned)nR * (step + 1));
-        for (int e = threadIdx.x; e < a.E; e += kPThreads) s_logits[e] = __ldcg(a.logits_ws + e);
-        __syncthreads();
-        if (warp == 0) topk_dispatch(s_logits, a.E, a.K, s_sel, s_w);
-        __syncthreads();
-        const int u = c - n_sh;
-        const int sslot = u / per_slot, j = u % per_slot;
-        int e = s_sel[sslot];
-        if (e < 0 || e >= a.E) { raise_status(FLINT_ERR_INVALID_ARG); e = 0; }
-        if (threadIdx.x == 0)
-          issue_unit_copy(s_wbuf, &s_bar, H, P.gate, P.up, P.dcc_codes, P.dcc_scales,
-                          (size_t)e * a.F + (size_t)j * kSlice, (size_t)e * per_slot + j);
-        if (u == 0 && threadIdx.x < a.K) {
-          const size_t o = ((size_t)t * a.L + l) * a.K + threadIdx.x;
-          if (a.idx_out) a.idx_out[o] = s_sel[threadIdx.x];
-          if (a.w_out) a.w_out[o] = s_w[threadIdx.x];
-        }
-        mbar_wait(&s_bar, phase, sync);
-        phase ^= 1;
-        unit_compute<CPL>(s_wbuf, H, P.gate.tsc[e], P.up.tsc[e], P.down_tsc[e], s_w[sslot], xs, s_h,
-                          s_part);
-        for (int n = 4 * threadIdx.x; n < H; n += 4 * kPThreads)
-          red_add_v4(acc_next + n, s_part[n], s_part[n + 1], s_part[n + 2], s_part[n + 3]);
-        signal_count(sync, kSyncDone);
+        *reinterpret_cast<float4*>(acc_next + n) = v;
+#pragma unroll
+        for (int cp = 1; cp < kAccCopies; ++cp)
+          *reinterpret_cast<float4*>(acc_next + cp * H + n) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      if (static_bytes) { mbar_wait(&s_bar_st, ph_st, sync); ph_st ^= 1; }
+      __syncthreads();                               // residual share written by all threads
+      // ---- router rows -> tagged logits (release: publishes the residual share too).
+      // Row r takes threads [64 r, 64 r + 64): 16-byte pieces of weights and x_l.
+      if (my_rows > 0) {
+        const int r = threadIdx.x >> 6, tr = threadIdx.x & 63;
+        float acc = 0.f;
+        if (r < my_rows) {
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+          const uint16_t* row = reinterpret_cast<const uint16_t*>(s_router) + (size_t)r * H;
+          for (int e = 8 * tr; e < H; e += 8 * 64) {
+            const uint4 wv = *reinterpret_cast<const uint4*>(row + e);
+            const uint4 xv = *reinterpret_cast<const uint4*>(s_xb + e);
+            fma2_bf16(a0, a1, wv.x, xv.x);
+            fma2_bf16(a2, a3, wv.y, xv.y);
+            fma2_bf16(a0, a1, wv.z, xv.z);
+            fma2_bf16(a2, a3, wv.w, xv.w);
+          }
+          acc = (a0 + a1) + (a2 + a3);
+        }
+        acc = sum_lanes<32>(acc);
+        if (lane == 0) s_rp[warp] = acc;
+        __syncthreads();
+        if (threadIdx.x < my_rows) {
+          const float v = (s_rp[2 * threadIdx.x] + s_rp[2 * threadIdx.x + 1]) + s_bias[threadIdx.x];
+          st_release_u64(a.logits_tag + c + threadIdx.x * G,
+                         ((unsigned long long)tag << 32) | __float_as_uint(v));
+        }
+      } else if (threadIdx.x == 0) {
+        // no router row: a presence tag in slot E + c
+        st_release_u64(a.logits_tag + a.E + c, (unsigned long long)tag << 32);
+      }
+      // ---- shared units (need only x_l)
+      XStage<CPL, 1> xs;
+      pairs_from_smem<CPL>(xs.p[0], s_xf, sl, LPR);
+      xs.unscale = stg.unscale;
+      float part[4] = {0.f, 0.f, 0.f, 0.f};
+      int par = 0;                                   // scratch parity
+      for (int i = 0; i < my_sh; ++i, par ^= 1)
+        unit_compute<CPL>(s_static + (size_t)i * U.bytes, H, P.sh_gate.tsc[0], P.sh_up.tsc[0],
+                          P.sh_down_tsc[0], 1.0f, xs, s_gu[par], s_hs[par], part);
+      // ---- all logits (and every CTA's residual share), then the top-k
+      // slots [0, E) are the logits; slots E + c' for the CTAs c' >= E without a row
+      for (int i = threadIdx.x; i < n_wait; i += kPThreads) {
+        const float v = wait_tagged(a.logits_tag + (i < a.E ? i : a.E + i), tag, sync);
+        if (i < a.E) s_logits[i] = v;
+      }
+      __syncthreads();                               // also: router rows and shared units consumed
+      if (warp == 0) topk_dispatch(s_logits, a.E, a.K, s_sel, s_w);
+      __syncthreads();
+      if (warp == 0) {
+        if (lane < my_rt) mbar_expect_tx(&s_bar_rt[lane], U.bytes);
+        __syncwarp();
+        for (int q = lane; q < 6 * my_rt; q += 32) {
+          const int i = q / 6, piece = q % 6;
+          const int r = c + i * G;
+          const int slot = r / per_slot, j = r % per_slot;
+          int e = s_sel[slot];
+          if (e < 0 || e >= a.E) { raise_status(FLINT_ERR_INVALID_ARG); e = 0; }
+          unit_copy_piece(piece, s_routed + (size_t)i * U.bytes, &s_bar_rt[i], H, P.gate, P.up,
+                          P.dcc_codes, P.dcc_scales, (size_t)e * a.F + (size_t)j * kUnit, (size_t)e,
+                          per_slot, j);
+        }
+        if (more && my_rt == 0) issue_static(l_next);
+      }
+      if (c == 0 && threadIdx.x < a.K) {
+        const size_t o = ((size_t)t * a.L + l) * a.K + threadIdx.x;
+        if (a.idx_out) a.idx_out[o] = s_sel[threadIdx.x];
+        if (a.w_out) a.w_out[o] = s_w[threadIdx.x];
+      }
+      // ---- routed units, each as soon as its copy lands
+      for (int i = 0; i < my_rt; ++i) {
+        const int r = c + i * G;
+        const int slot = r / per_slot;
+        int e = s_sel[slot];
+        if (e < 0 || e >= a.E) e = 0;
+        mbar_wait(&s_bar_rt[i], ph_rt, sync);
+        // the next layer's static copies go out once this step's routed bytes are in
+        if (more && i == my_rt - 1 && warp == 0) issue_static(l_next);
+        unit_compute<CPL>(s_routed + (size_t)i * U.bytes, H, P.gate.tsc[e], P.up.tsc[e],
+                          P.down_tsc[e], s_w[slot], xs, s_gu[par], s_hs[par], part);
+        par ^= 1;
+      }
+      ph_rt ^= 1;
+      // ---- this CTA's down contributions -> h_{l+1}
+      if (my_sh + my_rt > 0 && 4 * threadIdx.x < H)
+        red_add_v4(acc_next + (c % kAccCopies) * H + 4 * threadIdx.x, part[0], part[1], part[2], part[3]);
+      signal_count(sync, kSyncDone);
     }
     // ---------------- outputs of token t
-    wait_count(sync, kSyncDone, (unsigned)n_units * step);
-    const float* hfin = a.acc + (step & 1) * H;
+    wait_count(sync, kSyncDone, (unsigned)G * step);
+    const float* hfin = a.acc + (step & 1) * (kAccCopies * H);
     if (a.out)
-      for (int n = c * kPThreads + threadIdx.x; n < H; n += nC * kPThreads)
-        a.out[(size_t)t * H + n] = __ldcg(hfin + n);
+      for (int n = c * kPThreads + threadIdx.x; n < H; n += G * kPThreads) {
+        float v = __ldcg(hfin + n);
+#pragma unroll
+        for (int cp = 1; cp < kAccCopies; ++cp) v += __ldcg(hfin + cp * H + n);
+        a.out[(size_t)t * H + n] = v;
+      }
     if (a.x_out || a.head.codes) {
       const Staged stg = cta_stage(hfin, nullptr, H, a.eps, s_hx, s_xb, s_xf, s_red);
       if (a.x_out && c == 0)
@@ -588,12 +800,12 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         }
         signal_count(sync, kSyncHead);
         if (c == 0) {
-          wait_count(sync, kSyncHead, (unsigned)nC * (t + 1));
+          wait_count(sync, kSyncHead, (unsigned)G * (t + 1));
           if (warp == 0) {
             const int ln = threadIdx.x & 31;
             float v = -INFINITY;
             int i = 0x7FFFFFFF;
-            for (int k = ln; k < nC; k += 32) {
+            for (int k = ln; k < G; k += 32) {
               const float kv = __ldcg(best_v + k);
               const int ki = __ldcg(best_i + k);
               if (kv > v || (kv == v && ki < i)) { v = kv; i = ki; }
@@ -605,16 +817,17 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
       }
     }
   }
-  // No bulk copy is in flight at exit: copies are issued only while `more` holds, and
-  // every issued copy is waited for in the step that follows.
+  // No bulk copy is in flight at exit: copies are issued only while `more` holds (or
+  // for the current step), and every issued copy is waited for in the step it serves.
 }
 
 // ---------------------------------------------------------------- column-chunk repack
+// codes [m][rows][cols/2] -> [m][cols/8][rows][4];  scales [m][rows][cols/16] -> [m][cols/16][rows]
 __global__ void k_column_chunks(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
                                 int rows, int cols, uint8_t* __restrict__ codes_cc,
                                 uint8_t* __restrict__ scales_cc) {
   const int m = blockIdx.y;
-  const int nch = cols / 32;
+  const int nch = cols / 8;
   const int64_t n = (int64_t)rows * nch;
   const uint8_t* cm = codes + (size_t)m * rows * (cols / 2);
   const uint8_t* sm = scales + (size_t)m * rows * (cols / 16);
@@ -622,17 +835,16 @@ __global__ void k_column_chunks(const uint8_t* __restrict__ codes, const uint8_t
   uint8_t* so = scales_cc + (size_t)m * rows * (cols / 16);
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / nch, ch = i % nch;        // source: row r, chunk ch
-    const uint4 v = *reinterpret_cast<const uint4*>(cm + r * (cols / 2) + ch * 16);
-    const uint16_t s = *reinterpret_cast<const uint16_t*>(sm + r * (cols / 16) + ch * 2);
-    *reinterpret_cast<uint4*>(co + (ch * rows + r) * 16) = v;
-    *reinterpret_cast<uint16_t*>(so + (ch * rows + r) * 2) = s;
+    const int64_t r = i / nch, ch = i % nch;        // source: row r, 8-column chunk ch
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(cm + r * (cols / 2) + ch * 4);
+    *reinterpret_cast<uint32_t*>(co + (ch * rows + r) * 4) = v;
+    if ((ch & 1) == 0) so[(ch / 2) * rows + r] = sm[r * (cols / 16) + ch / 2];
   }
 }
 
 cudaError_t launch_column_chunks(const uint8_t* codes, const uint8_t* scales, int n_mat, int rows,
                                  int cols, uint8_t* codes_cc, uint8_t* scales_cc, cudaStream_t st) {
-  const int64_t n = (int64_t)rows * (cols / 32);
+  const int64_t n = (int64_t)rows * (cols / 8);
   int g = (int)((n + 255) / 256);
   if (g > 4096) g = 4096;
   k_column_chunks<<<dim3(g, n_mat), 256, 0, st>>>(codes, scales, rows, cols, codes_cc, scales_cc);
@@ -642,16 +854,21 @@ cudaError_t launch_column_chunks(const uint8_t* codes, const uint8_t* scales, in
 // ---------------------------------------------------------------- host side
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Bytes at the start of the workspace that every launch clears: sync words + tags.
+static size_t decode_cleared_bytes(int E) {
+  return sizeof(unsigned) * kSyncWords + align256(sizeof(unsigned long long) * (E + kMaxCtas));
+}
+
 size_t decode_workspace_bytes(int H, int E) {
-  return sizeof(unsigned) * kSyncWords + align256(sizeof(float) * E) +
-         align256(sizeof(float) * 2 * H) + 2 * align256(2 * kMaxCtas * sizeof(float));
+  return decode_cleared_bytes(E) + align256(sizeof(float) * 2 * kAccCopies * H) +
+         2 * align256(2 * kMaxCtas * sizeof(float));
 }
 
 void decode_carve(PersistArgs& a, void* ws) {
   char* p = static_cast<char*>(ws);
   a.bar = reinterpret_cast<unsigned*>(p); p += sizeof(unsigned) * kSyncWords;
-  a.logits_ws = reinterpret_cast<float*>(p); p += align256(sizeof(float) * a.E);
-  a.acc = reinterpret_cast<float*>(p); p += align256(sizeof(float) * 2 * a.H);
+  a.logits_tag = reinterpret_cast<unsigned long long*>(p); p += align256(sizeof(unsigned long long) * (a.E + kMaxCtas));
+  a.acc = reinterpret_cast<float*>(p); p += align256(sizeof(float) * 2 * kAccCopies * a.H);
   a.best_v = reinterpret_cast<float*>(p); p += align256(2 * kMaxCtas * sizeof(float));
   a.best_i = reinterpret_cast<int*>(p);
 }
@@ -667,22 +884,26 @@ int decode_grid() {
   return g_sms;
 }
 
-size_t decode_smem_bytes(int H, int E, int nR) {
-  const size_t unit = UnitLayout::of(H).bytes;
-  const size_t router = (size_t)((E + nR - 1) / nR) * H * 2;
-  return (2 * sizeof(float) + 2 * sizeof(uint16_t)) * H + (unit > router ? unit : router);
+DecodePlan decode_plan(int H, int E, int K, int F, int Fs, int G) {
+  DecodePlan p = {};
+  if (G <= 0) return p;                              // no device
+  p.router_rows = (E + G - 1) / G;
+  p.shared_units = (Fs / kUnit + G - 1) / G;
+  p.routed_units = (K * (F / kUnit) + G - 1) / G;
+  p.smem = (size_t)H * (4 + 2 + 2) + (size_t)p.router_rows * H * 2 +
+           (size_t)(p.shared_units + p.routed_units) * UnitLayout::of(H).bytes;
+  p.ok = p.router_rows <= kMaxRouterRows && p.routed_units <= kMaxRoutedUnits &&
+         p.smem <= kMaxDecodeSmem && F % (2 * kUnit) == 0 && Fs % (2 * kUnit) == 0;
+  return p;
 }
 
 template <int CPL>
-static cudaError_t launch_persistent_cpl(const PersistArgs& a, cudaStream_t st) {
-  const int grid = decode_grid();
-  const int nR = grid - (a.Fs / kSlice + a.K * (a.F / kSlice));
-  const size_t smem = decode_smem_bytes(a.H, a.E, nR);
+static cudaError_t launch_persistent_cpl(const PersistArgs& a, size_t smem, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(k_decode_persistent<CPL>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = dim3(decode_grid());
   cfg.blockDim = dim3(kPThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -694,11 +915,15 @@ static cudaError_t launch_persistent_cpl(const PersistArgs& a, cudaStream_t st) 
   return cudaLaunchKernelEx(&cfg, k_decode_persistent<CPL>, a);
 }
 
+// a.max_router_rows / a.max_shared_units must hold decode_plan's counts.
 cudaError_t launch_persistent(const PersistArgs& a, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(a.bar, 0, sizeof(unsigned) * kSyncWords, st);
+  const DecodePlan p = decode_plan(a.H, a.E, a.K, a.F, a.Fs, decode_grid());
+  if (!p.ok || a.max_router_rows != p.router_rows || a.max_shared_units != p.shared_units)
+    return cudaErrorInvalidConfiguration;
+  cudaError_t e = cudaMemsetAsync(a.bar, 0, decode_cleared_bytes(a.E), st);
   if (e != cudaSuccess) return e;
-  if (a.H <= 1024) return launch_persistent_cpl<1>(a, st);
-  return launch_persistent_cpl<2>(a, st);
+  if (a.H <= 1024) return launch_persistent_cpl<1>(a, p.smem, st);
+  return launch_persistent_cpl<2>(a, p.smem, st);
 }
 
 }  // namespace flint

@@ -39,16 +39,25 @@ struct PersistArgs {
   float* w_out;            // [T, L, K] or null
   // workspace
   unsigned* bar;           // grid barrier {arrivals, generation, abort}
-  float* logits_ws;        // [E]
-  float* acc;              // [2][H] residual ping-pong
+  unsigned long long* logits_tag;   // [E] {logit bits, step + 1}
+  float* acc;              // [2][copies][H] residual ping-pong
   float* best_v;           // [grid]
   int* best_i;             // [grid]
+  int max_router_rows;     // per-CTA buffer sizes (decode_plan)
+  int max_shared_units;
   LayerPtrs layer[kMaxLayers];
 };
 
+// Per-CTA work bounds and shared memory of the persistent decode on G CTAs.
+struct DecodePlan {
+  int router_rows, shared_units, routed_units;
+  size_t smem;
+  bool ok;
+};
+DecodePlan decode_plan(int H, int E, int K, int F, int Fs, int G);
+
 size_t decode_workspace_bytes(int H, int E);
 int decode_grid();                                   // CTAs of the persistent kernel
-size_t decode_smem_bytes(int H, int E, int n_router_ctas);
 void decode_carve(PersistArgs& a, void* ws);
 cudaError_t launch_persistent(const PersistArgs& a, cudaStream_t st);
 cudaError_t launch_column_chunks(const uint8_t* codes, const uint8_t* scales, int n_mat, int rows,

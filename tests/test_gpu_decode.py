@@ -220,12 +220,12 @@ def test_column_chunks_bitexact():
     w = synth.normal_bf16(synth.tensor_key(9), 3 * 64 * 256, 0.02).view(3, 64, 256).to(DEV)
     m = flint.quantize_nvfp4(w)
     cc, sc = flint.nvfp4_column_chunks(m)
-    codes = m.codes.cpu().numpy().reshape(3, 64, 8, 16)          # [n][rows][chunk][16]
-    scales = m.scales.cpu().numpy().reshape(3, 64, 8, 2)
-    np.testing.assert_array_equal(cc.cpu().numpy().reshape(3, 8, 64, 16),
+    codes = m.codes.cpu().numpy().reshape(3, 64, 32, 4)          # [n][rows][8-col chunk][4]
+    scales = m.scales.cpu().numpy().reshape(3, 64, 16)           # [n][rows][16-col block]
+    np.testing.assert_array_equal(cc.cpu().numpy().reshape(3, 32, 64, 4),
                                   codes.transpose(0, 2, 1, 3))
-    np.testing.assert_array_equal(sc.cpu().numpy().reshape(3, 8, 64, 2),
-                                  scales.transpose(0, 2, 1, 3))
+    np.testing.assert_array_equal(sc.cpu().numpy().reshape(3, 16, 64),
+                                  scales.transpose(0, 2, 1))
 
 
 def _chain_case(orc, shape, n_layers, T, seed, zipf, with_head):
