@@ -93,8 +93,10 @@ typedef struct {
  *   sh_gate, sh_up : [1, Fs, H]   sh_down : [1, H, Fs]
  * router_w is bf16 [E, H]; router_bias fp32 [E] or NULL (added to the logits).
  * down_cc / sh_down_cc: column-chunk copies of down / sh_down, required by the
- * decode entry points (flint_moe_decode, flint_decode_tokens); the prefill path
- * reads the row-major stacks. */
+ * decode entry points (flint_moe_decode, flint_decode_tokens).
+ * mma_scales: MMA scale copies (flint_nvfp4_mma_scales) of gate, up, down, sh_gate,
+ * sh_up, sh_down in that order, required by flint_moe_prefill, which reads the
+ * row-major codes and these scales. */
 typedef struct {
   int hidden, n_experts, top_k, expert_width, shared_width;
   const void* router_w;
@@ -102,6 +104,7 @@ typedef struct {
   flint_nvfp4 gate, up, down;
   flint_nvfp4 sh_gate, sh_up, sh_down;
   flint_nvfp4_cc down_cc, sh_down_cc;
+  const uint8_t* mma_scales[6];
 } flint_moe_layer;
 
 /* Limits of this build. */
@@ -128,6 +131,16 @@ typedef struct {
 flint_status flint_quantize_nvfp4(const void* w_bf16, int n_mat, int rows, int cols,
                                   uint8_t* codes, uint8_t* scales, float* tensor_scale,
                                   void* ws, size_t ws_bytes, flint_stream stream);
+
+/* MMA scale copy of an NVFP4 stack: its block scales rearranged into the layout the
+ * block-scaled tensor-core products of the prompt path read, so that the scales of a
+ * 128-row tile and 64 columns are one contiguous 512-byte piece.  For matrix m,
+ * row r = 128 rt + i, 16-column block b = 4 k + j (i < 128, j < 4):
+ *   scales_mma[m][rt][k][16 (i % 32) + 4 (i / 32) + j] = scales[m][r][b]
+ * Requires rows % 128 == 0 and cols % 64 == 0; scales_mma (device, 16-byte aligned)
+ * has the size of the row-major scales.  Errors: FLINT_ERR_SHAPE for other sizes. */
+flint_status flint_nvfp4_mma_scales(const flint_nvfp4* m, uint8_t* scales_mma,
+                                    flint_stream stream);
 
 /* Reorder an NVFP4 stack (row-major) into its column-chunk copy (see
  * flint_nvfp4_cc).  codes_cc / scales_cc: device outputs of the same sizes as

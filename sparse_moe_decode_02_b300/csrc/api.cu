@@ -231,6 +231,17 @@ flint_status flint_moe_decode(const flint_moe_layer* L, const void* x_bf16, cons
                             nullptr, nullptr, topk_idx, topk_w, ws, ws_bytes, stream);
 }
 
+flint_status flint_nvfp4_mma_scales(const flint_nvfp4* m, uint8_t* scales_mma,
+                                    flint_stream stream) {
+  if (!m || !scales_mma) return FLINT_ERR_INVALID_ARG;
+  if (m->n_mat <= 0 || m->rows <= 0 || m->cols <= 0) return FLINT_ERR_INVALID_ARG;
+  if (m->rows % 128 || m->cols % 64) return FLINT_ERR_SHAPE;
+  if (!m->scales) return FLINT_ERR_INVALID_ARG;
+  if (!aligned16(m->scales) || !aligned16(scales_mma)) return FLINT_ERR_ALIGNMENT;
+  return from_cuda(flint::launch_mma_scales(m->scales, m->n_mat, m->rows, m->cols, scales_mma,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 flint_status flint_nvfp4_column_chunks(const flint_nvfp4* m, uint8_t* codes_cc,
                                        uint8_t* scales_cc, flint_stream stream) {
   if (!m || !codes_cc || !scales_cc) return FLINT_ERR_INVALID_ARG;
@@ -279,6 +290,10 @@ flint_status flint_moe_prefill(const flint_moe_layer* L, const void* x_bf16, flo
   if (T <= 0) return FLINT_ERR_INVALID_ARG;
   if (!flint::prefill_shape_ok(L->hidden, L->n_experts, L->top_k, L->expert_width, L->shared_width))
     return FLINT_ERR_UNSUPPORTED;
+  for (int i = 0; i < 6; ++i) {
+    if (!L->mma_scales[i]) return FLINT_ERR_INVALID_ARG;
+    if (!aligned16(L->mma_scales[i])) return FLINT_ERR_ALIGNMENT;
+  }
   if (!aligned16(x_bf16) || !aligned16(out) || (topk_idx && !aligned4(topk_idx)) ||
       (topk_w && !aligned4(topk_w)) || (expert_counts && !aligned4(expert_counts)) ||
       (pair_order && !aligned4(pair_order)))
@@ -299,6 +314,7 @@ flint_status flint_moe_prefill(const flint_moe_layer* L, const void* x_bf16, flo
   a.out = out;
   a.idx_out = topk_idx; a.w_out = topk_w;
   a.counts_out = expert_counts; a.order_out = pair_order;
+  for (int i = 0; i < 6; ++i) a.sf[i] = L->mma_scales[i];
   return from_cuda(flint::launch_prefill(a, ws, static_cast<cudaStream_t>(stream)));
 }
 

@@ -607,8 +607,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = blockIdx.x, G = gridDim.x;
-  const int LPR = H / (32 * CPL), RPP = 32 / LPR;
-  const int slice = lane / LPR, sl = lane % LPR;
+  const int LPR = H / (32 * CPL), sl = lane % LPR;
   const int n_sh = a.Fs / kUnit;                    // shared units
   const int per_slot = a.F / kUnit;                 // routed units per selected expert
   const int n_rt = a.K * per_slot;                  // routed units

@@ -15,10 +15,10 @@ struct LayerPtrs {
   const uint16_t* router_w;
   const float* router_bias;
   NVPtr gate, up, sh_gate, sh_up;
-  const uint8_t* dcc_codes;       // column-chunk copy of down [E][F/32][H][16]
-  const uint8_t* dcc_scales;      // [E][F/32][H][2]
+  const uint8_t* dcc_codes;       // column-chunk copy of down [E][F/8][H][4]
+  const uint8_t* dcc_scales;      // [E][F/16][H]
   const float* down_tsc;          // [E]
-  const uint8_t* sh_dcc_codes;    // column-chunk copy of sh_down [1][Fs/32][H][16]
+  const uint8_t* sh_dcc_codes;    // column-chunk copy of sh_down [1][Fs/8][H][4]
   const uint8_t* sh_dcc_scales;
   const float* sh_down_tsc;       // [1]
 };
@@ -74,11 +74,14 @@ struct PrefillArgs {
   float* w_out;
   int32_t* counts_out;
   int32_t* order_out;
+  const uint8_t* sf[6];    // MMA scale copies: gate, up, down, sh_gate, sh_up, sh_down
 };
 
 size_t prefill_workspace_bytes(int H, int E, int K, int F, int Fs, int T);
 bool prefill_shape_ok(int H, int E, int K, int F, int Fs);
 cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st);
+cudaError_t launch_mma_scales(const uint8_t* scales, int n_mat, int rows, int cols, uint8_t* out,
+                              cudaStream_t st);
 
 size_t lm_head_workspace_bytes(int H, int V, int B);
 cudaError_t launch_lm_head(const uint8_t* codes, const uint8_t* scales, const float* tsc, int V,

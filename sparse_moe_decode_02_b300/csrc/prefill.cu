@@ -2,27 +2,31 @@
 // Coding Model Hits 125 tok/s on MacBook Pro", section "Custom Inference Kernels": prompt
 // processing), as a token-permuted grouped GEMM on block-scaled FP4 tensor cores.
 //
-//   1 router      logits[T, E] = x Wr^T (+ bias): tcgen05 kind::f16 (bf16 in, fp32 acc)
+//   1 router      logits[T, E] = x Wr^T (+ bias): tcgen05 kind::f16 (bf16 in, fp32 acc),
+//                 128 tokens x 64 experts per CTA
 //   2 top-k       per token (one warp): softmax top-k, renormalised weights; per-expert
 //                 token bitmaps
-//   3 scan        per-expert counts and exclusive offsets (expert-major order, tokens
-//                 ascending within an expert), and the device-side tile lists
-//   4 scatter     every (token, slot) pair gets its position; its x row is quantised
-//                 to NVFP4 (unit tensor scale) into the permuted operand Xp; slot 0
-//                 also writes the unpermuted Xq used by the shared expert
+//   3 scan        per-expert counts, offsets (plain and padded to 128-row tiles) and the
+//                 device-side item lists
+//   4 scatter     per token: x quantised to NVFP4 once (unit tensor scale) and written
+//                 to the shared expert's operand Xq and to the K expert-major rows of Xp
+//                 (each expert's rows start on a 128-row tile); out[t] = x[t]
 //   5 gate/up     grouped GEMM, tcgen05 kind::mxf4nvf4 (E2M1 x E2M1, E4M3 scale per
 //                 16): per 128-row tile of one expert, the gate and up tiles accumulate
 //                 in TMEM; the epilogue applies the tensor scales, SwiGLU, and
 //                 quantises h to NVFP4 (unit tensor scale)
-//   6 down        grouped GEMM as 5; the shared expert writes out = x + y, then the
-//                 routed tiles add w_pair * y into out (red.global.add.v4.f32): the
-//                 un-permuting combine
+//   6 down        grouped GEMM as 5 over the shared and the routed tiles; the epilogue
+//                 scales each row (w_pair for routed rows) and adds it into out[token]
+//                 with TMA bulk reduce-adds: the un-permuting combine
 //
-// GEMM CTAs are warp-specialised (8 warps): warp 0 issues TMA loads of the operand
-// tiles (128-byte swizzle), warp 1 gathers the block scales into the layout the MMA
-// expects, warp 2 allocates TMEM and issues tcgen05.cp / tcgen05.mma, warps 4-7 read the
-// accumulator back (tcgen05.ld) for the epilogue.  Stages are handed over with mbarriers
-// whose waits are bounded: on expiry the CTA records FLINT_ERR_TIMEOUT and unwinds.
+// Every FP4 operand's block scales are kept in the MMA scale layout (512 bytes per
+// 128-row tile and 64 columns, see flint.h), so one pipeline stage of a GEMM is four
+// TMA transfers: A codes and B codes (2D tensor maps, 128-byte swizzle) and A and B
+// scales (bulk copies).  GEMM CTAs are warp-specialised (12 warps): warp 0 issues the
+// TMA loads, warp 1 allocates TMEM and issues tcgen05.cp / tcgen05.mma, warps 4-11 read
+// the accumulator back (tcgen05.ld; two warps per TMEM lane quarter, one per column
+// half) and hand it back to the MMA warp before their arithmetic.  Waits are bounded:
+// on expiry the CTA records FLINT_ERR_TIMEOUT and unwinds.
 #include <cstring>
 
 #include <cuda.h>
@@ -34,48 +38,58 @@
 namespace flint {
 namespace pf {
 
-constexpr int kBM = 128;          // tokens per tile (TMEM lanes)
-constexpr int kBN = 128;          // output columns per tile
-constexpr int kStages = 3;
-constexpr int kGThreads = 256;    // 8 warps
-constexpr int kWarpTMA = 0, kWarpScale = 1, kWarpMMA = 2, kWarpEpi0 = 4;
+constexpr int kBM = 128;          // rows per tile (TMEM lanes)
+constexpr int kBN = 128;          // output columns per B tile
+constexpr int kGThreads = 384;    // 12 warps
+constexpr int kWarpTMA = 0, kWarpMMA = 1, kWarpEpi0 = 4, kEpiWarps = 8;
 
 struct Item {
   int kind;     // 0 shared expert, 1 routed expert
   int expert;
-  int row0;     // first A row of the tile
+  int row0;     // first A row of the tile (a multiple of 128)
   int rows;     // valid rows (<= kBM)
   int n0;       // first output column
 };
 
-enum Mode { kGateUp = 1, kDown = 2, kRouter = 3 };
+enum Mode { kGateUp = 1, kDown = 2 };
+
+template <int MODE>
+struct Cfg {
+  static constexpr int kB = MODE == kGateUp ? 2 : 1;      // B tiles per stage (gate + up)
+  static constexpr int kStages = 4;
+  static constexpr int a = 0;                             // A codes, 128 rows x 128 B
+  static constexpr int b = 16384;                         // B codes, kB x 16 KB
+  static constexpr int sfa = b + kB * 16384;              // A scales, 4 x 512 B
+  static constexpr int sfb = sfa + 2048;                  // B scales, kB x 4 x 512 B
+  static constexpr int bytes = sfb + kB * 2048;
+  static constexpr int stride = (bytes + 1023) / 1024 * 1024;
+  static constexpr int staging = MODE == kDown ? kBM * kBN * 4 : 0;   // fp32 rows to reduce
+  static constexpr int smem = kStages * stride + staging + 1024;
+  static constexpr int dcols = kB * kBN;                  // accumulator columns
+  static constexpr int sf_step = 4 + 4 * kB;              // TMEM scale columns per K=64 step
+  static constexpr uint32_t tmem_cols = MODE == kGateUp ? 512 : 256;
+  static_assert(dcols + kStages * 4 * sf_step <= (int)tmem_cols, "TMEM budget");
+};
 
 struct GemmArgs {
-  CUtensorMap mapA[2];          // A operand: [0] shared-expert rows, [1] expert-major rows
+  CUtensorMap mapA[2];          // A codes: [0] shared-expert rows, [1] expert-major rows
   CUtensorMap mapB[4];          // gate/up: sh_gate, sh_up, gate, up; down: sh_down, -, down, -
-  const uint8_t* sclA[2];       // A block scales, row-major [rows][K/16]
-  int rowsA[2];
-  const uint8_t* sclB[4];       // weight block scales, row-major
+  const uint8_t* sfA[2];        // A scales, MMA scale layout
+  const uint8_t* sfB[4];        // B scales, MMA scale layout
   int Kel[2];                   // K in elements: shared / routed
   int rowsB[2];                 // rows of one weight matrix: shared / routed
   const Item* items;
-  const int* n_items;           // device count (total items)
-  int item_begin;               // first item this launch processes
-  int item_end_host;            // upper bound from the host (-1: use *n_items)
+  const int* n_items;           // device count
   // epilogues
-  const float* tscA[2];         // gate / sh_gate (or down / sh_down) tensor scales
+  const float* tscA[2];         // gate / sh_gate (down: down / sh_down) tensor scales
   const float* tscB[2];         // up / sh_up tensor scales
-  uint8_t* hcodes[2];           // gate/up output: [0] shared h, [1] routed h
-  uint8_t* hscales[2];
+  uint8_t* hcodes[2];           // gate/up output codes: [0] shared h [Tp][Fs/2], [1] routed h
+  uint8_t* hsf[2];              // gate/up output scales, MMA scale layout
   int Fout[2];
-  const uint16_t* x;            // [T][H] bf16
   float* out;                   // [T][H]
-  const int32_t* order;         // position -> pair id
+  const int32_t* order;         // padded routed row -> pair id
   const float* wpair;           // [T*K]
-  int H, K, T, E;
-  const float* bias;            // router
-  float* logits;                // router output [T][E]
-  int nE;                       // router N (E rounded up to 16)
+  int H, K;
 };
 
 // ---------------------------------------------------------------- primitives
@@ -133,6 +147,19 @@ __device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* m, int x, in
                "[%0], [%1, {%2, %3}], [%4];"
                :: "r"(sh(dst)), "l"(m), "r"(x), "r"(y), "r"(sh(bar)) : "memory");
 }
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(sh(dst)), "l"(src), "r"(bytes), "r"(sh(bar)) : "memory");
+}
+// out[0 .. bytes/4) += smem[0 .. bytes/4)  (fp32, performed by the TMA unit)
+__device__ __forceinline__ void bulk_reduce_add(float* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
+               :: "l"(dst), "r"(sh(src)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_commit(uint64_t* b) {
@@ -153,32 +180,26 @@ __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uin
                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
                :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
-// 32 lanes x N consecutive fp32 columns; thread (lane) gets its row.
-template <int N>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]);
-template <>
-__device__ __forceinline__ void tmem_ld<16>(uint32_t t, float (&v)[16]) {
-  uint32_t r[16];
+// 32 lanes x 16 consecutive fp32 columns; thread (lane) gets its row.  No wait.
+__device__ __forceinline__ void tmem_ld16(uint32_t t, uint32_t (&r)[16]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
                  "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
                : "r"(t));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void red_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" :: "l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+// Byte offset of (row, 64-column step k) in an MMA scale layout with K/64 steps per row tile.
+__device__ __forceinline__ size_t sf_word_offset(int row, int k, int ksteps) {
+  return ((size_t)(row >> 7) * ksteps + k) * 512 + 16 * (row & 31) + 4 * ((row & 127) >> 5);
 }
 
 // 16 fp32 values -> one NVFP4 block with unit tensor scale (the quantiser's recipe).
-__device__ __forceinline__ void quant_block_unit(const float (&v)[16], uint2& codes, uint8_t& scale) {
+__device__ __forceinline__ void quant_block_unit(const float* v, uint2& codes, uint32_t& scale) {
   float amax = 0.f;
 #pragma unroll
   for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
-  const float t = __fdiv_rn(__fdiv_rn(amax, 6.0f), 1.0f);
-  const uint32_t s = to_e4m3(t);
+  const uint32_t s = to_e4m3(__fdiv_rn(__fdiv_rn(amax, 6.0f), 1.0f));
   const float eff = e4m3_value(s);
   uint32_t packed[2] = {0u, 0u};
   if (eff != 0.f) {
@@ -189,139 +210,116 @@ __device__ __forceinline__ void quant_block_unit(const float (&v)[16], uint2& co
     }
   }
   codes = make_uint2(packed[0], packed[1]);
-  scale = (uint8_t)s;
+  scale = s;
 }
 
-// ---------------------------------------------------------------- grouped FP4 GEMM
-// Shared-memory stage: A tile (16 KB), B tiles (16 KB each), scale chunks.
-template <int MODE>
-struct StageLayout {
-  static constexpr int kB = MODE == kGateUp ? 2 : 1;
-  static constexpr int a = 0;
-  static constexpr int b = 16384;
-  static constexpr int sfa = b + kB * 16384;            // 4 chunks of 512 B
-  static constexpr int sfb = sfa + 2048;                // kB x 4 chunks of 512 B
-  static constexpr int bytes = sfb + kB * 2048;
-  static constexpr int stride = (bytes + 1023) / 1024 * 1024;
-};
+// The same recipe for the GEMM epilogue: the block's effective scale is applied as a
+// product with its reciprocal, and SwiGLU uses the fast exponential and division.
+// (h comes from fp32 accumulators, so its codes are compared within tolerance, never
+// bit for bit.)
+__device__ __forceinline__ void quant_block_unit_fast(const float* v, uint2& codes, uint32_t& scale) {
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  const uint32_t s = to_e4m3(__fdiv_rn(amax, 6.0f));
+  const float eff = e4m3_value(s);
+  uint32_t packed[2] = {0u, 0u};
+  if (eff != 0.f) {
+    const float inv = __frcp_rn(eff);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t byte = to_e2m1x2(v[2 * j] * inv, v[2 * j + 1] * inv);
+      packed[j >> 2] |= byte << (8 * (j & 3));
+    }
+  }
+  codes = make_uint2(packed[0], packed[1]);
+  scale = s;
+}
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
+// ---------------------------------------------------------------- grouped FP4 GEMM
 template <int MODE>
 __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant__ GemmArgs g) {
-  using SL = StageLayout<MODE>;
-  constexpr int kB = SL::kB;
-  constexpr uint32_t kTmemCols = MODE == kGateUp ? 512 : 256;
-  constexpr int kDCols = kB * kBN;                        // accumulator columns
-  constexpr int kSfPerStep = 4 + 4 * kB;                  // TMEM columns of scales per K=64 step
+  using C = Cfg<MODE>;
+  constexpr int S = C::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], accf, acce;
+  uint8_t* staging = smem + S * C::stride;
+  __shared__ __align__(8) uint64_t full[S], empty[S], accf, acce;
   __shared__ uint32_t tmem_base;
   __shared__ volatile int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) { mb_init(&full[s], 1 + 32); mb_init(&empty[s], 1); }
+    for (int s = 0; s < S; ++s) { mb_init(&full[s], 1); mb_init(&empty[s], 1); }
     mb_init(&accf, 1);
-    mb_init(&acce, 4);
+    mb_init(&acce, kEpiWarps);
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kWarpMMA) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 :: "r"(sh(&tmem_base)), "r"(kTmemCols));
+                 :: "r"(sh(&tmem_base)), "r"(C::tmem_cols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const int n_items = g.item_end_host >= 0 ? g.item_end_host : __ldcg(g.n_items);
+  const int n_items = __ldcg(g.n_items);
   const uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
 
   if (warp == kWarpTMA && lane == 0) {
     uint32_t it = 0;
-    for (int i = g.item_begin + blockIdx.x; i < n_items && !abort_flag; i += gridDim.x) {
+    for (int i = blockIdx.x; i < n_items && !abort_flag; i += gridDim.x) {
       const Item item = g.items[i];
-      const int kt_n = g.Kel[item.kind] / 256;
-      for (int kt = 0; kt < kt_n; ++kt, ++it) {
-        const int s = it % kStages;
-        if (it >= kStages && !mb_wait(&empty[s], ((it / kStages) - 1) & 1, &abort_flag)) break;
-        uint8_t* st = smem + s * SL::stride;
-        mb_expect(&full[s], 16384 * (1 + kB));
-        tma2d(st + SL::a, &g.mapA[item.kind], kt * 128, item.row0, &full[s]);
-        const int brow = item.expert * g.rowsB[item.kind] + item.n0;
-        tma2d(st + SL::b, &g.mapB[2 * item.kind], kt * 128, brow, &full[s]);
-        if (kB == 2) tma2d(st + SL::b + 16384, &g.mapB[2 * item.kind + 1], kt * 128, brow, &full[s]);
-      }
-    }
-  } else if (warp == kWarpScale) {
-    uint32_t it = 0;
-    for (int i = g.item_begin + blockIdx.x; i < n_items && !abort_flag; i += gridDim.x) {
-      const Item item = g.items[i];
-      const int K = g.Kel[item.kind];
-      const int kt_n = K / 256;
-      const int ldk = K / 16;
-      for (int kt = 0; kt < kt_n; ++kt, ++it) {
-        const int s = it % kStages;
-        if (it >= kStages && !mb_wait(&empty[s], ((it / kStages) - 1) & 1, &abort_flag)) break;
-        uint8_t* st = smem + s * SL::stride;
-        // A scales: 128 rows, 16 bytes (blocks 16 kt .. 16 kt + 15) per row
-        for (int r = lane; r < kBM; r += 32) {
-          const int row = item.row0 + r;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (row < g.rowsA[item.kind])
-            v = __ldg(reinterpret_cast<const uint4*>(g.sclA[item.kind] + (size_t)row * ldk + kt * 16));
-          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-          uint8_t* base = st + SL::sfa + 16 * (r & 31) + 4 * (r >> 5);
+      const int K = g.Kel[item.kind], ksteps = K / 64;
+      const int brow = item.expert * g.rowsB[item.kind] + item.n0;
+      const uint8_t* sfa = g.sfA[item.kind] + (size_t)(item.row0 >> 7) * ksteps * 512;
+      for (int kt = 0; kt < K / 256; ++kt, ++it) {
+        const int s = it % S;
+        if (it >= S && !mb_wait(&empty[s], ((it / S) - 1) & 1, &abort_flag)) break;
+        uint8_t* st = smem + s * C::stride;
+        mb_expect(&full[s], C::bytes);
+        tma2d(st + C::a, &g.mapA[item.kind], kt * 128, item.row0, &full[s]);
+        bulk_g2s(st + C::sfa, sfa + (size_t)kt * 2048, 2048, &full[s]);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) *reinterpret_cast<uint32_t*>(base + kk * 512) = w4[kk];
+        for (int b = 0; b < C::kB; ++b) {
+          tma2d(st + C::b + b * 16384, &g.mapB[2 * item.kind + b], kt * 128, brow, &full[s]);
+          bulk_g2s(st + C::sfb + b * 2048,
+                   g.sfB[2 * item.kind + b] + ((size_t)(brow >> 7) * ksteps + 4 * kt) * 512, 2048, &full[s]);
         }
-        // B scales: kB matrices x 128 rows
-#pragma unroll
-        for (int b = 0; b < kB; ++b) {
-          const uint8_t* src = g.sclB[2 * item.kind + b];
-          const size_t row0 = (size_t)item.expert * g.rowsB[item.kind] + item.n0;
-          for (int r = lane; r < kBN; r += 32) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + (row0 + r) * ldk + kt * 16));
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-            uint8_t* base = st + SL::sfb + b * 2048 + 16 * (r & 31) + 4 * (r >> 5);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) *reinterpret_cast<uint32_t*>(base + kk * 512) = w4[kk];
-          }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mb_arrive(&full[s]);
       }
     }
   } else if (warp == kWarpMMA && lane == 0) {
     uint32_t it = 0, done = 0;
-    for (int i = g.item_begin + blockIdx.x; i < n_items && !abort_flag; i += gridDim.x, ++done) {
+    for (int i = blockIdx.x; i < n_items && !abort_flag; i += gridDim.x, ++done) {
       const Item item = g.items[i];
       const int kt_n = g.Kel[item.kind] / 256;
       if (done > 0 && !mb_wait(&acce, (done - 1) & 1, &abort_flag)) break;
       tc_fence_after();
       bool ok = true;
       for (int kt = 0; kt < kt_n; ++kt, ++it) {
-        const int s = it % kStages;
-        if (!mb_wait(&full[s], (it / kStages) & 1, &abort_flag)) { ok = false; break; }
+        const int s = it % S;
+        if (!mb_wait(&full[s], (it / S) & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after();
-        uint8_t* st = smem + s * SL::stride;
-        const uint32_t sf0 = tmem + kDCols + (uint32_t)(s * 4 * kSfPerStep);
+        uint8_t* st = smem + s * C::stride;
+        const uint32_t sf0 = tmem + C::dcols + (uint32_t)(s * 4 * C::sf_step);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t sfs = sf0 + kk * kSfPerStep;
-          tc_cp_sf(sfs, sf_desc(sh(st + SL::sfa + kk * 512)));
+          const uint32_t sfs = sf0 + kk * C::sf_step;
+          tc_cp_sf(sfs, sf_desc(sh(st + C::sfa + kk * 512)));
 #pragma unroll
-          for (int b = 0; b < kB; ++b) tc_cp_sf(sfs + 4 + 4 * b, sf_desc(sh(st + SL::sfb + b * 2048 + kk * 512)));
+          for (int b = 0; b < C::kB; ++b) tc_cp_sf(sfs + 4 + 4 * b, sf_desc(sh(st + C::sfb + b * 2048 + kk * 512)));
         }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t sfs = sf0 + kk * kSfPerStep;
-          const uint64_t ad = umma_desc_sw128(sh(st + SL::a) + kk * 32);
+          const uint32_t sfs = sf0 + kk * C::sf_step;
+          const uint64_t ad = umma_desc_sw128(sh(st + C::a) + kk * 32);
           const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
 #pragma unroll
-          for (int b = 0; b < kB; ++b) {
-            const uint64_t bd = umma_desc_sw128(sh(st + SL::b + b * 16384) + kk * 32);
+          for (int b = 0; b < C::kB; ++b) {
+            const uint64_t bd = umma_desc_sw128(sh(st + C::b + b * 16384) + kk * 32);
             mma_fp4(tmem + b * kBN, ad, bd, idesc, acc, sfs, sfs + 4 + 4 * b);
           }
         }
@@ -332,10 +330,11 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
     }
   } else if (warp >= kWarpEpi0) {
     const int q = warp & 3;                                 // TMEM lane quarter
+    const int hf = (warp - kWarpEpi0) >> 2;                 // column half: [64 hf, 64 hf + 64)
     const int r = q * 32 + lane;                            // tile row of this thread
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t done = 0;
-    for (int i = g.item_begin + blockIdx.x; i < n_items && !abort_flag; i += gridDim.x, ++done) {
+    for (int i = blockIdx.x; i < n_items && !abort_flag; i += gridDim.x, ++done) {
       const Item item = g.items[i];
       if (!mb_wait(&accf, done & 1, &abort_flag)) break;
       tc_fence_after();
@@ -344,60 +343,71 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
       if (MODE == kGateUp) {
         const float tg = g.tscA[item.kind][item.kind ? item.expert : 0];
         const float tu = g.tscB[item.kind][item.kind ? item.expert : 0];
-        const int F = g.Fout[item.kind];
-        uint8_t* hc = g.hcodes[item.kind] + (size_t)arow * (F / 2);
-        uint8_t* hs = g.hscales[item.kind] + (size_t)arow * (F / 16);
-#pragma unroll 1
-        for (int c0 = 0; c0 < kBN; c0 += 16) {
-          float gv[16], uv[16], hv[16];
-          tmem_ld<16>(lane_base + c0, gv);
-          tmem_ld<16>(lane_base + kBN + c0, uv);
+        float h[64];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) hv[j] = silu(gv[j] * tg) * (uv[j] * tu);
-          uint2 cw;
-          uint8_t sc;
-          quant_block_unit(hv, cw, sc);
-          if (valid) {
-            *reinterpret_cast<uint2*>(hc + (item.n0 + c0) / 2) = cw;
-            hs[(item.n0 + c0) / 16] = sc;
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+          uint32_t gv[16], uv[16];
+          tmem_ld16(lane_base + 64 * hf + c0, gv);
+          tmem_ld16(lane_base + kBN + 64 * hf + c0, uv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            h[c0 + j] = silu_fast(__uint_as_float(gv[j]) * tg) * (__uint_as_float(uv[j]) * tu);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mb_arrive(&acce);                  // accumulator free for the next item
+        if (valid) {
+          const int F = g.Fout[item.kind];
+          const int col = item.n0 + 64 * hf;
+          uint8_t* hc = g.hcodes[item.kind] + (size_t)arow * (F / 2) + col / 2;
+          uint32_t sw = 0;
+          uint2 cw[4];
+#pragma unroll
+          for (int b4 = 0; b4 < 4; ++b4) {
+            uint32_t sc;
+            quant_block_unit_fast(h + 16 * b4, cw[b4], sc);
+            sw |= sc << (8 * b4);
           }
+          *reinterpret_cast<uint4*>(hc) = make_uint4(cw[0].x, cw[0].y, cw[1].x, cw[1].y);
+          *reinterpret_cast<uint4*>(hc + 16) = make_uint4(cw[2].x, cw[2].y, cw[3].x, cw[3].y);
+          *reinterpret_cast<uint32_t*>(g.hsf[item.kind] + sf_word_offset(arow, col / 64, F / 64)) = sw;
         }
       } else {  // down
-        const float td = g.tscA[item.kind][item.kind ? item.expert : 0];
-        const int H = g.H;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kBN; c0 += 16) {
-          float yv[16];
-          tmem_ld<16>(lane_base + c0, yv);
-          if (!valid) continue;
-          if (item.kind == 0) {
-            const int t = arow;
-            const uint16_t* xr = g.x + (size_t)t * H + item.n0 + c0;
-            float* o = g.out + (size_t)t * H + item.n0 + c0;
+        float y[64];
 #pragma unroll
-            for (int j = 0; j < 16; j += 4) {
-              const uint2 xb = *reinterpret_cast<const uint2*>(xr + j);
-              float4 v;
-              v.x = bf16_bits_to_f32(xb.x & 0xFFFFu) + yv[j] * td;
-              v.y = bf16_bits_to_f32(xb.x >> 16) + yv[j + 1] * td;
-              v.z = bf16_bits_to_f32(xb.y & 0xFFFFu) + yv[j + 2] * td;
-              v.w = bf16_bits_to_f32(xb.y >> 16) + yv[j + 3] * td;
-              *reinterpret_cast<float4*>(o + j) = v;
-            }
-          } else {
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(lane_base + 64 * hf + c0, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) y[c0 + j] = __uint_as_float(v[j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mb_arrive(&acce);
+        if (valid) {
+          const float td = g.tscA[item.kind][item.kind ? item.expert : 0];
+          int t = arow;
+          float scale = td;
+          if (item.kind) {
             const int pair = g.order[arow];
-            const int t = pair / g.K;
-            const float w = g.wpair[pair] * td;
-            float* o = g.out + (size_t)t * H + item.n0 + c0;
-#pragma unroll
-            for (int j = 0; j < 16; j += 4) red_v4(o + j, yv[j] * w, yv[j + 1] * w, yv[j + 2] * w, yv[j + 3] * w);
+            t = pair / g.K;
+            scale = td * g.wpair[pair];
           }
+          float* slot = reinterpret_cast<float*>(staging) + r * kBN + 64 * hf;
+          bulk_wait_read();                                // the previous reduce has read the slot
+#pragma unroll
+          for (int j = 0; j < 64; j += 4)
+            *reinterpret_cast<float4*>(slot + j) =
+                make_float4(y[j] * scale, y[j + 1] * scale, y[j + 2] * scale, y[j + 3] * scale);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          bulk_reduce_add(g.out + (size_t)t * g.H + item.n0 + 64 * hf, slot, 256);
+          bulk_commit();
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mb_arrive(&acce);
     }
+    if (MODE == kDown) bulk_wait_all();
   }
   // unwind: every role is done (or gave up); no MMA may be in flight at dealloc
   __syncthreads();
@@ -412,17 +422,28 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
     }
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(kTmemCols));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(C::tmem_cols));
   }
 }
 
 // ---------------------------------------------------------------- router GEMM (bf16)
-// logits[t][e] = x[t] . Wr[e] (+ bias[e]); A = x rows (TMA, 64 bf16 = 128 B per K-tile),
-// B = Wr rows (N = nE <= 256), tcgen05 kind::f16 with K = 16 per instruction.
+// logits[t][e] = x[t] . Wr[e] (+ bias[e]) for 128 tokens x 64 experts per CTA; A = x rows
+// (TMA, 64 bf16 = 128 B per K-tile), B = 64 router rows, tcgen05 kind::f16 (K = 16 per
+// instruction).
 constexpr int kRStages = 4;
+constexpr int kRN = 64;
+constexpr int kRThreads = 256;
 
-__global__ void __launch_bounds__(kGThreads, 1) k_router_gemm(const __grid_constant__ GemmArgs g) {
-  constexpr int kStageBytes = 16384 + 32768;
+struct RouterArgs {
+  CUtensorMap mapX;
+  CUtensorMap mapW;
+  const float* bias;
+  float* logits;
+  int T, E, H;
+};
+
+__global__ void __launch_bounds__(kRThreads, 1) k_router_gemm(const __grid_constant__ RouterArgs g) {
+  constexpr int kStageBytes = 16384 + kRN * 128;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t full[kRStages], empty[kRStages], accf;
@@ -436,25 +457,25 @@ __global__ void __launch_bounds__(kGThreads, 1) k_router_gemm(const __grid_const
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kWarpMMA) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(sh(&tmem_base)), "r"(256));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(sh(&tmem_base)), "r"(kRN));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const int row0 = blockIdx.x * kBM;
+  const int row0 = blockIdx.x * kBM, n0 = blockIdx.y * kRN;
   const int kt_n = g.H / 64;
-  const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(g.nE >> 3) << 17) |
+  const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kRN >> 3) << 17) |
                          ((uint32_t)(kBM >> 4) << 24);
   if (warp == kWarpTMA && lane == 0) {
     for (int kt = 0; kt < kt_n; ++kt) {
       const int s = kt % kRStages;
       if (kt >= kRStages && !mb_wait(&empty[s], ((kt / kRStages) - 1) & 1, &abort_flag)) break;
       uint8_t* st = smem + s * kStageBytes;
-      mb_expect(&full[s], 16384 + 128 * g.nE);
-      tma2d(st, &g.mapA[0], kt * 128, row0, &full[s]);
-      tma2d(st + 16384, &g.mapB[0], kt * 128, 0, &full[s]);
+      mb_expect(&full[s], kStageBytes);
+      tma2d(st, &g.mapX, kt * 128, row0, &full[s]);
+      tma2d(st + 16384, &g.mapW, kt * 128, n0, &full[s]);
     }
   } else if (warp == kWarpMMA && lane == 0) {
     bool ok = true;
@@ -470,19 +491,23 @@ __global__ void __launch_bounds__(kGThreads, 1) k_router_gemm(const __grid_const
       tc_commit(&empty[s]);
     }
     if (ok) tc_commit(&accf);
-  } else if (warp >= kWarpEpi0) {
+  } else if (warp >= 4) {
     const int q = warp & 3;
-    const int r = q * 32 + lane;
-    const int t = row0 + r;
+    const int t = row0 + q * 32 + lane;
     if (mb_wait(&accf, 0, &abort_flag)) {
       tc_fence_after();
-      for (int c0 = 0; c0 < g.nE; c0 += 16) {
-        float v[16];
-        tmem_ld<16>(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
-        if (t < g.T)
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < g.E) g.logits[(size_t)t * g.E + c0 + j] = v[j] + (g.bias ? g.bias[c0 + j] : 0.f);
+      for (int c0 = 0; c0 < kRN; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
+        tmem_wait_ld();
+        if (t < g.T) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int e = n0 + c0 + j;
+            if (e < g.E) g.logits[(size_t)t * g.E + e] = __uint_as_float(v[j]) + (g.bias ? g.bias[e] : 0.f);
+          }
+        }
       }
       tc_fence_before();
     }
@@ -499,7 +524,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_router_gemm(const __grid_const
     }
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(256));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(kRN));
   }
 }
 
@@ -514,7 +539,8 @@ struct RouteArgs {
   unsigned* bits;          // [E][W]
   int* wordpre;            // [E][W]
   int* counts;             // [E]
-  int* offsets;            // [E]
+  int* offsets;            // [E] expert-major offsets
+  int* offp;               // [E] the same, each expert padded to 128-row tiles
   int32_t* counts_out;
 };
 
@@ -538,7 +564,8 @@ __global__ void __launch_bounds__(256) k_topk(RouteArgs a) {
   }
 }
 
-// One CTA: per-expert word prefix counts, expert offsets, and the tile lists.
+// One CTA: per-expert word prefix counts, expert offsets (plain and tile-padded), and
+// the item lists of both GEMMs.
 struct ScanArgs {
   RouteArgs r;
   Item* items_gu;          // gate/up items: shared first, then routed
@@ -550,8 +577,8 @@ struct ScanArgs {
 
 __global__ void __launch_bounds__(1024) k_scan(ScanArgs s) {
   const RouteArgs& a = s.r;
-  __shared__ int s_tiles[FLINT_MAX_EXPERTS];
-  __shared__ int s_tile_off[FLINT_MAX_EXPERTS];
+  __shared__ int s_cnt[FLINT_MAX_EXPERTS], s_toff[FLINT_MAX_EXPERTS];
+  __shared__ int s_wsum[2][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int e = warp; e < a.E; e += 32) {
     int run = 0;
@@ -567,28 +594,39 @@ __global__ void __launch_bounds__(1024) k_scan(ScanArgs s) {
       if (w < a.W) a.wordpre[(size_t)e * a.W + w] = run + incl - v;
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) {
-      a.counts[e] = run;
-      if (a.counts_out) a.counts_out[e] = run;
-      s_tiles[e] = (run + kBM - 1) / kBM;
-    }
+    if (lane == 0) s_cnt[e] = run;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int off = 0, toff = 0;
-    for (int e = 0; e < a.E; ++e) {
-      a.offsets[e] = off;
-      off += a.counts[e];
-      s_tile_off[e] = toff;
-      toff += s_tiles[e];
-    }
-    const int mt_sh = (a.T + kBM - 1) / kBM;
-    *s.n_items_gu = mt_sh * (s.Fs / kBN) + toff * (s.F / kBN);
-    *s.n_items_dn = mt_sh * (s.H / kBN) + toff * (s.H / kBN);
+  // exclusive scans over experts of the counts and of the 128-row tile counts
+  const int e = threadIdx.x;
+  const int cnt = e < a.E ? s_cnt[e] : 0;
+  const int til = (cnt + kBM - 1) / kBM;
+  int ic = cnt, it = til;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int nc = __shfl_up_sync(0xffffffffu, ic, o), nt = __shfl_up_sync(0xffffffffu, it, o);
+    if (lane >= o) { ic += nc; it += nt; }
   }
+  if (lane == 31) { s_wsum[0][warp] = ic; s_wsum[1][warp] = it; }
   __syncthreads();
+  int pc = 0, pt = 0;
+  for (int w = 0; w < warp; ++w) { pc += s_wsum[0][w]; pt += s_wsum[1][w]; }
+  const int off = pc + ic - cnt, toff = pt + it - til;
+  if (e < a.E) {
+    s_toff[e] = toff;
+    a.counts[e] = cnt;
+    a.offsets[e] = off;
+    a.offp[e] = toff * kBM;
+    if (a.counts_out) a.counts_out[e] = cnt;
+  }
+  int tot_tiles = 0;
+  for (int w = 0; w < 32; ++w) tot_tiles += s_wsum[1][w];
   const int mt_sh = (a.T + kBM - 1) / kBM;
-  // shared-expert items
+  if (threadIdx.x == 0) {
+    *s.n_items_gu = mt_sh * (s.Fs / kBN) + tot_tiles * (s.F / kBN);
+    *s.n_items_dn = mt_sh * (s.H / kBN) + tot_tiles * (s.H / kBN);
+  }
+  __syncthreads();
   for (int i = threadIdx.x; i < mt_sh * (s.Fs / kBN); i += blockDim.x) {
     const int mt = i / (s.Fs / kBN), nt = i % (s.Fs / kBN);
     s.items_gu[i] = Item{0, 0, mt * kBM, min(kBM, a.T - mt * kBM), nt * kBN};
@@ -597,80 +635,127 @@ __global__ void __launch_bounds__(1024) k_scan(ScanArgs s) {
     const int mt = i / (s.H / kBN), nt = i % (s.H / kBN);
     s.items_dn[i] = Item{0, 0, mt * kBM, min(kBM, a.T - mt * kBM), nt * kBN};
   }
-  // routed items, expert by expert
   const int base_gu = mt_sh * (s.Fs / kBN), base_dn = mt_sh * (s.H / kBN);
-  for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
-    const int cnt = a.counts[e], off = a.offsets[e];
-    for (int mt = 0; mt < s_tiles[e]; ++mt) {
-      const int rows = min(kBM, cnt - mt * kBM);
+  for (int x = threadIdx.x; x < a.E; x += blockDim.x) {
+    const int c = s_cnt[x], tiles = (c + kBM - 1) / kBM;
+    for (int mt = 0; mt < tiles; ++mt) {
+      const int rows = min(kBM, c - mt * kBM);
+      const int row0 = (s_toff[x] + mt) * kBM;
       for (int nt = 0; nt < s.F / kBN; ++nt)
-        s.items_gu[base_gu + (s_tile_off[e] + mt) * (s.F / kBN) + nt] = Item{1, e, off + mt * kBM, rows, nt * kBN};
+        s.items_gu[base_gu + (s_toff[x] + mt) * (s.F / kBN) + nt] = Item{1, x, row0, rows, nt * kBN};
       for (int nt = 0; nt < s.H / kBN; ++nt)
-        s.items_dn[base_dn + (s_tile_off[e] + mt) * (s.H / kBN) + nt] = Item{1, e, off + mt * kBM, rows, nt * kBN};
+        s.items_dn[base_dn + (s_toff[x] + mt) * (s.H / kBN) + nt] = Item{1, x, row0, rows, nt * kBN};
     }
   }
 }
 
-// One warp per (token, slot) pair: its expert-major position, and its x row quantised to
-// NVFP4 with unit tensor scale (slot 0 also writes the unpermuted copy).
+// One warp per token: x[t] quantised to NVFP4 once (unit tensor scale), written to the
+// shared expert's operand row t and to the token's K expert-major rows; out[t] = x[t];
+// the pair order (plain and padded positions).
 struct ScatterArgs {
   RouteArgs r;
   const uint16_t* x;
+  float* out;
   int H;
-  int32_t* pos_of_pair;   // [T*K]
-  int32_t* order;         // [P]
-  int32_t* order_out;
-  uint8_t* xq_codes;  uint8_t* xq_scales;   // [T][H/2], [T][H/16]
-  uint8_t* xp_codes;  uint8_t* xp_scales;   // [P+128][H/2], [P+128][H/16]
+  int32_t* order_pad;      // padded row -> pair
+  int32_t* order_out;      // plain position -> pair (optional)
+  uint8_t* xq_codes;  uint8_t* xq_sf;   // [Tp][H/2], MMA scale layout
+  uint8_t* xp_codes;  uint8_t* xp_sf;   // [Pp][H/2], MMA scale layout
 };
 
 __global__ void __launch_bounds__(256) k_scatter_quant(ScatterArgs s) {
   const RouteArgs& a = s.r;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pair = blockIdx.x * 8 + warp;
-  if (pair >= a.T * a.K) return;
-  const int t = pair / a.K, j = pair % a.K;
-  const int e = a.idx[pair];
-  const unsigned word = a.bits[(size_t)e * a.W + (t >> 5)];
-  const int pos = a.offsets[e] + a.wordpre[(size_t)e * a.W + (t >> 5)] + __popc(word & ((1u << (t & 31)) - 1u));
-  if (lane == 0) {
-    s.pos_of_pair[pair] = pos;
-    s.order[pos] = pair;
-    if (s.order_out) s.order_out[pos] = pair;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= a.T) return;
+  // rows of this token's K pairs (lanes < K), shared through the warp
+  int mypos = 0;
+  if (lane < a.K) {
+    const int pair = t * a.K + lane;
+    const int e = a.idx[pair];
+    const unsigned word = a.bits[(size_t)e * a.W + (t >> 5)];
+    const int rank = a.wordpre[(size_t)e * a.W + (t >> 5)] + __popc(word & ((1u << (t & 31)) - 1u));
+    mypos = a.offp[e] + rank;
+    s.order_pad[mypos] = pair;
+    if (s.order_out) s.order_out[a.offsets[e] + rank] = pair;
   }
-  const int H = s.H;
+  const int H = s.H, ks = H / 64;
   const uint16_t* xr = s.x + (size_t)t * H;
-  for (int b = lane; b < H / 16; b += 32) {
-    const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(xr + 16 * b));
-    const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(xr + 16 * b + 8));
-    const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    float f[16];
+  for (int gk = lane; gk < ks; gk += 32) {
+    float f[64];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) { f[2 * q] = bf16_bits_to_f32(u[q] & 0xFFFFu); f[2 * q + 1] = bf16_bits_to_f32(u[q] >> 16); }
-    uint2 cw;
-    uint8_t sc;
-    quant_block_unit(f, cw, sc);
-    *reinterpret_cast<uint2*>(s.xp_codes + (size_t)pos * (H / 2) + 8 * b) = cw;
-    s.xp_scales[(size_t)pos * (H / 16) + b] = sc;
-    if (j == 0) {
-      *reinterpret_cast<uint2*>(s.xq_codes + (size_t)t * (H / 2) + 8 * b) = cw;
-      s.xq_scales[(size_t)t * (H / 16) + b] = sc;
+    for (int p = 0; p < 8; ++p) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + 64 * gk + 8 * p));
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        f[8 * p + 2 * q] = bf16_bits_to_f32(u[q] & 0xFFFFu);
+        f[8 * p + 2 * q + 1] = bf16_bits_to_f32(u[q] >> 16);
+      }
     }
+    float* orow = s.out + (size_t)t * H + 64 * gk;
+#pragma unroll
+    for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4*>(orow + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+    uint2 cw[4];
+    uint32_t sw = 0;
+#pragma unroll
+    for (int b4 = 0; b4 < 4; ++b4) {
+      uint32_t sc;
+      quant_block_unit(f + 16 * b4, cw[b4], sc);
+      sw |= sc << (8 * b4);
+    }
+    const uint4 c0 = make_uint4(cw[0].x, cw[0].y, cw[1].x, cw[1].y);
+    const uint4 c1 = make_uint4(cw[2].x, cw[2].y, cw[3].x, cw[3].y);
+    uint8_t* q = s.xq_codes + (size_t)t * (H / 2) + 32 * gk;
+    *reinterpret_cast<uint4*>(q) = c0;
+    *reinterpret_cast<uint4*>(q + 16) = c1;
+    *reinterpret_cast<uint32_t*>(s.xq_sf + sf_word_offset(t, gk, ks)) = sw;
+    for (int j = 0; j < a.K; ++j) {
+      const int pos = __shfl_sync(0xffffffffu, mypos, j);
+      uint8_t* p = s.xp_codes + (size_t)pos * (H / 2) + 32 * gk;
+      *reinterpret_cast<uint4*>(p) = c0;
+      *reinterpret_cast<uint4*>(p + 16) = c1;
+      *reinterpret_cast<uint32_t*>(s.xp_sf + sf_word_offset(pos, gk, ks)) = sw;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- MMA scale copies
+// scales [m][rows][cols/16] -> [m][rows/128][cols/64][512] (see flint.h)
+__global__ void k_mma_scales(const uint8_t* __restrict__ scales, int rows, int cols,
+                             uint8_t* __restrict__ out) {
+  const int m = blockIdx.y;
+  const int ks = cols / 64;
+  const int64_t n = (int64_t)rows * ks;
+  const uint8_t* sm = scales + (size_t)m * rows * (cols / 16);
+  uint8_t* om = out + (size_t)m * rows * (cols / 16);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(i / ks), k = (int)(i % ks);
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(sm + (size_t)r * (cols / 16) + 4 * k);
+    *reinterpret_cast<uint32_t*>(om + sf_word_offset(r, k, ks)) = v;
   }
 }
 
 // ---------------------------------------------------------------- host side
 struct WsLayout {
-  size_t logits, idx, w, bits, wordpre, counts, offsets, pos, order, xq_c, xq_s, xp_c, xp_s, hs_c,
+  size_t logits, idx, w, bits, wordpre, counts, offsets, offp, order, xq_c, xq_s, xp_c, xp_s, hs_c,
       hs_s, hq_c, hq_s, items_gu, items_dn, nitems, total;
 };
 
 static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Rows of the padded expert-major operands: every expert's rows start on a 128-row tile.
+static size_t padded_rows(int T, int K, int E) {
+  const size_t P = (size_t)T * K;
+  const size_t touched = P < (size_t)E ? P : (size_t)E;
+  return (P + touched * (kBM - 1) + kBM - 1) / kBM * kBM;
+}
+
 static WsLayout ws_layout(int H, int E, int K, int F, int Fs, int T) {
   WsLayout L;
-  const size_t P = (size_t)T * K, PP = P + kBM, W = (T + 31) / 32;
-  const size_t mt_sh = (T + kBM - 1) / kBM, mt_rt = P / kBM + E;
+  const size_t P = (size_t)T * K, Pp = padded_rows(T, K, E), W = (T + 31) / 32;
+  const size_t Tp = (T + kBM - 1) / kBM * kBM;
+  const size_t mt_sh = Tp / kBM, mt_rt = Pp / kBM;
   size_t o = 0;
   L.logits = o;   o += a256(sizeof(float) * T * E);
   L.idx = o;      o += a256(sizeof(int) * P);
@@ -679,16 +764,16 @@ static WsLayout ws_layout(int H, int E, int K, int F, int Fs, int T) {
   L.wordpre = o;  o += a256(sizeof(int) * E * W);
   L.counts = o;   o += a256(sizeof(int) * E);
   L.offsets = o;  o += a256(sizeof(int) * E);
-  L.pos = o;      o += a256(sizeof(int) * P);
-  L.order = o;    o += a256(sizeof(int) * PP);
-  L.xq_c = o;     o += a256((size_t)T * H / 2);
-  L.xq_s = o;     o += a256((size_t)T * H / 16);
-  L.xp_c = o;     o += a256(PP * H / 2);
-  L.xp_s = o;     o += a256(PP * H / 16);
-  L.hs_c = o;     o += a256((size_t)T * Fs / 2);
-  L.hs_s = o;     o += a256((size_t)T * Fs / 16);
-  L.hq_c = o;     o += a256(PP * F / 2);
-  L.hq_s = o;     o += a256(PP * F / 16);
+  L.offp = o;     o += a256(sizeof(int) * E);
+  L.order = o;    o += a256(sizeof(int) * Pp);
+  L.xq_c = o;     o += a256(Tp * H / 2);
+  L.xq_s = o;     o += a256(Tp * H / 16);
+  L.xp_c = o;     o += a256(Pp * H / 2);
+  L.xp_s = o;     o += a256(Pp * H / 16);
+  L.hs_c = o;     o += a256(Tp * Fs / 2);
+  L.hs_s = o;     o += a256(Tp * Fs / 16);
+  L.hq_c = o;     o += a256(Pp * F / 2);
+  L.hq_s = o;     o += a256(Pp * F / 16);
   L.items_gu = o; o += a256(sizeof(Item) * (mt_sh * (Fs / kBN) + mt_rt * (F / kBN)));
   L.items_dn = o; o += a256(sizeof(Item) * (mt_sh + mt_rt) * (H / kBN));
   L.nitems = o;   o += 256;
@@ -731,11 +816,20 @@ bool prefill_shape_ok(int H, int E, int K, int F, int Fs) {
          H <= 8192 && F <= 8192 && Fs <= 8192;
 }
 
+cudaError_t launch_mma_scales(const uint8_t* scales, int n_mat, int rows, int cols, uint8_t* out,
+                              cudaStream_t st) {
+  const int64_t n = (int64_t)rows * (cols / 64);
+  int g = (int)((n + 255) / 256);
+  if (g > 4096) g = 4096;
+  pf::k_mma_scales<<<dim3(g, n_mat), 256, 0, st>>>(scales, rows, cols, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st) {
   using namespace pf;
   if (!encode_init()) return cudaErrorNotSupported;
   const int H = a.H, E = a.E, K = a.K, F = a.F, Fs = a.Fs, T = a.T;
-  const size_t P = (size_t)T * K, PP = P + kBM;
+  const size_t Pp = padded_rows(T, K, E), Tp = (T + kBM - 1) / kBM * kBM;
   const WsLayout L = ws_layout(H, E, K, F, Fs, T);
   char* b = static_cast<char*>(ws);
   auto at = [&](size_t off) { return b + off; };
@@ -749,22 +843,23 @@ cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st) {
   r.wordpre = reinterpret_cast<int*>(at(L.wordpre));
   r.counts = reinterpret_cast<int*>(at(L.counts));
   r.offsets = reinterpret_cast<int*>(at(L.offsets));
+  r.offp = reinterpret_cast<int*>(at(L.offp));
   r.counts_out = a.counts_out;
   cudaError_t e = cudaMemsetAsync(r.bits, 0, sizeof(unsigned) * E * r.W, st);
   if (e != cudaSuccess) return e;
 
   // 1 router GEMM
-  GemmArgs gr;
-  memset(&gr, 0, sizeof(gr));
-  gr.H = H; gr.T = T; gr.E = E; gr.nE = E; gr.bias = a.router_bias; gr.logits = const_cast<float*>(r.logits);
-  if (!make_map(&gr.mapA[0], a.x, T, (uint64_t)H * 2, 128) || !make_map(&gr.mapB[0], a.router_w, E, (uint64_t)H * 2, E))
+  RouterArgs ra;
+  memset(&ra, 0, sizeof(ra));
+  ra.bias = a.router_bias; ra.logits = reinterpret_cast<float*>(at(L.logits)); ra.T = T; ra.E = E; ra.H = H;
+  if (!make_map(&ra.mapX, a.x, T, (uint64_t)H * 2, kBM) || !make_map(&ra.mapW, a.router_w, E, (uint64_t)H * 2, kRN))
     return cudaErrorInvalidValue;
-  const int smem_r = kRStages * (16384 + 32768) + 1024;
+  const int smem_r = kRStages * (16384 + kRN * 128) + 1024;
   e = cudaFuncSetAttribute(k_router_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_r);
   if (e != cudaSuccess) return e;
-  k_router_gemm<<<(T + kBM - 1) / kBM, kGThreads, smem_r, st>>>(gr);
+  k_router_gemm<<<dim3((T + kBM - 1) / kBM, (E + kRN - 1) / kRN), kRThreads, smem_r, st>>>(ra);
 
-  // 2 top-k + bitmaps, 3 scan + tile lists, 4 scatter + quantise
+  // 2 top-k + bitmaps, 3 scan + item lists, 4 scatter + quantise (+ out = x)
   k_topk<<<(T + 7) / 8, 256, 0, st>>>(r);
   ScanArgs sc;
   sc.r = r;
@@ -775,13 +870,12 @@ cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st) {
   sc.H = H; sc.F = F; sc.Fs = Fs;
   k_scan<<<1, 1024, 0, st>>>(sc);
   ScatterArgs sa;
-  sa.r = r; sa.x = a.x; sa.H = H;
-  sa.pos_of_pair = reinterpret_cast<int32_t*>(at(L.pos));
-  sa.order = reinterpret_cast<int32_t*>(at(L.order));
+  sa.r = r; sa.x = a.x; sa.out = a.out; sa.H = H;
+  sa.order_pad = reinterpret_cast<int32_t*>(at(L.order));
   sa.order_out = a.order_out;
-  sa.xq_codes = reinterpret_cast<uint8_t*>(at(L.xq_c)); sa.xq_scales = reinterpret_cast<uint8_t*>(at(L.xq_s));
-  sa.xp_codes = reinterpret_cast<uint8_t*>(at(L.xp_c)); sa.xp_scales = reinterpret_cast<uint8_t*>(at(L.xp_s));
-  k_scatter_quant<<<(int)((P + 7) / 8), 256, 0, st>>>(sa);
+  sa.xq_codes = reinterpret_cast<uint8_t*>(at(L.xq_c)); sa.xq_sf = reinterpret_cast<uint8_t*>(at(L.xq_s));
+  sa.xp_codes = reinterpret_cast<uint8_t*>(at(L.xp_c)); sa.xp_sf = reinterpret_cast<uint8_t*>(at(L.xp_s));
+  k_scatter_quant<<<(T + 7) / 8, 256, 0, st>>>(sa);
 
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -790,51 +884,43 @@ cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st) {
   // 5 gate/up grouped GEMM
   GemmArgs gu;
   memset(&gu, 0, sizeof(gu));
-  bool ok = make_map(&gu.mapA[0], sa.xq_codes, T, H / 2, 128) && make_map(&gu.mapA[1], sa.xp_codes, PP, H / 2, 128) &&
-            make_map(&gu.mapB[0], a.sh_gate.codes, Fs, H / 2, 128) && make_map(&gu.mapB[1], a.sh_up.codes, Fs, H / 2, 128) &&
-            make_map(&gu.mapB[2], a.gate.codes, (uint64_t)E * F, H / 2, 128) &&
-            make_map(&gu.mapB[3], a.up.codes, (uint64_t)E * F, H / 2, 128);
+  bool ok = make_map(&gu.mapA[0], sa.xq_codes, Tp, H / 2, kBM) && make_map(&gu.mapA[1], sa.xp_codes, Pp, H / 2, kBM) &&
+            make_map(&gu.mapB[0], a.sh_gate.codes, Fs, H / 2, kBN) && make_map(&gu.mapB[1], a.sh_up.codes, Fs, H / 2, kBN) &&
+            make_map(&gu.mapB[2], a.gate.codes, (uint64_t)E * F, H / 2, kBN) &&
+            make_map(&gu.mapB[3], a.up.codes, (uint64_t)E * F, H / 2, kBN);
   if (!ok) return cudaErrorInvalidValue;
-  gu.sclA[0] = sa.xq_scales; gu.sclA[1] = sa.xp_scales;
-  gu.rowsA[0] = T; gu.rowsA[1] = (int)PP;
-  gu.sclB[0] = a.sh_gate.scales; gu.sclB[1] = a.sh_up.scales; gu.sclB[2] = a.gate.scales; gu.sclB[3] = a.up.scales;
+  gu.sfA[0] = sa.xq_sf; gu.sfA[1] = sa.xp_sf;
+  gu.sfB[0] = a.sf[3]; gu.sfB[1] = a.sf[4]; gu.sfB[2] = a.sf[0]; gu.sfB[3] = a.sf[1];
   gu.Kel[0] = H; gu.Kel[1] = H;
   gu.rowsB[0] = Fs; gu.rowsB[1] = F;
-  gu.items = sc.items_gu; gu.n_items = sc.n_items_gu; gu.item_begin = 0; gu.item_end_host = -1;
+  gu.items = sc.items_gu; gu.n_items = sc.n_items_gu;
   gu.tscA[0] = a.sh_gate.tsc; gu.tscA[1] = a.gate.tsc; gu.tscB[0] = a.sh_up.tsc; gu.tscB[1] = a.up.tsc;
-  gu.hcodes[0] = reinterpret_cast<uint8_t*>(at(L.hs_c)); gu.hscales[0] = reinterpret_cast<uint8_t*>(at(L.hs_s));
-  gu.hcodes[1] = reinterpret_cast<uint8_t*>(at(L.hq_c)); gu.hscales[1] = reinterpret_cast<uint8_t*>(at(L.hq_s));
+  gu.hcodes[0] = reinterpret_cast<uint8_t*>(at(L.hs_c)); gu.hsf[0] = reinterpret_cast<uint8_t*>(at(L.hs_s));
+  gu.hcodes[1] = reinterpret_cast<uint8_t*>(at(L.hq_c)); gu.hsf[1] = reinterpret_cast<uint8_t*>(at(L.hq_s));
   gu.Fout[0] = Fs; gu.Fout[1] = F;
-  gu.H = H; gu.K = K; gu.T = T; gu.E = E;
-  const int smem_gu = kStages * StageLayout<kGateUp>::stride + 1024;
-  e = cudaFuncSetAttribute(k_gemm_fp4<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_gu);
+  gu.H = H; gu.K = K;
+  e = cudaFuncSetAttribute(k_gemm_fp4<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kGateUp>::smem);
   if (e != cudaSuccess) return e;
-  k_gemm_fp4<kGateUp><<<sms, kGThreads, smem_gu, st>>>(gu);
+  k_gemm_fp4<kGateUp><<<sms, kGThreads, Cfg<kGateUp>::smem, st>>>(gu);
 
-  // 6 down grouped GEMM: shared items (write out = x + y), then routed (red.add)
+  // 6 down grouped GEMM over the shared and routed tiles: out += rows (bulk reduce-add)
   GemmArgs dn;
   memset(&dn, 0, sizeof(dn));
-  ok = make_map(&dn.mapA[0], gu.hcodes[0], T, Fs / 2, 128) && make_map(&dn.mapA[1], gu.hcodes[1], PP, F / 2, 128) &&
-       make_map(&dn.mapB[0], a.sh_down.codes, H, Fs / 2, 128) &&
-       make_map(&dn.mapB[2], a.down.codes, (uint64_t)E * H, F / 2, 128);
+  ok = make_map(&dn.mapA[0], gu.hcodes[0], Tp, Fs / 2, kBM) && make_map(&dn.mapA[1], gu.hcodes[1], Pp, F / 2, kBM) &&
+       make_map(&dn.mapB[0], a.sh_down.codes, H, Fs / 2, kBN) &&
+       make_map(&dn.mapB[2], a.down.codes, (uint64_t)E * H, F / 2, kBN);
   if (!ok) return cudaErrorInvalidValue;
-  dn.sclA[0] = gu.hscales[0]; dn.sclA[1] = gu.hscales[1];
-  dn.rowsA[0] = T; dn.rowsA[1] = (int)PP;
-  dn.sclB[0] = a.sh_down.scales; dn.sclB[2] = a.down.scales;
+  dn.sfA[0] = gu.hsf[0]; dn.sfA[1] = gu.hsf[1];
+  dn.sfB[0] = a.sf[5]; dn.sfB[2] = a.sf[2];
   dn.Kel[0] = Fs; dn.Kel[1] = F;
   dn.rowsB[0] = H; dn.rowsB[1] = H;
   dn.items = sc.items_dn; dn.n_items = sc.n_items_dn;
   dn.tscA[0] = a.sh_down.tsc; dn.tscA[1] = a.down.tsc;
-  dn.x = a.x; dn.out = a.out; dn.order = sa.order; dn.wpair = r.w;
-  dn.H = H; dn.K = K; dn.T = T; dn.E = E;
-  const int smem_dn = kStages * StageLayout<kDown>::stride + 1024;
-  e = cudaFuncSetAttribute(k_gemm_fp4<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_dn);
+  dn.out = a.out; dn.order = sa.order_pad; dn.wpair = r.w;
+  dn.H = H; dn.K = K;
+  e = cudaFuncSetAttribute(k_gemm_fp4<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kDown>::smem);
   if (e != cudaSuccess) return e;
-  const int n_sh_dn = (T + kBM - 1) / kBM * (H / kBN);
-  dn.item_begin = 0; dn.item_end_host = n_sh_dn;
-  k_gemm_fp4<kDown><<<sms, kGThreads, smem_dn, st>>>(dn);
-  dn.item_begin = n_sh_dn; dn.item_end_host = -1;
-  k_gemm_fp4<kDown><<<sms, kGThreads, smem_dn, st>>>(dn);
+  k_gemm_fp4<kDown><<<sms, kGThreads, Cfg<kDown>::smem, st>>>(dn);
   return cudaGetLastError();
 }
 

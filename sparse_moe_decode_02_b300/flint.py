@@ -47,12 +47,13 @@ class _LayerC(ctypes.Structure):
                 ("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
                 ("gate", _NVFP4C), ("up", _NVFP4C), ("down", _NVFP4C),
                 ("sh_gate", _NVFP4C), ("sh_up", _NVFP4C), ("sh_down", _NVFP4C),
-                ("down_cc", _CCC), ("sh_down_cc", _CCC)]
+                ("down_cc", _CCC), ("sh_down_cc", _CCC), ("mma_scales", ctypes.c_void_p * 6)]
 
 
 _lib = None
 
 _SYMBOLS = ["flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_nvfp4_column_chunks",
+            "flint_nvfp4_mma_scales",
             "flint_moe_decode", "flint_decode_tokens", "flint_moe_prefill", "flint_lm_head",
             "flint_workspace_bytes", "flint_last_device_status", "flint_status_string",
             "flint_version"]
@@ -71,6 +72,7 @@ def lib() -> ctypes.CDLL:
     L.flint_quantize_nvfp4.argtypes = [vp, i, i, i, vp, vp, vp, vp, sz, vp]
     L.flint_dequantize_nvfp4.argtypes = [ctypes.POINTER(_NVFP4C), vp, vp]
     L.flint_nvfp4_column_chunks.argtypes = [ctypes.POINTER(_NVFP4C), vp, vp, vp]
+    L.flint_nvfp4_mma_scales.argtypes = [ctypes.POINTER(_NVFP4C), vp, vp]
     L.flint_decode_tokens.argtypes = [ctypes.POINTER(_LayerC), i, ctypes.POINTER(_NVFP4C), vp, vp,
                                       i, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.flint_decode_tokens_noalloc.argtypes = [ctypes.POINTER(_LayerC), i, ctypes.POINTER(_NVFP4C),
@@ -88,7 +90,7 @@ def lib() -> ctypes.CDLL:
     L.flint_status_string.restype = ctypes.c_char_p
     L.flint_version.restype = ctypes.c_char_p
     for name in ("flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_nvfp4_column_chunks",
-                 "flint_moe_decode", "flint_decode_tokens", "flint_decode_tokens_noalloc",
+                 "flint_nvfp4_mma_scales", "flint_moe_decode", "flint_decode_tokens", "flint_decode_tokens_noalloc",
                  "flint_moe_prefill", "flint_lm_head", "flint_last_device_status"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -155,6 +157,7 @@ class MoELayer:
     top_k: int
     down_cc: tuple | None = None      # (codes, scales) column-chunk copy of down
     sh_down_cc: tuple | None = None   # (codes, scales) column-chunk copy of sh_down
+    mma_scales: tuple | None = None   # MMA scale copies of gate, up, down, sh_gate, sh_up, sh_down
 
     @property
     def dims(self):
@@ -164,10 +167,12 @@ class MoELayer:
     def c(self) -> _LayerC:
         H, E, k, F, Fs = self.dims
         cc = lambda t: _CCC(None, None) if t is None else _CCC(t[0].data_ptr(), t[1].data_ptr())
+        sf = (ctypes.c_void_p * 6)(*([None] * 6 if self.mma_scales is None else
+                                     [m.data_ptr() for m in self.mma_scales]))
         return _LayerC(H, E, k, F, Fs, self.router_w.data_ptr(),
                        None if self.router_bias is None else self.router_bias.data_ptr(),
                        self.gate.c(), self.up.c(), self.down.c(), self.sh_gate.c(),
-                       self.sh_up.c(), self.sh_down.c(), cc(self.down_cc), cc(self.sh_down_cc))
+                       self.sh_up.c(), self.sh_down.c(), cc(self.down_cc), cc(self.sh_down_cc), sf)
 
     def nbytes(self) -> int:
         return (self.router_w.numel() * 2 + sum(m.nbytes() for m in (
@@ -201,6 +206,15 @@ def nvfp4_column_chunks(m: NVFP4, stream=None):
     _check(lib().flint_nvfp4_column_chunks(ctypes.byref(mc), _ptr(codes), _ptr(scales),
                                            _stream(stream)), "flint_nvfp4_column_chunks")
     return codes, scales
+
+
+def nvfp4_mma_scales(m: NVFP4, stream=None) -> torch.Tensor:
+    """MMA scale copy of an NVFP4 stack's block scales (see flint.h)."""
+    out = torch.empty_like(m.scales)
+    mc = m.c()
+    _check(lib().flint_nvfp4_mma_scales(ctypes.byref(mc), _ptr(out), _stream(stream)),
+           "flint_nvfp4_mma_scales")
+    return out
 
 
 def dequantize_nvfp4(m: NVFP4, stream=None) -> torch.Tensor:

@@ -23,11 +23,17 @@ def build_layer(spec: synth.LayerSpec, device="cuda", stream=None) -> flint.MoEL
     router = spec.weights_bf16(synth.KIND_ROUTER, device=device)[0].contiguous()
     bias = spec.bias()
     bias_t = None if bias is None else torch.from_numpy(bias).to(device)
-    down, sh_down = q(synth.KIND_DOWN), q(synth.KIND_SH_DOWN)
-    return flint.MoELayer(router, bias_t, q(synth.KIND_GATE), q(synth.KIND_UP), down,
-                          q(synth.KIND_SH_GATE), q(synth.KIND_SH_UP), sh_down, s.top_k,
+    gate, up, down = q(synth.KIND_GATE), q(synth.KIND_UP), q(synth.KIND_DOWN)
+    sh_gate, sh_up, sh_down = q(synth.KIND_SH_GATE), q(synth.KIND_SH_UP), q(synth.KIND_SH_DOWN)
+    stacks = (gate, up, down, sh_gate, sh_up, sh_down)
+    # the prompt path's MMA scale copies exist for 128-row, 64-column multiples
+    mma = None
+    if all(m.shape[1] % 128 == 0 and m.shape[2] % 64 == 0 for m in stacks):
+        mma = tuple(flint.nvfp4_mma_scales(m, stream=stream) for m in stacks)
+    return flint.MoELayer(router, bias_t, gate, up, down, sh_gate, sh_up, sh_down, s.top_k,
                           down_cc=flint.nvfp4_column_chunks(down, stream=stream),
-                          sh_down_cc=flint.nvfp4_column_chunks(sh_down, stream=stream))
+                          sh_down_cc=flint.nvfp4_column_chunks(sh_down, stream=stream),
+                          mma_scales=mma)
 
 
 def build_head(seed: int, vocab: int, hidden: int, device="cuda", stream=None) -> flint.NVFP4:

@@ -228,6 +228,17 @@ def test_column_chunks_bitexact():
                                   scales.transpose(0, 2, 1))
 
 
+def test_mma_scales_bitexact():
+    w = synth.normal_bf16(synth.tensor_key(10), 2 * 256 * 512, 0.02).view(2, 256, 512).to(DEV)
+    m = flint.quantize_nvfp4(w)
+    sf = flint.nvfp4_mma_scales(m).cpu().numpy().reshape(2, 2, 8, 512)   # [m][row tile][k64][512]
+    scales = m.scales.cpu().numpy().reshape(2, 2, 128, 8, 4)              # [m][rt][i][k64][j]
+    i = np.arange(128)
+    for j in range(4):
+        got = sf[:, :, :, 16 * (i % 32) + 4 * (i // 32) + j]              # [m][rt][k64][i]
+        np.testing.assert_array_equal(got, scales[:, :, :, :, j].transpose(0, 1, 3, 2))
+
+
 def _chain_case(orc, shape, n_layers, T, seed, zipf, with_head):
     """GPU: one flint_decode_tokens launch over n_layers (+ head), and the same chain one
     layer at a time (flint_moe_decode).  Each layer of the one-at-a-time chain is checked

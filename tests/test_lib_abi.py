@@ -54,10 +54,10 @@ def _nv(n, r, c, codes=FAKE):
     return flint._NVFP4C(codes, FAKE, FAKE, n, r, c)
 
 
-def _layer(H=256, E=16, k=2, F=64, Fs=128, router=FAKE, gate_cols=None, cc=FAKE):
+def _layer(H=256, E=16, k=2, F=64, Fs=128, router=FAKE, gate_cols=None, cc=FAKE, sf=FAKE):
     return flint._LayerC(H, E, k, F, Fs, router, None, _nv(E, F, gate_cols or H), _nv(E, F, H),
                          _nv(E, H, F), _nv(1, Fs, H), _nv(1, Fs, H), _nv(1, H, Fs),
-                         flint._CCC(cc, cc), flint._CCC(cc, cc))
+                         flint._CCC(cc, cc), flint._CCC(cc, cc), (ctypes.c_void_p * 6)(*[sf] * 6))
 
 
 def test_quantize_argument_checks(L):
@@ -123,6 +123,31 @@ def test_column_chunks_argument_checks(L):
     assert cc(ctypes.byref(m), FAKE, FAKE, None) == 3                   # cols % 32
     m2 = _nv(2, 64, 128)
     assert cc(ctypes.byref(m2), FAKE_MIS, FAKE, None) == 2
+
+
+def test_mma_scales_argument_checks(L):
+    ms = L.flint_nvfp4_mma_scales
+    assert ms(None, FAKE, None) == 1
+    assert ms(ctypes.byref(_nv(2, 128, 256)), None, None) == 1
+    assert ms(ctypes.byref(_nv(2, 64, 256)), FAKE, None) == 3             # rows % 128
+    assert ms(ctypes.byref(_nv(2, 128, 96)), FAKE, None) == 3             # cols % 64
+    assert ms(ctypes.byref(_nv(2, 128, 256)), FAKE_MIS, None) == 2
+
+
+def test_prefill_argument_checks(L):
+    p = L.flint_moe_prefill
+    H, E, k, F, Fs, T = 512, 32, 4, 256, 256, 64
+    ws = flint.workspace_bytes(flint.OP_MOE_PREFILL, H, E, k, F, Fs, 0, T)
+    good = _layer(H, E, k, F, Fs)
+    assert p(None, FAKE, FAKE, None, None, None, None, T, FAKE, ws, None) == 1
+    assert p(ctypes.byref(good), FAKE, FAKE, None, None, None, None, 0, FAKE, ws, None) == 1
+    assert p(ctypes.byref(_layer(H, E, k, F, Fs, sf=0)), FAKE, FAKE, None, None, None, None, T,
+             FAKE, ws, None) == 1                                          # no MMA scale copies
+    assert p(ctypes.byref(_layer(H, E, k, F, Fs, sf=FAKE_MIS)), FAKE, FAKE, None, None, None,
+             None, T, FAKE, ws, None) == 2
+    assert p(ctypes.byref(_layer(256, 16, 2, 64, 128)), FAKE, FAKE, None, None, None, None, T,
+             FAKE, ws, None) == 8                                          # F % 256
+    assert p(ctypes.byref(good), FAKE, FAKE, None, None, None, None, T, FAKE, 16, None) == 4
 
 
 def test_lm_head_argument_checks(L):
