@@ -43,8 +43,10 @@ constexpr int kPThreads = 32 * kPWarps;
 constexpr int kUnit = 8;            // SwiGLU outputs per unit (one 8-column chunk of down)
 constexpr int kMaxRouterRows = kPThreads / 64;   // router rows per CTA (64 threads each)
 constexpr int kMaxRoutedUnits = 6;  // routed units per CTA and step
+constexpr int kMaxSharedUnits = 4;  // shared units per CTA
+constexpr int kMaxUnits = kMaxRoutedUnits + kMaxSharedUnits;
 constexpr size_t kMaxDecodeSmem = 220 * 1024;
-constexpr int kMaxCtas = 1024;
+constexpr int kMaxCtas = 512;
 // Sync words, each on its own 128-byte line.
 constexpr int kSyncDone = 32, kSyncHead = 64, kSyncAbort = 96;
 constexpr int kSyncWords = 128;
@@ -60,7 +62,7 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
 }
 
 // Thread 0 spins (bounded) until *cnt >= target; the CTA then proceeds together.
-__device__ __forceinline__ void wait_count(unsigned* sync, int which, unsigned target) {
+__device__ __noinline__ void wait_count(unsigned* sync, int which, unsigned target) {
   if (threadIdx.x == 0) {
     const unsigned* cnt = sync + which;
     unsigned polls = 0;
@@ -91,15 +93,15 @@ __device__ __forceinline__ void signal_count(unsigned* sync, int which) {
   }
 }
 
-// Router logits travel as tagged 64-bit words {value bits, step + 1}: the writer's
-// release store publishes everything the CTA wrote before (the residual copy); a
-// reader that sees its tag needs no counter.  The tags are cleared before each launch.
-__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+// Router logits travel as tagged 64-bit words {value bits, step + 1}; a reader that
+// sees its tag has the value written with it (one single-copy-atomic word), so no
+// counter and no fence are needed.  The tags are cleared before each launch.
+__device__ __forceinline__ void st_tagged(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
   unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 // Waits (bounded) until *p carries `tag` and returns its value.
@@ -107,7 +109,7 @@ __device__ __forceinline__ float wait_tagged(const unsigned long long* p, unsign
   unsigned polls = 0;
   unsigned long long t0 = 0;
   for (;;) {
-    const unsigned long long v = ld_acquire_u64(p);
+    const unsigned long long v = ld_relaxed_u64(p);
     if ((unsigned)(v >> 32) == tag) return __uint_as_float((unsigned)v);
     if ((++polls & 63u) == 0) {
       if (ld_acquire_gpu(sync + kSyncAbort)) return 0.f;
@@ -147,7 +149,7 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for a bulk-copy phase; on expiry records FLINT_ERR_TIMEOUT.
-__device__ __forceinline__ void mbar_wait(uint64_t* b, uint32_t parity, unsigned* sync) {
+__device__ __noinline__ void mbar_wait(uint64_t* b, uint32_t parity, unsigned* sync) {
   unsigned long long t0 = 0;
   unsigned polls = 0;
   while (!mbar_try(b, parity)) {
@@ -169,38 +171,43 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 }
 
 // ---------------------------------------------------------------- activation staging
-// x_l is built once per CTA (thread t owns elements [4t, 4t+4); H <= 4 * 512):
-//   h    fp32 residual (global, L2) -> s_hx (kept for the residual copy)
-//   x    bf16(h * r), r = 1/sqrt(mean(h^2) + eps)  (r = 1 for a layer-0 input, which
-//        is bf16 already)                            -> s_xb
-//   xf   f16(x * 2^k), the GEMV operand; 2^k puts max|x| in [2^14, 2^15) -> s_xf
+// x_l is built once per CTA (thread t owns elements [4t, 4t+4); H <= 4 * 512).  Every
+// CTA keeps the residual h_l in s_hx, bit-identical across CTAs:
+//   layer 0:   x_0 = x[t] (bf16, used as is); h_0 = residual[t], or x[t]
+//   layer l:   h_l = h_{l-1} + sum of the accumulator copies (fixed order);
+//              x_l = bf16(h_l * r), r = 1/sqrt(mean(h_l^2) + eps)
+// and the GEMV operand xf = f16(x_l * 2^k), 2^k putting max|x_l| in [2^14, 2^15).
 // Sum of squares and max|h| come from one fixed-order block reduction, so every CTA
 // derives the same r and k (max|bf16(h r)| = bf16(max|h| r): rounding is monotone).
 struct Staged {
   float unscale;    // 2^-k
 };
 
-__device__ __forceinline__ Staged cta_stage(const float* h_f32, const uint16_t* x_bf16, int H,
-                                            float eps, float* s_hx, uint16_t* s_xb,
-                                            uint16_t* s_xf, float* s_red) {
+__device__ __noinline__ Staged cta_stage(const float* acc, const uint16_t* x_bf16,
+                                            const float* residual, int H, float eps, float* s_hx,
+                                            uint16_t* s_xb, uint16_t* s_xf, float* s_red) {
   const int n = 4 * threadIdx.x;
   const bool own = n < H;
   float v[4] = {0.f, 0.f, 0.f, 0.f};
   if (own) {
-    if (h_f32) {
-      // h = copy 0 + copy 1 + ... (fixed order: every CTA gets the same bits)
+    if (acc) {
       float4 f[kAccCopies];
 #pragma unroll
-      for (int c = 0; c < kAccCopies; ++c) f[c] = __ldcg(reinterpret_cast<const float4*>(h_f32 + c * H + n));
-      v[0] = f[0].x; v[1] = f[0].y; v[2] = f[0].z; v[3] = f[0].w;
+      for (int c = 0; c < kAccCopies; ++c) f[c] = __ldcg(reinterpret_cast<const float4*>(acc + c * H + n));
+      const float4 h = *reinterpret_cast<const float4*>(s_hx + n);
+      v[0] = h.x; v[1] = h.y; v[2] = h.z; v[3] = h.w;
 #pragma unroll
-      for (int c = 1; c < kAccCopies; ++c) { v[0] += f[c].x; v[1] += f[c].y; v[2] += f[c].z; v[3] += f[c].w; }
+      for (int c = 0; c < kAccCopies; ++c) { v[0] += f[c].x; v[1] += f[c].y; v[2] += f[c].z; v[3] += f[c].w; }
+      *reinterpret_cast<float4*>(s_hx + n) = make_float4(v[0], v[1], v[2], v[3]);
     } else {
       const uint2 b = __ldcg(reinterpret_cast<const uint2*>(x_bf16 + n));
       v[0] = bf16_bits_to_f32(b.x & 0xFFFFu); v[1] = bf16_bits_to_f32(b.x >> 16);
       v[2] = bf16_bits_to_f32(b.y & 0xFFFFu); v[3] = bf16_bits_to_f32(b.y >> 16);
+      *reinterpret_cast<float4*>(s_hx + n) =
+          residual ? make_float4(__ldcg(residual + n), __ldcg(residual + n + 1), __ldcg(residual + n + 2),
+                                 __ldcg(residual + n + 3))
+                   : make_float4(v[0], v[1], v[2], v[3]);
     }
-    *reinterpret_cast<float4*>(s_hx + n) = make_float4(v[0], v[1], v[2], v[3]);
   }
   float ss = 0.f, am = 0.f;
 #pragma unroll
@@ -213,7 +220,7 @@ __device__ __forceinline__ Staged cta_stage(const float* h_f32, const uint16_t* 
   float tot = 0.f, amax = 0.f;
 #pragma unroll
   for (int w = 0; w < kPWarps; ++w) { tot += s_red[w]; amax = fmaxf(amax, s_red[kPWarps + w]); }
-  const float r = h_f32 ? 1.0f / sqrtf(tot / (float)H + eps) : 1.0f;
+  const float r = acc ? 1.0f / sqrtf(tot / (float)H + eps) : 1.0f;
   const float xmax = bf16_bits_to_f32(f32_to_bf16_rn(amax * r));
   const int k = f16_stage_exponent(xmax);
   const float s = exp2i(k);
@@ -293,30 +300,33 @@ struct UnitLayout {
 // up scales, down codes, down scales): gate/up rows [row0, row0 + 8) of the stacks,
 // down code chunk `chunk` and scale block chunk / 2 of matrix `m`.  The six pieces are
 // issued by six lanes at once; the mbarrier's expected bytes are set beforehand.
-__device__ __forceinline__ void unit_copy_piece(int piece, uint8_t* buf, uint64_t* bar, int H,
+__device__ __noinline__ void unit_copy_piece(int piece, uint8_t* buf, uint64_t* bar, int H,
                                                 const NVPtr& gate, const NVPtr& up,
                                                 const uint8_t* dcc_codes, const uint8_t* dcc_scales,
                                                 size_t row0, size_t m, int chunks_per_mat, int chunk) {
   const UnitLayout L = UnitLayout::of(H);
-  switch (piece) {
-    case 0: bulk_g2s(buf + L.gc, gate.codes + row0 * (H / 2), kUnit * (H / 2), bar); break;
-    case 1: bulk_g2s(buf + L.gs, gate.scales + row0 * (H / 16), kUnit * (H / 16), bar); break;
-    case 2: bulk_g2s(buf + L.uc, up.codes + row0 * (H / 2), kUnit * (H / 2), bar); break;
-    case 3: bulk_g2s(buf + L.us, up.scales + row0 * (H / 16), kUnit * (H / 16), bar); break;
-    case 4: bulk_g2s(buf + L.dc, dcc_codes + (m * chunks_per_mat + chunk) * H * 4, H * 4, bar); break;
-    default: bulk_g2s(buf + L.ds, dcc_scales + (m * (chunks_per_mat / 2) + chunk / 2) * H, H, bar); break;
+  const NVPtr& gu = piece < 2 ? gate : up;
+  const bool sc = piece & 1;
+  const uint8_t* src;
+  uint32_t dst, bytes;
+  if (piece < 4) {
+    src = sc ? gu.scales + row0 * (H / 16) : gu.codes + row0 * (H / 2);
+    dst = piece == 0 ? L.gc : piece == 1 ? L.gs : piece == 2 ? L.uc : L.us;
+    bytes = sc ? kUnit * (H / 16) : kUnit * (H / 2);
+  } else {
+    src = sc ? dcc_scales + (m * (chunks_per_mat / 2) + chunk / 2) * H
+             : dcc_codes + (m * chunks_per_mat + chunk) * H * 4;
+    dst = sc ? L.ds : L.dc;
+    bytes = sc ? H : H * 4;
   }
+  bulk_g2s(buf + dst, src, bytes, bar);
 }
 
-// One unit from shared memory: the 16 gate/up row dot products (a warp per row), the 8
-// SwiGLU values, then this thread's 4 down rows [4t, 4t + 4) times wgt, added into
-// part[].  The buffer stays in use until the caller's next CTA barrier; consecutive
-// calls must alternate the s_gu / s_hs scratch.
+// Gate/up of one unit from shared memory: the 16 row dot products (a warp per row),
+// with tensor scales and 2^-k applied, into s_gu[0..16).  No barrier.
 template <int CPL>
-__device__ __forceinline__ void unit_compute(const uint8_t* buf, int H, float gate_tsc,
-                                             float up_tsc, float down_tsc, float wgt,
-                                             const XStage<CPL, 1>& xs, float* s_gu,
-                                             uint32_t* s_hs, float (&part)[4]) {
+__device__ __noinline__ void unit_gateup(const uint8_t* buf, int H, float gate_tsc, float up_tsc,
+                                            const XStage<CPL, 1>& xs, float* s_gu) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int LPR = H / (32 * CPL), RPP = 32 / LPR;
   const int slice = lane / LPR, sl = lane % LPR;
@@ -332,50 +342,60 @@ __device__ __forceinline__ void unit_compute(const uint8_t* buf, int H, float ga
     const float v = sum_lanes_rt(dot_row<CPL, 1>(w, xs), LPR);
     if (sl == 0 && r < 2 * kUnit) s_gu[r] = v * (is_up ? up_tsc : gate_tsc) * xs.unscale;
   }
-  __syncthreads();
-  // SwiGLU values, computed once by lanes 0-7 of warp 0 and staged as hi/lo f16 pairs
-  // scaled by 2^k: s_hs[0..3] hi pairs, s_hs[4..7] lo pairs, s_hs[8] the down scale.
-  if (warp == 0) {
-    const float hj = lane < kUnit ? silu(s_gu[lane]) * s_gu[kUnit + (lane & (kUnit - 1))] : 0.f;
+}
+
+// SwiGLU values of n units (warp 0; lane 8u + j holds output j of unit u), staged as
+// hi/lo f16 pairs scaled by 2^k per unit: s_hs[u][0..4) hi pairs, [4..8) lo pairs,
+// [8] the unit's down scale (down tensor scale x routing weight x 2^-k).
+__device__ __noinline__ void stage_swiglu(int n, const float* s_gu, const float* s_dscale,
+                                             uint32_t* s_hs) {
+  const int lane = threadIdx.x & 31;
+  for (int u0 = 0; u0 < n; u0 += 32 / kUnit) {
+    const int u = u0 + lane / kUnit, j = lane % kUnit;
+    const bool live = u < n;
+    const float hj = live ? silu(s_gu[u * 2 * kUnit + j]) * s_gu[u * 2 * kUnit + kUnit + j] : 0.f;
     float amax = fabsf(hj);
 #pragma unroll
     for (int o = kUnit / 2; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const int k = f16_stage_exponent(amax);
     const float v = hj * exp2i(k);
     const float w = __shfl_down_sync(0xffffffffu, v, 1);      // the odd partner
-    if (lane < kUnit && (lane & 1) == 0) {
+    if (live && (j & 1) == 0) {
       const uint32_t hi = pack_f16x2_rn(v, w);
       float ha, hb;
       f16x2_to_f32x2(hi, ha, hb);
-      s_hs[lane / 2] = hi;
-      s_hs[kUnit / 2 + lane / 2] = pack_f16x2_rn(v - ha, w - hb);
+      s_hs[u * (kUnit + 1) + j / 2] = hi;
+      s_hs[u * (kUnit + 1) + kUnit / 2 + j / 2] = pack_f16x2_rn(v - ha, w - hb);
     }
-    if (lane == 0) s_hs[kUnit] = __float_as_uint(down_tsc * exp2i(-k) * wgt);
+    if (live && j == 0) s_hs[u * (kUnit + 1) + kUnit] = __float_as_uint(s_dscale[u] * exp2i(-k));
   }
-  __syncthreads();
+}
+
+// Down contributions of one unit to this thread's rows [4t, 4t + 4), added into part[].
+__device__ __noinline__ void unit_down(const uint8_t* buf, int H, const uint32_t* hs, float (&part)[4]) {
+  const UnitLayout U = UnitLayout::of(H);
+  const int n0 = 4 * threadIdx.x;
+  if (n0 >= H) return;
   uint32_t hh[kUnit / 2], hl[kUnit / 2];
 #pragma unroll
-  for (int q = 0; q < kUnit / 2; ++q) { hh[q] = s_hs[q]; hl[q] = s_hs[kUnit / 2 + q]; }
-  const float scale = __uint_as_float(s_hs[kUnit]);
-  const int n0 = 4 * threadIdx.x;
-  if (n0 < H) {
-    const uint4 cw = *reinterpret_cast<const uint4*>(buf + U.dc + 4 * n0);
-    const uint32_t sw = *reinterpret_cast<const uint32_t*>(buf + U.ds + n0);
-    const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
+  for (int q = 0; q < kUnit / 2; ++q) { hh[q] = hs[q]; hl[q] = hs[kUnit / 2 + q]; }
+  const float scale = __uint_as_float(hs[kUnit]);
+  const uint4 cw = *reinterpret_cast<const uint4*>(buf + U.dc + 4 * n0);
+  const uint32_t sw = *reinterpret_cast<const uint32_t*>(buf + U.ds + n0);
+  const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t f[4];
-      e2m1x8_to_f16x2x4(wv[q], f[0], f[1], f[2], f[3]);
-      float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+  for (int q = 0; q < 4; ++q) {
+    uint32_t f[4];
+    e2m1x8_to_f16x2x4(wv[q], f[0], f[1], f[2], f[3]);
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        fma2_f16(a0, a1, f[i], hh[i]);
-        fma2_f16(b0, b1, f[i], hl[i]);
-      }
-      float s0, s1;
-      f16x2_to_f32x2(e4m3x2_to_f16x2((sw >> (8 * q)) & 0xFFu), s0, s1);
-      part[q] = fmaf((a0 + a1) + (b0 + b1), s0 * scale, part[q]);
+    for (int i = 0; i < 4; ++i) {
+      fma2_f16(a0, a1, f[i], hh[i]);
+      fma2_f16(b0, b1, f[i], hl[i]);
     }
+    float s0, s1;
+    f16x2_to_f32x2(e4m3x2_to_f16x2((sw >> (8 * q)) & 0xFFu), s0, s1);
+    part[q] = fmaf((a0 + a1) + (b0 + b1), s0 * scale, part[q]);
   }
 }
 
@@ -519,6 +539,16 @@ __device__ __forceinline__ void topk_per(const float* logits, int E, int K, int*
   topk_exact<PER>(logits, E, K, s_sel, s_w);
 }
 
+__device__ __forceinline__ void topk_exact_dispatch(const float* logits, int E, int K, int* s_sel,
+                                                    float* s_w) {
+  const int per_lane = (E + 31) / 32;
+  if (per_lane <= 1) topk_exact<1>(logits, E, K, s_sel, s_w);
+  else if (per_lane <= 2) topk_exact<2>(logits, E, K, s_sel, s_w);
+  else if (per_lane <= 4) topk_exact<4>(logits, E, K, s_sel, s_w);
+  else if (per_lane <= 8) topk_exact<8>(logits, E, K, s_sel, s_w);
+  else topk_exact<16>(logits, E, K, s_sel, s_w);
+}
+
 __device__ __forceinline__ void topk_dispatch(const float* logits, int E, int K, int* s_sel,
                                               float* s_w) {
   const int per_lane = (E + 31) / 32;
@@ -529,9 +559,33 @@ __device__ __forceinline__ void topk_dispatch(const float* logits, int E, int K,
   else topk_per<16>(logits, E, K, s_sel, s_w);
 }
 
+// Packed 32-bit selection key: the order key's upper bits, then (2^ib - 1 - e) in the
+// low ib bits, so larger keys win and equal upper bits go to the lower index.
+__device__ __forceinline__ unsigned packed_key(float l, int e, int ib) {
+  l = (l == l) ? l : -INFINITY;
+  return ((order_key(l) >> ib) << ib) | ((1u << ib) - 1u - (unsigned)e);
+}
+
+// The n best of one key per lane (0 = none; keys are distinct): lane s < n gets the
+// s-th best.  tie: two consecutive winners agree above the index bits (so their
+// order, and possibly the selection, needs the exact path).
+__device__ __forceinline__ unsigned warp_select(unsigned key, int n, int ib, bool& tie) {
+  const int lane = threadIdx.x & 31;
+  unsigned mine = 0u, prev = 0u;
+  tie = false;
+  for (int s = 0; s < n; ++s) {
+    const unsigned w = __reduce_max_sync(0xffffffffu, key);
+    if (s > 0 && w != 0u && (w >> ib) == (prev >> ib)) tie = true;
+    prev = w;
+    if (key == w) key = 0u;
+    if (lane == s) mine = w;
+  }
+  return mine;
+}
+
 // ---------------------------------------------------------------- head
 template <int CPL>
-__device__ __forceinline__ void head_rows(const PersistArgs& a, const XStage<CPL, 1>& xs, int t,
+__device__ __noinline__ void head_rows(const PersistArgs& a, const XStage<CPL, 1>& xs, int t,
                                           float& bv, int& bi) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int LPR = a.H / (32 * CPL), RPP = 32 / LPR;
@@ -572,28 +626,82 @@ __device__ __forceinline__ void best_reduce_warp(float& v, int& i) {
   }
 }
 
+// ---------------------------------------------------------------- copy issue (warp 0)
+// Data-independent copies of a layer for CTA c: its router rows e = c, c + G, ...
+__device__ __noinline__ void issue_router_rows(const LayerPtrs& P, uint8_t* s_router, uint64_t* bar, int H,
+                                               int c, int G, int my_rows) {
+  const int lane = threadIdx.x & 31;
+  if (my_rows == 0) return;
+  if (lane == 0) mbar_expect_tx(bar, (uint32_t)my_rows * H * 2);
+  __syncwarp();
+  if (lane < my_rows)
+    bulk_g2s(s_router + (size_t)lane * H * 2, P.router_w + (size_t)(c + lane * G) * H, H * 2, bar);
+}
+
+// ... and its shared units s = G-1-c, G-1-c + G, ...
+__device__ __noinline__ void issue_shared_units(const LayerPtrs& P, uint8_t* s_static, uint64_t* bar, int H,
+                                                int c, int G, int my_sh, int n_sh) {
+  const int lane = threadIdx.x & 31;
+  if (my_sh == 0) return;
+  const uint32_t ub = UnitLayout::of(H).bytes;
+  if (lane == 0) mbar_expect_tx(bar, (uint32_t)my_sh * ub);
+  __syncwarp();
+  for (int q = lane; q < 6 * my_sh; q += 32) {
+    const int i = q / 6, piece = q % 6;
+    const int su = (G - 1 - c) + i * G;
+    unit_copy_piece(piece, s_static + (size_t)i * ub, bar, H, P.sh_gate, P.sh_up, P.sh_dcc_codes,
+                    P.sh_dcc_scales, (size_t)su * kUnit, 0, n_sh, su);
+  }
+}
+
+// Routed units r = c, c + G, ... of the selected experts s_sel (one mbarrier each).
+__device__ __noinline__ void issue_routed_units(const LayerPtrs& P, uint8_t* s_routed, uint64_t* bars, int H,
+                                                int c, int G, int my_rt, int per_slot, int F, int E,
+                                                const int* s_sel) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t ub = UnitLayout::of(H).bytes;
+  if (lane < my_rt) mbar_expect_tx(&bars[lane], ub);
+  __syncwarp();
+  for (int q = lane; q < 6 * my_rt; q += 32) {
+    const int i = q / 6, piece = q % 6;
+    const int r = c + i * G;
+    const int slot = r / per_slot, j = r % per_slot;
+    int e = s_sel[slot];
+    if (e < 0 || e >= E) { raise_status(FLINT_ERR_INVALID_ARG); e = 0; }
+    unit_copy_piece(piece, s_routed + (size_t)i * ub, &bars[i], H, P.gate, P.up, P.dcc_codes, P.dcc_scales,
+                    (size_t)e * F + (size_t)j * kUnit, (size_t)e, per_slot, j);
+  }
+}
+
 // ---------------------------------------------------------------- the kernel
 // Work of CTA c (of G) in every layer step, all CTAs running the same code:
 //   router rows      e = c, c + G, ...                       (< E)
 //   shared units     s = G-1-c, G-1-c + G, ...               (< Fs/8)
 //   routed units     r = c, c + G, ...                       (< K*F/8)
 // Routed units fill CTAs from the front and shared units from the back, so the
-// busiest CTAs hold at most one unit more than the least busy.  Shared units and
-// router rows do not depend on the data: their copies for the next step are issued as
-// soon as this step has consumed them.
+// busiest CTAs hold at most one unit more than the least busy.  Router rows and
+// shared units do not depend on the data: their copies for the next step are issued
+// as soon as this step has consumed them.
+// Residual accumulators rotate over three buffers: step s adds its down contributions
+// into B(s) = (s + 1) % 3, which the next step's staging reads; B(s + 1) is cleared
+// by step s (each CTA a share), ordered before step s + 1's additions by the done
+// counter.
 template <int CPL>
 __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid_constant__ PersistArgs a) {
-  __shared__ float s_gu[2][2 * kUnit];              // alternating per unit
-  __shared__ uint32_t s_hs[2][kUnit + 1];
+  __shared__ float s_gu[kMaxUnits * 2 * kUnit];
+  __shared__ uint32_t s_hs[kMaxUnits * (kUnit + 1)];
+  __shared__ float s_dscale[kMaxUnits];
   __shared__ float s_rp[kPWarps];
   __shared__ int s_sel[FLINT_MAX_TOP_K];
   __shared__ float s_w[FLINT_MAX_TOP_K];
+  __shared__ unsigned s_cand[(FLINT_MAX_EXPERTS / 32) * (FLINT_MAX_TOP_K + 1)];
+  __shared__ int s_tie;
   __shared__ float s_bv[kPWarps];
   __shared__ int s_bi[kPWarps];
   __shared__ float s_red[2 * kPWarps];
   __shared__ float s_logits[FLINT_MAX_EXPERTS];
   __shared__ float s_bias[kMaxRouterRows];
-  __shared__ __align__(8) uint64_t s_bar_st;
+  __shared__ __align__(8) uint64_t s_bar_rr, s_bar_sh;
   __shared__ __align__(8) uint64_t s_bar_rt[kMaxRoutedUnits];
   extern __shared__ __align__(128) uint8_t s_dyn[];
   const int H = a.H;
@@ -614,72 +722,51 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
   const int my_rows = c < a.E ? (a.E - 1 - c) / G + 1 : 0;
   const int my_sh = (G - 1 - c) < n_sh ? (n_sh - 1 - (G - 1 - c)) / G + 1 : 0;
   const int my_rt = c < n_rt ? (n_rt - 1 - c) / G + 1 : 0;
-  const int n_wait = a.E > G ? a.E : G;             // tags every CTA waits for (see below)
+  const int ib = a.E > 256 ? 9 : 8;                 // index bits of the packed top-k keys
+  const int nw_e = (a.E + 31) / 32;                 // warps that hold logits
   unsigned* sync = a.bar;
-  uint32_t ph_st = 0, ph_rt = 0;                    // mbarrier parities
+  uint32_t ph_rr = 0, ph_sh = 0, ph_rt = 0;         // mbarrier parities
 
   if (threadIdx.x == 0) {
-    mbar_init(&s_bar_st, 1);
+    mbar_init(&s_bar_rr, 1);
+    mbar_init(&s_bar_sh, 1);
     for (int i = 0; i < kMaxRoutedUnits; ++i) mbar_init(&s_bar_rt[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  // Data-independent copies of layer l: this CTA's router rows and shared units, one
-  // copy per lane of warp 0 (the calling warp).
-  const uint32_t static_bytes = (uint32_t)my_rows * H * 2 + (uint32_t)my_sh * U.bytes;
-  auto issue_static = [&](int l) {
-    if (static_bytes == 0) return;
-    const LayerPtrs& P = a.layer[l];
-    if (lane == 0) mbar_expect_tx(&s_bar_st, static_bytes);
-    __syncwarp();
-    for (int q = lane; q < my_rows + 6 * my_sh; q += 32) {
-      if (q < my_rows) {
-        bulk_g2s(s_router + (size_t)q * H * 2, P.router_w + (size_t)(c + q * G) * H, H * 2, &s_bar_st);
-      } else {
-        const int i = (q - my_rows) / 6, piece = (q - my_rows) % 6;
-        const int su = (G - 1 - c) + i * G;
-        unit_copy_piece(piece, s_static + (size_t)i * U.bytes, &s_bar_st, H, P.sh_gate, P.sh_up,
-                        P.sh_dcc_codes, P.sh_dcc_scales, (size_t)su * kUnit, 0, n_sh, su);
-      }
-    }
-  };
-  if (warp == 0) issue_static(0);
+  if (warp == 0) {
+    issue_router_rows(a.layer[0], s_router, &s_bar_rr, H, c, G, my_rows);
+    issue_shared_units(a.layer[0], s_static, &s_bar_sh, H, c, G, my_sh, n_sh);
+  }
 
   unsigned step = 0;                                 // global layer step
   for (int t = 0; t < a.T; ++t) {
     for (int l = 0; l < a.L; ++l, ++step) {
       const LayerPtrs& P = a.layer[l];
-      float* acc_cur = a.acc + (step & 1) * (kAccCopies * H);
-      float* acc_next = a.acc + ((step + 1) & 1) * (kAccCopies * H);
+      float* acc_cur = a.acc + (step % 3) * (kAccCopies * H);         // B(step - 1)
+      float* acc_out = a.acc + ((step + 1) % 3) * (kAccCopies * H);   // B(step)
+      float* acc_clr = a.acc + ((step + 2) % 3) * (kAccCopies * H);   // B(step + 1)
       const int l_next = (l + 1 < a.L) ? l + 1 : 0;
       const bool more = (l + 1 < a.L) || (t + 1 < a.T);
       const unsigned tag = step + 1;
       for (int i = threadIdx.x; i < my_rows; i += kPThreads)
         s_bias[i] = P.router_bias ? __ldg(P.router_bias + c + i * G) : 0.f;
+      if (threadIdx.x == 0) s_tie = 0;               // read after the barriers below
       // ---- h_l complete: stage x_l
       if (step > 0) wait_count(sync, kSyncDone, (unsigned)G * step);
-      const Staged stg = cta_stage(l == 0 ? nullptr : acc_cur, a.x + (size_t)t * H, H, a.eps, s_hx,
-                                   s_xb, s_xf, s_red);
-      // ---- next residual buffers <- (h_l, 0, ...): each CTA a share, published by its tags
-      for (int n = 4 * (c + G * threadIdx.x); n < H; n += 4 * G * kPThreads) {
-        float4 v;
-        if (l == 0 && a.residual) {
-          const float* rp = a.residual + (size_t)t * H + n;
-          v = make_float4(rp[0], rp[1], rp[2], rp[3]);
-        } else {
-          v = *reinterpret_cast<const float4*>(s_hx + n);
-        }
-        *reinterpret_cast<float4*>(acc_next + n) = v;
+      const Staged stg = cta_stage(l == 0 ? nullptr : acc_cur, a.x + (size_t)t * H,
+                                   (l == 0 && a.residual) ? a.residual + (size_t)t * H : nullptr,
+                                   H, a.eps, s_hx, s_xb, s_xf, s_red);
+      // ---- clear this CTA's share of B(step + 1) (published by this step's done signal)
+      for (int n = 4 * (c + G * threadIdx.x); n < H; n += 4 * G * kPThreads)
 #pragma unroll
-        for (int cp = 1; cp < kAccCopies; ++cp)
-          *reinterpret_cast<float4*>(acc_next + cp * H + n) = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      if (static_bytes) { mbar_wait(&s_bar_st, ph_st, sync); ph_st ^= 1; }
-      __syncthreads();                               // residual share written by all threads
-      // ---- router rows -> tagged logits (release: publishes the residual share too).
-      // Row r takes threads [64 r, 64 r + 64): 16-byte pieces of weights and x_l.
+        for (int cp = 0; cp < kAccCopies; ++cp)
+          *reinterpret_cast<float4*>(acc_clr + cp * H + n) = make_float4(0.f, 0.f, 0.f, 0.f);
+      // ---- router rows -> tagged logits; row r takes threads [64 r, 64 r + 64)
       if (my_rows > 0) {
+        mbar_wait(&s_bar_rr, ph_rr, sync);
+        ph_rr ^= 1;
         const int r = threadIdx.x >> 6, tr = threadIdx.x & 63;
         float acc = 0.f;
         if (r < my_rows) {
@@ -700,121 +787,150 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         __syncthreads();
         if (threadIdx.x < my_rows) {
           const float v = (s_rp[2 * threadIdx.x] + s_rp[2 * threadIdx.x + 1]) + s_bias[threadIdx.x];
-          st_release_u64(a.logits_tag + c + threadIdx.x * G,
-                         ((unsigned long long)tag << 32) | __float_as_uint(v));
+          st_tagged(a.logits_tag + c + threadIdx.x * G, ((unsigned long long)tag << 32) | __float_as_uint(v));
         }
-      } else if (threadIdx.x == 0) {
-        // no router row: a presence tag in slot E + c
-        st_release_u64(a.logits_tag + a.E + c, (unsigned long long)tag << 32);
       }
-      // ---- shared units (need only x_l)
+      // ---- shared units' gate/up (need only x_l)
       XStage<CPL, 1> xs;
       pairs_from_smem<CPL>(xs.p[0], s_xf, sl, LPR);
       xs.unscale = stg.unscale;
-      float part[4] = {0.f, 0.f, 0.f, 0.f};
-      int par = 0;                                   // scratch parity
-      for (int i = 0; i < my_sh; ++i, par ^= 1)
-        unit_compute<CPL>(s_static + (size_t)i * U.bytes, H, P.sh_gate.tsc[0], P.sh_up.tsc[0],
-                          P.sh_down_tsc[0], 1.0f, xs, s_gu[par], s_hs[par], part);
-      // ---- all logits (and every CTA's residual share), then the top-k
-      // slots [0, E) are the logits; slots E + c' for the CTAs c' >= E without a row
-      for (int i = threadIdx.x; i < n_wait; i += kPThreads) {
-        const float v = wait_tagged(a.logits_tag + (i < a.E ? i : a.E + i), tag, sync);
-        if (i < a.E) s_logits[i] = v;
+      if (my_sh > 0) {
+        mbar_wait(&s_bar_sh, ph_sh, sync);
+        ph_sh ^= 1;
+        for (int i = 0; i < my_sh; ++i)
+          unit_gateup<CPL>(s_static + (size_t)i * U.bytes, H, P.sh_gate.tsc[0], P.sh_up.tsc[0], xs,
+                           s_gu + i * 2 * kUnit);
+        if (threadIdx.x < my_sh) s_dscale[threadIdx.x] = P.sh_down_tsc[0];
       }
-      __syncthreads();                               // also: router rows and shared units consumed
-      if (warp == 0) topk_dispatch(s_logits, a.E, a.K, s_sel, s_w);
+      // ---- all logits; each logit warp selects its K + 1 best while the rest arrive
+      if (warp < nw_e) {
+        const int i = threadIdx.x;
+        unsigned key = 0u;
+        if (i < a.E) {
+          const float v = wait_tagged(a.logits_tag + i, tag, sync);
+          s_logits[i] = v;
+          key = packed_key(v, i, ib);
+        }
+        bool tie;
+        const unsigned cand = warp_select(key, a.K + 2, ib, tie);
+        if (lane <= a.K) s_cand[warp * (a.K + 1) + lane] = cand;
+        if (tie && lane == 0) atomicOr(&s_tie, 1);
+      }
       __syncthreads();
       if (warp == 0) {
-        if (lane < my_rt) mbar_expect_tx(&s_bar_rt[lane], U.bytes);
-        __syncwarp();
-        for (int q = lane; q < 6 * my_rt; q += 32) {
-          const int i = q / 6, piece = q % 6;
-          const int r = c + i * G;
-          const int slot = r / per_slot, j = r % per_slot;
-          int e = s_sel[slot];
-          if (e < 0 || e >= a.E) { raise_status(FLINT_ERR_INVALID_ARG); e = 0; }
-          unit_copy_piece(piece, s_routed + (size_t)i * U.bytes, &s_bar_rt[i], H, P.gate, P.up,
-                          P.dcc_codes, P.dcc_scales, (size_t)e * a.F + (size_t)j * kUnit, (size_t)e,
-                          per_slot, j);
+        // merge the warps' candidates (distinct keys, in shared memory)
+        const int n_c = nw_e * (a.K + 1);
+        unsigned prev = 0u, mine = 0u;
+        bool tie = s_tie != 0;
+        for (int sr = 0; sr <= a.K; ++sr) {
+          unsigned m = 0u;
+#pragma unroll 1
+          for (int j = lane; j < n_c; j += 32) m = max(m, s_cand[j]);
+          const unsigned w = __reduce_max_sync(0xffffffffu, m);
+          if (sr > 0 && w != 0u && (w >> ib) == (prev >> ib)) tie = true;
+          prev = w;
+#pragma unroll 1
+          for (int j = lane; j < n_c; j += 32)
+            if (s_cand[j] == w) s_cand[j] = 0u;
+          __syncwarp();
+          if (lane == sr) mine = w;
         }
-        if (more && my_rt == 0) issue_static(l_next);
+        if (tie) {
+          topk_exact_dispatch(s_logits, a.E, a.K, s_sel, s_w);
+        } else {
+          const int e = (int)((1u << ib) - 1u - (mine & ((1u << ib) - 1u)));
+          float lv = lane < a.K ? s_logits[e] : 0.f;
+          lv = (lv == lv) ? lv : -INFINITY;
+          const float l0 = __shfl_sync(0xffffffffu, lv, 0);
+          const float pr = lane < a.K ? expf(lv - l0) : 0.f;
+          float z = pr;
+#pragma unroll
+          for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+          if (lane < a.K) { s_sel[lane] = e; s_w[lane] = pr / z; }
+        }
+        __syncwarp();
+        // routed copies (with the next layer's router rows behind them)
+        issue_routed_units(P, s_routed, s_bar_rt, H, c, G, my_rt, per_slot, a.F, a.E, s_sel);
+        if (more) issue_router_rows(a.layer[l_next], s_router, &s_bar_rr, H, c, G, my_rows);
       }
+      __syncthreads();
       if (c == 0 && threadIdx.x < a.K) {
         const size_t o = ((size_t)t * a.L + l) * a.K + threadIdx.x;
         if (a.idx_out) a.idx_out[o] = s_sel[threadIdx.x];
         if (a.w_out) a.w_out[o] = s_w[threadIdx.x];
       }
-      // ---- routed units, each as soon as its copy lands
+      // ---- routed units' gate/up, each as soon as its copy lands
       for (int i = 0; i < my_rt; ++i) {
         const int r = c + i * G;
         const int slot = r / per_slot;
         int e = s_sel[slot];
         if (e < 0 || e >= a.E) e = 0;
         mbar_wait(&s_bar_rt[i], ph_rt, sync);
-        // the next layer's static copies go out once this step's routed bytes are in
-        if (more && i == my_rt - 1 && warp == 0) issue_static(l_next);
-        unit_compute<CPL>(s_routed + (size_t)i * U.bytes, H, P.gate.tsc[e], P.up.tsc[e],
-                          P.down_tsc[e], s_w[slot], xs, s_gu[par], s_hs[par], part);
-        par ^= 1;
+        unit_gateup<CPL>(s_routed + (size_t)i * U.bytes, H, P.gate.tsc[e], P.up.tsc[e], xs,
+                         s_gu + (my_sh + i) * 2 * kUnit);
+        if (threadIdx.x == 0) s_dscale[my_sh + i] = P.down_tsc[e] * s_w[slot];
       }
       ph_rt ^= 1;
-      // ---- this CTA's down contributions -> h_{l+1}
-      if (my_sh + my_rt > 0 && 4 * threadIdx.x < H)
-        red_add_v4(acc_next + (c % kAccCopies) * H + 4 * threadIdx.x, part[0], part[1], part[2], part[3]);
-      signal_count(sync, kSyncDone);
+      __syncthreads();
+      // ---- SwiGLU of all units, then one down pass over them
+      const int n_units = my_sh + my_rt;
+      if (warp == 0) stage_swiglu(n_units, s_gu, s_dscale, s_hs);
+      __syncthreads();
+      float part[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int u = 0; u < n_units; ++u)
+        unit_down(u < my_sh ? s_static + (size_t)u * U.bytes : s_routed + (size_t)(u - my_sh) * U.bytes, H,
+                  s_hs + u * (kUnit + 1), part);
+      if (n_units > 0 && 4 * threadIdx.x < H)
+        red_add_v4(acc_out + (c % kAccCopies) * H + 4 * threadIdx.x, part[0], part[1], part[2], part[3]);
+      signal_count(sync, kSyncDone);                 // begins with a CTA barrier
+      // the shared-unit buffers are free again
+      if (more && warp == 0) issue_shared_units(a.layer[l_next], s_static, &s_bar_sh, H, c, G, my_sh, n_sh);
     }
     // ---------------- outputs of token t
     wait_count(sync, kSyncDone, (unsigned)G * step);
-    const float* hfin = a.acc + (step & 1) * (kAccCopies * H);
+    const float* hfin = a.acc + (step % 3) * (kAccCopies * H);         // B(step - 1)
+    const Staged stg = cta_stage(hfin, nullptr, nullptr, H, a.eps, s_hx, s_xb, s_xf, s_red);
     if (a.out)
-      for (int n = c * kPThreads + threadIdx.x; n < H; n += G * kPThreads) {
-        float v = __ldcg(hfin + n);
-#pragma unroll
-        for (int cp = 1; cp < kAccCopies; ++cp) v += __ldcg(hfin + cp * H + n);
-        a.out[(size_t)t * H + n] = v;
+      for (int n = c * kPThreads + threadIdx.x; n < H; n += G * kPThreads) a.out[(size_t)t * H + n] = s_hx[n];
+    if (a.x_out && c == 0)
+      for (int n = 4 * threadIdx.x; n < H; n += 4 * kPThreads)
+        *reinterpret_cast<uint2*>(a.x_out + (size_t)t * H + n) = *reinterpret_cast<const uint2*>(s_xb + n);
+    if (a.head.codes) {
+      XStage<CPL, 1> xs;
+      pairs_from_smem<CPL>(xs.p[0], s_xf, sl, LPR);
+      xs.unscale = stg.unscale;
+      float bv = -INFINITY;
+      int bi = 0x7FFFFFFF;
+      head_rows<CPL>(a, xs, t, bv, bi);
+      best_reduce_warp(bv, bi);
+      if ((threadIdx.x & 31) == 0) { s_bv[warp] = bv; s_bi[warp] = bi; }
+      __syncthreads();
+      float* best_v = a.best_v + (t & 1) * kMaxCtas;
+      int* best_i = a.best_i + (t & 1) * kMaxCtas;
+      if (threadIdx.x == 0) {
+        for (int w = 1; w < kPWarps; ++w)
+          if (s_bv[w] > bv || (s_bv[w] == bv && s_bi[w] < bi)) { bv = s_bv[w]; bi = s_bi[w]; }
+        best_v[c] = bv;
+        best_i[c] = bi;
       }
-    if (a.x_out || a.head.codes) {
-      const Staged stg = cta_stage(hfin, nullptr, H, a.eps, s_hx, s_xb, s_xf, s_red);
-      if (a.x_out && c == 0)
-        for (int n = 4 * threadIdx.x; n < H; n += 4 * kPThreads)
-          *reinterpret_cast<uint2*>(a.x_out + (size_t)t * H + n) = *reinterpret_cast<const uint2*>(s_xb + n);
-      if (a.head.codes) {
-        XStage<CPL, 1> xs;
-        pairs_from_smem<CPL>(xs.p[0], s_xf, sl, LPR);
-        xs.unscale = stg.unscale;
-        float bv = -INFINITY;
-        int bi = 0x7FFFFFFF;
-        head_rows<CPL>(a, xs, t, bv, bi);
-        best_reduce_warp(bv, bi);
-        if ((threadIdx.x & 31) == 0) { s_bv[warp] = bv; s_bi[warp] = bi; }
-        __syncthreads();
-        float* best_v = a.best_v + (t & 1) * kMaxCtas;
-        int* best_i = a.best_i + (t & 1) * kMaxCtas;
-        if (threadIdx.x == 0) {
-          for (int w = 1; w < kPWarps; ++w)
-            if (s_bv[w] > bv || (s_bv[w] == bv && s_bi[w] < bi)) { bv = s_bv[w]; bi = s_bi[w]; }
-          best_v[c] = bv;
-          best_i[c] = bi;
-        }
-        signal_count(sync, kSyncHead);
-        if (c == 0) {
-          wait_count(sync, kSyncHead, (unsigned)G * (t + 1));
-          if (warp == 0) {
-            const int ln = threadIdx.x & 31;
-            float v = -INFINITY;
-            int i = 0x7FFFFFFF;
-            for (int k = ln; k < G; k += 32) {
-              const float kv = __ldcg(best_v + k);
-              const int ki = __ldcg(best_i + k);
-              if (kv > v || (kv == v && ki < i)) { v = kv; i = ki; }
-            }
-            best_reduce_warp(v, i);
-            if (ln == 0 && a.argmax) a.argmax[t] = (i < a.V) ? i : 0;
+      signal_count(sync, kSyncHead);
+      if (c == 0) {
+        wait_count(sync, kSyncHead, (unsigned)G * (t + 1));
+        if (warp == 0) {
+          const int ln = threadIdx.x & 31;
+          float v = -INFINITY;
+          int i = 0x7FFFFFFF;
+          for (int k = ln; k < G; k += 32) {
+            const float kv = __ldcg(best_v + k);
+            const int ki = __ldcg(best_i + k);
+            if (kv > v || (kv == v && ki < i)) { v = kv; i = ki; }
           }
+          best_reduce_warp(v, i);
+          if (ln == 0 && a.argmax) a.argmax[t] = (i < a.V) ? i : 0;
         }
       }
     }
+    __syncthreads();                                 // s_hx is rewritten by the next token
   }
   // No bulk copy is in flight at exit: copies are issued only while `more` holds (or
   // for the current step), and every issued copy is waited for in the step it serves.
@@ -854,20 +970,20 @@ cudaError_t launch_column_chunks(const uint8_t* codes, const uint8_t* scales, in
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Bytes at the start of the workspace that every launch clears: sync words + tags.
-static size_t decode_cleared_bytes(int E) {
-  return sizeof(unsigned) * kSyncWords + align256(sizeof(unsigned long long) * (E + kMaxCtas));
+static size_t decode_cleared_bytes(int H, int E) {
+  return sizeof(unsigned) * kSyncWords + align256(sizeof(unsigned long long) * E) +
+         align256(sizeof(float) * 3 * kAccCopies * H);
 }
 
 size_t decode_workspace_bytes(int H, int E) {
-  return decode_cleared_bytes(E) + align256(sizeof(float) * 2 * kAccCopies * H) +
-         2 * align256(2 * kMaxCtas * sizeof(float));
+  return decode_cleared_bytes(H, E) + 2 * align256(2 * kMaxCtas * sizeof(float));
 }
 
 void decode_carve(PersistArgs& a, void* ws) {
   char* p = static_cast<char*>(ws);
   a.bar = reinterpret_cast<unsigned*>(p); p += sizeof(unsigned) * kSyncWords;
-  a.logits_tag = reinterpret_cast<unsigned long long*>(p); p += align256(sizeof(unsigned long long) * (a.E + kMaxCtas));
-  a.acc = reinterpret_cast<float*>(p); p += align256(sizeof(float) * 2 * kAccCopies * a.H);
+  a.logits_tag = reinterpret_cast<unsigned long long*>(p); p += align256(sizeof(unsigned long long) * a.E);
+  a.acc = reinterpret_cast<float*>(p); p += align256(sizeof(float) * 3 * kAccCopies * a.H);
   a.best_v = reinterpret_cast<float*>(p); p += align256(2 * kMaxCtas * sizeof(float));
   a.best_i = reinterpret_cast<int*>(p);
 }
@@ -892,6 +1008,7 @@ DecodePlan decode_plan(int H, int E, int K, int F, int Fs, int G) {
   p.smem = (size_t)H * (4 + 2 + 2) + (size_t)p.router_rows * H * 2 +
            (size_t)(p.shared_units + p.routed_units) * UnitLayout::of(H).bytes;
   p.ok = p.router_rows <= kMaxRouterRows && p.routed_units <= kMaxRoutedUnits &&
+         p.shared_units <= kMaxSharedUnits &&
          p.smem <= kMaxDecodeSmem && F % (2 * kUnit) == 0 && Fs % (2 * kUnit) == 0;
   return p;
 }
@@ -919,7 +1036,7 @@ cudaError_t launch_persistent(const PersistArgs& a, cudaStream_t st) {
   const DecodePlan p = decode_plan(a.H, a.E, a.K, a.F, a.Fs, decode_grid());
   if (!p.ok || a.max_router_rows != p.router_rows || a.max_shared_units != p.shared_units)
     return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaMemsetAsync(a.bar, 0, decode_cleared_bytes(a.E), st);
+  cudaError_t e = cudaMemsetAsync(a.bar, 0, decode_cleared_bytes(a.H, a.E), st);
   if (e != cudaSuccess) return e;
   if (a.H <= 1024) return launch_persistent_cpl<1>(a, p.smem, st);
   return launch_persistent_cpl<2>(a, p.smem, st);

@@ -15,9 +15,10 @@
 //                 16): per 128-row tile of one expert, the gate and up tiles accumulate
 //                 in TMEM; the epilogue applies the tensor scales, SwiGLU, and
 //                 quantises h to NVFP4 (unit tensor scale)
-//   6 down        grouped GEMM as 5 over the shared and the routed tiles; the epilogue
-//                 scales each row (w_pair for routed rows) and adds it into out[token]
-//                 with TMA bulk reduce-adds: the un-permuting combine
+//   6 down        grouped GEMM as 5 over the shared and the routed tiles; the shared
+//                 tiles write out = x + y, the routed tiles write w_pair * y as f16 rows
+//   7 combine     per token, out[t] += its K routed rows (slot order): the
+//                 un-permuting combine
 //
 // Every FP4 operand's block scales are kept in the MMA scale layout (512 bytes per
 // 128-row tile and 64 columns, see flint.h), so one pipeline stage of a GEMM is four
@@ -43,31 +44,35 @@ constexpr int kBN = 128;          // output columns per B tile
 constexpr int kGThreads = 384;    // 12 warps
 constexpr int kWarpTMA = 0, kWarpMMA = 1, kWarpEpi0 = 4, kEpiWarps = 8;
 
-struct Item {
-  int kind;     // 0 shared expert, 1 routed expert
-  int expert;
+struct __align__(16) Item {
+  int kx;       // kind << 16 | expert; kind 0 = shared expert, 1 = routed expert
   int row0;     // first A row of the tile (a multiple of 128)
   int rows;     // valid rows (<= kBM)
   int n0;       // first output column
+  __device__ int kind() const { return kx >> 16; }
+  __device__ int expert() const { return kx & 0xFFFF; }
 };
+__device__ __forceinline__ Item load_item(const Item* p) {
+  const int4 v = __ldcg(reinterpret_cast<const int4*>(p));
+  return Item{v.x, v.y, v.z, v.w};
+}
 
 enum Mode { kGateUp = 1, kDown = 2 };
 
 template <int MODE>
 struct Cfg {
   static constexpr int kB = MODE == kGateUp ? 2 : 1;      // B tiles per stage (gate + up)
-  static constexpr int kStages = 4;
+  static constexpr int kStages = MODE == kGateUp ? 4 : 6;
   static constexpr int a = 0;                             // A codes, 128 rows x 128 B
   static constexpr int b = 16384;                         // B codes, kB x 16 KB
   static constexpr int sfa = b + kB * 16384;              // A scales, 4 x 512 B
   static constexpr int sfb = sfa + 2048;                  // B scales, kB x 4 x 512 B
   static constexpr int bytes = sfb + kB * 2048;
   static constexpr int stride = (bytes + 1023) / 1024 * 1024;
-  static constexpr int staging = MODE == kDown ? kBM * kBN * 4 : 0;   // fp32 rows to reduce
-  static constexpr int smem = kStages * stride + staging + 1024;
+  static constexpr int smem = kStages * stride + 1024;
   static constexpr int dcols = kB * kBN;                  // accumulator columns
   static constexpr int sf_step = 4 + 4 * kB;              // TMEM scale columns per K=64 step
-  static constexpr uint32_t tmem_cols = MODE == kGateUp ? 512 : 256;
+  static constexpr uint32_t tmem_cols = 512;
   static_assert(dcols + kStages * 4 * sf_step <= (int)tmem_cols, "TMEM budget");
 };
 
@@ -86,7 +91,9 @@ struct GemmArgs {
   uint8_t* hcodes[2];           // gate/up output codes: [0] shared h [Tp][Fs/2], [1] routed h
   uint8_t* hsf[2];              // gate/up output scales, MMA scale layout
   int Fout[2];
-  float* out;                   // [T][H]
+  float* out;                   // [T][H]: shared-expert tiles write x + y here
+  const uint16_t* x;            // [T][H] bf16
+  uint16_t* yp;                 // [Pp][H] f16: routed rows, w_pair * y
   const int32_t* order;         // padded routed row -> pair id
   const float* wpair;           // [T*K]
   int H, K;
@@ -151,15 +158,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                :: "r"(sh(dst)), "l"(src), "r"(bytes), "r"(sh(bar)) : "memory");
 }
-// out[0 .. bytes/4) += smem[0 .. bytes/4)  (fp32, performed by the TMA unit)
-__device__ __forceinline__ void bulk_reduce_add(float* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
-               :: "l"(dst), "r"(sh(src)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_commit(uint64_t* b) {
@@ -244,7 +242,6 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
   constexpr int S = C::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint8_t* staging = smem + S * C::stride;
   __shared__ __align__(8) uint64_t full[S], empty[S], accf, acce;
   __shared__ uint32_t tmem_base;
   __shared__ volatile int abort_flag;
@@ -271,31 +268,35 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
 
   if (warp == kWarpTMA && lane == 0) {
     uint32_t it = 0;
+    Item nxt = blockIdx.x < n_items ? load_item(g.items + blockIdx.x) : Item{0, 0, 0, 0};
     for (int i = blockIdx.x; i < n_items && !abort_flag; i += gridDim.x) {
-      const Item item = g.items[i];
-      const int K = g.Kel[item.kind], ksteps = K / 64;
-      const int brow = item.expert * g.rowsB[item.kind] + item.n0;
-      const uint8_t* sfa = g.sfA[item.kind] + (size_t)(item.row0 >> 7) * ksteps * 512;
+      const Item item = nxt;
+      if (i + (int)gridDim.x < n_items) nxt = load_item(g.items + i + gridDim.x);
+      const int K = g.Kel[item.kind()], ksteps = K / 64;
+      const int brow = item.expert() * g.rowsB[item.kind()] + item.n0;
+      const uint8_t* sfa = g.sfA[item.kind()] + (size_t)(item.row0 >> 7) * ksteps * 512;
       for (int kt = 0; kt < K / 256; ++kt, ++it) {
         const int s = it % S;
         if (it >= S && !mb_wait(&empty[s], ((it / S) - 1) & 1, &abort_flag)) break;
         uint8_t* st = smem + s * C::stride;
         mb_expect(&full[s], C::bytes);
-        tma2d(st + C::a, &g.mapA[item.kind], kt * 128, item.row0, &full[s]);
+        tma2d(st + C::a, &g.mapA[item.kind()], kt * 128, item.row0, &full[s]);
         bulk_g2s(st + C::sfa, sfa + (size_t)kt * 2048, 2048, &full[s]);
 #pragma unroll
         for (int b = 0; b < C::kB; ++b) {
-          tma2d(st + C::b + b * 16384, &g.mapB[2 * item.kind + b], kt * 128, brow, &full[s]);
+          tma2d(st + C::b + b * 16384, &g.mapB[2 * item.kind() + b], kt * 128, brow, &full[s]);
           bulk_g2s(st + C::sfb + b * 2048,
-                   g.sfB[2 * item.kind + b] + ((size_t)(brow >> 7) * ksteps + 4 * kt) * 512, 2048, &full[s]);
+                   g.sfB[2 * item.kind() + b] + ((size_t)(brow >> 7) * ksteps + 4 * kt) * 512, 2048, &full[s]);
         }
       }
     }
   } else if (warp == kWarpMMA && lane == 0) {
     uint32_t it = 0, done = 0;
+    Item nxt = blockIdx.x < n_items ? load_item(g.items + blockIdx.x) : Item{0, 0, 0, 0};
     for (int i = blockIdx.x; i < n_items && !abort_flag; i += gridDim.x, ++done) {
-      const Item item = g.items[i];
-      const int kt_n = g.Kel[item.kind] / 256;
+      const Item item = nxt;
+      if (i + (int)gridDim.x < n_items) nxt = load_item(g.items + i + gridDim.x);
+      const int kt_n = g.Kel[item.kind()] / 256;
       if (done > 0 && !mb_wait(&acce, (done - 1) & 1, &abort_flag)) break;
       tc_fence_after();
       bool ok = true;
@@ -334,15 +335,17 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
     const int r = q * 32 + lane;                            // tile row of this thread
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t done = 0;
+    Item nxt = blockIdx.x < n_items ? load_item(g.items + blockIdx.x) : Item{0, 0, 0, 0};
     for (int i = blockIdx.x; i < n_items && !abort_flag; i += gridDim.x, ++done) {
-      const Item item = g.items[i];
+      const Item item = nxt;
+      if (i + (int)gridDim.x < n_items) nxt = load_item(g.items + i + gridDim.x);
       if (!mb_wait(&accf, done & 1, &abort_flag)) break;
       tc_fence_after();
       const bool valid = r < item.rows;
       const int arow = item.row0 + r;
       if (MODE == kGateUp) {
-        const float tg = g.tscA[item.kind][item.kind ? item.expert : 0];
-        const float tu = g.tscB[item.kind][item.kind ? item.expert : 0];
+        const float tg = g.tscA[item.kind()][item.kind() ? item.expert() : 0];
+        const float tu = g.tscB[item.kind()][item.kind() ? item.expert() : 0];
         float h[64];
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 16) {
@@ -358,9 +361,9 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
         __syncwarp();
         if (lane == 0) mb_arrive(&acce);                  // accumulator free for the next item
         if (valid) {
-          const int F = g.Fout[item.kind];
+          const int F = g.Fout[item.kind()];
           const int col = item.n0 + 64 * hf;
-          uint8_t* hc = g.hcodes[item.kind] + (size_t)arow * (F / 2) + col / 2;
+          uint8_t* hc = g.hcodes[item.kind()] + (size_t)arow * (F / 2) + col / 2;
           uint32_t sw = 0;
           uint2 cw[4];
 #pragma unroll
@@ -371,7 +374,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
           }
           *reinterpret_cast<uint4*>(hc) = make_uint4(cw[0].x, cw[0].y, cw[1].x, cw[1].y);
           *reinterpret_cast<uint4*>(hc + 16) = make_uint4(cw[2].x, cw[2].y, cw[3].x, cw[3].y);
-          *reinterpret_cast<uint32_t*>(g.hsf[item.kind] + sf_word_offset(arow, col / 64, F / 64)) = sw;
+          *reinterpret_cast<uint32_t*>(g.hsf[item.kind()] + sf_word_offset(arow, col / 64, F / 64)) = sw;
         }
       } else {  // down
         float y[64];
@@ -387,27 +390,45 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
         __syncwarp();
         if (lane == 0) mb_arrive(&acce);
         if (valid) {
-          const float td = g.tscA[item.kind][item.kind ? item.expert : 0];
-          int t = arow;
-          float scale = td;
-          if (item.kind) {
-            const int pair = g.order[arow];
-            t = pair / g.K;
-            scale = td * g.wpair[pair];
-          }
-          float* slot = reinterpret_cast<float*>(staging) + r * kBN + 64 * hf;
-          bulk_wait_read();                                // the previous reduce has read the slot
+          const float td = g.tscA[item.kind()][item.kind() ? item.expert() : 0];
+          const int col = item.n0 + 64 * hf;
+          if (item.kind() == 0) {
+            // shared expert: out[t] = x[t] + y (the only write of these elements)
+            const uint16_t* xr = g.x + (size_t)arow * g.H + col;
+            float* o = g.out + (size_t)arow * g.H + col;
 #pragma unroll
-          for (int j = 0; j < 64; j += 4)
-            *reinterpret_cast<float4*>(slot + j) =
-                make_float4(y[j] * scale, y[j + 1] * scale, y[j + 2] * scale, y[j + 3] * scale);
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          bulk_reduce_add(g.out + (size_t)t * g.H + item.n0 + 64 * hf, slot, 256);
-          bulk_commit();
+            for (int j = 0; j < 64; j += 8) {
+              const uint4 xb = *reinterpret_cast<const uint4*>(xr + j);
+              const uint32_t xw[4] = {xb.x, xb.y, xb.z, xb.w};
+              float4 lo, hi;
+              lo.x = bf16_bits_to_f32(xw[0] & 0xFFFFu) + y[j] * td;
+              lo.y = bf16_bits_to_f32(xw[0] >> 16) + y[j + 1] * td;
+              lo.z = bf16_bits_to_f32(xw[1] & 0xFFFFu) + y[j + 2] * td;
+              lo.w = bf16_bits_to_f32(xw[1] >> 16) + y[j + 3] * td;
+              hi.x = bf16_bits_to_f32(xw[2] & 0xFFFFu) + y[j + 4] * td;
+              hi.y = bf16_bits_to_f32(xw[2] >> 16) + y[j + 5] * td;
+              hi.z = bf16_bits_to_f32(xw[3] & 0xFFFFu) + y[j + 6] * td;
+              hi.w = bf16_bits_to_f32(xw[3] >> 16) + y[j + 7] * td;
+              *reinterpret_cast<float4*>(o + j) = lo;
+              *reinterpret_cast<float4*>(o + j + 4) = hi;
+            }
+          } else {
+            // routed row: w_pair * y as f16, summed per token by the combine kernel
+            const float scale = td * g.wpair[g.order[arow]];
+            uint16_t* yr = g.yp + (size_t)arow * g.H + col;
+#pragma unroll
+            for (int j = 0; j < 64; j += 8) {
+              uint4 pk;
+              pk.x = pack_f16x2_rn(y[j] * scale, y[j + 1] * scale);
+              pk.y = pack_f16x2_rn(y[j + 2] * scale, y[j + 3] * scale);
+              pk.z = pack_f16x2_rn(y[j + 4] * scale, y[j + 5] * scale);
+              pk.w = pack_f16x2_rn(y[j + 6] * scale, y[j + 7] * scale);
+              *reinterpret_cast<uint4*>(yr + j) = pk;
+            }
+          }
         }
       }
     }
-    if (MODE == kDown) bulk_wait_all();
   }
   // unwind: every role is done (or gave up); no MMA may be in flight at dealloc
   __syncthreads();
@@ -430,7 +451,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
 // logits[t][e] = x[t] . Wr[e] (+ bias[e]) for 128 tokens x 64 experts per CTA; A = x rows
 // (TMA, 64 bf16 = 128 B per K-tile), B = 64 router rows, tcgen05 kind::f16 (K = 16 per
 // instruction).
-constexpr int kRStages = 4;
+constexpr int kRStages = 8;
 constexpr int kRN = 64;
 constexpr int kRThreads = 256;
 
@@ -627,36 +648,45 @@ __global__ void __launch_bounds__(1024) k_scan(ScanArgs s) {
     *s.n_items_dn = mt_sh * (s.H / kBN) + tot_tiles * (s.H / kBN);
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < mt_sh * (s.Fs / kBN); i += blockDim.x) {
-    const int mt = i / (s.Fs / kBN), nt = i % (s.Fs / kBN);
-    s.items_gu[i] = Item{0, 0, mt * kBM, min(kBM, a.T - mt * kBM), nt * kBN};
+  const int nt_gu = s.Fs / kBN, nt_dn = s.H / kBN;
+  for (int i = threadIdx.x; i < mt_sh * nt_gu; i += blockDim.x) {
+    const int mt = i / nt_gu, nt = i % nt_gu;
+    s.items_gu[i] = Item{0, mt * kBM, min(kBM, a.T - mt * kBM), nt * kBN};
   }
-  for (int i = threadIdx.x; i < mt_sh * (s.H / kBN); i += blockDim.x) {
-    const int mt = i / (s.H / kBN), nt = i % (s.H / kBN);
-    s.items_dn[i] = Item{0, 0, mt * kBM, min(kBM, a.T - mt * kBM), nt * kBN};
+  for (int i = threadIdx.x; i < mt_sh * nt_dn; i += blockDim.x) {
+    const int mt = i / nt_dn, nt = i % nt_dn;
+    s.items_dn[i] = Item{0, mt * kBM, min(kBM, a.T - mt * kBM), nt * kBN};
   }
-  const int base_gu = mt_sh * (s.Fs / kBN), base_dn = mt_sh * (s.H / kBN);
-  for (int x = threadIdx.x; x < a.E; x += blockDim.x) {
-    const int c = s_cnt[x], tiles = (c + kBM - 1) / kBM;
-    for (int mt = 0; mt < tiles; ++mt) {
-      const int rows = min(kBM, c - mt * kBM);
-      const int row0 = (s_toff[x] + mt) * kBM;
-      for (int nt = 0; nt < s.F / kBN; ++nt)
-        s.items_gu[base_gu + (s_toff[x] + mt) * (s.F / kBN) + nt] = Item{1, x, row0, rows, nt * kBN};
-      for (int nt = 0; nt < s.H / kBN; ++nt)
-        s.items_dn[base_dn + (s_toff[x] + mt) * (s.H / kBN) + nt] = Item{1, x, row0, rows, nt * kBN};
+  // routed items: tile (expert-major, padded) x N tile; the expert of a tile by binary
+  // search over the tile offsets
+  const int rt_gu = s.F / kBN;
+  const int n_rt_tiles = tot_tiles;
+  for (int i = threadIdx.x; i < n_rt_tiles * (rt_gu + nt_dn); i += blockDim.x) {
+    const bool gu = i < n_rt_tiles * rt_gu;
+    const int ii = gu ? i : i - n_rt_tiles * rt_gu;
+    const int nt_n = gu ? rt_gu : nt_dn;
+    const int tile = ii / nt_n, nt = ii % nt_n;
+    int lo = 0, hi = a.E - 1;                        // last e with s_toff[e] <= tile
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_toff[mid] <= tile) lo = mid; else hi = mid - 1;
     }
+    while (lo < a.E - 1 && s_cnt[lo] == 0) ++lo;     // empty experts share the offset
+    const int mt = tile - s_toff[lo];
+    const Item it = Item{(1 << 16) | lo, tile * kBM, min(kBM, s_cnt[lo] - mt * kBM), nt * kBN};
+    if (gu) s.items_gu[mt_sh * nt_gu + ii] = it;
+    else s.items_dn[mt_sh * nt_dn + ii] = it;
   }
 }
 
 // One warp per token: x[t] quantised to NVFP4 once (unit tensor scale), written to the
-// shared expert's operand row t and to the token's K expert-major rows; out[t] = x[t];
-// the pair order (plain and padded positions).
+// shared expert's operand row t and to the token's K expert-major rows; the pair order
+// (plain and padded positions).
 struct ScatterArgs {
   RouteArgs r;
   const uint16_t* x;
-  float* out;
   int H;
+  int32_t* pos_of_pair;    // pair -> padded row
   int32_t* order_pad;      // padded row -> pair
   int32_t* order_out;      // plain position -> pair (optional)
   uint8_t* xq_codes;  uint8_t* xq_sf;   // [Tp][H/2], MMA scale layout
@@ -677,6 +707,7 @@ __global__ void __launch_bounds__(256) k_scatter_quant(ScatterArgs s) {
     const int rank = a.wordpre[(size_t)e * a.W + (t >> 5)] + __popc(word & ((1u << (t & 31)) - 1u));
     mypos = a.offp[e] + rank;
     s.order_pad[mypos] = pair;
+    s.pos_of_pair[pair] = mypos;
     if (s.order_out) s.order_out[a.offsets[e] + rank] = pair;
   }
   const int H = s.H, ks = H / 64;
@@ -693,9 +724,6 @@ __global__ void __launch_bounds__(256) k_scatter_quant(ScatterArgs s) {
         f[8 * p + 2 * q + 1] = bf16_bits_to_f32(u[q] >> 16);
       }
     }
-    float* orow = s.out + (size_t)t * H + 64 * gk;
-#pragma unroll
-    for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4*>(orow + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
     uint2 cw[4];
     uint32_t sw = 0;
 #pragma unroll
@@ -720,6 +748,44 @@ __global__ void __launch_bounds__(256) k_scatter_quant(ScatterArgs s) {
   }
 }
 
+// One warp per token: out[t] += sum over the token's K routed rows of Yp (f16, already
+// scaled by the routing weights), slots in order.  out[t] holds x[t] + shared y[t].
+struct CombineArgs {
+  const uint16_t* yp;
+  const int32_t* pos_of_pair;
+  float* out;
+  int T, H, K;
+};
+
+__global__ void __launch_bounds__(256) k_combine(CombineArgs c) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= c.T) return;
+  const int pos_l = lane < c.K ? c.pos_of_pair[t * c.K + lane] : 0;
+  float* o = c.out + (size_t)t * c.H;
+  for (int n0 = 8 * lane; n0 < c.H; n0 += 8 * 32) {
+    float acc[8];
+    const float4 a = *reinterpret_cast<const float4*>(o + n0);
+    const float4 b = *reinterpret_cast<const float4*>(o + n0 + 4);
+    acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+    acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+    for (int j = 0; j < c.K; ++j) {
+      const int pos = __shfl_sync(0xffffffffu, pos_l, j);
+      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(c.yp + (size_t)pos * c.H + n0));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float lo, hi;
+        f16x2_to_f32x2(w[q], lo, hi);
+        acc[2 * q] += lo;
+        acc[2 * q + 1] += hi;
+      }
+    }
+    *reinterpret_cast<float4*>(o + n0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(o + n0 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
 // ---------------------------------------------------------------- MMA scale copies
 // scales [m][rows][cols/16] -> [m][rows/128][cols/64][512] (see flint.h)
 __global__ void k_mma_scales(const uint8_t* __restrict__ scales, int rows, int cols,
@@ -738,8 +804,8 @@ __global__ void k_mma_scales(const uint8_t* __restrict__ scales, int rows, int c
 
 // ---------------------------------------------------------------- host side
 struct WsLayout {
-  size_t logits, idx, w, bits, wordpre, counts, offsets, offp, order, xq_c, xq_s, xp_c, xp_s, hs_c,
-      hs_s, hq_c, hq_s, items_gu, items_dn, nitems, total;
+  size_t logits, idx, w, bits, wordpre, counts, offsets, offp, order, pos, xq_c, xq_s, xp_c, xp_s, hs_c,
+      hs_s, hq_c, hq_s, yp, items_gu, items_dn, nitems, total;
 };
 
 static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -766,6 +832,7 @@ static WsLayout ws_layout(int H, int E, int K, int F, int Fs, int T) {
   L.offsets = o;  o += a256(sizeof(int) * E);
   L.offp = o;     o += a256(sizeof(int) * E);
   L.order = o;    o += a256(sizeof(int) * Pp);
+  L.pos = o;      o += a256(sizeof(int) * P);
   L.xq_c = o;     o += a256(Tp * H / 2);
   L.xq_s = o;     o += a256(Tp * H / 16);
   L.xp_c = o;     o += a256(Pp * H / 2);
@@ -774,6 +841,7 @@ static WsLayout ws_layout(int H, int E, int K, int F, int Fs, int T) {
   L.hs_s = o;     o += a256(Tp * Fs / 16);
   L.hq_c = o;     o += a256(Pp * F / 2);
   L.hq_s = o;     o += a256(Pp * F / 16);
+  L.yp = o;       o += a256(Pp * H * 2);
   L.items_gu = o; o += a256(sizeof(Item) * (mt_sh * (Fs / kBN) + mt_rt * (F / kBN)));
   L.items_dn = o; o += a256(sizeof(Item) * (mt_sh + mt_rt) * (H / kBN));
   L.nitems = o;   o += 256;
@@ -870,8 +938,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st) {
   sc.H = H; sc.F = F; sc.Fs = Fs;
   k_scan<<<1, 1024, 0, st>>>(sc);
   ScatterArgs sa;
-  sa.r = r; sa.x = a.x; sa.out = a.out; sa.H = H;
+  sa.r = r; sa.x = a.x; sa.H = H;
   sa.order_pad = reinterpret_cast<int32_t*>(at(L.order));
+  sa.pos_of_pair = reinterpret_cast<int32_t*>(at(L.pos));
   sa.order_out = a.order_out;
   sa.xq_codes = reinterpret_cast<uint8_t*>(at(L.xq_c)); sa.xq_sf = reinterpret_cast<uint8_t*>(at(L.xq_s));
   sa.xp_codes = reinterpret_cast<uint8_t*>(at(L.xp_c)); sa.xp_sf = reinterpret_cast<uint8_t*>(at(L.xp_s));
@@ -916,11 +985,17 @@ cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st) {
   dn.rowsB[0] = H; dn.rowsB[1] = H;
   dn.items = sc.items_dn; dn.n_items = sc.n_items_dn;
   dn.tscA[0] = a.sh_down.tsc; dn.tscA[1] = a.down.tsc;
-  dn.out = a.out; dn.order = sa.order_pad; dn.wpair = r.w;
+  dn.out = a.out; dn.x = a.x; dn.yp = reinterpret_cast<uint16_t*>(at(L.yp));
+  dn.order = sa.order_pad; dn.wpair = r.w;
   dn.H = H; dn.K = K;
   e = cudaFuncSetAttribute(k_gemm_fp4<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kDown>::smem);
   if (e != cudaSuccess) return e;
   k_gemm_fp4<kDown><<<sms, kGThreads, Cfg<kDown>::smem, st>>>(dn);
+
+  // 7 combine: out[t] += routed rows
+  CombineArgs cb;
+  cb.yp = dn.yp; cb.pos_of_pair = sa.pos_of_pair; cb.out = a.out; cb.T = T; cb.H = H; cb.K = K;
+  k_combine<<<(T + 7) / 8, 256, 0, st>>>(cb);
   return cudaGetLastError();
 }
 
