@@ -62,7 +62,7 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
 }
 
 // Thread 0 spins (bounded) until *cnt >= target; the CTA then proceeds together.
-__device__ __noinline__ void wait_count(unsigned* sync, int which, unsigned target) {
+__device__ __forceinline__ void wait_count(unsigned* sync, int which, unsigned target) {
   if (threadIdx.x == 0) {
     const unsigned* cnt = sync + which;
     unsigned polls = 0;
@@ -149,7 +149,7 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for a bulk-copy phase; on expiry records FLINT_ERR_TIMEOUT.
-__device__ __noinline__ void mbar_wait(uint64_t* b, uint32_t parity, unsigned* sync) {
+__device__ __forceinline__ void mbar_wait(uint64_t* b, uint32_t parity, unsigned* sync) {
   unsigned long long t0 = 0;
   unsigned polls = 0;
   while (!mbar_try(b, parity)) {
@@ -183,7 +183,7 @@ struct Staged {
   float unscale;    // 2^-k
 };
 
-__device__ __noinline__ Staged cta_stage(const float* acc, const uint16_t* x_bf16,
+__device__ __forceinline__ Staged cta_stage(const float* acc, const uint16_t* x_bf16,
                                             const float* residual, int H, float eps, float* s_hx,
                                             uint16_t* s_xb, uint16_t* s_xf, float* s_red) {
   const int n = 4 * threadIdx.x;
@@ -300,7 +300,7 @@ struct UnitLayout {
 // up scales, down codes, down scales): gate/up rows [row0, row0 + 8) of the stacks,
 // down code chunk `chunk` and scale block chunk / 2 of matrix `m`.  The six pieces are
 // issued by six lanes at once; the mbarrier's expected bytes are set beforehand.
-__device__ __noinline__ void unit_copy_piece(int piece, uint8_t* buf, uint64_t* bar, int H,
+__device__ __forceinline__ void unit_copy_piece(int piece, uint8_t* buf, uint64_t* bar, int H,
                                                 const NVPtr& gate, const NVPtr& up,
                                                 const uint8_t* dcc_codes, const uint8_t* dcc_scales,
                                                 size_t row0, size_t m, int chunks_per_mat, int chunk) {
@@ -325,7 +325,7 @@ __device__ __noinline__ void unit_copy_piece(int piece, uint8_t* buf, uint64_t* 
 // Gate/up of one unit from shared memory: the 16 row dot products (a warp per row),
 // with tensor scales and 2^-k applied, into s_gu[0..16).  No barrier.
 template <int CPL>
-__device__ __noinline__ void unit_gateup(const uint8_t* buf, int H, float gate_tsc, float up_tsc,
+__device__ __forceinline__ void unit_gateup(const uint8_t* buf, int H, float gate_tsc, float up_tsc,
                                             const XStage<CPL, 1>& xs, float* s_gu) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int LPR = H / (32 * CPL), RPP = 32 / LPR;
@@ -347,7 +347,7 @@ __device__ __noinline__ void unit_gateup(const uint8_t* buf, int H, float gate_t
 // SwiGLU values of n units (warp 0; lane 8u + j holds output j of unit u), staged as
 // hi/lo f16 pairs scaled by 2^k per unit: s_hs[u][0..4) hi pairs, [4..8) lo pairs,
 // [8] the unit's down scale (down tensor scale x routing weight x 2^-k).
-__device__ __noinline__ void stage_swiglu(int n, const float* s_gu, const float* s_dscale,
+__device__ __forceinline__ void stage_swiglu(int n, const float* s_gu, const float* s_dscale,
                                              uint32_t* s_hs) {
   const int lane = threadIdx.x & 31;
   for (int u0 = 0; u0 < n; u0 += 32 / kUnit) {
@@ -372,7 +372,7 @@ __device__ __noinline__ void stage_swiglu(int n, const float* s_gu, const float*
 }
 
 // Down contributions of one unit to this thread's rows [4t, 4t + 4), added into part[].
-__device__ __noinline__ void unit_down(const uint8_t* buf, int H, const uint32_t* hs, float (&part)[4]) {
+__device__ __forceinline__ void unit_down(const uint8_t* buf, int H, const uint32_t* hs, float (&part)[4]) {
   const UnitLayout U = UnitLayout::of(H);
   const int n0 = 4 * threadIdx.x;
   if (n0 >= H) return;
@@ -585,7 +585,7 @@ __device__ __forceinline__ unsigned warp_select(unsigned key, int n, int ib, boo
 
 // ---------------------------------------------------------------- head
 template <int CPL>
-__device__ __noinline__ void head_rows(const PersistArgs& a, const XStage<CPL, 1>& xs, int t,
+__device__ __forceinline__ void head_rows(const PersistArgs& a, const XStage<CPL, 1>& xs, int t,
                                           float& bv, int& bi) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int LPR = a.H / (32 * CPL), RPP = 32 / LPR;
@@ -628,7 +628,7 @@ __device__ __forceinline__ void best_reduce_warp(float& v, int& i) {
 
 // ---------------------------------------------------------------- copy issue (warp 0)
 // Data-independent copies of a layer for CTA c: its router rows e = c, c + G, ...
-__device__ __noinline__ void issue_router_rows(const LayerPtrs& P, uint8_t* s_router, uint64_t* bar, int H,
+__device__ __forceinline__ void issue_router_rows(const LayerPtrs& P, uint8_t* s_router, uint64_t* bar, int H,
                                                int c, int G, int my_rows) {
   const int lane = threadIdx.x & 31;
   if (my_rows == 0) return;
@@ -639,7 +639,7 @@ __device__ __noinline__ void issue_router_rows(const LayerPtrs& P, uint8_t* s_ro
 }
 
 // ... and its shared units s = G-1-c, G-1-c + G, ...
-__device__ __noinline__ void issue_shared_units(const LayerPtrs& P, uint8_t* s_static, uint64_t* bar, int H,
+__device__ __forceinline__ void issue_shared_units(const LayerPtrs& P, uint8_t* s_static, uint64_t* bar, int H,
                                                 int c, int G, int my_sh, int n_sh) {
   const int lane = threadIdx.x & 31;
   if (my_sh == 0) return;
@@ -655,7 +655,7 @@ __device__ __noinline__ void issue_shared_units(const LayerPtrs& P, uint8_t* s_s
 }
 
 // Routed units r = c, c + G, ... of the selected experts s_sel (one mbarrier each).
-__device__ __noinline__ void issue_routed_units(const LayerPtrs& P, uint8_t* s_routed, uint64_t* bars, int H,
+__device__ __forceinline__ void issue_routed_units(const LayerPtrs& P, uint8_t* s_routed, uint64_t* bars, int H,
                                                 int c, int G, int my_rt, int per_slot, int F, int E,
                                                 const int* s_sel) {
   const int lane = threadIdx.x & 31;
@@ -818,21 +818,23 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
       }
       __syncthreads();
       if (warp == 0) {
-        // merge the warps' candidates (distinct keys, in shared memory)
+        // merge the warps' candidates (keys are distinct); lane holds n_c / 32 of them
         const int n_c = nw_e * (a.K + 1);
+        constexpr int kCPL = (FLINT_MAX_EXPERTS / 32) * (FLINT_MAX_TOP_K + 1) / 32 + 1;
+        unsigned cl[kCPL];
+#pragma unroll
+        for (int j = 0; j < kCPL; ++j) cl[j] = (lane + 32 * j < n_c) ? s_cand[lane + 32 * j] : 0u;
         unsigned prev = 0u, mine = 0u;
         bool tie = s_tie != 0;
         for (int sr = 0; sr <= a.K; ++sr) {
-          unsigned m = 0u;
-#pragma unroll 1
-          for (int j = lane; j < n_c; j += 32) m = max(m, s_cand[j]);
+          unsigned m = cl[0];
+#pragma unroll
+          for (int j = 1; j < kCPL; ++j) m = max(m, cl[j]);
           const unsigned w = __reduce_max_sync(0xffffffffu, m);
           if (sr > 0 && w != 0u && (w >> ib) == (prev >> ib)) tie = true;
           prev = w;
-#pragma unroll 1
-          for (int j = lane; j < n_c; j += 32)
-            if (s_cand[j] == w) s_cand[j] = 0u;
-          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < kCPL; ++j) if (cl[j] == w) cl[j] = 0u;
           if (lane == sr) mine = w;
         }
         if (tie) {

@@ -291,6 +291,8 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
       }
     }
   } else if (warp == kWarpMMA && lane == 0) {
+    const uint64_t dA0 = umma_desc_sw128(sh(smem + C::a)), dB0 = umma_desc_sw128(sh(smem + C::b));
+    const uint64_t dSA0 = sf_desc(sh(smem + C::sfa)), dSB0 = sf_desc(sh(smem + C::sfb));
     uint32_t it = 0, done = 0;
     Item nxt = blockIdx.x < n_items ? load_item(g.items + blockIdx.x) : Item{0, 0, 0, 0};
     for (int i = blockIdx.x; i < n_items && !abort_flag; i += gridDim.x, ++done) {
@@ -304,25 +306,24 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
         const int s = it % S;
         if (!mb_wait(&full[s], (it / S) & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after();
-        uint8_t* st = smem + s * C::stride;
+        // descriptors of stage s: the stage-0 ones plus the stage offset (address field)
+        const uint64_t so = (uint64_t)(s * (C::stride >> 4));
         const uint32_t sf0 = tmem + C::dcols + (uint32_t)(s * 4 * C::sf_step);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint32_t sfs = sf0 + kk * C::sf_step;
-          tc_cp_sf(sfs, sf_desc(sh(st + C::sfa + kk * 512)));
+          tc_cp_sf(sfs, dSA0 + so + kk * (512 >> 4));
 #pragma unroll
-          for (int b = 0; b < C::kB; ++b) tc_cp_sf(sfs + 4 + 4 * b, sf_desc(sh(st + C::sfb + b * 2048 + kk * 512)));
+          for (int b = 0; b < C::kB; ++b) tc_cp_sf(sfs + 4 + 4 * b, dSB0 + so + ((b * 2048 + kk * 512) >> 4));
         }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint32_t sfs = sf0 + kk * C::sf_step;
-          const uint64_t ad = umma_desc_sw128(sh(st + C::a) + kk * 32);
           const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
 #pragma unroll
-          for (int b = 0; b < C::kB; ++b) {
-            const uint64_t bd = umma_desc_sw128(sh(st + C::b + b * 16384) + kk * 32);
-            mma_fp4(tmem + b * kBN, ad, bd, idesc, acc, sfs, sfs + 4 + 4 * b);
-          }
+          for (int b = 0; b < C::kB; ++b)
+            mma_fp4(tmem + b * kBN, dA0 + so + kk * 2, dB0 + so + ((b * 16384) >> 4) + kk * 2, idesc, acc, sfs,
+                    sfs + 4 + 4 * b);
         }
         tc_commit(&empty[s]);
       }
@@ -601,21 +602,45 @@ __global__ void __launch_bounds__(1024) k_scan(ScanArgs s) {
   __shared__ int s_cnt[FLINT_MAX_EXPERTS], s_toff[FLINT_MAX_EXPERTS];
   __shared__ int s_wsum[2][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = warp; e < a.E; e += 32) {
-    int run = 0;
-    for (int base = 0; base < a.W; base += 32) {
-      const int w = base + lane;
-      const int v = w < a.W ? __popc(a.bits[(size_t)e * a.W + w]) : 0;
-      int incl = v;
+  // per-expert prefix counts of the token bitmap words: warp w takes experts w, w + 32,
+  // ...; the words of all its experts are loaded before the scans (one latency)
+  constexpr int kEPW = 256 / 32;                     // experts per warp (E <= 256 here)
+  int run[kEPW];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
+  for (int q = 0; q < kEPW; ++q) run[q] = 0;
+  for (int base = 0; base < a.W; base += 128) {
+    int v[kEPW][4];
+#pragma unroll
+    for (int q = 0; q < kEPW; ++q) {
+      const int e = warp + 32 * q;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int w = base + 32 * k + lane;
+        v[q][k] = (e < a.E && w < a.W) ? __popc(__ldcg(a.bits + (size_t)e * a.W + w)) : 0;
       }
-      if (w < a.W) a.wordpre[(size_t)e * a.W + w] = run + incl - v;
-      run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) s_cnt[e] = run;
+#pragma unroll
+    for (int q = 0; q < kEPW; ++q) {
+      const int e = warp + 32 * q;
+      if (e >= a.E) continue;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int w = base + 32 * k + lane;
+        int incl = v[q][k];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += n;
+        }
+        if (w < a.W) a.wordpre[(size_t)e * a.W + w] = run[q] + incl - v[q][k];
+        run[q] += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < kEPW; ++q) {
+    const int e = warp + 32 * q;
+    if (e < a.E && lane == 0) s_cnt[e] = run[q];
   }
   __syncthreads();
   // exclusive scans over experts of the counts and of the 128-row tile counts
