@@ -654,25 +654,6 @@ __device__ __forceinline__ void issue_shared_units(const LayerPtrs& P, uint8_t* 
   }
 }
 
-// Routed units r = c, c + G, ... of the selected experts s_sel (one mbarrier each).
-__device__ __forceinline__ void issue_routed_units(const LayerPtrs& P, uint8_t* s_routed, uint64_t* bars, int H,
-                                                int c, int G, int my_rt, int per_slot, int F, int E,
-                                                const int* s_sel) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t ub = UnitLayout::of(H).bytes;
-  if (lane < my_rt) mbar_expect_tx(&bars[lane], ub);
-  __syncwarp();
-  for (int q = lane; q < 6 * my_rt; q += 32) {
-    const int i = q / 6, piece = q % 6;
-    const int r = c + i * G;
-    const int slot = r / per_slot, j = r % per_slot;
-    int e = s_sel[slot];
-    if (e < 0 || e >= E) { raise_status(FLINT_ERR_INVALID_ARG); e = 0; }
-    unit_copy_piece(piece, s_routed + (size_t)i * ub, &bars[i], H, P.gate, P.up, P.dcc_codes, P.dcc_scales,
-                    (size_t)e * F + (size_t)j * kUnit, (size_t)e, per_slot, j);
-  }
-}
-
 // ---------------------------------------------------------------- the kernel
 // Work of CTA c (of G) in every layer step, all CTAs running the same code:
 //   router rows      e = c, c + G, ...                       (< E)
@@ -790,17 +771,36 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
           st_tagged(a.logits_tag + c + threadIdx.x * G, ((unsigned long long)tag << 32) | __float_as_uint(v));
         }
       }
-      // ---- shared units' gate/up (need only x_l)
-      XStage<CPL, 1> xs;
-      pairs_from_smem<CPL>(xs.p[0], s_xf, sl, LPR);
-      xs.unscale = stg.unscale;
-      if (my_sh > 0) {
-        mbar_wait(&s_bar_sh, ph_sh, sync);
-        ph_sh ^= 1;
-        for (int i = 0; i < my_sh; ++i)
-          unit_gateup<CPL>(s_static + (size_t)i * U.bytes, H, P.sh_gate.tsc[0], P.sh_up.tsc[0], xs,
-                           s_gu + i * 2 * kUnit);
-        if (threadIdx.x < my_sh) s_dscale[threadIdx.x] = P.sh_down_tsc[0];
+      // ---- routed copy descriptors (lane q of warp 0: unit q / 6, piece q % 6), all but
+      // the expert, so that the copies go out right after the top-k
+      const uint8_t* cp_base = nullptr;
+      size_t cp_estride = 0;
+      uint32_t cp_dst = 0, cp_bytes = 0;
+      int cp_slot = 0;
+      if (warp == 0 && lane < 6 * my_rt) {
+        const int i = lane / 6, piece = lane % 6;
+        const int r = c + i * G;
+        cp_slot = r / per_slot;
+        const int j = r % per_slot;
+        const NVPtr& gu = piece < 2 ? P.gate : P.up;
+        if (piece < 4) {
+          const bool sc = piece & 1;
+          cp_base = sc ? gu.scales + (size_t)j * kUnit * (H / 16) : gu.codes + (size_t)j * kUnit * (H / 2);
+          cp_estride = sc ? (size_t)a.F * (H / 16) : (size_t)a.F * (H / 2);
+          cp_bytes = sc ? kUnit * (H / 16) : kUnit * (H / 2);
+          cp_dst = piece == 0 ? U.gc : piece == 1 ? U.gs : piece == 2 ? U.uc : U.us;
+        } else if (piece == 4) {
+          cp_base = P.dcc_codes + (size_t)j * H * 4;
+          cp_estride = (size_t)per_slot * H * 4;
+          cp_bytes = H * 4;
+          cp_dst = U.dc;
+        } else {
+          cp_base = P.dcc_scales + (size_t)(j / 2) * H;
+          cp_estride = (size_t)(per_slot / 2) * H;
+          cp_bytes = H;
+          cp_dst = U.ds;
+        }
+        cp_dst += (uint32_t)i * U.bytes;
       }
       // ---- all logits; each logit warp selects its K + 1 best while the rest arrive
       if (warp < nw_e) {
@@ -818,29 +818,40 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
       }
       __syncthreads();
       if (warp == 0) {
-        // merge the warps' candidates (keys are distinct); lane holds n_c / 32 of them
-        const int n_c = nw_e * (a.K + 1);
-        constexpr int kCPL = (FLINT_MAX_EXPERTS / 32) * (FLINT_MAX_TOP_K + 1) / 32 + 1;
-        unsigned cl[kCPL];
-#pragma unroll
-        for (int j = 0; j < kCPL; ++j) cl[j] = (lane + 32 * j < n_c) ? s_cand[lane + 32 * j] : 0u;
-        unsigned prev = 0u, mine = 0u;
+        // merge the warps' sorted candidate lists: lane w < nw_e holds the head of list w;
+        // each round takes the largest head (keys are distinct) and that lane advances
         bool tie = s_tie != 0;
+        int pos = 0;
+        unsigned head = lane < nw_e ? s_cand[lane * (a.K + 1)] : 0u;
+        unsigned prev = 0u, mine = 0u;
         for (int sr = 0; sr <= a.K; ++sr) {
-          unsigned m = cl[0];
-#pragma unroll
-          for (int j = 1; j < kCPL; ++j) m = max(m, cl[j]);
-          const unsigned w = __reduce_max_sync(0xffffffffu, m);
+          const unsigned w = __reduce_max_sync(0xffffffffu, head);
           if (sr > 0 && w != 0u && (w >> ib) == (prev >> ib)) tie = true;
           prev = w;
-#pragma unroll
-          for (int j = 0; j < kCPL; ++j) if (cl[j] == w) cl[j] = 0u;
           if (lane == sr) mine = w;
+          if (head == w && w != 0u) {
+            ++pos;
+            head = pos <= a.K ? s_cand[lane * (a.K + 1) + pos] : 0u;
+          }
         }
         if (tie) {
           topk_exact_dispatch(s_logits, a.E, a.K, s_sel, s_w);
-        } else {
-          const int e = (int)((1u << ib) - 1u - (mine & ((1u << ib) - 1u)));
+          __syncwarp();
+        } else if (lane < a.K) {
+          s_sel[lane] = (int)((1u << ib) - 1u - (mine & ((1u << ib) - 1u)));
+        }
+        __syncwarp();
+        // routed copies first: they gate the critical path
+        if (lane < my_rt) mbar_expect_tx(&s_bar_rt[lane], U.bytes);
+        __syncwarp();
+        if (lane < 6 * my_rt) {
+          int e = s_sel[cp_slot];
+          if (e < 0 || e >= a.E) { raise_status(FLINT_ERR_INVALID_ARG); e = 0; }
+          bulk_g2s(s_routed + cp_dst, cp_base + (size_t)e * cp_estride, cp_bytes, &s_bar_rt[lane / 6]);
+        }
+        // then the routing weights (needed only by the down pass)
+        if (!tie) {
+          const int e = lane < a.K ? s_sel[lane] : 0;
           float lv = lane < a.K ? s_logits[e] : 0.f;
           lv = (lv == lv) ? lv : -INFINITY;
           const float l0 = __shfl_sync(0xffffffffu, lv, 0);
@@ -848,14 +859,23 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
           float z = pr;
 #pragma unroll
           for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-          if (lane < a.K) { s_sel[lane] = e; s_w[lane] = pr / z; }
+          if (lane < a.K) s_w[lane] = pr / z;
         }
-        __syncwarp();
-        // routed copies (with the next layer's router rows behind them)
-        issue_routed_units(P, s_routed, s_bar_rt, H, c, G, my_rt, per_slot, a.F, a.E, s_sel);
-        if (more) issue_router_rows(a.layer[l_next], s_router, &s_bar_rr, H, c, G, my_rows);
       }
-      __syncthreads();
+      // ---- shared units' gate/up while the routed copies are in flight
+      XStage<CPL, 1> xs;
+      pairs_from_smem<CPL>(xs.p[0], s_xf, sl, LPR);
+      xs.unscale = stg.unscale;
+      if (my_sh > 0) {
+        mbar_wait(&s_bar_sh, ph_sh, sync);
+        ph_sh ^= 1;
+        for (int i = 0; i < my_sh; ++i)
+          unit_gateup<CPL>(s_static + (size_t)i * U.bytes, H, P.sh_gate.tsc[0], P.sh_up.tsc[0], xs,
+                           s_gu + i * 2 * kUnit);
+        if (threadIdx.x < my_sh) s_dscale[threadIdx.x] = P.sh_down_tsc[0];
+      }
+      __syncthreads();                               // s_sel / s_w visible to all
+      if (more && warp == 0) issue_router_rows(a.layer[l_next], s_router, &s_bar_rr, H, c, G, my_rows);
       if (c == 0 && threadIdx.x < a.K) {
         const size_t o = ((size_t)t * a.L + l) * a.K + threadIdx.x;
         if (a.idx_out) a.idx_out[o] = s_sel[threadIdx.x];

@@ -449,23 +449,23 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
 }
 
 // ---------------------------------------------------------------- router GEMM (bf16)
-// logits[t][e] = x[t] . Wr[e] (+ bias[e]) for 128 tokens x 64 experts per CTA; A = x rows
-// (TMA, 64 bf16 = 128 B per K-tile), B = 64 router rows, tcgen05 kind::f16 (K = 16 per
-// instruction).
-constexpr int kRStages = 8;
-constexpr int kRN = 64;
+// Partial logits over one K split: part[ks][t][e] = x[t, K_ks] . Wr[e, K_ks] for 128 tokens
+// and all E (<= 256) experts per CTA; A = x rows (TMA, 64 bf16 = 128 B per K-tile), B =
+// the router rows, tcgen05 kind::f16 (K = 16 per instruction), one N = E instruction per
+// K = 16.  The top-k kernel sums the kRSplit partials in order and adds the bias.
+constexpr int kRStages = 4;
+constexpr int kRSplit = 4;
 constexpr int kRThreads = 256;
 
 struct RouterArgs {
   CUtensorMap mapX;
   CUtensorMap mapW;
-  const float* bias;
-  float* logits;
+  float* part;             // [kRSplit][T][E]
   int T, E, H;
 };
 
 __global__ void __launch_bounds__(kRThreads, 1) k_router_gemm(const __grid_constant__ RouterArgs g) {
-  constexpr int kStageBytes = 16384 + kRN * 128;
+  constexpr int kStageBytes = 16384 + 256 * 128;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t full[kRStages], empty[kRStages], accf;
@@ -479,37 +479,38 @@ __global__ void __launch_bounds__(kRThreads, 1) k_router_gemm(const __grid_const
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kWarpMMA) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(sh(&tmem_base)), "r"(kRN));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(sh(&tmem_base)), "r"(256));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const int row0 = blockIdx.x * kBM, n0 = blockIdx.y * kRN;
-  const int kt_n = g.H / 64;
-  const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kRN >> 3) << 17) |
+  const int row0 = blockIdx.x * kBM, ks = blockIdx.y;
+  const int kt_n = g.H / 64 / kRSplit, kt0 = ks * kt_n;
+  const uint32_t stage_bytes = 16384 + (uint32_t)g.E * 128;
+  const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(g.E >> 3) << 17) |
                          ((uint32_t)(kBM >> 4) << 24);
   if (warp == kWarpTMA && lane == 0) {
     for (int kt = 0; kt < kt_n; ++kt) {
       const int s = kt % kRStages;
       if (kt >= kRStages && !mb_wait(&empty[s], ((kt / kRStages) - 1) & 1, &abort_flag)) break;
       uint8_t* st = smem + s * kStageBytes;
-      mb_expect(&full[s], kStageBytes);
-      tma2d(st, &g.mapX, kt * 128, row0, &full[s]);
-      tma2d(st + 16384, &g.mapW, kt * 128, n0, &full[s]);
+      mb_expect(&full[s], stage_bytes);
+      tma2d(st, &g.mapX, (kt0 + kt) * 128, row0, &full[s]);
+      tma2d(st + 16384, &g.mapW, (kt0 + kt) * 128, 0, &full[s]);
     }
   } else if (warp == kWarpMMA && lane == 0) {
+    const uint64_t dA0 = umma_desc_sw128(sh(smem)), dB0 = umma_desc_sw128(sh(smem + 16384));
     bool ok = true;
     for (int kt = 0; kt < kt_n; ++kt) {
       const int s = kt % kRStages;
       if (!mb_wait(&full[s], (kt / kRStages) & 1, &abort_flag)) { ok = false; break; }
       tc_fence_after();
-      uint8_t* st = smem + s * kStageBytes;
+      const uint64_t so = (uint64_t)(s * (kStageBytes >> 4));
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        mma_bf16(tmem, umma_desc_sw128(sh(st) + kk * 32), umma_desc_sw128(sh(st + 16384) + kk * 32), idesc,
-                 (kt > 0 || kk > 0) ? 1u : 0u);
+        mma_bf16(tmem, dA0 + so + kk * 2, dB0 + so + kk * 2, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
       tc_commit(&empty[s]);
     }
     if (ok) tc_commit(&accf);
@@ -518,18 +519,16 @@ __global__ void __launch_bounds__(kRThreads, 1) k_router_gemm(const __grid_const
     const int t = row0 + q * 32 + lane;
     if (mb_wait(&accf, 0, &abort_flag)) {
       tc_fence_after();
-#pragma unroll
-      for (int c0 = 0; c0 < kRN; c0 += 16) {
+      float* dst = g.part + ((size_t)ks * g.T + t) * g.E;
+      for (int c0 = 0; c0 < g.E; c0 += 16) {
         uint32_t v[16];
         tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
         tmem_wait_ld();
-        if (t < g.T) {
+        if (t < g.T)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int e = n0 + c0 + j;
-            if (e < g.E) g.logits[(size_t)t * g.E + e] = __uint_as_float(v[j]) + (g.bias ? g.bias[e] : 0.f);
-          }
-        }
+          for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                                                   __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
       }
       tc_fence_before();
     }
@@ -546,14 +545,15 @@ __global__ void __launch_bounds__(kRThreads, 1) k_router_gemm(const __grid_const
     }
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(kRN));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(256));
   }
 }
 
 // ---------------------------------------------------------------- routing bookkeeping
 struct RouteArgs {
   int T, E, K, W;          // W = words per expert bitmap = ceil(T/32)
-  const float* logits;     // [T][E]
+  const float* part;       // [kRSplit][T][E] partial logits
+  const float* bias;       // [E] or null
   int32_t* idx;            // [T][K]
   float* w;                // [T][K]
   int32_t* idx_out;
@@ -566,15 +566,23 @@ struct RouteArgs {
   int32_t* counts_out;
 };
 
-// One warp per token: top-k (the decode path's warp top-k) and the expert bitmaps.
+// One warp per token: the logits (partials summed in order, plus the bias), top-k (the
+// decode path's warp top-k) and the expert bitmaps.
 __global__ void __launch_bounds__(256) k_topk(RouteArgs a) {
   __shared__ int s_sel[8][FLINT_MAX_TOP_K];
   __shared__ float s_w[8][FLINT_MAX_TOP_K];
+  __shared__ float s_lg[8][256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= a.T) return;
-  const float* lg = a.logits + (size_t)t * a.E;
-  topk_dispatch(lg, a.E, a.K, s_sel[warp], s_w[warp]);
+  for (int e = lane; e < a.E; e += 32) {
+    float v = a.part[(size_t)t * a.E + e];
+#pragma unroll
+    for (int ks = 1; ks < kRSplit; ++ks) v += a.part[((size_t)ks * a.T + t) * a.E + e];
+    s_lg[warp][e] = v + (a.bias ? a.bias[e] : 0.f);
+  }
+  __syncwarp();
+  topk_dispatch(s_lg[warp], a.E, a.K, s_sel[warp], s_w[warp]);
   if (lane < a.K) {
     const int e = s_sel[warp][lane];
     const float wv = s_w[warp][lane];
@@ -586,8 +594,40 @@ __global__ void __launch_bounds__(256) k_topk(RouteArgs a) {
   }
 }
 
-// One CTA: per-expert word prefix counts, expert offsets (plain and tile-padded), and
-// the item lists of both GEMMs.
+// One warp per expert: prefix counts of its token-bitmap words (the rank of a token
+// among the expert's tokens is wordpre + popc of the lower bits of its word) and the
+// expert's token count.
+__global__ void __launch_bounds__(256) k_expert_prefix(RouteArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp;
+  if (e >= a.E) return;
+  const unsigned* bits = a.bits + (size_t)e * a.W;
+  int* pre = a.wordpre + (size_t)e * a.W;
+  int run = 0;
+  for (int base = 0; base < a.W; base += 128) {
+    int v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int w = base + 32 * k + lane;
+      v[k] = w < a.W ? __popc(__ldcg(bits + w)) : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int w = base + 32 * k + lane;
+      int incl = v[k];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (w < a.W) pre[w] = run + incl - v[k];
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  if (lane == 0) a.counts[e] = run;
+}
+
+// One CTA: expert offsets (plain and tile-padded) and the item lists of both GEMMs.
 struct ScanArgs {
   RouteArgs r;
   Item* items_gu;          // gate/up items: shared first, then routed
@@ -602,46 +642,7 @@ __global__ void __launch_bounds__(1024) k_scan(ScanArgs s) {
   __shared__ int s_cnt[FLINT_MAX_EXPERTS], s_toff[FLINT_MAX_EXPERTS];
   __shared__ int s_wsum[2][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // per-expert prefix counts of the token bitmap words: warp w takes experts w, w + 32,
-  // ...; the words of all its experts are loaded before the scans (one latency)
-  constexpr int kEPW = 256 / 32;                     // experts per warp (E <= 256 here)
-  int run[kEPW];
-#pragma unroll
-  for (int q = 0; q < kEPW; ++q) run[q] = 0;
-  for (int base = 0; base < a.W; base += 128) {
-    int v[kEPW][4];
-#pragma unroll
-    for (int q = 0; q < kEPW; ++q) {
-      const int e = warp + 32 * q;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int w = base + 32 * k + lane;
-        v[q][k] = (e < a.E && w < a.W) ? __popc(__ldcg(a.bits + (size_t)e * a.W + w)) : 0;
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < kEPW; ++q) {
-      const int e = warp + 32 * q;
-      if (e >= a.E) continue;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int w = base + 32 * k + lane;
-        int incl = v[q][k];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int n = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += n;
-        }
-        if (w < a.W) a.wordpre[(size_t)e * a.W + w] = run[q] + incl - v[q][k];
-        run[q] += __shfl_sync(0xffffffffu, incl, 31);
-      }
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < kEPW; ++q) {
-    const int e = warp + 32 * q;
-    if (e < a.E && lane == 0) s_cnt[e] = run[q];
-  }
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_cnt[e] = __ldcg(a.counts + e);
   __syncthreads();
   // exclusive scans over experts of the counts and of the 128-row tile counts
   const int e = threadIdx.x;
@@ -660,7 +661,6 @@ __global__ void __launch_bounds__(1024) k_scan(ScanArgs s) {
   const int off = pc + ic - cnt, toff = pt + it - til;
   if (e < a.E) {
     s_toff[e] = toff;
-    a.counts[e] = cnt;
     a.offsets[e] = off;
     a.offp[e] = toff * kBM;
     if (a.counts_out) a.counts_out[e] = cnt;
@@ -848,7 +848,7 @@ static WsLayout ws_layout(int H, int E, int K, int F, int Fs, int T) {
   const size_t Tp = (T + kBM - 1) / kBM * kBM;
   const size_t mt_sh = Tp / kBM, mt_rt = Pp / kBM;
   size_t o = 0;
-  L.logits = o;   o += a256(sizeof(float) * T * E);
+  L.logits = o;   o += a256(sizeof(float) * kRSplit * T * E);
   L.idx = o;      o += a256(sizeof(int) * P);
   L.w = o;        o += a256(sizeof(float) * P);
   L.bits = o;     o += a256(sizeof(unsigned) * E * W);
@@ -928,7 +928,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st) {
   auto at = [&](size_t off) { return b + off; };
   RouteArgs r;
   r.T = T; r.E = E; r.K = K; r.W = (T + 31) / 32;
-  r.logits = reinterpret_cast<float*>(at(L.logits));
+  r.part = reinterpret_cast<float*>(at(L.logits));
+  r.bias = a.router_bias;
   r.idx = reinterpret_cast<int32_t*>(at(L.idx));
   r.w = reinterpret_cast<float*>(at(L.w));
   r.idx_out = a.idx_out; r.w_out = a.w_out;
@@ -941,16 +942,16 @@ cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(r.bits, 0, sizeof(unsigned) * E * r.W, st);
   if (e != cudaSuccess) return e;
 
-  // 1 router GEMM
+  // 1 router GEMM (partial logits over kRSplit K ranges)
   RouterArgs ra;
   memset(&ra, 0, sizeof(ra));
-  ra.bias = a.router_bias; ra.logits = reinterpret_cast<float*>(at(L.logits)); ra.T = T; ra.E = E; ra.H = H;
-  if (!make_map(&ra.mapX, a.x, T, (uint64_t)H * 2, kBM) || !make_map(&ra.mapW, a.router_w, E, (uint64_t)H * 2, kRN))
+  ra.part = reinterpret_cast<float*>(at(L.logits)); ra.T = T; ra.E = E; ra.H = H;
+  if (!make_map(&ra.mapX, a.x, T, (uint64_t)H * 2, kBM) || !make_map(&ra.mapW, a.router_w, E, (uint64_t)H * 2, E))
     return cudaErrorInvalidValue;
-  const int smem_r = kRStages * (16384 + kRN * 128) + 1024;
+  const int smem_r = kRStages * (16384 + 256 * 128) + 1024;
   e = cudaFuncSetAttribute(k_router_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_r);
   if (e != cudaSuccess) return e;
-  k_router_gemm<<<dim3((T + kBM - 1) / kBM, (E + kRN - 1) / kRN), kRThreads, smem_r, st>>>(ra);
+  k_router_gemm<<<dim3((T + kBM - 1) / kBM, kRSplit), kRThreads, smem_r, st>>>(ra);
 
   // 2 top-k + bitmaps, 3 scan + item lists, 4 scatter + quantise (+ out = x)
   k_topk<<<(T + 7) / 8, 256, 0, st>>>(r);
@@ -961,6 +962,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st) {
   sc.n_items_gu = reinterpret_cast<int*>(at(L.nitems));
   sc.n_items_dn = reinterpret_cast<int*>(at(L.nitems)) + 1;
   sc.H = H; sc.F = F; sc.Fs = Fs;
+  k_expert_prefix<<<(E + 7) / 8, 256, 0, st>>>(r);
   k_scan<<<1, 1024, 0, st>>>(sc);
   ScatterArgs sa;
   sa.r = r; sa.x = a.x; sa.H = H;
