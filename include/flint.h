@@ -218,8 +218,11 @@ flint_status flint_decode_tokens(const flint_moe_layer* layers, int n_layers,
  *  - All calls share the one array.  Calls whose kernels overlap on the GPU (other
  *    streams, other host threads) race on it and must be serialised by the caller.
  *    Each call clears what must start at zero; the rest is rewritten before use.
- *  - A shape whose scratch would exceed FLINT_NOALLOC_SCRATCH_BYTES is rejected with
- *    FLINT_ERR_UNSUPPORTED (every shape flint_decode_tokens supports fits).
+ *  - The array holds fewer copies of the router-logit board than a full workspace
+ *    (each CTA polls one copy; fewer copies only mean more CTAs polling each), down
+ *    to one.  A shape whose scratch exceeds FLINT_NOALLOC_SCRATCH_BYTES even with one
+ *    copy is rejected with FLINT_ERR_UNSUPPORTED (every shape flint_decode_tokens
+ *    supports fits).
  * Arguments and results are those of flint_decode_tokens.
  * -------------------------------------------------------------------------- */
 #define FLINT_NOALLOC_SCRATCH_BYTES (64 * 1024)

@@ -109,7 +109,7 @@ size_t flint_workspace_bytes(int op, int hidden, int n_experts, int top_k, int w
       return ((size_t)(n_tokens > 0 ? n_tokens : 1) * sizeof(unsigned int) + 255) & ~(size_t)255;
     case FLINT_OP_MOE_DECODE:
       (void)top_k; (void)width; (void)shared_width;
-      return flint::decode_workspace_bytes(hidden, n_experts);
+      return flint::decode_workspace_bytes(hidden, n_experts, flint::decode_tag_copies(n_experts));
     case FLINT_OP_LM_HEAD:
       return flint::lm_head_workspace_bytes(hidden, vocab, n_tokens);
     case FLINT_OP_MOE_PREFILL:
@@ -152,7 +152,7 @@ static flint_status decode_tokens_impl(const flint_moe_layer* layers, int n_laye
                                        const float* residual, int T, float rms_eps, float* out,
                                        void* x_out_bf16, float* logits, int32_t* argmax,
                                        int32_t* topk_idx, float* topk_w, void* ws,
-                                       size_t ws_bytes, flint_stream stream) {
+                                       size_t ws_bytes, flint_stream stream, int tag_copies = 0) {
   if (!layers || !x_bf16 || !ws) return FLINT_ERR_INVALID_ARG;
   if (n_layers <= 0 || T <= 0) return FLINT_ERR_INVALID_ARG;
   if (n_layers > FLINT_MAX_LAYERS) return FLINT_ERR_UNSUPPORTED;
@@ -179,9 +179,9 @@ static flint_status decode_tokens_impl(const flint_moe_layer* layers, int n_laye
       (argmax && !aligned4(argmax)) || (topk_idx && !aligned4(topk_idx)) ||
       (topk_w && !aligned4(topk_w)))
     return FLINT_ERR_ALIGNMENT;
+  if (tag_copies <= 0) tag_copies = flint::decode_tag_copies(L0.n_experts);
   if (!aligned256(ws) ||
-      ws_bytes < flint_workspace_bytes(FLINT_OP_MOE_DECODE, L0.hidden, L0.n_experts, L0.top_k,
-                                       L0.expert_width, L0.shared_width, 0, T))
+      ws_bytes < flint::decode_workspace_bytes(L0.hidden, L0.n_experts, tag_copies))
     return FLINT_ERR_WORKSPACE;
   const flint::DecodePlan plan =
       flint::decode_plan(L0.hidden, L0.n_experts, L0.top_k, L0.expert_width, L0.shared_width,
@@ -193,6 +193,7 @@ static flint_status decode_tokens_impl(const flint_moe_layer* layers, int n_laye
   a.max_shared_units = plan.shared_units;
   a.H = L0.hidden; a.E = L0.n_experts; a.K = L0.top_k; a.F = L0.expert_width;
   a.Fs = L0.shared_width; a.L = n_layers; a.T = T; a.eps = rms_eps;
+  a.tag_copies = tag_copies;
   a.x = static_cast<const uint16_t*>(x_bf16);
   a.residual = residual;
   a.out = out;

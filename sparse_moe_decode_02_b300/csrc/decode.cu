@@ -53,6 +53,7 @@ constexpr int kSyncWords = 128;
 // Copies of the residual accumulator: unit u adds into copy u % kAccCopies, which
 // spreads the atomic traffic; readers sum the copies in a fixed order.
 constexpr int kAccCopies = 2;
+constexpr int kTagBoardBytes = 128 * 1024;   // logit board copies (see decode_tag_copies)
 
 // ---------------------------------------------------------------- sync primitives
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
@@ -123,6 +124,11 @@ __device__ __forceinline__ float wait_tagged(const unsigned long long* p, unsign
       }
     }
   }
+}
+
+// Barrier `id` (1-15) over the first `n` threads of the CTA (a multiple of 32).
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
 }
 
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
@@ -322,16 +328,16 @@ __device__ __forceinline__ void unit_copy_piece(int piece, uint8_t* buf, uint64_
   bulk_g2s(buf + dst, src, bytes, bar);
 }
 
-// Gate/up of one unit from shared memory: the 16 row dot products (a warp per row),
-// with tensor scales and 2^-k applied, into s_gu[0..16).  No barrier.
+// Gate/up of one unit from shared memory: the 16 row dot products (a warp per row, by
+// warps [w0, w0 + nw)), with tensor scales and 2^-k applied, into s_gu[0..16).  No barrier.
 template <int CPL>
 __device__ __forceinline__ void unit_gateup(const uint8_t* buf, int H, float gate_tsc, float up_tsc,
-                                            const XStage<CPL, 1>& xs, float* s_gu) {
+                                            const XStage<CPL, 1>& xs, float* s_gu, int w0, int nw) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int LPR = H / (32 * CPL), RPP = 32 / LPR;
   const int slice = lane / LPR, sl = lane % LPR;
   const UnitLayout U = UnitLayout::of(H);
-  for (int r0 = warp * RPP; r0 < 2 * kUnit; r0 += kPWarps * RPP) {
+  for (int r0 = (warp - w0) * RPP; r0 < 2 * kUnit; r0 += nw * RPP) {
     const int r = r0 + slice;
     const int rr = r < 2 * kUnit ? r : 0;
     const bool is_up = rr >= kUnit;
@@ -675,12 +681,13 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
   __shared__ float s_rp[kPWarps];
   __shared__ int s_sel[FLINT_MAX_TOP_K];
   __shared__ float s_w[FLINT_MAX_TOP_K];
-  __shared__ unsigned s_cand[(FLINT_MAX_EXPERTS / 32) * (FLINT_MAX_TOP_K + 1)];
-  __shared__ int s_tie;
+  __shared__ unsigned s_wmax[FLINT_MAX_EXPERTS / 32];
+  __shared__ int s_nc;
+  __shared__ float s_lsel[FLINT_MAX_TOP_K];
   __shared__ float s_bv[kPWarps];
   __shared__ int s_bi[kPWarps];
   __shared__ float s_red[2 * kPWarps];
-  __shared__ float s_logits[FLINT_MAX_EXPERTS];
+  __shared__ unsigned long long s_c64[FLINT_MAX_EXPERTS];
   __shared__ float s_bias[kMaxRouterRows];
   __shared__ __align__(8) uint64_t s_bar_rr, s_bar_sh;
   __shared__ __align__(8) uint64_t s_bar_rt[kMaxRoutedUnits];
@@ -703,8 +710,9 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
   const int my_rows = c < a.E ? (a.E - 1 - c) / G + 1 : 0;
   const int my_sh = (G - 1 - c) < n_sh ? (n_sh - 1 - (G - 1 - c)) / G + 1 : 0;
   const int my_rt = c < n_rt ? (n_rt - 1 - c) / G + 1 : 0;
-  const int ib = a.E > 256 ? 9 : 8;                 // index bits of the packed top-k keys
-  const int nw_e = (a.E + 31) / 32;                 // warps that hold logits
+  const int nw_e = (a.E + 31) / 32;                 // warps that poll the logits
+  const bool early_sh = nw_e < kPWarps;             // the others run the shared gate/up meanwhile
+  const unsigned long long* board = a.logits_tag + (size_t)(c % a.tag_copies) * a.tag_stride;
   unsigned* sync = a.bar;
   uint32_t ph_rr = 0, ph_sh = 0, ph_rt = 0;         // mbarrier parities
 
@@ -733,7 +741,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
       const unsigned tag = step + 1;
       for (int i = threadIdx.x; i < my_rows; i += kPThreads)
         s_bias[i] = P.router_bias ? __ldg(P.router_bias + c + i * G) : 0.f;
-      if (threadIdx.x == 0) s_tie = 0;               // read after the barriers below
+      if (threadIdx.x == 0) s_nc = 0;                // read after the barriers below
       // ---- h_l complete: stage x_l
       if (step > 0) wait_count(sync, kSyncDone, (unsigned)G * step);
       const Staged stg = cta_stage(l == 0 ? nullptr : acc_cur, a.x + (size_t)t * H,
@@ -766,13 +774,17 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         acc = sum_lanes<32>(acc);
         if (lane == 0) s_rp[warp] = acc;
         __syncthreads();
-        if (threadIdx.x < my_rows) {
-          const float v = (s_rp[2 * threadIdx.x] + s_rp[2 * threadIdx.x + 1]) + s_bias[threadIdx.x];
-          st_tagged(a.logits_tag + c + threadIdx.x * G, ((unsigned long long)tag << 32) | __float_as_uint(v));
+        // every board copy gets the rows; readers spread their polls over the copies
+        for (int q = threadIdx.x; q < my_rows * a.tag_copies; q += kPThreads) {
+          const int rr = q % my_rows, cp = q / my_rows;
+          const float v = (s_rp[2 * rr] + s_rp[2 * rr + 1]) + s_bias[rr];
+          st_tagged(a.logits_tag + (size_t)cp * a.tag_stride + c + rr * G,
+                    ((unsigned long long)tag << 32) | __float_as_uint(v));
         }
       }
       // ---- routed copy descriptors (lane q of warp 0: unit q / 6, piece q % 6), all but
-      // the expert, so that the copies go out right after the top-k
+      // the expert, computed before the poll so that the copies go out right after the
+      // top-k
       const uint8_t* cp_base = nullptr;
       size_t cp_estride = 0;
       uint32_t cp_dst = 0, cp_bytes = 0;
@@ -802,58 +814,61 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         }
         cp_dst += (uint32_t)i * U.bytes;
       }
-      // ---- all logits; each logit warp selects its K + 1 best while the rest arrive
+      asm volatile("" :: "l"(cp_base), "l"(cp_estride), "r"(cp_dst), "r"(cp_bytes), "r"(cp_slot));
+      XStage<CPL, 1> xs;
+      pairs_from_smem<CPL>(xs.p[0], s_xf, sl, LPR);
+      xs.unscale = stg.unscale;
       if (warp < nw_e) {
+        // ---- top-k.  Every logit is polled by one thread; the K-th largest of the warp
+        // maxima is a threshold that the K best logits all reach (at least K warps hold
+        // a logit at or above it).  The logits at or above it are ranked exactly by
+        // (value, lower index first).
         const int i = threadIdx.x;
-        unsigned key = 0u;
+        unsigned key = 0u;                             // 0: no logit; every logit's key is >= 1
+        float v = -INFINITY;
         if (i < a.E) {
-          const float v = wait_tagged(a.logits_tag + i, tag, sync);
-          s_logits[i] = v;
-          key = packed_key(v, i, ib);
+          v = wait_tagged(board + i, tag, sync);
+          v = (v == v) ? v : -INFINITY;
+          key = order_key(v);
         }
-        bool tie;
-        const unsigned cand = warp_select(key, a.K + 2, ib, tie);
-        if (lane <= a.K) s_cand[warp * (a.K + 1) + lane] = cand;
-        if (tie && lane == 0) atomicOr(&s_tie, 1);
-      }
-      __syncthreads();
-      if (warp == 0) {
-        // merge the warps' sorted candidate lists: lane w < nw_e holds the head of list w;
-        // each round takes the largest head (keys are distinct) and that lane advances
-        bool tie = s_tie != 0;
-        int pos = 0;
-        unsigned head = lane < nw_e ? s_cand[lane * (a.K + 1)] : 0u;
-        unsigned prev = 0u, mine = 0u;
-        for (int sr = 0; sr <= a.K; ++sr) {
-          const unsigned w = __reduce_max_sync(0xffffffffu, head);
-          if (sr > 0 && w != 0u && (w >> ib) == (prev >> ib)) tie = true;
-          prev = w;
-          if (lane == sr) mine = w;
-          if (head == w && w != 0u) {
-            ++pos;
-            head = pos <= a.K ? s_cand[lane * (a.K + 1) + pos] : 0u;
+        const unsigned wm = __reduce_max_sync(0xffffffffu, key);
+        if (lane == 0) s_wmax[warp] = wm;
+        named_bar(1, nw_e * 32);
+        unsigned thr = 0u;
+        if (nw_e >= a.K) {
+          const unsigned m = lane < nw_e ? s_wmax[lane] : 0u;
+          int ge = 0;
+          for (int u = 0; u < nw_e; ++u) ge += __shfl_sync(0xffffffffu, m, u) >= m ? 1 : 0;
+          thr = __reduce_max_sync(0xffffffffu, (lane < nw_e && ge >= a.K) ? m : 0u);
+        }
+        const bool cand = key != 0u && key >= thr;
+        const unsigned long long ck = ((unsigned long long)key << 32) | (unsigned)(~i);
+        const unsigned bal = __ballot_sync(0xffffffffu, cand);
+        int base = 0;
+        if (lane == 0 && bal) base = atomicAdd(&s_nc, __popc(bal));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (cand) s_c64[base + __popc(bal & ((1u << lane) - 1u))] = ck;
+        named_bar(1, nw_e * 32);
+        if (cand) {
+          const int n = s_nc;
+          int rank = 0;
+          for (int j = 0; j < n; ++j) rank += s_c64[j] > ck ? 1 : 0;
+          if (rank < a.K) { s_sel[rank] = i; s_lsel[rank] = v; }
+        }
+        named_bar(1, nw_e * 32);
+        if (warp == 0) {
+          // routed copies first: they gate the critical path
+          if (lane < my_rt) mbar_expect_tx(&s_bar_rt[lane], U.bytes);
+          __syncwarp();
+          if (lane < 6 * my_rt) {
+            int e = s_sel[cp_slot];
+            if (e < 0 || e >= a.E) { raise_status(FLINT_ERR_INVALID_ARG); e = 0; }
+            bulk_g2s(s_routed + cp_dst, cp_base + (size_t)e * cp_estride, cp_bytes, &s_bar_rt[lane / 6]);
           }
         }
-        if (tie) {
-          topk_exact_dispatch(s_logits, a.E, a.K, s_sel, s_w);
-          __syncwarp();
-        } else if (lane < a.K) {
-          s_sel[lane] = (int)((1u << ib) - 1u - (mine & ((1u << ib) - 1u)));
-        }
-        __syncwarp();
-        // routed copies first: they gate the critical path
-        if (lane < my_rt) mbar_expect_tx(&s_bar_rt[lane], U.bytes);
-        __syncwarp();
-        if (lane < 6 * my_rt) {
-          int e = s_sel[cp_slot];
-          if (e < 0 || e >= a.E) { raise_status(FLINT_ERR_INVALID_ARG); e = 0; }
-          bulk_g2s(s_routed + cp_dst, cp_base + (size_t)e * cp_estride, cp_bytes, &s_bar_rt[lane / 6]);
-        }
-        // then the routing weights (needed only by the down pass)
-        if (!tie) {
-          const int e = lane < a.K ? s_sel[lane] : 0;
-          float lv = lane < a.K ? s_logits[e] : 0.f;
-          lv = (lv == lv) ? lv : -INFINITY;
+        if (warp == (nw_e > 1 ? 1 : 0)) {
+          // routing weights: softmax over the selected, renormalised
+          const float lv = lane < a.K ? s_lsel[lane] : 0.f;
           const float l0 = __shfl_sync(0xffffffffu, lv, 0);
           const float pr = lane < a.K ? expf(lv - l0) : 0.f;
           float z = pr;
@@ -861,25 +876,36 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
           for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
           if (lane < a.K) s_w[lane] = pr / z;
         }
-      }
-      // ---- shared units' gate/up while the routed copies are in flight
-      XStage<CPL, 1> xs;
-      pairs_from_smem<CPL>(xs.p[0], s_xf, sl, LPR);
-      xs.unscale = stg.unscale;
-      if (my_sh > 0) {
+      } else if (my_sh > 0) {
+        // ---- shared units' gate/up by the warps that do not poll
         mbar_wait(&s_bar_sh, ph_sh, sync);
-        ph_sh ^= 1;
         for (int i = 0; i < my_sh; ++i)
           unit_gateup<CPL>(s_static + (size_t)i * U.bytes, H, P.sh_gate.tsc[0], P.sh_up.tsc[0], xs,
-                           s_gu + i * 2 * kUnit);
-        if (threadIdx.x < my_sh) s_dscale[threadIdx.x] = P.sh_down_tsc[0];
+                           s_gu + i * 2 * kUnit, nw_e, kPWarps - nw_e);
       }
-      __syncthreads();                               // s_sel / s_w visible to all
+      if (!early_sh && my_sh > 0) {
+        // (every warp polls: the shared gate/up follows the top-k)
+        __syncthreads();
+        mbar_wait(&s_bar_sh, ph_sh, sync);
+        for (int i = 0; i < my_sh; ++i)
+          unit_gateup<CPL>(s_static + (size_t)i * U.bytes, H, P.sh_gate.tsc[0], P.sh_up.tsc[0], xs,
+                           s_gu + i * 2 * kUnit, 0, kPWarps);
+      }
+      if (my_sh > 0) ph_sh ^= 1;
+      if (threadIdx.x < my_sh) s_dscale[threadIdx.x] = P.sh_down_tsc[0];
+      __syncthreads();                               // s_sel, s_w and the shared s_gu visible
       if (more && warp == 0) issue_router_rows(a.layer[l_next], s_router, &s_bar_rr, H, c, G, my_rows);
       if (c == 0 && threadIdx.x < a.K) {
         const size_t o = ((size_t)t * a.L + l) * a.K + threadIdx.x;
         if (a.idx_out) a.idx_out[o] = s_sel[threadIdx.x];
         if (a.w_out) a.w_out[o] = s_w[threadIdx.x];
+      }
+      // ---- shared units' SwiGLU and down while the routed copies are in flight
+      float part[4] = {0.f, 0.f, 0.f, 0.f};
+      if (my_sh > 0) {
+        if (warp == 0) stage_swiglu(my_sh, s_gu, s_dscale, s_hs);
+        __syncthreads();
+        for (int u = 0; u < my_sh; ++u) unit_down(s_static + (size_t)u * U.bytes, H, s_hs + u * (kUnit + 1), part);
       }
       // ---- routed units' gate/up, each as soon as its copy lands
       for (int i = 0; i < my_rt; ++i) {
@@ -889,24 +915,23 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         if (e < 0 || e >= a.E) e = 0;
         mbar_wait(&s_bar_rt[i], ph_rt, sync);
         unit_gateup<CPL>(s_routed + (size_t)i * U.bytes, H, P.gate.tsc[e], P.up.tsc[e], xs,
-                         s_gu + (my_sh + i) * 2 * kUnit);
+                         s_gu + (my_sh + i) * 2 * kUnit, 0, kPWarps);
         if (threadIdx.x == 0) s_dscale[my_sh + i] = P.down_tsc[e] * s_w[slot];
       }
       ph_rt ^= 1;
       __syncthreads();
-      // ---- SwiGLU of all units, then one down pass over them
-      const int n_units = my_sh + my_rt;
-      if (warp == 0) stage_swiglu(n_units, s_gu, s_dscale, s_hs);
-      __syncthreads();
-      float part[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int u = 0; u < n_units; ++u)
-        unit_down(u < my_sh ? s_static + (size_t)u * U.bytes : s_routed + (size_t)(u - my_sh) * U.bytes, H,
-                  s_hs + u * (kUnit + 1), part);
-      if (n_units > 0 && 4 * threadIdx.x < H)
-        red_add_v4(acc_out + (c % kAccCopies) * H + 4 * threadIdx.x, part[0], part[1], part[2], part[3]);
-      signal_count(sync, kSyncDone);                 // begins with a CTA barrier
       // the shared-unit buffers are free again
       if (more && warp == 0) issue_shared_units(a.layer[l_next], s_static, &s_bar_sh, H, c, G, my_sh, n_sh);
+      // ---- routed units' SwiGLU and down
+      if (my_rt > 0) {
+        if (warp == 0) stage_swiglu(my_rt, s_gu + my_sh * 2 * kUnit, s_dscale + my_sh, s_hs + my_sh * (kUnit + 1));
+        __syncthreads();
+        for (int u = 0; u < my_rt; ++u)
+          unit_down(s_routed + (size_t)u * U.bytes, H, s_hs + (my_sh + u) * (kUnit + 1), part);
+      }
+      if (my_sh + my_rt > 0 && 4 * threadIdx.x < H)
+        red_add_v4(acc_out + (c % kAccCopies) * H + 4 * threadIdx.x, part[0], part[1], part[2], part[3]);
+      signal_count(sync, kSyncDone);                 // begins with a CTA barrier
     }
     // ---------------- outputs of token t
     wait_count(sync, kSyncDone, (unsigned)G * step);
@@ -992,19 +1017,30 @@ cudaError_t launch_column_chunks(const uint8_t* codes, const uint8_t* scales, in
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Bytes at the start of the workspace that every launch clears: sync words + tags.
-static size_t decode_cleared_bytes(int H, int E) {
-  return sizeof(unsigned) * kSyncWords + align256(sizeof(unsigned long long) * E) +
+// Copies of the logit board: each logit is written to every copy and CTA c polls copy
+// c % copies, so the polls of all CTAs do not pile onto the same few L2 lines.
+int decode_tag_stride(int E) { return (E + 15) & ~15; }   // 128-byte rows
+int decode_tag_copies(int E) {
+  const int c = kTagBoardBytes / (8 * decode_tag_stride(E));
+  return c < 1 ? 1 : (c > kMaxCtas ? kMaxCtas : c);
+}
+
+static size_t decode_cleared_bytes(int H, int E, int copies) {
+  return sizeof(unsigned) * kSyncWords +
+         align256(sizeof(unsigned long long) * decode_tag_stride(E) * copies) +
          align256(sizeof(float) * 3 * kAccCopies * H);
 }
 
-size_t decode_workspace_bytes(int H, int E) {
-  return decode_cleared_bytes(H, E) + 2 * align256(2 * kMaxCtas * sizeof(float));
+size_t decode_workspace_bytes(int H, int E, int copies) {
+  return decode_cleared_bytes(H, E, copies) + 2 * align256(2 * kMaxCtas * sizeof(float));
 }
 
 void decode_carve(PersistArgs& a, void* ws) {
   char* p = static_cast<char*>(ws);
   a.bar = reinterpret_cast<unsigned*>(p); p += sizeof(unsigned) * kSyncWords;
-  a.logits_tag = reinterpret_cast<unsigned long long*>(p); p += align256(sizeof(unsigned long long) * a.E);
+  a.tag_stride = decode_tag_stride(a.E);
+  a.logits_tag = reinterpret_cast<unsigned long long*>(p);
+  p += align256(sizeof(unsigned long long) * a.tag_stride * a.tag_copies);
   a.acc = reinterpret_cast<float*>(p); p += align256(sizeof(float) * 3 * kAccCopies * a.H);
   a.best_v = reinterpret_cast<float*>(p); p += align256(2 * kMaxCtas * sizeof(float));
   a.best_i = reinterpret_cast<int*>(p);
@@ -1058,7 +1094,8 @@ cudaError_t launch_persistent(const PersistArgs& a, cudaStream_t st) {
   const DecodePlan p = decode_plan(a.H, a.E, a.K, a.F, a.Fs, decode_grid());
   if (!p.ok || a.max_router_rows != p.router_rows || a.max_shared_units != p.shared_units)
     return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaMemsetAsync(a.bar, 0, decode_cleared_bytes(a.H, a.E), st);
+  if (a.tag_copies < 1) return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(a.bar, 0, decode_cleared_bytes(a.H, a.E, a.tag_copies), st);
   if (e != cudaSuccess) return e;
   if (a.H <= 1024) return launch_persistent_cpl<1>(a, p.smem, st);
   return launch_persistent_cpl<2>(a, p.smem, st);

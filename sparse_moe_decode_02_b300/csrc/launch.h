@@ -39,7 +39,8 @@ struct PersistArgs {
   float* w_out;            // [T, L, K] or null
   // workspace
   unsigned* bar;           // grid barrier {arrivals, generation, abort}
-  unsigned long long* logits_tag;   // [E] {logit bits, step + 1}
+  unsigned long long* logits_tag;   // [tag_copies][tag_stride] {logit bits, step + 1}
+  int tag_copies, tag_stride;
   float* acc;              // [2][copies][H] residual ping-pong
   float* best_v;           // [grid]
   int* best_i;             // [grid]
@@ -56,9 +57,12 @@ struct DecodePlan {
 };
 DecodePlan decode_plan(int H, int E, int K, int F, int Fs, int G);
 
-size_t decode_workspace_bytes(int H, int E);
+// Workspace of the persistent decode with `copies` copies of the logit board;
+// decode_tag_copies(E) is the number a full workspace holds.
+size_t decode_workspace_bytes(int H, int E, int copies);
+int decode_tag_copies(int E);
 int decode_grid();                                   // CTAs of the persistent kernel
-void decode_carve(PersistArgs& a, void* ws);
+void decode_carve(PersistArgs& a, void* ws);          // a.H, a.E, a.tag_copies set
 cudaError_t launch_persistent(const PersistArgs& a, cudaStream_t st);
 cudaError_t launch_column_chunks(const uint8_t* codes, const uint8_t* scales, int n_mat, int rows,
                                  int cols, uint8_t* codes_cc, uint8_t* scales_cc, cudaStream_t st);

@@ -45,14 +45,18 @@ extern "C" flint_status flint_decode_tokens_noalloc(
     int32_t* argmax, int32_t* topk_idx, float* topk_w, flint_stream stream) {
   if (!layers || n_layers <= 0) return FLINT_ERR_INVALID_ARG;
   const flint_moe_layer& L0 = layers[0];
-  const size_t need = flint_workspace_bytes(FLINT_OP_MOE_DECODE, L0.hidden, L0.n_experts,
-                                            L0.top_k, L0.expert_width, L0.shared_width, 0, T);
-  if (need > flint::kNoAllocScratchBytes) return FLINT_ERR_UNSUPPORTED;
+  // as many copies of the logit board as the fixed array holds (at least one)
+  int copies = flint::decode_tag_copies(L0.n_experts);
+  while (copies > 1 && flint::decode_workspace_bytes(L0.hidden, L0.n_experts, copies) >
+                           flint::kNoAllocScratchBytes)
+    --copies;
+  if (flint::decode_workspace_bytes(L0.hidden, L0.n_experts, copies) > flint::kNoAllocScratchBytes)
+    return FLINT_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   if (flint::noalloc_scratch(&scratch) != cudaSuccess) return FLINT_ERR_CUDA;
   // The sync words at the start of the scratch are cleared by every launch; the rest
   // is written before it is read within one call.
   return decode_tokens_impl(layers, n_layers, head, x_bf16, residual, T, rms_eps, out,
                             x_out_bf16, logits, argmax, topk_idx, topk_w, scratch,
-                            flint::kNoAllocScratchBytes, stream);
+                            flint::kNoAllocScratchBytes, stream, copies);
 }
