@@ -337,6 +337,7 @@ __device__ __forceinline__ void unit_gateup(const uint8_t* buf, int H, float gat
   const int LPR = H / (32 * CPL), RPP = 32 / LPR;
   const int slice = lane / LPR, sl = lane % LPR;
   const UnitLayout U = UnitLayout::of(H);
+  #pragma unroll 1
   for (int r0 = (warp - w0) * RPP; r0 < 2 * kUnit; r0 += nw * RPP) {
     const int r = r0 + slice;
     const int rr = r < 2 * kUnit ? r : 0;
@@ -356,6 +357,7 @@ __device__ __forceinline__ void unit_gateup(const uint8_t* buf, int H, float gat
 __device__ __forceinline__ void stage_swiglu(int n, const float* s_gu, const float* s_dscale,
                                              uint32_t* s_hs) {
   const int lane = threadIdx.x & 31;
+  #pragma unroll 1
   for (int u0 = 0; u0 < n; u0 += 32 / kUnit) {
     const int u = u0 + lane / kUnit, j = lane % kUnit;
     const bool live = u < n;
@@ -652,6 +654,7 @@ __device__ __forceinline__ void issue_shared_units(const LayerPtrs& P, uint8_t* 
   const uint32_t ub = UnitLayout::of(H).bytes;
   if (lane == 0) mbar_expect_tx(bar, (uint32_t)my_sh * ub);
   __syncwarp();
+  #pragma unroll 1
   for (int q = lane; q < 6 * my_sh; q += 32) {
     const int i = q / 6, piece = q % 6;
     const int su = (G - 1 - c) + i * G;
@@ -739,6 +742,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
       const int l_next = (l + 1 < a.L) ? l + 1 : 0;
       const bool more = (l + 1 < a.L) || (t + 1 < a.T);
       const unsigned tag = step + 1;
+      #pragma unroll 1
       for (int i = threadIdx.x; i < my_rows; i += kPThreads)
         s_bias[i] = P.router_bias ? __ldg(P.router_bias + c + i * G) : 0.f;
       if (threadIdx.x == 0) s_nc = 0;                // read after the barriers below
@@ -748,6 +752,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
                                    (l == 0 && a.residual) ? a.residual + (size_t)t * H : nullptr,
                                    H, a.eps, s_hx, s_xb, s_xf, s_red);
       // ---- clear this CTA's share of B(step + 1) (published by this step's done signal)
+      #pragma unroll 1
       for (int n = 4 * (c + G * threadIdx.x); n < H; n += 4 * G * kPThreads)
 #pragma unroll
         for (int cp = 0; cp < kAccCopies; ++cp)
@@ -761,6 +766,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         if (r < my_rows) {
           float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
           const uint16_t* row = reinterpret_cast<const uint16_t*>(s_router) + (size_t)r * H;
+          #pragma unroll 1
           for (int e = 8 * tr; e < H; e += 8 * 64) {
             const uint4 wv = *reinterpret_cast<const uint4*>(row + e);
             const uint4 xv = *reinterpret_cast<const uint4*>(s_xb + e);
@@ -775,6 +781,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         if (lane == 0) s_rp[warp] = acc;
         __syncthreads();
         // every board copy gets the rows; readers spread their polls over the copies
+        #pragma unroll 1
         for (int q = threadIdx.x; q < my_rows * a.tag_copies; q += kPThreads) {
           const int rr = q % my_rows, cp = q / my_rows;
           const float v = (s_rp[2 * rr] + s_rp[2 * rr + 1]) + s_bias[rr];
@@ -838,6 +845,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         if (nw_e >= a.K) {
           const unsigned m = lane < nw_e ? s_wmax[lane] : 0u;
           int ge = 0;
+          #pragma unroll 1
           for (int u = 0; u < nw_e; ++u) ge += __shfl_sync(0xffffffffu, m, u) >= m ? 1 : 0;
           thr = __reduce_max_sync(0xffffffffu, (lane < nw_e && ge >= a.K) ? m : 0u);
         }
@@ -852,6 +860,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         if (cand) {
           const int n = s_nc;
           int rank = 0;
+          #pragma unroll 1
           for (int j = 0; j < n; ++j) rank += s_c64[j] > ck ? 1 : 0;
           if (rank < a.K) { s_sel[rank] = i; s_lsel[rank] = v; }
         }
@@ -879,6 +888,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
       } else if (my_sh > 0) {
         // ---- shared units' gate/up by the warps that do not poll
         mbar_wait(&s_bar_sh, ph_sh, sync);
+        #pragma unroll 1
         for (int i = 0; i < my_sh; ++i)
           unit_gateup<CPL>(s_static + (size_t)i * U.bytes, H, P.sh_gate.tsc[0], P.sh_up.tsc[0], xs,
                            s_gu + i * 2 * kUnit, nw_e, kPWarps - nw_e);
@@ -887,6 +897,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         // (every warp polls: the shared gate/up follows the top-k)
         __syncthreads();
         mbar_wait(&s_bar_sh, ph_sh, sync);
+        #pragma unroll 1
         for (int i = 0; i < my_sh; ++i)
           unit_gateup<CPL>(s_static + (size_t)i * U.bytes, H, P.sh_gate.tsc[0], P.sh_up.tsc[0], xs,
                            s_gu + i * 2 * kUnit, 0, kPWarps);
@@ -905,9 +916,11 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
       if (my_sh > 0) {
         if (warp == 0) stage_swiglu(my_sh, s_gu, s_dscale, s_hs);
         __syncthreads();
+        #pragma unroll 1
         for (int u = 0; u < my_sh; ++u) unit_down(s_static + (size_t)u * U.bytes, H, s_hs + u * (kUnit + 1), part);
       }
       // ---- routed units' gate/up, each as soon as its copy lands
+      #pragma unroll 1
       for (int i = 0; i < my_rt; ++i) {
         const int r = c + i * G;
         const int slot = r / per_slot;
@@ -926,6 +939,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
       if (my_rt > 0) {
         if (warp == 0) stage_swiglu(my_rt, s_gu + my_sh * 2 * kUnit, s_dscale + my_sh, s_hs + my_sh * (kUnit + 1));
         __syncthreads();
+        #pragma unroll 1
         for (int u = 0; u < my_rt; ++u)
           unit_down(s_routed + (size_t)u * U.bytes, H, s_hs + (my_sh + u) * (kUnit + 1), part);
       }
