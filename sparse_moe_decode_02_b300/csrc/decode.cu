@@ -42,7 +42,8 @@ constexpr int kPWarps = 16;
 constexpr int kPThreads = 32 * kPWarps;
 constexpr int kUnit = 8;            // SwiGLU outputs per unit (one 8-column chunk of down)
 constexpr int kMaxRouterRows = kPThreads / 64;   // router rows per CTA (64 threads each)
-constexpr int kMaxRoutedUnits = 6;  // routed units per CTA and step
+static_assert((kMaxRouterRows & (kMaxRouterRows - 1)) == 0, "router rows: a power of two");
+constexpr int kMaxRoutedUnits = 5;  // routed units per CTA and step (6 pieces each <= 32 lanes)
 constexpr int kMaxSharedUnits = 4;  // shared units per CTA
 constexpr int kMaxUnits = kMaxRoutedUnits + kMaxSharedUnits;
 constexpr size_t kMaxDecodeSmem = 220 * 1024;
@@ -301,32 +302,6 @@ struct UnitLayout {
     return u;
   }
 };
-
-// One of the six bulk copies of a unit (piece 0-5: gate codes, gate scales, up codes,
-// up scales, down codes, down scales): gate/up rows [row0, row0 + 8) of the stacks,
-// down code chunk `chunk` and scale block chunk / 2 of matrix `m`.  The six pieces are
-// issued by six lanes at once; the mbarrier's expected bytes are set beforehand.
-__device__ __forceinline__ void unit_copy_piece(int piece, uint8_t* buf, uint64_t* bar, int H,
-                                                const NVPtr& gate, const NVPtr& up,
-                                                const uint8_t* dcc_codes, const uint8_t* dcc_scales,
-                                                size_t row0, size_t m, int chunks_per_mat, int chunk) {
-  const UnitLayout L = UnitLayout::of(H);
-  const NVPtr& gu = piece < 2 ? gate : up;
-  const bool sc = piece & 1;
-  const uint8_t* src;
-  uint32_t dst, bytes;
-  if (piece < 4) {
-    src = sc ? gu.scales + row0 * (H / 16) : gu.codes + row0 * (H / 2);
-    dst = piece == 0 ? L.gc : piece == 1 ? L.gs : piece == 2 ? L.uc : L.us;
-    bytes = sc ? kUnit * (H / 16) : kUnit * (H / 2);
-  } else {
-    src = sc ? dcc_scales + (m * (chunks_per_mat / 2) + chunk / 2) * H
-             : dcc_codes + (m * chunks_per_mat + chunk) * H * 4;
-    dst = sc ? L.ds : L.dc;
-    bytes = sc ? H : H * 4;
-  }
-  bulk_g2s(buf + dst, src, bytes, bar);
-}
 
 // Gate/up of one unit from shared memory: the 16 row dot products (a warp per row, by
 // warps [w0, w0 + nw)), with tensor scales and 2^-k applied, into s_gu[0..16).  No barrier.
@@ -646,21 +621,86 @@ __device__ __forceinline__ void issue_router_rows(const LayerPtrs& P, uint8_t* s
     bulk_g2s(s_router + (size_t)lane * H * 2, P.router_w + (size_t)(c + lane * G) * H, H * 2, bar);
 }
 
-// ... and its shared units s = G-1-c, G-1-c + G, ...
-__device__ __forceinline__ void issue_shared_units(const LayerPtrs& P, uint8_t* s_static, uint64_t* bar, int H,
-                                                int c, int G, int my_sh, int n_sh) {
+// Layer-independent part of one bulk copy of a unit piece (see UnitLayout): the layer
+// matrix it reads (which), the byte offset in it, the per-expert stride (routed units),
+// the destination offset in the unit buffers and the size.  Lane q of warp 0 owns piece
+// q % 6 of unit q / 6; the descriptors are built once per launch.
+struct PieceDesc {
+  unsigned long long off, estride;
+  uint32_t dst, bytes;
+  int which, slot;            // which < 0: no piece for this lane
+};
+
+// Piece `piece` of unit row block `row0` (8 gate/up rows) / down column chunk `chunk`
+// of a stack whose matrices have F = rows_per_mat gate/up rows.
+__device__ __forceinline__ PieceDesc piece_desc(int piece, int H, size_t row0, int chunk,
+                                                size_t rows_per_mat, int chunks_per_mat) {
+  const UnitLayout L = UnitLayout::of(H);
+  PieceDesc d;
+  d.which = piece;
+  d.slot = 0;
+  const bool sc = piece & 1;
+  if (piece < 4) {
+    d.off = sc ? row0 * (H / 16) : row0 * (H / 2);
+    d.estride = sc ? rows_per_mat * (H / 16) : rows_per_mat * (H / 2);
+    d.bytes = sc ? kUnit * (H / 16) : kUnit * (H / 2);
+    d.dst = piece == 0 ? L.gc : piece == 1 ? L.gs : piece == 2 ? L.uc : L.us;
+  } else {
+    d.off = sc ? (size_t)(chunk / 2) * H : (size_t)chunk * H * 4;
+    d.estride = sc ? (size_t)(chunks_per_mat / 2) * H : (size_t)chunks_per_mat * H * 4;
+    d.bytes = sc ? H : H * 4;
+    d.dst = sc ? L.ds : L.dc;
+  }
+  return d;
+}
+
+// The matrix a routed (gate, up, down column chunks) or shared piece reads.
+__device__ __forceinline__ const uint8_t* piece_base(const LayerPtrs& P, int which, bool shared) {
+  const NVPtr& g = shared ? P.sh_gate : P.gate;
+  const NVPtr& u = shared ? P.sh_up : P.up;
+  switch (which) {
+    case 0: return g.codes;
+    case 1: return g.scales;
+    case 2: return u.codes;
+    case 3: return u.scales;
+    case 4: return shared ? P.sh_dcc_codes : P.dcc_codes;
+    default: return shared ? P.sh_dcc_scales : P.dcc_scales;
+  }
+}
+
+// Shared units of a layer (warp 0): data-independent, issued one layer ahead.
+__device__ __forceinline__ void issue_shared(const LayerPtrs& P, uint8_t* s_static, uint64_t* bar,
+                                             const PieceDesc* s_shd, int my_sh, uint32_t unit_bytes) {
   const int lane = threadIdx.x & 31;
   if (my_sh == 0) return;
-  const uint32_t ub = UnitLayout::of(H).bytes;
-  if (lane == 0) mbar_expect_tx(bar, (uint32_t)my_sh * ub);
+  if (lane == 0) mbar_expect_tx(bar, (uint32_t)my_sh * unit_bytes);
   __syncwarp();
-  #pragma unroll 1
-  for (int q = lane; q < 6 * my_sh; q += 32) {
-    const int i = q / 6, piece = q % 6;
-    const int su = (G - 1 - c) + i * G;
-    unit_copy_piece(piece, s_static + (size_t)i * ub, bar, H, P.sh_gate, P.sh_up, P.sh_dcc_codes,
-                    P.sh_dcc_scales, (size_t)su * kUnit, 0, n_sh, su);
-  }
+  const PieceDesc d = s_shd[lane];
+  if (d.which >= 0) bulk_g2s(s_static + d.dst, piece_base(P, d.which, true) + d.off, d.bytes, bar);
+}
+
+// ---------------------------------------------------------------- layer tables
+// The per-layer values every step reads, held in shared memory one layer ahead (the
+// kernel parameter's table sits in the constant bank, where each layer's first use
+// would miss): the pointer table, the shared expert's three tensor scales and this
+// CTA's router bias entries.
+struct LayerSmem {
+  LayerPtrs p;
+  float sh_tsc[3];              // shared gate, up, down tensor scales
+  float bias[kMaxRouterRows];   // router bias of rows c, c + G, ...
+};
+constexpr int kLayerWords = (int)(sizeof(LayerPtrs) / 8);
+static_assert(sizeof(LayerPtrs) % 8 == 0 && kLayerWords <= 32, "layer table: at most 32 words");
+
+// One warp: layer `l` into `dst`.
+__device__ __forceinline__ void load_layer(const PersistArgs& a, int l, LayerSmem* dst, int c, int G,
+                                           int my_rows) {
+  const int lane = threadIdx.x & 31;
+  const LayerPtrs& P = a.layer[l];
+  if (lane < kLayerWords)
+    reinterpret_cast<unsigned long long*>(&dst->p)[lane] = reinterpret_cast<const unsigned long long*>(&P)[lane];
+  if (lane < 3) dst->sh_tsc[lane] = __ldg(lane == 0 ? P.sh_gate.tsc : lane == 1 ? P.sh_up.tsc : P.sh_down_tsc);
+  if (lane < my_rows) dst->bias[lane] = P.router_bias ? __ldg(P.router_bias + c + lane * G) : 0.f;
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -684,14 +724,18 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
   __shared__ float s_rp[kPWarps];
   __shared__ int s_sel[FLINT_MAX_TOP_K];
   __shared__ float s_w[FLINT_MAX_TOP_K];
-  __shared__ unsigned s_wmax[FLINT_MAX_EXPERTS / 32];
-  __shared__ int s_nc;
   __shared__ float s_lsel[FLINT_MAX_TOP_K];
+  __shared__ unsigned s_wmax[8];
+  __shared__ int s_nc;
+  __shared__ int s_slot[kMaxRoutedUnits];
+  __shared__ PieceDesc s_rtd[32], s_shd[32];
   __shared__ float s_bv[kPWarps];
   __shared__ int s_bi[kPWarps];
   __shared__ float s_red[2 * kPWarps];
+  __shared__ float s_val[FLINT_MAX_EXPERTS];
   __shared__ unsigned long long s_c64[FLINT_MAX_EXPERTS];
-  __shared__ float s_bias[kMaxRouterRows];
+  __shared__ LayerSmem s_ly[2];                      // layer tables, by step parity
+  __shared__ float s_tsc[FLINT_MAX_TOP_K][3];         // selected experts: gate, up, down x weight
   __shared__ __align__(8) uint64_t s_bar_rr, s_bar_sh;
   __shared__ __align__(8) uint64_t s_bar_rt[kMaxRoutedUnits];
   extern __shared__ __align__(128) uint8_t s_dyn[];
@@ -713,38 +757,59 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
   const int my_rows = c < a.E ? (a.E - 1 - c) / G + 1 : 0;
   const int my_sh = (G - 1 - c) < n_sh ? (n_sh - 1 - (G - 1 - c)) / G + 1 : 0;
   const int my_rt = c < n_rt ? (n_rt - 1 - c) / G + 1 : 0;
-  const int nw_e = (a.E + 31) / 32;                 // warps that poll the logits
-  const bool early_sh = nw_e < kPWarps;             // the others run the shared gate/up meanwhile
+  const int nw_e = (a.E + 31) / 32;
+  const int npw = nw_e < 8 ? nw_e : 8;              // warps that poll the logits; the rest
+                                                    // run the shared gate/up meanwhile
   const unsigned long long* board = a.logits_tag + (size_t)(c % a.tag_copies) * a.tag_stride;
   unsigned* sync = a.bar;
   uint32_t ph_rr = 0, ph_sh = 0, ph_rt = 0;         // mbarrier parities
 
+  if (warp == kPWarps - 1) load_layer(a, 0, &s_ly[0], c, G, my_rows);
   if (threadIdx.x == 0) {
     mbar_init(&s_bar_rr, 1);
     mbar_init(&s_bar_sh, 1);
     for (int i = 0; i < kMaxRoutedUnits; ++i) mbar_init(&s_bar_rt[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // copy descriptors (lane q: piece q % 6 of unit q / 6) and routed-unit expert slots
+  if (warp == 0) {
+    const int q = lane, i = q / 6, piece = q % 6;
+    PieceDesc d = {0ull, 0ull, 0u, 0u, -1, 0};
+    if (i < my_rt) {
+      const int r = c + i * G;
+      d = piece_desc(piece, H, (size_t)(r % per_slot) * kUnit, r % per_slot, a.F, per_slot);
+      d.slot = r / per_slot;
+      d.dst += (uint32_t)i * U.bytes;
+    }
+    s_rtd[q] = d;
+    d = PieceDesc{0ull, 0ull, 0u, 0u, -1, 0};
+    if (i < my_sh) {
+      const int su = (G - 1 - c) + i * G;
+      d = piece_desc(piece, H, (size_t)su * kUnit, su, 0, n_sh);
+      d.dst += (uint32_t)i * U.bytes;
+    }
+    s_shd[q] = d;
+    if (lane < my_rt) s_slot[lane] = (c + lane * G) / per_slot;
+  }
   __syncthreads();
 
   if (warp == 0) {
     issue_router_rows(a.layer[0], s_router, &s_bar_rr, H, c, G, my_rows);
-    issue_shared_units(a.layer[0], s_static, &s_bar_sh, H, c, G, my_sh, n_sh);
+    issue_shared(a.layer[0], s_static, &s_bar_sh, s_shd, my_sh, U.bytes);
   }
 
   unsigned step = 0;                                 // global layer step
   for (int t = 0; t < a.T; ++t) {
+#pragma unroll 1
     for (int l = 0; l < a.L; ++l, ++step) {
-      const LayerPtrs& P = a.layer[l];
+      const LayerSmem& LY = s_ly[step & 1];
+      const LayerPtrs& P = LY.p;
       float* acc_cur = a.acc + (step % 3) * (kAccCopies * H);         // B(step - 1)
       float* acc_out = a.acc + ((step + 1) % 3) * (kAccCopies * H);   // B(step)
       float* acc_clr = a.acc + ((step + 2) % 3) * (kAccCopies * H);   // B(step + 1)
       const int l_next = (l + 1 < a.L) ? l + 1 : 0;
       const bool more = (l + 1 < a.L) || (t + 1 < a.T);
       const unsigned tag = step + 1;
-      #pragma unroll 1
-      for (int i = threadIdx.x; i < my_rows; i += kPThreads)
-        s_bias[i] = P.router_bias ? __ldg(P.router_bias + c + i * G) : 0.f;
       if (threadIdx.x == 0) s_nc = 0;                // read after the barriers below
       // ---- h_l complete: stage x_l
       if (step > 0) wait_count(sync, kSyncDone, (unsigned)G * step);
@@ -752,7 +817,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
                                    (l == 0 && a.residual) ? a.residual + (size_t)t * H : nullptr,
                                    H, a.eps, s_hx, s_xb, s_xf, s_red);
       // ---- clear this CTA's share of B(step + 1) (published by this step's done signal)
-      #pragma unroll 1
+#pragma unroll 1
       for (int n = 4 * (c + G * threadIdx.x); n < H; n += 4 * G * kPThreads)
 #pragma unroll
         for (int cp = 0; cp < kAccCopies; ++cp)
@@ -766,7 +831,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         if (r < my_rows) {
           float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
           const uint16_t* row = reinterpret_cast<const uint16_t*>(s_router) + (size_t)r * H;
-          #pragma unroll 1
+#pragma unroll 1
           for (int e = 8 * tr; e < H; e += 8 * 64) {
             const uint4 wv = *reinterpret_cast<const uint4*>(row + e);
             const uint4 xv = *reinterpret_cast<const uint4*>(s_xb + e);
@@ -780,102 +845,83 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         acc = sum_lanes<32>(acc);
         if (lane == 0) s_rp[warp] = acc;
         __syncthreads();
-        // every board copy gets the rows; readers spread their polls over the copies
-        #pragma unroll 1
-        for (int q = threadIdx.x; q < my_rows * a.tag_copies; q += kPThreads) {
-          const int rr = q % my_rows, cp = q / my_rows;
-          const float v = (s_rp[2 * rr] + s_rp[2 * rr + 1]) + s_bias[rr];
-          st_tagged(a.logits_tag + (size_t)cp * a.tag_stride + c + rr * G,
-                    ((unsigned long long)tag << 32) | __float_as_uint(v));
+        // every board copy gets the rows (thread 8 q + rr: copy q, row rr); readers
+        // spread their polls over the copies
+        const int rr = threadIdx.x & (kMaxRouterRows - 1);
+        if (rr < my_rows) {
+          const float v = (s_rp[2 * rr] + s_rp[2 * rr + 1]) + LY.bias[rr];
+          const unsigned long long word = ((unsigned long long)tag << 32) | __float_as_uint(v);
+#pragma unroll 1
+          for (int cp = threadIdx.x / kMaxRouterRows; cp < a.tag_copies; cp += kPThreads / kMaxRouterRows)
+            st_tagged(a.logits_tag + (size_t)cp * a.tag_stride + c + rr * G, word);
         }
       }
-      // ---- routed copy descriptors (lane q of warp 0: unit q / 6, piece q % 6), all but
-      // the expert, computed before the poll so that the copies go out right after the
-      // top-k
-      const uint8_t* cp_base = nullptr;
-      size_t cp_estride = 0;
-      uint32_t cp_dst = 0, cp_bytes = 0;
-      int cp_slot = 0;
-      if (warp == 0 && lane < 6 * my_rt) {
-        const int i = lane / 6, piece = lane % 6;
-        const int r = c + i * G;
-        cp_slot = r / per_slot;
-        const int j = r % per_slot;
-        const NVPtr& gu = piece < 2 ? P.gate : P.up;
-        if (piece < 4) {
-          const bool sc = piece & 1;
-          cp_base = sc ? gu.scales + (size_t)j * kUnit * (H / 16) : gu.codes + (size_t)j * kUnit * (H / 2);
-          cp_estride = sc ? (size_t)a.F * (H / 16) : (size_t)a.F * (H / 2);
-          cp_bytes = sc ? kUnit * (H / 16) : kUnit * (H / 2);
-          cp_dst = piece == 0 ? U.gc : piece == 1 ? U.gs : piece == 2 ? U.uc : U.us;
-        } else if (piece == 4) {
-          cp_base = P.dcc_codes + (size_t)j * H * 4;
-          cp_estride = (size_t)per_slot * H * 4;
-          cp_bytes = H * 4;
-          cp_dst = U.dc;
-        } else {
-          cp_base = P.dcc_scales + (size_t)(j / 2) * H;
-          cp_estride = (size_t)(per_slot / 2) * H;
-          cp_bytes = H;
-          cp_dst = U.ds;
-        }
-        cp_dst += (uint32_t)i * U.bytes;
-      }
-      asm volatile("" :: "l"(cp_base), "l"(cp_estride), "r"(cp_dst), "r"(cp_bytes), "r"(cp_slot));
       XStage<CPL, 1> xs;
       pairs_from_smem<CPL>(xs.p[0], s_xf, sl, LPR);
       xs.unscale = stg.unscale;
-      if (warp < nw_e) {
-        // ---- top-k.  Every logit is polled by one thread; the K-th largest of the warp
-        // maxima is a threshold that the K best logits all reach (at least K warps hold
-        // a logit at or above it).  The logits at or above it are ranked exactly by
-        // (value, lower index first).
-        const int i = threadIdx.x;
-        unsigned key = 0u;                             // 0: no logit; every logit's key is >= 1
-        float v = -INFINITY;
-        if (i < a.E) {
-          v = wait_tagged(board + i, tag, sync);
+      if (warp < npw) {
+        // ---- top-k.  Warps [0, npw) poll the logits (thread i: logits i, i + 32 npw, ...).
+        // The K-th largest warp maximum is a threshold that the K best logits all reach
+        // (at least K warps hold a logit at or above it); the logits at or above it are
+        // ranked exactly by (value, lower index first).
+        unsigned wmax = 0u;                            // every logit's order key is >= 1
+#pragma unroll 1
+        for (int e = threadIdx.x; e < a.E; e += npw * 32) {
+          float v = wait_tagged(board + e, tag, sync);
           v = (v == v) ? v : -INFINITY;
-          key = order_key(v);
+          s_val[e] = v;
+          wmax = max(wmax, order_key(v));
         }
-        const unsigned wm = __reduce_max_sync(0xffffffffu, key);
-        if (lane == 0) s_wmax[warp] = wm;
-        named_bar(1, nw_e * 32);
+        wmax = __reduce_max_sync(0xffffffffu, wmax);
+        if (lane == 0) s_wmax[warp] = wmax;
+        named_bar(1, npw * 32);
         unsigned thr = 0u;
-        if (nw_e >= a.K) {
-          const unsigned m = lane < nw_e ? s_wmax[lane] : 0u;
+        if (npw >= a.K) {
+          const unsigned m = lane < npw ? s_wmax[lane] : 0u;
           int ge = 0;
-          #pragma unroll 1
-          for (int u = 0; u < nw_e; ++u) ge += __shfl_sync(0xffffffffu, m, u) >= m ? 1 : 0;
-          thr = __reduce_max_sync(0xffffffffu, (lane < nw_e && ge >= a.K) ? m : 0u);
+#pragma unroll 1
+          for (int u = 0; u < npw; ++u) ge += __shfl_sync(0xffffffffu, m, u) >= m ? 1 : 0;
+          thr = __reduce_max_sync(0xffffffffu, (lane < npw && ge >= a.K) ? m : 0u);
         }
-        const bool cand = key != 0u && key >= thr;
-        const unsigned long long ck = ((unsigned long long)key << 32) | (unsigned)(~i);
-        const unsigned bal = __ballot_sync(0xffffffffu, cand);
-        int base = 0;
-        if (lane == 0 && bal) base = atomicAdd(&s_nc, __popc(bal));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        if (cand) s_c64[base + __popc(bal & ((1u << lane) - 1u))] = ck;
-        named_bar(1, nw_e * 32);
-        if (cand) {
-          const int n = s_nc;
+#pragma unroll 1
+        for (int e0 = warp * 32; e0 < a.E; e0 += npw * 32) {
+          const int e = e0 + lane;
+          const unsigned key = e < a.E ? order_key(s_val[e]) : 0u;
+          const bool cand = key != 0u && key >= thr;
+          const unsigned bal = __ballot_sync(0xffffffffu, cand);
+          int base = 0;
+          if (lane == 0 && bal) base = atomicAdd(&s_nc, __popc(bal));
+          base = __shfl_sync(0xffffffffu, base, 0);
+          if (cand) s_c64[base + __popc(bal & ((1u << lane) - 1u))] = ((unsigned long long)key << 32) | (unsigned)(~e);
+        }
+        named_bar(1, npw * 32);
+        const int n = s_nc;
+#pragma unroll 1
+        for (int j = threadIdx.x; j < n; j += npw * 32) {
+          const unsigned long long ck = s_c64[j];
           int rank = 0;
-          #pragma unroll 1
-          for (int j = 0; j < n; ++j) rank += s_c64[j] > ck ? 1 : 0;
-          if (rank < a.K) { s_sel[rank] = i; s_lsel[rank] = v; }
+#pragma unroll 1
+          for (int m = 0; m < n; ++m) rank += s_c64[m] > ck ? 1 : 0;
+          if (rank < a.K) {
+            const int e = (int)(~(unsigned)ck);
+            s_sel[rank] = e;
+            s_lsel[rank] = s_val[e];
+          }
         }
-        named_bar(1, nw_e * 32);
+        named_bar(1, npw * 32);
         if (warp == 0) {
           // routed copies first: they gate the critical path
           if (lane < my_rt) mbar_expect_tx(&s_bar_rt[lane], U.bytes);
           __syncwarp();
-          if (lane < 6 * my_rt) {
-            int e = s_sel[cp_slot];
+          const PieceDesc d = s_rtd[lane];
+          if (d.which >= 0) {
+            int e = s_sel[d.slot];
             if (e < 0 || e >= a.E) { raise_status(FLINT_ERR_INVALID_ARG); e = 0; }
-            bulk_g2s(s_routed + cp_dst, cp_base + (size_t)e * cp_estride, cp_bytes, &s_bar_rt[lane / 6]);
+            bulk_g2s(s_routed + d.dst, piece_base(P, d.which, false) + d.off + (size_t)e * d.estride, d.bytes,
+                     &s_bar_rt[lane / 6]);
           }
         }
-        if (warp == (nw_e > 1 ? 1 : 0)) {
+        if (warp == (npw > 1 ? 1 : 0)) {
           // routing weights: softmax over the selected, renormalised
           const float lv = lane < a.K ? s_lsel[lane] : 0.f;
           const float l0 = __shfl_sync(0xffffffffu, lv, 0);
@@ -883,65 +929,65 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
           float z = pr;
 #pragma unroll
           for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-          if (lane < a.K) s_w[lane] = pr / z;
+          if (lane < a.K) {
+            const int e = s_sel[lane];
+            const bool ok = e >= 0 && e < a.E;
+            s_w[lane] = pr / z;
+            s_tsc[lane][0] = ok ? __ldg(P.gate.tsc + e) : 0.f;
+            s_tsc[lane][1] = ok ? __ldg(P.up.tsc + e) : 0.f;
+            s_tsc[lane][2] = ok ? __ldg(P.down_tsc + e) * (pr / z) : 0.f;
+          }
         }
-      } else if (my_sh > 0) {
-        // ---- shared units' gate/up by the warps that do not poll
-        mbar_wait(&s_bar_sh, ph_sh, sync);
-        #pragma unroll 1
-        for (int i = 0; i < my_sh; ++i)
-          unit_gateup<CPL>(s_static + (size_t)i * U.bytes, H, P.sh_gate.tsc[0], P.sh_up.tsc[0], xs,
-                           s_gu + i * 2 * kUnit, nw_e, kPWarps - nw_e);
-      }
-      if (!early_sh && my_sh > 0) {
-        // (every warp polls: the shared gate/up follows the top-k)
-        __syncthreads();
-        mbar_wait(&s_bar_sh, ph_sh, sync);
-        #pragma unroll 1
-        for (int i = 0; i < my_sh; ++i)
-          unit_gateup<CPL>(s_static + (size_t)i * U.bytes, H, P.sh_gate.tsc[0], P.sh_up.tsc[0], xs,
-                           s_gu + i * 2 * kUnit, 0, kPWarps);
+      } else {
+        // ---- shared units' gate/up by the warps that do not poll; the last of them
+        // then fetches the next layer's table
+        if (my_sh > 0) {
+          mbar_wait(&s_bar_sh, ph_sh, sync);
+#pragma unroll 1
+          for (int i = 0; i < my_sh; ++i)
+            unit_gateup<CPL>(s_static + (size_t)i * U.bytes, H, LY.sh_tsc[0], LY.sh_tsc[1], xs,
+                             s_gu + i * 2 * kUnit, npw, kPWarps - npw);
+        }
+        if (more && warp == kPWarps - 1) load_layer(a, l_next, &s_ly[(step + 1) & 1], c, G, my_rows);
       }
       if (my_sh > 0) ph_sh ^= 1;
-      if (threadIdx.x < my_sh) s_dscale[threadIdx.x] = P.sh_down_tsc[0];
+      if (threadIdx.x < my_sh) s_dscale[threadIdx.x] = LY.sh_tsc[2];
       __syncthreads();                               // s_sel, s_w and the shared s_gu visible
-      if (more && warp == 0) issue_router_rows(a.layer[l_next], s_router, &s_bar_rr, H, c, G, my_rows);
+      const LayerPtrs& PN = s_ly[(step + 1) & 1].p;   // next layer (written before the barrier above)
+      if (more && warp == 0) issue_router_rows(PN, s_router, &s_bar_rr, H, c, G, my_rows);
       if (c == 0 && threadIdx.x < a.K) {
         const size_t o = ((size_t)t * a.L + l) * a.K + threadIdx.x;
         if (a.idx_out) a.idx_out[o] = s_sel[threadIdx.x];
         if (a.w_out) a.w_out[o] = s_w[threadIdx.x];
       }
-      // ---- shared units' SwiGLU and down while the routed copies are in flight
+      // ---- group 0: the shared units (SwiGLU and down while the routed copies are in
+      // flight); group 1: the routed units, each gate/up as soon as its copy lands
       float part[4] = {0.f, 0.f, 0.f, 0.f};
-      if (my_sh > 0) {
-        if (warp == 0) stage_swiglu(my_sh, s_gu, s_dscale, s_hs);
-        __syncthreads();
-        #pragma unroll 1
-        for (int u = 0; u < my_sh; ++u) unit_down(s_static + (size_t)u * U.bytes, H, s_hs + u * (kUnit + 1), part);
-      }
-      // ---- routed units' gate/up, each as soon as its copy lands
-      #pragma unroll 1
-      for (int i = 0; i < my_rt; ++i) {
-        const int r = c + i * G;
-        const int slot = r / per_slot;
-        int e = s_sel[slot];
-        if (e < 0 || e >= a.E) e = 0;
-        mbar_wait(&s_bar_rt[i], ph_rt, sync);
-        unit_gateup<CPL>(s_routed + (size_t)i * U.bytes, H, P.gate.tsc[e], P.up.tsc[e], xs,
-                         s_gu + (my_sh + i) * 2 * kUnit, 0, kPWarps);
-        if (threadIdx.x == 0) s_dscale[my_sh + i] = P.down_tsc[e] * s_w[slot];
-      }
-      ph_rt ^= 1;
-      __syncthreads();
-      // the shared-unit buffers are free again
-      if (more && warp == 0) issue_shared_units(a.layer[l_next], s_static, &s_bar_sh, H, c, G, my_sh, n_sh);
-      // ---- routed units' SwiGLU and down
-      if (my_rt > 0) {
-        if (warp == 0) stage_swiglu(my_rt, s_gu + my_sh * 2 * kUnit, s_dscale + my_sh, s_hs + my_sh * (kUnit + 1));
-        __syncthreads();
-        #pragma unroll 1
-        for (int u = 0; u < my_rt; ++u)
-          unit_down(s_routed + (size_t)u * U.bytes, H, s_hs + (my_sh + u) * (kUnit + 1), part);
+#pragma unroll 1
+      for (int g = 0; g < 2; ++g) {
+        const int n = g ? my_rt : my_sh;
+        const int off = g ? my_sh : 0;
+        const uint8_t* ubase = g ? s_routed : s_static;
+        if (g) {
+#pragma unroll 1
+          for (int i = 0; i < my_rt; ++i) {
+            const int slot = s_slot[i];
+            mbar_wait(&s_bar_rt[i], ph_rt, sync);
+            unit_gateup<CPL>(s_routed + (size_t)i * U.bytes, H, s_tsc[slot][0], s_tsc[slot][1], xs,
+                             s_gu + (my_sh + i) * 2 * kUnit, 0, kPWarps);
+            if (threadIdx.x == 0) s_dscale[my_sh + i] = s_tsc[slot][2];
+          }
+          ph_rt ^= 1;
+          __syncthreads();
+          // the shared-unit buffers are free again
+          if (more && warp == 0) issue_shared(PN, s_static, &s_bar_sh, s_shd, my_sh, U.bytes);
+        }
+        if (n > 0) {
+          if (warp == 0) stage_swiglu(n, s_gu + off * 2 * kUnit, s_dscale + off, s_hs + off * (kUnit + 1));
+          __syncthreads();
+#pragma unroll 1
+          for (int u = 0; u < n; ++u) unit_down(ubase + (size_t)u * U.bytes, H, s_hs + (off + u) * (kUnit + 1), part);
+        }
       }
       if (my_sh + my_rt > 0 && 4 * threadIdx.x < H)
         red_add_v4(acc_out + (c % kAccCopies) * H + 4 * threadIdx.x, part[0], part[1], part[2], part[3]);
