@@ -75,25 +75,30 @@ typedef struct {
   int n_mat, rows, cols;
 } flint_nvfp4;
 
-/* Column-chunk copy of an NVFP4 stack: the same bytes reordered so that the codes of
- * each 8-column chunk, and the scales of each 16-column block, of all rows of a
- * matrix are contiguous:
- *   codes  [n_mat][cols/8][rows][4]     scales [n_mat][cols/16][rows]
- * The decode kernel reads the down projections in this layout (a unit of 8 SwiGLU
- * outputs then multiplies one contiguous block of codes and one of scales).  Build it
- * once with flint_nvfp4_column_chunks; the tensor scales are those of the row-major
- * stack.  The buffers have the sizes of the row-major codes and scales. */
-typedef struct {
-  const uint8_t* codes;
-  const uint8_t* scales;
-} flint_nvfp4_cc;
+/* Decode-unit copy of an expert's three matrices: the bytes a decode step needs for 8
+ * consecutive SwiGLU outputs j = 8u .. 8u + 7 of expert m, packed into one block so
+ * that one bulk copy fetches them.  Unit (m, u), FLINT_UNIT_BYTES(H) bytes, holds in
+ * order:
+ *   gate codes  rows 8u..8u+7 of gate[m]   8 x H/2 bytes   (row-major, as in the stack)
+ *   gate scales the same rows              8 x H/16
+ *   up codes, up scales                    likewise
+ *   down codes  for each of the H rows r of down[m], the 4 code bytes of columns
+ *               8u..8u+7                   H x 4
+ *   down scales for each row r, the scale byte of the 16-column block holding
+ *               columns 8u..8u+7           H
+ * units: [n_mat][F/8][FLINT_UNIT_BYTES(H)] for gate, up [n_mat, F, H] and down
+ * [n_mat, H, F].  Build it once with flint_decode_units; the tensor scales are those
+ * of the row-major stacks. */
+#define FLINT_UNIT_BYTES(H) ((size_t)14 * (size_t)(H))
 
 /* One MoE layer.  Routed experts are stacks of n_experts matrices:
  *   gate, up : [E, F, H]      down : [E, H, F]
  *   sh_gate, sh_up : [1, Fs, H]   sh_down : [1, H, Fs]
  * router_w is bf16 [E, H]; router_bias fp32 [E] or NULL (added to the logits).
- * down_cc / sh_down_cc: column-chunk copies of down / sh_down, required by the
- * decode entry points (flint_moe_decode, flint_decode_tokens).
+ * units / sh_units: decode-unit copies of (gate, up, down) / (sh_gate, sh_up,
+ * sh_down), required by the decode entry points (flint_moe_decode,
+ * flint_decode_tokens, flint_decode_tokens_noalloc), which read the experts' weights
+ * only there (and their tensor scales from the stacks).
  * mma_scales: MMA scale copies (flint_nvfp4_mma_scales) of gate, up, down, sh_gate,
  * sh_up, sh_down in that order, required by flint_moe_prefill, which reads the
  * row-major codes and these scales. */
@@ -103,7 +108,8 @@ typedef struct {
   const float* router_bias;
   flint_nvfp4 gate, up, down;
   flint_nvfp4 sh_gate, sh_up, sh_down;
-  flint_nvfp4_cc down_cc, sh_down_cc;
+  const uint8_t* units;        /* [E][F/8][FLINT_UNIT_BYTES(H)] */
+  const uint8_t* sh_units;     /* [1][Fs/8][FLINT_UNIT_BYTES(H)] */
   const uint8_t* mma_scales[6];
 } flint_moe_layer;
 
@@ -142,11 +148,13 @@ flint_status flint_quantize_nvfp4(const void* w_bf16, int n_mat, int rows, int c
 flint_status flint_nvfp4_mma_scales(const flint_nvfp4* m, uint8_t* scales_mma,
                                     flint_stream stream);
 
-/* Reorder an NVFP4 stack (row-major) into its column-chunk copy (see
- * flint_nvfp4_cc).  codes_cc / scales_cc: device outputs of the same sizes as
- * m->codes / m->scales.  Weight preparation, like quantisation. */
-flint_status flint_nvfp4_column_chunks(const flint_nvfp4* m, uint8_t* codes_cc,
-                                       uint8_t* scales_cc, flint_stream stream);
+/* Pack the decode-unit copy (see FLINT_UNIT_BYTES) of gate, up [n_mat, F, H] and
+ * down [n_mat, H, F] (row-major NVFP4 stacks of one expert set).  units: device
+ * output of n_mat * (F/8) * FLINT_UNIT_BYTES(H) bytes, 16-byte aligned.  Weight
+ * preparation, like quantisation.  Errors: FLINT_ERR_SHAPE unless the three shapes
+ * agree and F % 32 == 0, H % 32 == 0; FLINT_ERR_ALIGNMENT for a misaligned units. */
+flint_status flint_decode_units(const flint_nvfp4* gate, const flint_nvfp4* up,
+                                const flint_nvfp4* down, uint8_t* units, flint_stream stream);
 
 /* Dequantise an NVFP4 stack to fp32 [n_mat, rows, cols] (the value formula above).
  * A check and debugging aid; no workspace. */

@@ -55,14 +55,13 @@ flint_status check_layer(const flint_moe_layer* L) {
 
 NVPtr nv(const flint_nvfp4& m) { return NVPtr{m.codes, m.scales, m.tensor_scale}; }
 
-// The decode path also reads the column-chunk copies of the down projections.
+// The decode path also reads the decode-unit copies of the experts.
 flint_status check_decode_layer(const flint_moe_layer* L) {
   flint_status s = check_layer(L);
   if (s != FLINT_OK) return s;
-  if (!L->down_cc.codes || !L->down_cc.scales || !L->sh_down_cc.codes || !L->sh_down_cc.scales)
+  if (!L->units || !L->sh_units)
     return FLINT_ERR_INVALID_ARG;
-  if (!aligned16(L->down_cc.codes) || !aligned16(L->down_cc.scales) ||
-      !aligned16(L->sh_down_cc.codes) || !aligned16(L->sh_down_cc.scales))
+  if (!aligned16(L->units) || !aligned16(L->sh_units))
     return FLINT_ERR_ALIGNMENT;
   return FLINT_OK;
 }
@@ -72,9 +71,8 @@ flint::LayerPtrs layer_ptrs(const flint_moe_layer& L) {
   p.router_w = static_cast<const uint16_t*>(L.router_w);
   p.router_bias = L.router_bias;
   p.gate = nv(L.gate); p.up = nv(L.up); p.sh_gate = nv(L.sh_gate); p.sh_up = nv(L.sh_up);
-  p.dcc_codes = L.down_cc.codes; p.dcc_scales = L.down_cc.scales;
+  p.units = L.units; p.sh_units = L.sh_units;
   p.down_tsc = L.down.tensor_scale;
-  p.sh_dcc_codes = L.sh_down_cc.codes; p.sh_dcc_scales = L.sh_down_cc.scales;
   p.sh_down_tsc = L.sh_down.tensor_scale;
   return p;
 }
@@ -191,6 +189,7 @@ static flint_status decode_tokens_impl(const flint_moe_layer* layers, int n_laye
   std::memset(&a, 0, sizeof(a));
   a.max_router_rows = plan.router_rows;
   a.max_shared_units = plan.shared_units;
+  a.max_routed_units = plan.routed_units;
   a.H = L0.hidden; a.E = L0.n_experts; a.K = L0.top_k; a.F = L0.expert_width;
   a.Fs = L0.shared_width; a.L = n_layers; a.T = T; a.eps = rms_eps;
   a.tag_copies = tag_copies;
@@ -243,17 +242,19 @@ flint_status flint_nvfp4_mma_scales(const flint_nvfp4* m, uint8_t* scales_mma,
                                             static_cast<cudaStream_t>(stream)));
 }
 
-flint_status flint_nvfp4_column_chunks(const flint_nvfp4* m, uint8_t* codes_cc,
-                                       uint8_t* scales_cc, flint_stream stream) {
-  if (!m || !codes_cc || !scales_cc) return FLINT_ERR_INVALID_ARG;
-  if (m->n_mat <= 0 || m->rows <= 0 || m->cols <= 0) return FLINT_ERR_INVALID_ARG;
-  if (m->cols % 32) return FLINT_ERR_SHAPE;
-  flint_status s = check_nvfp4(*m, m->n_mat, m->rows, m->cols);
-  if (s != FLINT_OK) return s;
-  if (!aligned16(codes_cc) || !aligned16(scales_cc)) return FLINT_ERR_ALIGNMENT;
-  return from_cuda(flint::launch_column_chunks(m->codes, m->scales, m->n_mat, m->rows, m->cols,
-                                               codes_cc, scales_cc,
-                                               static_cast<cudaStream_t>(stream)));
+flint_status flint_decode_units(const flint_nvfp4* gate, const flint_nvfp4* up,
+                                const flint_nvfp4* down, uint8_t* units, flint_stream stream) {
+  if (!gate || !up || !down || !units) return FLINT_ERR_INVALID_ARG;
+  const int n = gate->n_mat, F = gate->rows, H = gate->cols;
+  if (n <= 0 || F <= 0 || H <= 0) return FLINT_ERR_INVALID_ARG;
+  if (F % 32 || H % 32) return FLINT_ERR_SHAPE;
+  flint_status s;
+  if ((s = check_nvfp4(*gate, n, F, H)) != FLINT_OK) return s;
+  if ((s = check_nvfp4(*up, n, F, H)) != FLINT_OK) return s;
+  if ((s = check_nvfp4(*down, n, H, F)) != FLINT_OK) return s;
+  if (!aligned16(units)) return FLINT_ERR_ALIGNMENT;
+  return from_cuda(flint::launch_unit_pack(nv(*gate), nv(*up), nv(*down), n, H, F, units,
+                                           static_cast<cudaStream_t>(stream)));
 }
 
 flint_status flint_lm_head(const flint_nvfp4* W, const void* x_bf16, float* logits,

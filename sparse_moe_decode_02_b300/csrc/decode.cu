@@ -7,26 +7,32 @@
 // Flint's architecture work?") needs every active weight once per token and has one
 // dependency no schedule can hide: which experts are read depends on the router.
 //
-// CTA roles (fixed for the launch).  With n_sh = Fs/32 shared-expert slices and
-// n_rt = k*F/32 routed slices ("units": 32 SwiGLU outputs and their down block):
-//   shared CTAs  [0, n_sh)              one shared-expert unit each
-//   routed CTAs  [n_sh, n_sh + n_rt)    one (slot, slice) unit of the selected experts
-//   router CTAs  the rest               router rows, and the copy of h_l into the next
-//                                       residual buffer
-// Step s = one layer of one token.  Two monotonic counters replace grid barriers:
-//   logits(s) -- bumped by each router CTA once its logits and its share of the
-//                residual copy are written;
-//   done(s)   -- bumped by each unit CTA once its down contribution is red.added.
-// Every CTA waits for done(s-1) (h_l complete) and stages x_l = bf16(RMSNorm(h_l)) in
-// registers from one CTA-wide read of h_l.  Router CTAs compute logits and signal.
-// Shared CTAs compute their unit right away (it needs only x_l), then wait for
-// logits(s) before red.adding.  Routed CTAs wait for logits(s), compute the softmax
-// top-k, then stream their unit.  Unit and router weights move global -> shared
-// memory by TMA bulk copies (cp.async.bulk + mbarrier); router rows and shared units
-// do not depend on the data, so the copies for step s+1 are issued as soon as step s
-// has consumed the buffer.  The down projection of a unit is a split-K contribution to
-// all H rows (a contiguous column-chunk block, see flint.h), summed into the next
-// residual with red.global.add.v4.f32.
+// Work split (fixed for the launch; G CTAs, every CTA runs the same code).  A "unit"
+// is 8 consecutive SwiGLU outputs of one expert with the down-projection column chunk
+// they feed; the decode-unit copy of the weights (flint.h) stores each unit as one
+// contiguous block, fetched by one TMA bulk copy.  CTA c owns
+//   router rows   e = c, c + G, ...        (of E)
+//   shared units  s = G-1-c, G-1-c + G, ... (of Fs/8)
+//   routed units  r = c, c + G, ...        (of k*F/8: unit r % (F/8) of slot r / (F/8))
+// Step s = one layer of one token:
+//   1. wait until done(s-1) = G*s (h_l complete) and stage x_l = bf16(RMSNorm(h_l))
+//      in shared memory from one fixed-order CTA reduction (identical in every CTA);
+//   2. compute the router rows and post each logit, tagged with s+1, to every copy of
+//      a logit board (one 64-bit store: no fence, no counter);
+//   3. warps 0-7 poll all E logits on this CTA's board copy and select the top k
+//      exactly (threshold from the warp maxima, then ranks); warp 0 issues the routed
+//      units' copies, warp 1 computes the routing weights and the selected experts'
+//      tensor scales; meanwhile warps 8-15 compute the shared units' gate/up;
+//   4. the shared units' SwiGLU and down pass run while the routed copies are in
+//      flight; each routed unit's gate/up runs as soon as its copy lands, then their
+//      SwiGLU and down pass;
+//   5. the CTA's down contributions (all H rows) are red.added (fp32) into the next
+//      residual buffer, and done(s) is bumped with a release add.
+// Router rows and shared units do not depend on the data: their copies for step s+1
+// are issued as soon as step s has consumed the buffers.  The per-layer pointer table,
+// shared tensor scales and router bias are prefetched into shared memory a step ahead.
+// The loops of the step stay rolled: the step runs far more distinct instructions
+// than the instruction caches hold, so its time follows its code size.
 //
 // After the last layer of a token the head GEMV (optional) runs over all CTAs; each
 // CTA posts its best (logit, index) and CTA 0 reduces them.  Every wait is bounded by
@@ -46,7 +52,7 @@ static_assert((kMaxRouterRows & (kMaxRouterRows - 1)) == 0, "router rows: a powe
 constexpr int kMaxRoutedUnits = 5;  // routed units per CTA and step (6 pieces each <= 32 lanes)
 constexpr int kMaxSharedUnits = 4;  // shared units per CTA
 constexpr int kMaxUnits = kMaxRoutedUnits + kMaxSharedUnits;
-constexpr size_t kMaxDecodeSmem = 220 * 1024;
+constexpr size_t kMaxDecodeSmem = 216 * 1024;   // dynamic; the static arrays take about 9 KB of the 227 KB
 constexpr int kMaxCtas = 512;
 // Sync words, each on its own 128-byte line.
 constexpr int kSyncDone = 32, kSyncHead = 64, kSyncAbort = 96;
@@ -86,13 +92,12 @@ __device__ __forceinline__ void wait_count(unsigned* sync, int which, unsigned t
   __syncthreads();
 }
 
-// Publishes every write of this CTA made before the call, then bumps the counter.
+// Publishes every write of this CTA made before the call, then bumps the counter
+// (the barrier orders the CTA's writes before thread 0's release-add).
 __device__ __forceinline__ void signal_count(unsigned* sync, int which) {
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(sync + which, 1u);
-  }
+  if (threadIdx.x == 0)
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(sync + which) : "memory");
 }
 
 // Router logits travel as tagged 64-bit words {value bits, step + 1}; a reader that
@@ -286,8 +291,9 @@ __device__ __forceinline__ void lds_row_bf16(RowBF16<CPL>& r, const uint16_t* ro
 // ---------------------------------------------------------------- units
 // A unit is kUnit = 8 consecutive SwiGLU outputs of one expert (routed or shared): 8
 // gate rows, 8 up rows, and the matching 8-column chunk of the down matrix (H rows x
-// 4 code bytes, plus the H scale bytes of the 16-column block that holds it), each
-// contiguous in HBM (see the column-chunk layout in flint.h).  Its shared-memory image:
+// 4 code bytes, plus the H scale bytes of the 16-column block that holds it).  The
+// decode-unit copy (flint.h) stores each unit as one block in this layout, which is
+// also its shared-memory image:
 struct UnitLayout {
   uint32_t gc, gs, uc, us, dc, ds, bytes;
   __host__ __device__ static UnitLayout of(int H) {
@@ -621,62 +627,16 @@ __device__ __forceinline__ void issue_router_rows(const LayerPtrs& P, uint8_t* s
     bulk_g2s(s_router + (size_t)lane * H * 2, P.router_w + (size_t)(c + lane * G) * H, H * 2, bar);
 }
 
-// Layer-independent part of one bulk copy of a unit piece (see UnitLayout): the layer
-// matrix it reads (which), the byte offset in it, the per-expert stride (routed units),
-// the destination offset in the unit buffers and the size.  Lane q of warp 0 owns piece
-// q % 6 of unit q / 6; the descriptors are built once per launch.
-struct PieceDesc {
-  unsigned long long off, estride;
-  uint32_t dst, bytes;
-  int which, slot;            // which < 0: no piece for this lane
-};
-
-// Piece `piece` of unit row block `row0` (8 gate/up rows) / down column chunk `chunk`
-// of a stack whose matrices have F = rows_per_mat gate/up rows.
-__device__ __forceinline__ PieceDesc piece_desc(int piece, int H, size_t row0, int chunk,
-                                                size_t rows_per_mat, int chunks_per_mat) {
-  const UnitLayout L = UnitLayout::of(H);
-  PieceDesc d;
-  d.which = piece;
-  d.slot = 0;
-  const bool sc = piece & 1;
-  if (piece < 4) {
-    d.off = sc ? row0 * (H / 16) : row0 * (H / 2);
-    d.estride = sc ? rows_per_mat * (H / 16) : rows_per_mat * (H / 2);
-    d.bytes = sc ? kUnit * (H / 16) : kUnit * (H / 2);
-    d.dst = piece == 0 ? L.gc : piece == 1 ? L.gs : piece == 2 ? L.uc : L.us;
-  } else {
-    d.off = sc ? (size_t)(chunk / 2) * H : (size_t)chunk * H * 4;
-    d.estride = sc ? (size_t)(chunks_per_mat / 2) * H : (size_t)chunks_per_mat * H * 4;
-    d.bytes = sc ? H : H * 4;
-    d.dst = sc ? L.ds : L.dc;
-  }
-  return d;
-}
-
-// The matrix a routed (gate, up, down column chunks) or shared piece reads.
-__device__ __forceinline__ const uint8_t* piece_base(const LayerPtrs& P, int which, bool shared) {
-  const NVPtr& g = shared ? P.sh_gate : P.gate;
-  const NVPtr& u = shared ? P.sh_up : P.up;
-  switch (which) {
-    case 0: return g.codes;
-    case 1: return g.scales;
-    case 2: return u.codes;
-    case 3: return u.scales;
-    case 4: return shared ? P.sh_dcc_codes : P.dcc_codes;
-    default: return shared ? P.sh_dcc_scales : P.dcc_scales;
-  }
-}
-
-// Shared units of a layer (warp 0): data-independent, issued one layer ahead.
+// Shared units of a layer (warp 0; lane i fetches shared unit s_su[i] into buffer i):
+// data-independent, issued one layer ahead.
 __device__ __forceinline__ void issue_shared(const LayerPtrs& P, uint8_t* s_static, uint64_t* bar,
-                                             const PieceDesc* s_shd, int my_sh, uint32_t unit_bytes) {
+                                             const int* s_su, int my_sh, uint32_t unit_bytes) {
   const int lane = threadIdx.x & 31;
   if (my_sh == 0) return;
   if (lane == 0) mbar_expect_tx(bar, (uint32_t)my_sh * unit_bytes);
   __syncwarp();
-  const PieceDesc d = s_shd[lane];
-  if (d.which >= 0) bulk_g2s(s_static + d.dst, piece_base(P, d.which, true) + d.off, d.bytes, bar);
+  if (lane < my_sh)
+    bulk_g2s(s_static + (size_t)lane * unit_bytes, P.sh_units + (size_t)s_su[lane] * unit_bytes, unit_bytes, bar);
 }
 
 // ---------------------------------------------------------------- layer tables
@@ -727,8 +687,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
   __shared__ float s_lsel[FLINT_MAX_TOP_K];
   __shared__ unsigned s_wmax[8];
   __shared__ int s_nc;
-  __shared__ int s_slot[kMaxRoutedUnits];
-  __shared__ PieceDesc s_rtd[32], s_shd[32];
+  __shared__ int s_slot[kMaxRoutedUnits], s_jrt[kMaxRoutedUnits], s_su[kMaxSharedUnits];
   __shared__ float s_bv[kPWarps];
   __shared__ int s_bi[kPWarps];
   __shared__ float s_red[2 * kPWarps];
@@ -747,6 +706,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
   uint8_t* s_router = reinterpret_cast<uint8_t*>(s_xf + H);            // [RR][H] bf16 rows
   uint8_t* s_static = s_router + (size_t)a.max_router_rows * H * 2;   // shared units
   uint8_t* s_routed = s_static + (size_t)a.max_shared_units * U.bytes; // routed units
+  float* s_etsc = reinterpret_cast<float*>(s_routed + (size_t)a.max_routed_units * U.bytes);  // [3][E]
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = blockIdx.x, G = gridDim.x;
@@ -771,31 +731,19 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
     for (int i = 0; i < kMaxRoutedUnits; ++i) mbar_init(&s_bar_rt[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // copy descriptors (lane q: piece q % 6 of unit q / 6) and routed-unit expert slots
-  if (warp == 0) {
-    const int q = lane, i = q / 6, piece = q % 6;
-    PieceDesc d = {0ull, 0ull, 0u, 0u, -1, 0};
-    if (i < my_rt) {
-      const int r = c + i * G;
-      d = piece_desc(piece, H, (size_t)(r % per_slot) * kUnit, r % per_slot, a.F, per_slot);
-      d.slot = r / per_slot;
-      d.dst += (uint32_t)i * U.bytes;
-    }
-    s_rtd[q] = d;
-    d = PieceDesc{0ull, 0ull, 0u, 0u, -1, 0};
-    if (i < my_sh) {
-      const int su = (G - 1 - c) + i * G;
-      d = piece_desc(piece, H, (size_t)su * kUnit, su, 0, n_sh);
-      d.dst += (uint32_t)i * U.bytes;
-    }
-    s_shd[q] = d;
-    if (lane < my_rt) s_slot[lane] = (c + lane * G) / per_slot;
+  // this CTA's units: routed unit i is unit j of the expert in slot `slot`; shared
+  // unit i is unit s_su[i] of the shared expert
+  if (threadIdx.x < my_rt) {
+    const int r = c + threadIdx.x * G;
+    s_slot[threadIdx.x] = r / per_slot;
+    s_jrt[threadIdx.x] = r % per_slot;
   }
+  if (threadIdx.x < my_sh) s_su[threadIdx.x] = (G - 1 - c) + threadIdx.x * G;
   __syncthreads();
 
   if (warp == 0) {
     issue_router_rows(a.layer[0], s_router, &s_bar_rr, H, c, G, my_rows);
-    issue_shared(a.layer[0], s_static, &s_bar_sh, s_shd, my_sh, U.bytes);
+    issue_shared(a.layer[0], s_static, &s_bar_sh, s_su, my_sh, U.bytes);
   }
 
   unsigned step = 0;                                 // global layer step
@@ -867,7 +815,12 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         unsigned wmax = 0u;                            // every logit's order key is >= 1
 #pragma unroll 1
         for (int e = threadIdx.x; e < a.E; e += npw * 32) {
+          // the expert's tensor scales load while its logit is awaited
+          const float tg = __ldg(P.gate.tsc + e), tu = __ldg(P.up.tsc + e), td = __ldg(P.down_tsc + e);
           float v = wait_tagged(board + e, tag, sync);
+          s_etsc[e] = tg;
+          s_etsc[a.E + e] = tu;
+          s_etsc[2 * a.E + e] = td;
           v = (v == v) ? v : -INFINITY;
           s_val[e] = v;
           wmax = max(wmax, order_key(v));
@@ -913,12 +866,11 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
           // routed copies first: they gate the critical path
           if (lane < my_rt) mbar_expect_tx(&s_bar_rt[lane], U.bytes);
           __syncwarp();
-          const PieceDesc d = s_rtd[lane];
-          if (d.which >= 0) {
-            int e = s_sel[d.slot];
+          if (lane < my_rt) {
+            int e = s_sel[s_slot[lane]];
             if (e < 0 || e >= a.E) { raise_status(FLINT_ERR_INVALID_ARG); e = 0; }
-            bulk_g2s(s_routed + d.dst, piece_base(P, d.which, false) + d.off + (size_t)e * d.estride, d.bytes,
-                     &s_bar_rt[lane / 6]);
+            bulk_g2s(s_routed + (size_t)lane * U.bytes,
+                     P.units + ((size_t)e * per_slot + s_jrt[lane]) * U.bytes, U.bytes, &s_bar_rt[lane]);
           }
         }
         if (warp == (npw > 1 ? 1 : 0)) {
@@ -933,9 +885,9 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
             const int e = s_sel[lane];
             const bool ok = e >= 0 && e < a.E;
             s_w[lane] = pr / z;
-            s_tsc[lane][0] = ok ? __ldg(P.gate.tsc + e) : 0.f;
-            s_tsc[lane][1] = ok ? __ldg(P.up.tsc + e) : 0.f;
-            s_tsc[lane][2] = ok ? __ldg(P.down_tsc + e) * (pr / z) : 0.f;
+            s_tsc[lane][0] = ok ? s_etsc[e] : 0.f;
+            s_tsc[lane][1] = ok ? s_etsc[a.E + e] : 0.f;
+            s_tsc[lane][2] = ok ? s_etsc[2 * a.E + e] * (pr / z) : 0.f;
           }
         }
       } else {
@@ -980,7 +932,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
           ph_rt ^= 1;
           __syncthreads();
           // the shared-unit buffers are free again
-          if (more && warp == 0) issue_shared(PN, s_static, &s_bar_sh, s_shd, my_sh, U.bytes);
+          if (more && warp == 0) issue_shared(PN, s_static, &s_bar_sh, s_su, my_sh, U.bytes);
         }
         if (n > 0) {
           if (warp == 0) stage_swiglu(n, s_gu + off * 2 * kUnit, s_dscale + off, s_hs + off * (kUnit + 1));
@@ -1043,33 +995,44 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
   // for the current step), and every issued copy is waited for in the step it serves.
 }
 
-// ---------------------------------------------------------------- column-chunk repack
-// codes [m][rows][cols/2] -> [m][cols/8][rows][4];  scales [m][rows][cols/16] -> [m][cols/16][rows]
-__global__ void k_column_chunks(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-                                int rows, int cols, uint8_t* __restrict__ codes_cc,
-                                uint8_t* __restrict__ scales_cc) {
-  const int m = blockIdx.y;
-  const int nch = cols / 8;
-  const int64_t n = (int64_t)rows * nch;
-  const uint8_t* cm = codes + (size_t)m * rows * (cols / 2);
-  const uint8_t* sm = scales + (size_t)m * rows * (cols / 16);
-  uint8_t* co = codes_cc + (size_t)m * rows * (cols / 2);
-  uint8_t* so = scales_cc + (size_t)m * rows * (cols / 16);
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / nch, ch = i % nch;        // source: row r, 8-column chunk ch
-    const uint32_t v = *reinterpret_cast<const uint32_t*>(cm + r * (cols / 2) + ch * 4);
-    *reinterpret_cast<uint32_t*>(co + (ch * rows + r) * 4) = v;
-    if ((ch & 1) == 0) so[(ch / 2) * rows + r] = sm[r * (cols / 16) + ch / 2];
+// ---------------------------------------------------------------- decode-unit pack
+// CTA (q, m) builds units 4q .. 4q + 3 of matrix m (see UnitLayout): gate/up rows
+// 32q .. 32q + 31 split by 8, and the down codes of columns 32q .. 32q + 31 (16 bytes
+// per row) with the scales of blocks 2q, 2q + 1 spread over the four units.
+__device__ __forceinline__ void copy16(uint8_t* dst, const uint8_t* src, uint32_t bytes) {
+  for (uint32_t i = threadIdx.x; i < bytes / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(src)[i];
+}
+
+__global__ void k_unit_pack(NVPtr gate, NVPtr up, NVPtr down, int H, int F, uint8_t* __restrict__ units) {
+  const int m = blockIdx.y, q = blockIdx.x;
+  const UnitLayout L = UnitLayout::of(H);
+  uint8_t* out = units + ((size_t)m * (F / kUnit) + 4 * q) * L.bytes;
+#pragma unroll 1
+  for (int u = 0; u < 4; ++u) {
+    uint8_t* o = out + (size_t)u * L.bytes;
+    const size_t row0 = (size_t)m * F + 32 * q + kUnit * u;
+    copy16(o + L.gc, gate.codes + row0 * (H / 2), kUnit * (H / 2));
+    copy16(o + L.gs, gate.scales + row0 * (H / 16), kUnit * (H / 16));
+    copy16(o + L.uc, up.codes + row0 * (H / 2), kUnit * (H / 2));
+    copy16(o + L.us, up.scales + row0 * (H / 16), kUnit * (H / 16));
+  }
+  for (int r = threadIdx.x; r < H; r += blockDim.x) {
+    const size_t row = (size_t)m * H + r;
+    const uint4 v = *reinterpret_cast<const uint4*>(down.codes + row * (F / 2) + 16 * q);
+    const uint8_t s0 = down.scales[row * (F / 16) + 2 * q], s1 = down.scales[row * (F / 16) + 2 * q + 1];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      *reinterpret_cast<uint32_t*>(out + (size_t)u * L.bytes + L.dc + 4 * r) = w[u];
+      out[(size_t)u * L.bytes + L.ds + r] = u < 2 ? s0 : s1;
+    }
   }
 }
 
-cudaError_t launch_column_chunks(const uint8_t* codes, const uint8_t* scales, int n_mat, int rows,
-                                 int cols, uint8_t* codes_cc, uint8_t* scales_cc, cudaStream_t st) {
-  const int64_t n = (int64_t)rows * (cols / 8);
-  int g = (int)((n + 255) / 256);
-  if (g > 4096) g = 4096;
-  k_column_chunks<<<dim3(g, n_mat), 256, 0, st>>>(codes, scales, rows, cols, codes_cc, scales_cc);
+cudaError_t launch_unit_pack(const NVPtr& gate, const NVPtr& up, const NVPtr& down, int n_mat, int H,
+                             int F, uint8_t* units, cudaStream_t st) {
+  k_unit_pack<<<dim3(F / 32, n_mat), 256, 0, st>>>(gate, up, down, H, F, units);
   return cudaGetLastError();
 }
 
@@ -1124,7 +1087,8 @@ DecodePlan decode_plan(int H, int E, int K, int F, int Fs, int G) {
   p.shared_units = (Fs / kUnit + G - 1) / G;
   p.routed_units = (K * (F / kUnit) + G - 1) / G;
   p.smem = (size_t)H * (4 + 2 + 2) + (size_t)p.router_rows * H * 2 +
-           (size_t)(p.shared_units + p.routed_units) * UnitLayout::of(H).bytes;
+           (size_t)(p.shared_units + p.routed_units) * UnitLayout::of(H).bytes +
+           (size_t)3 * E * sizeof(float);
   p.ok = p.router_rows <= kMaxRouterRows && p.routed_units <= kMaxRoutedUnits &&
          p.shared_units <= kMaxSharedUnits &&
          p.smem <= kMaxDecodeSmem && F % (2 * kUnit) == 0 && Fs % (2 * kUnit) == 0;
@@ -1152,7 +1116,8 @@ static cudaError_t launch_persistent_cpl(const PersistArgs& a, size_t smem, cuda
 // a.max_router_rows / a.max_shared_units must hold decode_plan's counts.
 cudaError_t launch_persistent(const PersistArgs& a, cudaStream_t st) {
   const DecodePlan p = decode_plan(a.H, a.E, a.K, a.F, a.Fs, decode_grid());
-  if (!p.ok || a.max_router_rows != p.router_rows || a.max_shared_units != p.shared_units)
+  if (!p.ok || a.max_router_rows != p.router_rows || a.max_shared_units != p.shared_units ||
+      a.max_routed_units != p.routed_units)
     return cudaErrorInvalidConfiguration;
   if (a.tag_copies < 1) return cudaErrorInvalidValue;
   cudaError_t e = cudaMemsetAsync(a.bar, 0, decode_cleared_bytes(a.H, a.E, a.tag_copies), st);

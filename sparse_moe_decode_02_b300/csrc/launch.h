@@ -14,12 +14,10 @@ struct NVPtr {
 struct LayerPtrs {
   const uint16_t* router_w;
   const float* router_bias;
-  NVPtr gate, up, sh_gate, sh_up;
-  const uint8_t* dcc_codes;       // column-chunk copy of down [E][F/8][H][4]
-  const uint8_t* dcc_scales;      // [E][F/16][H]
+  NVPtr gate, up, sh_gate, sh_up;  // the tensor scales are read from these stacks
+  const uint8_t* units;           // decode units of (gate, up, down) [E][F/8][14 H]
+  const uint8_t* sh_units;        // of (sh_gate, sh_up, sh_down) [1][Fs/8][14 H]
   const float* down_tsc;          // [E]
-  const uint8_t* sh_dcc_codes;    // column-chunk copy of sh_down [1][Fs/8][H][4]
-  const uint8_t* sh_dcc_scales;
   const float* sh_down_tsc;       // [1]
 };
 
@@ -46,6 +44,7 @@ struct PersistArgs {
   int* best_i;             // [grid]
   int max_router_rows;     // per-CTA buffer sizes (decode_plan)
   int max_shared_units;
+  int max_routed_units;
   LayerPtrs layer[kMaxLayers];
 };
 
@@ -64,8 +63,8 @@ int decode_tag_copies(int E);
 int decode_grid();                                   // CTAs of the persistent kernel
 void decode_carve(PersistArgs& a, void* ws);          // a.H, a.E, a.tag_copies set
 cudaError_t launch_persistent(const PersistArgs& a, cudaStream_t st);
-cudaError_t launch_column_chunks(const uint8_t* codes, const uint8_t* scales, int n_mat, int rows,
-                                 int cols, uint8_t* codes_cc, uint8_t* scales_cc, cudaStream_t st);
+cudaError_t launch_unit_pack(const NVPtr& gate, const NVPtr& up, const NVPtr& down, int n_mat, int H,
+                             int F, uint8_t* units, cudaStream_t st);
 
 struct PrefillArgs {
   int H, E, K, F, Fs, T;

@@ -37,22 +37,19 @@ class _NVFP4C(ctypes.Structure):
                 ("rows", ctypes.c_int), ("cols", ctypes.c_int)]
 
 
-class _CCC(ctypes.Structure):
-    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
-
-
 class _LayerC(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
                 ("expert_width", ctypes.c_int), ("shared_width", ctypes.c_int),
                 ("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
                 ("gate", _NVFP4C), ("up", _NVFP4C), ("down", _NVFP4C),
                 ("sh_gate", _NVFP4C), ("sh_up", _NVFP4C), ("sh_down", _NVFP4C),
-                ("down_cc", _CCC), ("sh_down_cc", _CCC), ("mma_scales", ctypes.c_void_p * 6)]
+                ("units", ctypes.c_void_p), ("sh_units", ctypes.c_void_p),
+                ("mma_scales", ctypes.c_void_p * 6)]
 
 
 _lib = None
 
-_SYMBOLS = ["flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_nvfp4_column_chunks",
+_SYMBOLS = ["flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_decode_units",
             "flint_nvfp4_mma_scales",
             "flint_moe_decode", "flint_decode_tokens", "flint_moe_prefill", "flint_lm_head",
             "flint_workspace_bytes", "flint_last_device_status", "flint_status_string",
@@ -71,7 +68,7 @@ def lib() -> ctypes.CDLL:
     vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     L.flint_quantize_nvfp4.argtypes = [vp, i, i, i, vp, vp, vp, vp, sz, vp]
     L.flint_dequantize_nvfp4.argtypes = [ctypes.POINTER(_NVFP4C), vp, vp]
-    L.flint_nvfp4_column_chunks.argtypes = [ctypes.POINTER(_NVFP4C), vp, vp, vp]
+    L.flint_decode_units.argtypes = [ctypes.POINTER(_NVFP4C)] * 3 + [vp, vp]
     L.flint_nvfp4_mma_scales.argtypes = [ctypes.POINTER(_NVFP4C), vp, vp]
     L.flint_decode_tokens.argtypes = [ctypes.POINTER(_LayerC), i, ctypes.POINTER(_NVFP4C), vp, vp,
                                       i, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -89,7 +86,7 @@ def lib() -> ctypes.CDLL:
     L.flint_status_string.argtypes = [i]
     L.flint_status_string.restype = ctypes.c_char_p
     L.flint_version.restype = ctypes.c_char_p
-    for name in ("flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_nvfp4_column_chunks",
+    for name in ("flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_decode_units",
                  "flint_nvfp4_mma_scales", "flint_moe_decode", "flint_decode_tokens", "flint_decode_tokens_noalloc",
                  "flint_moe_prefill", "flint_lm_head", "flint_last_device_status"):
         getattr(L, name).restype = ctypes.c_int
@@ -155,8 +152,8 @@ class MoELayer:
     sh_up: NVFP4
     sh_down: NVFP4
     top_k: int
-    down_cc: tuple | None = None      # (codes, scales) column-chunk copy of down
-    sh_down_cc: tuple | None = None   # (codes, scales) column-chunk copy of sh_down
+    units: torch.Tensor | None = None     # decode-unit copy of (gate, up, down)
+    sh_units: torch.Tensor | None = None  # decode-unit copy of (sh_gate, sh_up, sh_down)
     mma_scales: tuple | None = None   # MMA scale copies of gate, up, down, sh_gate, sh_up, sh_down
 
     @property
@@ -166,13 +163,13 @@ class MoELayer:
 
     def c(self) -> _LayerC:
         H, E, k, F, Fs = self.dims
-        cc = lambda t: _CCC(None, None) if t is None else _CCC(t[0].data_ptr(), t[1].data_ptr())
+        ptr = lambda t: None if t is None else t.data_ptr()
         sf = (ctypes.c_void_p * 6)(*([None] * 6 if self.mma_scales is None else
                                      [m.data_ptr() for m in self.mma_scales]))
         return _LayerC(H, E, k, F, Fs, self.router_w.data_ptr(),
                        None if self.router_bias is None else self.router_bias.data_ptr(),
                        self.gate.c(), self.up.c(), self.down.c(), self.sh_gate.c(),
-                       self.sh_up.c(), self.sh_down.c(), cc(self.down_cc), cc(self.sh_down_cc), sf)
+                       self.sh_up.c(), self.sh_down.c(), ptr(self.units), ptr(self.sh_units), sf)
 
     def nbytes(self) -> int:
         return (self.router_w.numel() * 2 + sum(m.nbytes() for m in (
@@ -198,14 +195,19 @@ def quantize_nvfp4(w: torch.Tensor, stream=None, ws=None) -> NVFP4:
     return q
 
 
-def nvfp4_column_chunks(m: NVFP4, stream=None):
-    """Column-chunk copy (codes, scales) of an NVFP4 stack (see flint.h)."""
-    codes = torch.empty_like(m.codes)
-    scales = torch.empty_like(m.scales)
-    mc = m.c()
-    _check(lib().flint_nvfp4_column_chunks(ctypes.byref(mc), _ptr(codes), _ptr(scales),
-                                           _stream(stream)), "flint_nvfp4_column_chunks")
-    return codes, scales
+def decode_units(gate: NVFP4, up: NVFP4, down: NVFP4, stream=None) -> torch.Tensor:
+    """Decode-unit copy of (gate [n, F, H], up, down [n, H, F]) (see flint.h)."""
+    n, F, H = gate.shape
+    out = torch.empty(n, F // 8, unit_bytes(H), dtype=torch.uint8, device=gate.codes.device)
+    g, u, d = gate.c(), up.c(), down.c()
+    _check(lib().flint_decode_units(ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), _ptr(out),
+                                    _stream(stream)), "flint_decode_units")
+    return out
+
+
+def unit_bytes(hidden: int) -> int:
+    """Bytes of one decode unit (FLINT_UNIT_BYTES)."""
+    return 14 * hidden
 
 
 def nvfp4_mma_scales(m: NVFP4, stream=None) -> torch.Tensor:

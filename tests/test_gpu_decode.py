@@ -216,16 +216,25 @@ def test_lm_head_argmax_only():
 
 
 # ------------------------------------------------------------------ persistent multi-layer decode
-def test_column_chunks_bitexact():
-    w = synth.normal_bf16(synth.tensor_key(9), 3 * 64 * 256, 0.02).view(3, 64, 256).to(DEV)
-    m = flint.quantize_nvfp4(w)
-    cc, sc = flint.nvfp4_column_chunks(m)
-    codes = m.codes.cpu().numpy().reshape(3, 64, 32, 4)          # [n][rows][8-col chunk][4]
-    scales = m.scales.cpu().numpy().reshape(3, 64, 16)           # [n][rows][16-col block]
-    np.testing.assert_array_equal(cc.cpu().numpy().reshape(3, 32, 64, 4),
-                                  codes.transpose(0, 2, 1, 3))
-    np.testing.assert_array_equal(sc.cpu().numpy().reshape(3, 16, 64),
-                                  scales.transpose(0, 2, 1))
+def test_decode_units_bitexact():
+    # the decode-unit copy against the layout of FLINT_UNIT_BYTES, rebuilt with numpy
+    n, F, H = 3, 64, 256
+    key = synth.tensor_key(9)
+    g = flint.quantize_nvfp4(synth.normal_bf16(key, n * F * H, 0.02).view(n, F, H).to(DEV))
+    u = flint.quantize_nvfp4(synth.normal_bf16(key + 1, n * F * H, 0.02).view(n, F, H).to(DEV))
+    d = flint.quantize_nvfp4(synth.normal_bf16(key + 2, n * H * F, 0.02).view(n, H, F).to(DEV))
+    got = flint.decode_units(g, u, d).cpu().numpy()
+    assert got.shape == (n, F // 8, 14 * H)
+    gc, gs = g.codes.cpu().numpy(), g.scales.cpu().numpy()
+    uc, us = u.codes.cpu().numpy(), u.scales.cpu().numpy()
+    dc, ds = d.codes.cpu().numpy(), d.scales.cpu().numpy()
+    for m in range(n):
+        for j in range(F // 8):
+            rows = slice(8 * j, 8 * j + 8)
+            want = np.concatenate([gc[m, rows].ravel(), gs[m, rows].ravel(),
+                                   uc[m, rows].ravel(), us[m, rows].ravel(),
+                                   dc[m, :, 4 * j:4 * j + 4].ravel(), ds[m, :, j // 2]])
+            np.testing.assert_array_equal(got[m, j], want)
 
 
 def test_mma_scales_bitexact():

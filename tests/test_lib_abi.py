@@ -54,10 +54,10 @@ def _nv(n, r, c, codes=FAKE):
     return flint._NVFP4C(codes, FAKE, FAKE, n, r, c)
 
 
-def _layer(H=256, E=16, k=2, F=64, Fs=128, router=FAKE, gate_cols=None, cc=FAKE, sf=FAKE):
+def _layer(H=256, E=16, k=2, F=64, Fs=128, router=FAKE, gate_cols=None, units=FAKE, sf=FAKE):
     return flint._LayerC(H, E, k, F, Fs, router, None, _nv(E, F, gate_cols or H), _nv(E, F, H),
                          _nv(E, H, F), _nv(1, Fs, H), _nv(1, Fs, H), _nv(1, H, Fs),
-                         flint._CCC(cc, cc), flint._CCC(cc, cc), (ctypes.c_void_p * 6)(*[sf] * 6))
+                         units, units, (ctypes.c_void_p * 6)(*[sf] * 6))
 
 
 def test_quantize_argument_checks(L):
@@ -89,8 +89,8 @@ def test_decode_argument_checks(L):
     assert call(_layer(H=250), args()) == 3                             # not a multiple of 32
     assert call(_layer(gate_cols=512), args()) == 3                     # stack shape mismatch
     assert call(_layer(router=FAKE_MIS), args()) == 2
-    assert call(_layer(cc=None), args()) == 1                           # no column-chunk copy
-    assert call(_layer(cc=FAKE_MIS), args()) == 2
+    assert call(_layer(units=None), args()) == 1                        # no decode-unit copy
+    assert call(_layer(units=FAKE_MIS), args()) == 2
 
 
 def test_decode_tokens_argument_checks(L):
@@ -116,13 +116,17 @@ def test_decode_tokens_argument_checks(L):
     assert call(ok(wsb=16)) == 4
 
 
-def test_column_chunks_argument_checks(L):
-    cc = L.flint_nvfp4_column_chunks
-    m = _nv(2, 64, 80)
-    assert cc(ctypes.byref(m), None, FAKE, None) == 1
-    assert cc(ctypes.byref(m), FAKE, FAKE, None) == 3                   # cols % 32
-    m2 = _nv(2, 64, 128)
-    assert cc(ctypes.byref(m2), FAKE_MIS, FAKE, None) == 2
+def test_decode_units_argument_checks(L):
+    du = L.flint_decode_units
+    g, u, d = _nv(2, 64, 128), _nv(2, 64, 128), _nv(2, 128, 64)
+    r = ctypes.byref
+    assert du(r(g), r(u), r(d), None, None) == 1
+    assert du(None, r(u), r(d), FAKE, None) == 1
+    assert du(r(g), r(u), r(d), FAKE_MIS, None) == 2
+    g80, u80, d80 = _nv(2, 80, 128), _nv(2, 80, 128), _nv(2, 128, 80)
+    assert du(r(g80), r(u80), r(d80), FAKE, None) == 3                  # F % 32
+    assert du(r(g), r(u), r(_nv(2, 64, 128)), FAKE, None) == 3          # down not [n, H, F]
+    assert du(r(g), r(_nv(3, 64, 128)), r(d), FAKE, None) == 3          # up of another count
 
 
 def test_mma_scales_argument_checks(L):
