@@ -309,26 +309,50 @@ struct UnitLayout {
   }
 };
 
-// Gate/up of one unit from shared memory: the 16 row dot products (a warp per row, by
-// warps [w0, w0 + nw)), with tensor scales and 2^-k applied, into s_gu[0..16).  No barrier.
+// Gate/up of n units from shared memory (unit u at buf + u * ub): their 16 n row dot
+// products, by warps [w0, w0 + nw), with tensor scales (unit u: gate tsc[2 u s],
+// up tsc[2 u s + 1], s = tsc_stride) and 2^-k applied, into s_gu[16 u + row].  A warp
+// takes up to kGURows rows per pass and interleaves them, so that their load, FMA and
+// shuffle latencies overlap.  No barrier.
+constexpr int kGURows = 3;
 template <int CPL>
-__device__ __forceinline__ void unit_gateup(const uint8_t* buf, int H, float gate_tsc, float up_tsc,
-                                            const XStage<CPL, 1>& xs, float* s_gu, int w0, int nw) {
+__device__ __forceinline__ void units_gateup(const uint8_t* buf, uint32_t ub, int n, int H, const float* tsc,
+                                             int tsc_stride, const XStage<CPL, 1>& xs, float* s_gu, int w0,
+                                             int nw) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int LPR = H / (32 * CPL), RPP = 32 / LPR;
   const int slice = lane / LPR, sl = lane % LPR;
   const UnitLayout U = UnitLayout::of(H);
-  #pragma unroll 1
-  for (int r0 = (warp - w0) * RPP; r0 < 2 * kUnit; r0 += nw * RPP) {
-    const int r = r0 + slice;
-    const int rr = r < 2 * kUnit ? r : 0;
-    const bool is_up = rr >= kUnit;
-    const int row = is_up ? rr - kUnit : rr;
-    RowRegs<CPL> w;
-    lds_row<CPL>(w, buf + (is_up ? U.uc : U.gc) + row * (H / 2),
-                 buf + (is_up ? U.us : U.gs) + row * (H / 16), sl, LPR);
-    const float v = sum_lanes_rt(dot_row<CPL, 1>(w, xs), LPR);
-    if (sl == 0 && r < 2 * kUnit) s_gu[r] = v * (is_up ? up_tsc : gate_tsc) * xs.unscale;
+  const int R = 2 * kUnit * n, step = nw * RPP;
+#pragma unroll 1
+  for (int b0 = (warp - w0) * RPP; b0 < R; b0 += kGURows * step) {
+    RowRegs<CPL> w[kGURows];
+#pragma unroll
+    for (int k = 0; k < kGURows; ++k) {
+      const int r = b0 + k * step + slice;
+      const int rc = r < R ? r : 0;
+      const int q = rc % (2 * kUnit);
+      const uint8_t* ubuf = buf + (size_t)(rc / (2 * kUnit)) * ub;
+      const bool up = q >= kUnit;
+      const int row = up ? q - kUnit : q;
+      lds_row<CPL>(w[k], ubuf + (up ? U.uc : U.gc) + row * (H / 2), ubuf + (up ? U.us : U.gs) + row * (H / 16),
+                   sl, LPR);
+    }
+    float v[kGURows];
+#pragma unroll
+    for (int k = 0; k < kGURows; ++k) v[k] = dot_row<CPL, 1>(w[k], xs);
+#pragma unroll 1
+    for (int o = LPR / 2; o; o >>= 1)
+#pragma unroll
+      for (int k = 0; k < kGURows; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
+#pragma unroll
+    for (int k = 0; k < kGURows; ++k) {
+      const int r = b0 + k * step + slice;
+      if (sl == 0 && r < R) {
+        const int u = r / (2 * kUnit), q = r % (2 * kUnit);
+        s_gu[r] = v[k] * tsc[2 * u * tsc_stride + (q >= kUnit ? 1 : 0)] * xs.unscale;
+      }
+    }
   }
 }
 
@@ -695,6 +719,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
   __shared__ unsigned long long s_c64[FLINT_MAX_EXPERTS];
   __shared__ LayerSmem s_ly[2];                      // layer tables, by step parity
   __shared__ float s_tsc[FLINT_MAX_TOP_K][3];         // selected experts: gate, up, down x weight
+  __shared__ float s_rtsc[kMaxRoutedUnits][2];        // routed units: gate, up tensor scales
   __shared__ __align__(8) uint64_t s_bar_rr, s_bar_sh;
   __shared__ __align__(8) uint64_t s_bar_rt[kMaxRoutedUnits];
   extern __shared__ __align__(128) uint8_t s_dyn[];
@@ -889,16 +914,18 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
             s_tsc[lane][1] = ok ? s_etsc[a.E + e] : 0.f;
             s_tsc[lane][2] = ok ? s_etsc[2 * a.E + e] * (pr / z) : 0.f;
           }
+          __syncwarp();
+          if (lane < my_rt) {
+            s_rtsc[lane][0] = s_tsc[s_slot[lane]][0];
+            s_rtsc[lane][1] = s_tsc[s_slot[lane]][1];
+          }
         }
       } else {
         // ---- shared units' gate/up by the warps that do not poll; the last of them
         // then fetches the next layer's table
         if (my_sh > 0) {
           mbar_wait(&s_bar_sh, ph_sh, sync);
-#pragma unroll 1
-          for (int i = 0; i < my_sh; ++i)
-            unit_gateup<CPL>(s_static + (size_t)i * U.bytes, H, LY.sh_tsc[0], LY.sh_tsc[1], xs,
-                             s_gu + i * 2 * kUnit, npw, kPWarps - npw);
+          units_gateup<CPL>(s_static, U.bytes, my_sh, H, LY.sh_tsc, 0, xs, s_gu, npw, kPWarps - npw);
         }
         if (more && warp == kPWarps - 1) load_layer(a, l_next, &s_ly[(step + 1) & 1], c, G, my_rows);
       }
@@ -921,14 +948,12 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         const int off = g ? my_sh : 0;
         const uint8_t* ubase = g ? s_routed : s_static;
         if (g) {
+          // all routed units at once (they land close together; the interleaved rows
+          // hide each other's latency)
 #pragma unroll 1
-          for (int i = 0; i < my_rt; ++i) {
-            const int slot = s_slot[i];
-            mbar_wait(&s_bar_rt[i], ph_rt, sync);
-            unit_gateup<CPL>(s_routed + (size_t)i * U.bytes, H, s_tsc[slot][0], s_tsc[slot][1], xs,
-                             s_gu + (my_sh + i) * 2 * kUnit, 0, kPWarps);
-            if (threadIdx.x == 0) s_dscale[my_sh + i] = s_tsc[slot][2];
-          }
+          for (int i = 0; i < my_rt; ++i) mbar_wait(&s_bar_rt[i], ph_rt, sync);
+          units_gateup<CPL>(s_routed, U.bytes, my_rt, H, &s_rtsc[0][0], 1, xs, s_gu + my_sh * 2 * kUnit, 0, kPWarps);
+          if (threadIdx.x < my_rt) s_dscale[my_sh + threadIdx.x] = s_tsc[s_slot[threadIdx.x]][2];
           ph_rt ^= 1;
           __syncthreads();
           // the shared-unit buffers are free again
