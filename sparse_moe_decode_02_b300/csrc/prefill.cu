@@ -3,10 +3,11 @@
 // processing), as a token-permuted grouped GEMM on block-scaled FP4 tensor cores.
 //
 //   1 router      logits[T, E] = x Wr^T (+ bias): tcgen05 kind::f16 (bf16 in, fp32 acc),
-//                 128 tokens x 64 experts per CTA
-//   2 top-k       per token (one warp): softmax top-k, renormalised weights; per-expert
-//                 token bitmaps
-//   3 scan        per-expert counts, offsets (plain and padded to 128-row tiles) and the
+//                 128 tokens x all E experts per CTA, split 4 ways along K
+//   2 top-k       per token (one warp): the partial logits summed in order plus the
+//                 bias, softmax top-k, renormalised weights; per-expert token bitmaps
+//   3 scan        per expert (one warp): prefix counts of its bitmap words; then one CTA:
+//                 counts, offsets (plain and padded to 128-row tiles) and the
 //                 device-side item lists
 //   4 scatter     per token: x quantised to NVFP4 once (unit tensor scale) and written
 //                 to the shared expert's operand Xq and to the K expert-major rows of Xp
@@ -567,7 +568,7 @@ struct RouteArgs {
 };
 
 // One warp per token: the logits (partials summed in order, plus the bias), top-k (the
-// decode path's warp top-k) and the expert bitmaps.
+// exact warp top-k of topk_dispatch) and the expert bitmaps.
 __global__ void __launch_bounds__(256) k_topk(RouteArgs a) {
   __shared__ int s_sel[8][FLINT_MAX_TOP_K];
   __shared__ float s_w[8][FLINT_MAX_TOP_K];
