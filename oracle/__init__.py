@@ -53,7 +53,10 @@ class _Layer(ctypes.Structure):
                 ("shared_width", ctypes.c_int),
                 ("router_w", _u16p), ("router_bias", _f32p),
                 ("gate", _NVFP4), ("up", _NVFP4), ("down", _NVFP4),
-                ("sh_gate", _NVFP4), ("sh_up", _NVFP4), ("sh_down", _NVFP4)]
+                ("sh_gate", _NVFP4), ("sh_up", _NVFP4), ("sh_down", _NVFP4),
+                ("router_score", ctypes.c_int)]
+
+ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
 
 
 _lib = None
@@ -188,13 +191,15 @@ def quantize_rows_unit(v: np.ndarray):
 class Layer:
     """Oracle-side MoE layer.  Matrices are NVFP4 stacks; router_w is bf16 bits."""
 
-    def __init__(self, router_w, router_bias, gate, up, down, sh_gate, sh_up, sh_down, top_k):
+    def __init__(self, router_w, router_bias, gate, up, down, sh_gate, sh_up, sh_down, top_k,
+                 router_score=ROUTER_SOFTMAX):
         self.router_w = _bits16(router_w)
         self.router_bias = (None if router_bias is None
                             else np.ascontiguousarray(router_bias, dtype=np.float32))
         self.gate, self.up, self.down = gate, up, down
         self.sh_gate, self.sh_up, self.sh_down = sh_gate, sh_up, sh_down
         self.top_k = int(top_k)
+        self.router_score = int(router_score)
         self.n_experts, self.hidden = self.router_w.shape
         self.expert_width = gate.shape[1]
         self.shared_width = sh_gate.shape[1]
@@ -203,7 +208,8 @@ class Layer:
         return _Layer(self.hidden, self.n_experts, self.top_k, self.expert_width,
                       self.shared_width, _p(self.router_w, _u16p),
                       _p(self.router_bias, _f32p), self.gate.c(), self.up.c(),
-                      self.down.c(), self.sh_gate.c(), self.sh_up.c(), self.sh_down.c())
+                      self.down.c(), self.sh_gate.c(), self.sh_up.c(), self.sh_down.c(),
+                      self.router_score)
 
 
 def router(layer: Layer, x_bf16):

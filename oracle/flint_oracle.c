@@ -257,12 +257,17 @@ void orc_router(const orc_layer* L, const uint16_t* x, double* logits, int32_t* 
       acc += orc_bf16_value(L->router_w[(int64_t)e * H + h]) * orc_bf16_value(x[h]);
     l[e] = acc + (L->router_bias ? (double)L->router_bias[e] : 0.0);
   }
-  /* softmax over all experts */
-  double mx = l[0];
-  for (int e = 1; e < E; ++e) if (l[e] > mx) mx = l[e];
-  double z = 0.0;
-  for (int e = 0; e < E; ++e) { p[e] = exp(l[e] - mx); z += p[e]; }
-  for (int e = 0; e < E; ++e) p[e] /= z;
+  if (L->router_score == ORC_ROUTER_SIGMOID) {
+    /* an independent score per expert */
+    for (int e = 0; e < E; ++e) p[e] = 1.0 / (1.0 + exp(-l[e]));
+  } else {
+    /* softmax over all experts */
+    double mx = l[0];
+    for (int e = 1; e < E; ++e) if (l[e] > mx) mx = l[e];
+    double z = 0.0;
+    for (int e = 0; e < E; ++e) { p[e] = exp(l[e] - mx); z += p[e]; }
+    for (int e = 0; e < E; ++e) p[e] /= z;
+  }
   /* top-k by logit, ties to the lower index */
   double psel = 0.0;
   for (int i = 0; i < k; ++i) {
@@ -348,7 +353,8 @@ static void forward_tokens_fn(void* p, int64_t lo, int64_t hi) {
 int orc_moe_forward(const orc_layer* L, const uint16_t* x, const double* residual,
                     int64_t n_tok, int quantize_acts, double* out, int32_t* idx, double* w) {
   if (!L || L->top_k < 1 || L->top_k > L->n_experts || L->hidden % 16 ||
-      L->expert_width % 16 || L->shared_width % 16)
+      L->expert_width % 16 || L->shared_width % 16 ||
+      (L->router_score != ORC_ROUTER_SOFTMAX && L->router_score != ORC_ROUTER_SIGMOID))
     return ORC_ERR_ARG;
   fwdctx c = {L, x, residual, quantize_acts, out, idx, w};
   parallel_for(n_tok, forward_tokens_fn, &c);

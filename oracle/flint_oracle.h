@@ -77,11 +77,20 @@ typedef struct {
   orc_nvfp4 down;             /* [E, H, F] */
   orc_nvfp4 sh_gate, sh_up;   /* [1, Fs, H] */
   orc_nvfp4 sh_down;          /* [1, H, Fs] */
+  int router_score;           /* ORC_ROUTER_SOFTMAX or ORC_ROUTER_SIGMOID */
 } orc_layer;
 
-/* Router: logits = Wr x + b (fp64); softmax over all experts; the top_k experts by
- * logit (ties to the lower index) in that order; weights = p_i / sum of the
- * selected p.  logits may be NULL. */
+enum { ORC_ROUTER_SOFTMAX = 0, ORC_ROUTER_SIGMOID = 1 };
+
+/* Router: logits = Wr x + b (fp64); the top_k experts by logit (ties to the lower
+ * index) in that order; weights = p_i / sum of the selected p, where p is
+ *  - ORC_ROUTER_SOFTMAX: the softmax over all experts (the default reading);
+ *  - ORC_ROUTER_SIGMOID: the sigmoid of each logit, the scoring named in "Flint: 125
+ *    tokens a second is what 2.5B active parameters buy at 273 GB/s", section "The
+ *    shape, read from the headers".  Sigmoid is increasing, so the top_k by score
+ *    are the top_k by logit; ranking by logit keeps that exact where fp64 sigmoids
+ *    of large logits round to equal values.
+ * logits may be NULL. */
 void orc_router(const orc_layer* L, const uint16_t* x, double* logits, int32_t* idx,
                 double* w);
 

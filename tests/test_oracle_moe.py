@@ -36,7 +36,7 @@ def _x(n, H, seed=1):
     return torch.randn(n, H, generator=g).to(torch.bfloat16)
 
 
-def _numpy_forward(L, x_bits, quantize_acts=False, orc=None):
+def _numpy_forward(L, x_bits, quantize_acts=False, orc=None, sigmoid=False):
     """Independent restatement: numpy matmul over weights decoded by indep."""
     deq = lambda m: indep.dequantize_np(m.codes, m.scales, m.tsc).astype(np.float64)
     Wg, Wu, Wd = deq(L.gate), deq(L.up), deq(L.down)
@@ -47,7 +47,8 @@ def _numpy_forward(L, x_bits, quantize_acts=False, orc=None):
     for x in xs:
         logits = Wr @ x + (0 if L.router_bias is None else L.router_bias.astype(np.float64))
         order = np.argsort(-logits, kind="stable")[:L.top_k]
-        w = softmax(logits[order])
+        w = (expit(logits[order]) / expit(logits[order]).sum() if sigmoid
+             else softmax(logits[order]))
         xin = x
         if quantize_acts:
             xin = _requant(orc, x)
@@ -90,6 +91,63 @@ def test_router_topk_bruteforce_and_weights(orc):
             if L.router_bias is not None:
                 want = want + L.router_bias
             np.testing.assert_allclose(logits, want, rtol=1e-12, atol=1e-15)
+
+
+def _with_score(orc, L, score, router_w=None, bias=None):
+    return orc.Layer(L.router_w if router_w is None else router_w,
+                     L.router_bias if bias is None else bias, L.gate, L.up, L.down, L.sh_gate,
+                     L.sh_up, L.sh_down, L.top_k, router_score=score)
+
+
+def test_router_sigmoid_bruteforce_and_weights(orc):
+    """Sigmoid scoring: the selected set is the size-k subset with the largest sum of
+    sigmoid scores, ordered by score; weights are the selected scores over their sum;
+    the set is the one softmax scoring selects (sigmoid is increasing)."""
+    for seed in range(6):
+        for E, k in [(4, 1), (5, 2), (8, 3), (8, 8), (6, 6)]:
+            L = _tiny_layer(orc, seed=seed, E=E, k=k, H=32, F=16, Fs=16, bias=seed % 2 == 1)
+            Ls = _with_score(orc, L, orc.ROUTER_SIGMOID)
+            x = _x(1, 32, seed=10 + seed)
+            logits, idx, w = orc.router(Ls, x)
+            sc = expit(logits)
+            best = max(itertools.combinations(range(E), k), key=lambda st: sum(sc[i] for i in st))
+            assert sorted(idx.tolist()) == sorted(best)
+            assert all(sc[idx[i]] >= sc[idx[i + 1]] for i in range(k - 1))
+            np.testing.assert_allclose(w, sc[idx] / sc[idx].sum(), rtol=1e-13)
+            assert abs(w.sum() - 1.0) < 1e-12
+            _, idx_soft, _ = orc.router(L, x)
+            np.testing.assert_array_equal(idx, idx_soft)
+
+
+def test_router_sigmoid_closed_form(orc):
+    """Zero router weights make the logits equal the bias.  Logits 0, ln 3, -ln 3 score
+    1/2, 3/4, 1/4, so top-2 picks experts 1 then 0 with weights 3/5 and 2/5; with all
+    logits equal every selected expert gets 1/k."""
+    L = _tiny_layer(orc, E=4, k=2, H=32, F=16, Fs=16)
+    zero = np.zeros_like(L.router_w)
+    ln3 = math.log(3.0)
+    Ls = _with_score(orc, L, orc.ROUTER_SIGMOID, router_w=zero,
+                     bias=np.array([0.0, ln3, -ln3, -2 * ln3], np.float32))
+    logits, idx, w = orc.router(Ls, _x(1, 32))
+    np.testing.assert_array_equal(idx, [1, 0])
+    np.testing.assert_allclose(w, [0.6, 0.4], rtol=1e-7)
+    Le = _with_score(orc, L, orc.ROUTER_SIGMOID, router_w=zero,
+                     bias=np.full(4, 0.7, np.float32))
+    _, idx, w = orc.router(Le, _x(1, 32))
+    np.testing.assert_array_equal(idx, [0, 1])          # ties to the lower index
+    np.testing.assert_allclose(w, [0.5, 0.5], rtol=1e-15)
+
+
+def test_layer_sigmoid_matches_numpy_restatement(orc):
+    L = _with_score(orc, _tiny_layer(orc, seed=4, E=8, k=3, H=64, F=32, Fs=48, bias=True),
+                    orc.ROUTER_SIGMOID)
+    x = _x(5, 64, seed=6)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    out, idx, w = orc.moe_forward(L, x)
+    ref, ridx, rw = _numpy_forward(L, xb, sigmoid=True)
+    np.testing.assert_array_equal(idx, ridx)
+    np.testing.assert_allclose(w, rw, rtol=1e-12)
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-13)
 
 
 def test_router_ties_go_to_lower_index(orc):
