@@ -111,7 +111,20 @@ typedef struct {
   const uint8_t* units;        /* [E][F/8][FLINT_UNIT_BYTES(H)] */
   const uint8_t* sh_units;     /* [1][Fs/8][FLINT_UNIT_BYTES(H)] */
   const uint8_t* mma_scales[6];
+  int router_score;            /* FLINT_ROUTER_SOFTMAX (0) or FLINT_ROUTER_SIGMOID (1) */
 } flint_moe_layer;
+
+/* Router scoring of a layer (flint_moe_layer.router_score).  Both select the top_k
+ * experts by logit, ties to the lower index, and renormalise over the selected:
+ *  - FLINT_ROUTER_SOFTMAX: w_i = exp(l_i - l_max) / sum over the selected (the
+ *    softmax over all E, renormalised);
+ *  - FLINT_ROUTER_SIGMOID: w_i = sigmoid(l_i) / sum of the selected sigmoids.  This is
+ *    the scoring "Flint: 125 tokens a second is what 2.5B active parameters buy at 273
+ *    GB/s", section "The shape, read from the headers", names.  Sigmoid is
+ *    increasing, so the same experts are selected.
+ * Any other value is FLINT_ERR_INVALID_ARG. */
+#define FLINT_ROUTER_SOFTMAX 0
+#define FLINT_ROUTER_SIGMOID 1
 
 /* Limits of this build. */
 #define FLINT_MAX_DECODE_TOKENS 8     /* B of flint_moe_decode / flint_lm_head */

@@ -34,6 +34,8 @@ flint_status check_layer(const flint_moe_layer* L) {
       L->shared_width <= 0)
     return FLINT_ERR_INVALID_ARG;
   if (L->top_k > L->n_experts) return FLINT_ERR_INVALID_ARG;
+  if (L->router_score != FLINT_ROUTER_SOFTMAX && L->router_score != FLINT_ROUTER_SIGMOID)
+    return FLINT_ERR_INVALID_ARG;
   if (L->top_k > FLINT_MAX_TOP_K || L->n_experts > FLINT_MAX_EXPERTS) return FLINT_ERR_UNSUPPORTED;
   if (L->hidden % 32 || L->expert_width % 32 || L->shared_width % 32) return FLINT_ERR_SHAPE;
   if (!gemv_width_ok(L->hidden) || !gemv_width_ok(L->expert_width) ||
@@ -74,6 +76,8 @@ flint::LayerPtrs layer_ptrs(const flint_moe_layer& L) {
   p.units = L.units; p.sh_units = L.sh_units;
   p.down_tsc = L.down.tensor_scale;
   p.sh_down_tsc = L.sh_down.tensor_scale;
+  p.router_score = L.router_score;
+  p.pad_ = 0;
   return p;
 }
 
@@ -310,6 +314,7 @@ flint_status flint_moe_prefill(const flint_moe_layer* L, const void* x_bf16, flo
   a.Fs = L->shared_width; a.T = T;
   a.router_w = static_cast<const uint16_t*>(L->router_w);
   a.router_bias = L->router_bias;
+  a.router_score = L->router_score;
   a.gate = nv(L->gate); a.up = nv(L->up); a.down = nv(L->down);
   a.sh_gate = nv(L->sh_gate); a.sh_up = nv(L->sh_up); a.sh_down = nv(L->sh_down);
   a.x = static_cast<const uint16_t*>(x_bf16);

@@ -899,10 +899,12 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
           }
         }
         if (warp == (npw > 1 ? 1 : 0)) {
-          // routing weights: softmax over the selected, renormalised
+          // routing weights: the selected scores (softmax or sigmoid), renormalised
           const float lv = lane < a.K ? s_lsel[lane] : 0.f;
           const float l0 = __shfl_sync(0xffffffffu, lv, 0);
-          const float pr = lane < a.K ? expf(lv - l0) : 0.f;
+          const float pr = lane >= a.K ? 0.f
+                           : P.router_score == FLINT_ROUTER_SIGMOID ? 1.0f / (1.0f + expf(-lv))
+                                                                    : expf(lv - l0);
           float z = pr;
 #pragma unroll
           for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);

@@ -19,6 +19,8 @@ struct LayerPtrs {
   const uint8_t* sh_units;        // of (sh_gate, sh_up, sh_down) [1][Fs/8][14 H]
   const float* down_tsc;          // [E]
   const float* sh_down_tsc;       // [1]
+  int router_score;               // FLINT_ROUTER_SOFTMAX / FLINT_ROUTER_SIGMOID
+  int pad_;
 };
 
 constexpr int kMaxLayers = 64;
@@ -78,6 +80,7 @@ struct PrefillArgs {
   int32_t* counts_out;
   int32_t* order_out;
   const uint8_t* sf[6];    // MMA scale copies: gate, up, down, sh_gate, sh_up, sh_down
+  int router_score;        // FLINT_ROUTER_SOFTMAX / FLINT_ROUTER_SIGMOID
 };
 
 size_t prefill_workspace_bytes(int H, int E, int K, int F, int Fs, int T);

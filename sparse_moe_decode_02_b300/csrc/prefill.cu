@@ -555,6 +555,7 @@ struct RouteArgs {
   int T, E, K, W;          // W = words per expert bitmap = ceil(T/32)
   const float* part;       // [kRSplit][T][E] partial logits
   const float* bias;       // [E] or null
+  int sigmoid;             // weights from sigmoid scores instead of the softmax
   int32_t* idx;            // [T][K]
   float* w;                // [T][K]
   int32_t* idx_out;
@@ -584,6 +585,20 @@ __global__ void __launch_bounds__(256) k_topk(RouteArgs a) {
   }
   __syncwarp();
   topk_dispatch(s_lg[warp], a.E, a.K, s_sel[warp], s_w[warp]);
+  if (a.sigmoid) {
+    // the same experts; weights = their sigmoid scores over the selected sum
+    float p = 0.f;
+    if (lane < a.K) {
+      float l = s_lg[warp][s_sel[warp][lane]];
+      l = (l == l) ? l : -INFINITY;
+      p = 1.0f / (1.0f + expf(-l));
+    }
+    float z = p;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    if (lane < a.K) s_w[warp][lane] = p / z;
+    __syncwarp();
+  }
   if (lane < a.K) {
     const int e = s_sel[warp][lane];
     const float wv = s_w[warp][lane];
@@ -931,6 +946,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st) {
   r.T = T; r.E = E; r.K = K; r.W = (T + 31) / 32;
   r.part = reinterpret_cast<float*>(at(L.logits));
   r.bias = a.router_bias;
+  r.sigmoid = a.router_score == FLINT_ROUTER_SIGMOID;
   r.idx = reinterpret_cast<int32_t*>(at(L.idx));
   r.w = reinterpret_cast<float*>(at(L.w));
   r.idx_out = a.idx_out; r.w_out = a.w_out;

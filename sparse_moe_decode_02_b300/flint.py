@@ -44,7 +44,9 @@ class _LayerC(ctypes.Structure):
                 ("gate", _NVFP4C), ("up", _NVFP4C), ("down", _NVFP4C),
                 ("sh_gate", _NVFP4C), ("sh_up", _NVFP4C), ("sh_down", _NVFP4C),
                 ("units", ctypes.c_void_p), ("sh_units", ctypes.c_void_p),
-                ("mma_scales", ctypes.c_void_p * 6)]
+                ("mma_scales", ctypes.c_void_p * 6), ("router_score", ctypes.c_int)]
+
+ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
 
 
 _lib = None
@@ -155,6 +157,7 @@ class MoELayer:
     units: torch.Tensor | None = None     # decode-unit copy of (gate, up, down)
     sh_units: torch.Tensor | None = None  # decode-unit copy of (sh_gate, sh_up, sh_down)
     mma_scales: tuple | None = None   # MMA scale copies of gate, up, down, sh_gate, sh_up, sh_down
+    router_score: int = 0             # ROUTER_SOFTMAX or ROUTER_SIGMOID
 
     @property
     def dims(self):
@@ -169,7 +172,8 @@ class MoELayer:
         return _LayerC(H, E, k, F, Fs, self.router_w.data_ptr(),
                        None if self.router_bias is None else self.router_bias.data_ptr(),
                        self.gate.c(), self.up.c(), self.down.c(), self.sh_gate.c(),
-                       self.sh_up.c(), self.sh_down.c(), ptr(self.units), ptr(self.sh_units), sf)
+                       self.sh_up.c(), self.sh_down.c(), ptr(self.units), ptr(self.sh_units), sf,
+                       self.router_score)
 
     def nbytes(self) -> int:
         return (self.router_w.numel() * 2 + sum(m.nbytes() for m in (

@@ -144,6 +144,7 @@ class LayerSpec:
     seed: int
     layer: int = 0
     zipf: float | None = None          # router bias exponent, None = no bias
+    router_score: int = 0              # 0 softmax, 1 sigmoid scoring (a layer flag)
 
     def key(self, kind: int) -> int:
         return tensor_key(self.seed, self.layer, kind)

@@ -33,7 +33,7 @@ def build_layer(spec: synth.LayerSpec, device="cuda", stream=None) -> flint.MoEL
     return flint.MoELayer(router, bias_t, gate, up, down, sh_gate, sh_up, sh_down, s.top_k,
                           units=flint.decode_units(gate, up, down, stream=stream),
                           sh_units=flint.decode_units(sh_gate, sh_up, sh_down, stream=stream),
-                          mma_scales=mma)
+                          mma_scales=mma, router_score=spec.router_score)
 
 
 def build_head(seed: int, vocab: int, hidden: int, device="cuda", stream=None) -> flint.NVFP4:

@@ -40,7 +40,7 @@ def oracle_layer(orc, spec: synth.LayerSpec, experts=None):
     return orc.Layer(router, spec.bias(), mk(synth.KIND_GATE, experts),
                      mk(synth.KIND_UP, experts), mk(synth.KIND_DOWN, experts),
                      mk(synth.KIND_SH_GATE, [0]), mk(synth.KIND_SH_UP, [0]),
-                     mk(synth.KIND_SH_DOWN, [0]), s.top_k)
+                     mk(synth.KIND_SH_DOWN, [0]), s.top_k, router_score=spec.router_score)
 
 
 def router_only_layer(orc, spec: synth.LayerSpec):
@@ -51,7 +51,7 @@ def router_only_layer(orc, spec: synth.LayerSpec):
     H, E, F, Fs = s.hidden, s.n_experts, s.expert_width, s.shared_width
     return orc.Layer(bits16(spec.weights_bf16(synth.KIND_ROUTER)[0]), spec.bias(),
                      z(1, F, H), z(1, F, H), z(1, H, F), z(1, Fs, H), z(1, Fs, H), z(1, H, Fs),
-                     s.top_k)
+                     s.top_k, router_score=spec.router_score)
 
 
 def oracle_routes(orc, spec, x_bits: np.ndarray):

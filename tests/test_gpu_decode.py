@@ -121,6 +121,20 @@ def test_decode_tiny_bias_residual(orc):
     _decode_case(orc, spec, x, 2, residual=res)
 
 
+def test_decode_tiny_sigmoid_router(orc):
+    # FLINT_ROUTER_SIGMOID: the same selection, weights from the selected sigmoids
+    spec = synth.LayerSpec(synth.TINY, seed=7, zipf=1.1, router_score=1)
+    x = synth.tokens_bf16(7, synth.TINY.hidden, 12)
+    _decode_case(orc, spec, x, 3)
+
+
+def test_decode_flint_layer_sigmoid_sampled(orc):
+    spec = synth.LayerSpec(synth.FLINT, seed=2, zipf=1.1, router_score=1)
+    idx = [0, 500, 999]
+    x = torch.cat([synth.tokens_bf16(2, synth.FLINT.hidden, 1, start_tok=t) for t in idx])
+    _decode_case(orc, spec, x, 1)
+
+
 def test_decode_flint_layer_sampled(orc):
     """Full-size Flint layer (hidden 2048, 256 experts, top-6, shared 1024), tokens of the
     seeded 1000-token stream checked one at a time, as the benchmark runs them."""

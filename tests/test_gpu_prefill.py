@@ -47,9 +47,11 @@ def _check_bookkeeping(orc, gidx, counts, order, E):
     np.testing.assert_array_equal(order, operm)
 
 
-@pytest.mark.parametrize("T,zipf", [(300, None), (1, None), (257, 1.1)])
-def test_prefill_mid_all_tokens(orc, T, zipf):
-    spec = synth.LayerSpec(MID, seed=31, zipf=zipf)
+@pytest.mark.parametrize("T,zipf,score", [(300, None, 0), (1, None, 0), (257, 1.1, 0),
+                                          (200, 1.1, 1)])
+def test_prefill_mid_all_tokens(orc, T, zipf, score):
+    # score 1: the sigmoid router scoring (FLINT_ROUTER_SIGMOID)
+    spec = synth.LayerSpec(MID, seed=31, zipf=zipf, router_score=score)
     layer = workload.build_layer(spec, DEV)
     x = synth.tokens_bf16(31, MID.hidden, T, stream=7)
     out, gidx, gw, counts, order = _prefill(layer, x.to(DEV), MID.n_experts, MID.top_k)

@@ -54,10 +54,10 @@ def _nv(n, r, c, codes=FAKE):
     return flint._NVFP4C(codes, FAKE, FAKE, n, r, c)
 
 
-def _layer(H=256, E=16, k=2, F=64, Fs=128, router=FAKE, gate_cols=None, units=FAKE, sf=FAKE):
+def _layer(H=256, E=16, k=2, F=64, Fs=128, router=FAKE, gate_cols=None, units=FAKE, sf=FAKE, score=0):
     return flint._LayerC(H, E, k, F, Fs, router, None, _nv(E, F, gate_cols or H), _nv(E, F, H),
                          _nv(E, H, F), _nv(1, Fs, H), _nv(1, Fs, H), _nv(1, H, Fs),
-                         units, units, (ctypes.c_void_p * 6)(*[sf] * 6))
+                         units, units, (ctypes.c_void_p * 6)(*[sf] * 6), score)
 
 
 def test_quantize_argument_checks(L):
@@ -91,6 +91,8 @@ def test_decode_argument_checks(L):
     assert call(_layer(router=FAKE_MIS), args()) == 2
     assert call(_layer(units=None), args()) == 1                        # no decode-unit copy
     assert call(_layer(units=FAKE_MIS), args()) == 2
+    assert call(_layer(score=2), args()) == 1                           # unknown router scoring
+    assert call(_layer(score=-1), args()) == 1
 
 
 def test_decode_tokens_argument_checks(L):
