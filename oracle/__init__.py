@@ -81,6 +81,9 @@ def lib():
         L.orc_quantize_rows_unit.argtypes = [_f32p, _i64, _i64, _u8p, _u8p]
         L.orc_dequantize_nvfp4.argtypes = [_u8p, _u8p, _f32p, _i64, _i64, _i64, _f32p]
         L.orc_router.argtypes = [ctypes.POINTER(_Layer), _u16p, _f64p, _i32p, _f64p]
+        L.orc_sample.argtypes = [_f32p, ctypes.c_int64, ctypes.c_double, ctypes.c_int,
+                                 ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_int)]
+        L.orc_sample.restype = ctypes.c_int32
         L.orc_moe_forward.argtypes = [ctypes.POINTER(_Layer), _u16p, _f64p, _i64,
                                       ctypes.c_int, _f64p, _i32p, _f64p]
         L.orc_rmsnorm_bf16.argtypes = [_f64p, _i64, ctypes.c_double, _u16p]
@@ -263,6 +266,15 @@ def lm_head(W: NVFP4, x_bf16):
     lib().orc_lm_head(ctypes.byref(cw), V, H, _p(x, _u16p), B, _p(logits, _f64p),
                       _p(am, _i32p))
     return logits, am
+
+
+def sample(logits_f32, temperature: float, top_k: int, top_p: float, u: float):
+    """(vocabulary index, kept prefix size m) drawn from one row of fp32 logits."""
+    lg = np.ascontiguousarray(logits_f32, dtype=np.float32).reshape(-1)
+    m = ctypes.c_int(0)
+    idx = lib().orc_sample(_p(lg, _f32p), lg.size, float(temperature), int(top_k), float(top_p),
+                           float(u), ctypes.byref(m))
+    return int(idx), int(m.value)
 
 
 def expert_order(idx: np.ndarray, n_experts: int):

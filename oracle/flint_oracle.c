@@ -414,3 +414,56 @@ void orc_expert_order(const int32_t* idx, int64_t n_tok, int k, int n_experts,
     }
   free(fill);
 }
+
+/* ------------------------------------------------------------------------- */
+/* Sampling after the output head                                            */
+/* ------------------------------------------------------------------------- */
+static double logit_or_ninf(float v) { return v == v ? (double)v : -INFINITY; }
+
+int32_t orc_sample(const float* logits, int64_t V, double temperature, int top_k, double top_p,
+                   double u, int* m_out) {
+  if (top_k > V) top_k = (int)V;
+  if (top_k < 1) top_k = 1;
+  int64_t* cand = (int64_t*)malloc(sizeof(int64_t) * top_k);
+  char* taken = (char*)calloc(V, 1);
+  /* 1. top_k by repeated scans: the largest not yet taken, lowest index on ties */
+  for (int i = 0; i < top_k; ++i) {
+    int64_t best = -1;
+    for (int64_t v = 0; v < V; ++v) {
+      if (taken[v]) continue;
+      if (best < 0 || logit_or_ninf(logits[v]) > logit_or_ninf(logits[best])) best = v;
+    }
+    taken[best] = 1;
+    cand[i] = best;
+  }
+  const double l0 = logit_or_ninf(logits[cand[0]]);
+  int32_t pick = (int32_t)cand[0];
+  int m = 1;
+  if (l0 != -INFINITY) {
+    double* p = (double*)malloc(sizeof(double) * top_k);
+    /* 2. softmax with temperature over the candidates */
+    double z = 0.0;
+    for (int i = 0; i < top_k; ++i) { p[i] = exp((logit_or_ninf(logits[cand[i]]) - l0) / temperature); z += p[i]; }
+    for (int i = 0; i < top_k; ++i) p[i] /= z;
+    /* 3. the shortest prefix reaching top_p */
+    double cum = 0.0;
+    m = top_k;
+    for (int i = 0; i < top_k; ++i) {
+      cum += p[i];
+      if (cum >= top_p) { m = i + 1; break; }
+    }
+    double zm = 0.0;
+    for (int i = 0; i < m; ++i) zm += p[i];
+    /* 4.-5. renormalise and draw */
+    double c = 0.0;
+    pick = (int32_t)cand[m - 1];
+    for (int i = 0; i < m; ++i) {
+      c += p[i] / zm;
+      if (u < c) { pick = (int32_t)cand[i]; break; }
+    }
+    free(p);
+  }
+  if (m_out) *m_out = m;
+  free(cand); free(taken);
+  return pick;
+}

@@ -103,6 +103,21 @@ void orc_router(const orc_layer* L, const uint16_t* x, double* logits, int32_t* 
 int orc_moe_forward(const orc_layer* L, const uint16_t* x, const double* residual,
                     int64_t n_tok, int quantize_acts, double* out, int32_t* idx, double* w);
 
+/* Sampling from one row of output-head logits.  "Recursive Releases Flint, a 40B MoE
+ * Coding Model That Runs Locally at 125 Tokens per Second", section "How does Flint
+ * perform on coding benchmarks?", samples at temperature 1.0, top-p 0.95 and top-k
+ * 20 and says no more; the order taken is the usual one:
+ *   1. the top_k logits (NaN read as -inf; ties to the lower index), descending;
+ *   2. p_i = exp((l_i - l_0) / temperature) / sum of the same over the top_k;
+ *   3. keep the shortest prefix i < m whose p sum reaches top_p (m >= 1);
+ *   4. q_i = p_i / (p_0 + ... + p_{m-1});
+ *   5. the draw is the first i < m with u < q_0 + ... + q_i (i = m - 1 if rounding
+ *      leaves none), for an input u in [0, 1).
+ * If every candidate is -inf the first candidate is drawn.  Returns its vocabulary
+ * index; *m_out (may be NULL) receives m.  top_k is clipped to V. */
+int32_t orc_sample(const float* logits, int64_t V, double temperature, int top_k, double top_p,
+                   double u, int* m_out);
+
 /* x_next = bf16(h / sqrt(mean(h^2) + eps)), gain 1. */
 void orc_rmsnorm_bf16(const double* h, int64_t n, double eps, uint16_t* out);
 
