@@ -227,6 +227,7 @@ def run_flint(args):
         "clocks": clk.summary(),
         "device_status": status,
         "prefill": None,
+        "sampling": measure_sampling(dev),
     }
     if not args.no_prefill:
         del layers, head
@@ -237,6 +238,37 @@ def run_flint(args):
     if world > 1:
         dist.destroy_process_group()
     return result if rank == 0 else None
+
+
+def measure_sampling(dev, reps: int = 20):
+    """flint_sample_logits on fp32 logits over the Flint vocabulary (150,144) with the
+    pages' settings (temperature 1.0, top-p 0.95, top-k 20), 1 and 8 rows; the logits
+    are rewritten before each timed call, and the bytes counted are one read of them."""
+    import torch
+
+    from sparse_moe_decode_02_b300 import flint
+
+    V = 150144
+    res = {"workload": "sampling over V=150144 fp32 logits, T=1.0, top-p 0.95, top-k 20"}
+    for B in (1, 8):
+        g = torch.Generator(device=dev).manual_seed(SEED + B)
+        lg = torch.randn(B, V, device=dev, generator=g) * 3
+        u = torch.rand(B, device=dev, generator=g)
+        for _ in range(3):
+            flint.sample_logits(lg, u)
+        ts = []
+        for _ in range(reps):
+            lg.mul_(1.0)                       # logits rewritten: a new head output
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            flint.sample_logits(lg, u)
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = sum(ts) / len(ts)
+        res["B%d_us" % B] = round(ms * 1e3, 2)
+        res["B%d_read_GBs" % B] = round(B * V * 4 / (ms * 1e-3) / 1e9, 1)
+    return res
 
 
 def measure_prefill(dev, reps: int = 10):

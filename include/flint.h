@@ -282,6 +282,31 @@ flint_status flint_lm_head(const flint_nvfp4* W, const void* x_bf16, float* logi
                            int32_t* argmax, int B, void* ws, size_t ws_bytes,
                            flint_stream stream);
 
+/* ----------------------------------------------------------------------------
+ * flint_sample_logits -- draw one token per row of output-head logits.  "Recursive
+ * Releases Flint, a 40B MoE Coding Model That Runs Locally at 125 Tokens per Second",
+ * section "How does Flint perform on coding benchmarks?", samples at temperature
+ * 1.0, top-p 0.95 and top-k 20; the pages give no more, and the order taken is the
+ * usual one.  Per row b:
+ *   1. the top_k logits (NaN read as -inf; ties to the lower index), descending;
+ *   2. p_i = exp((l_i - l_0) / temperature) / sum of the same over them;
+ *   3. the shortest prefix i < m whose p sum reaches top_p (m >= 1);
+ *   4. out[b] = the vocabulary index of the first i < m with
+ *      uniforms[b] < (p_0 + ... + p_i) / (p_0 + ... + p_{m-1})
+ *      (i = m - 1 if rounding leaves none); all candidates -inf: the first one.
+ * The random numbers are the caller's: uniforms fp32 [B] in [0, 1).  Computed in
+ * fp32, so a draw may differ from an exact one only where uniforms[b] or top_p lies
+ * within float rounding of a cumulative sum.
+ * logits fp32 [B, V], out int32 [B] (device, 4-byte aligned).  top_k is clipped to V.
+ * Errors: FLINT_ERR_INVALID_ARG for null pointers, B or V <= 0, top_k < 1,
+ * temperature not > 0 and finite, top_p outside (0, 1]; FLINT_ERR_UNSUPPORTED for
+ * top_k > FLINT_MAX_SAMPLE_TOP_K.  No workspace.
+ * -------------------------------------------------------------------------- */
+#define FLINT_MAX_SAMPLE_TOP_K 32
+flint_status flint_sample_logits(const float* logits, int B, int V, float temperature, int top_k,
+                                 float top_p, const float* uniforms, int32_t* out,
+                                 flint_stream stream);
+
 enum {
   FLINT_OP_QUANTIZE = 0,
   FLINT_OP_MOE_DECODE = 1,

@@ -1,5 +1,6 @@
 // api.cu -- the extern "C" entry points declared in include/flint.h: argument checks on
 // the host (nothing is enqueued when a check fails), workspace carving, launches.
+#include <cmath>
 #include <cstring>
 
 #include "../../include/flint.h"
@@ -284,6 +285,19 @@ flint_status flint_lm_head(const flint_nvfp4* W, const void* x_bf16, float* logi
   return from_cuda(flint::launch_lm_head(W->codes, W->scales, W->tensor_scale, W->rows, W->cols,
                                          static_cast<const uint16_t*>(x_bf16), B, logits, argmax,
                                          ws, st));
+}
+
+flint_status flint_sample_logits(const float* logits, int B, int V, float temperature, int top_k,
+                                 float top_p, const float* uniforms, int32_t* out,
+                                 flint_stream stream) {
+  if (!logits || !uniforms || !out) return FLINT_ERR_INVALID_ARG;
+  if (B <= 0 || V <= 0 || top_k < 1) return FLINT_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || !std::isfinite(temperature)) return FLINT_ERR_INVALID_ARG;
+  if (!(top_p > 0.f) || top_p > 1.f) return FLINT_ERR_INVALID_ARG;
+  if (top_k > FLINT_MAX_SAMPLE_TOP_K) return FLINT_ERR_UNSUPPORTED;
+  if (!aligned4(logits) || !aligned4(uniforms) || !aligned4(out)) return FLINT_ERR_ALIGNMENT;
+  return from_cuda(flint::launch_sample(logits, B, V, temperature, top_k, top_p, uniforms, out,
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 flint_status flint_moe_prefill(const flint_moe_layer* L, const void* x_bf16, float* out,

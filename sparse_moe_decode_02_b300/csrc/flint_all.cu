@@ -4,5 +4,6 @@
 #include "decode.cu"
 #include "lm_head.cu"
 #include "prefill.cu"
+#include "sample.cu"
 #include "api.cu"
 #include "noalloc.cu"

@@ -94,6 +94,9 @@ cudaError_t launch_lm_head(const uint8_t* codes, const uint8_t* scales, const fl
                            int H, const uint16_t* x, int B, float* logits, int32_t* argmax,
                            void* ws, cudaStream_t st);
 
+cudaError_t launch_sample(const float* logits, int B, int V, float temperature, int top_k, float top_p,
+                          const float* uniforms, int32_t* out, cudaStream_t st);
+
 cudaError_t launch_quantize(const uint16_t* w, int n_mat, int rows, int cols, uint8_t* codes,
                             uint8_t* scales, float* tsc, void* ws, cudaStream_t st);
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, const float* tsc,

@@ -52,7 +52,7 @@ ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
 _lib = None
 
 _SYMBOLS = ["flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_decode_units",
-            "flint_nvfp4_mma_scales",
+            "flint_nvfp4_mma_scales", "flint_sample_logits",
             "flint_moe_decode", "flint_decode_tokens", "flint_moe_prefill", "flint_lm_head",
             "flint_workspace_bytes", "flint_last_device_status", "flint_status_string",
             "flint_version"]
@@ -82,6 +82,7 @@ def lib() -> ctypes.CDLL:
     L.flint_moe_prefill.argtypes = [ctypes.POINTER(_LayerC), vp, vp, vp, vp, vp, vp, i, vp, sz,
                                     vp]
     L.flint_lm_head.argtypes = [ctypes.POINTER(_NVFP4C), vp, vp, vp, i, vp, sz, vp]
+    L.flint_sample_logits.argtypes = [vp, i, i, ctypes.c_float, i, ctypes.c_float, vp, vp, vp]
     L.flint_workspace_bytes.argtypes = [i] * 8
     L.flint_workspace_bytes.restype = sz
     L.flint_last_device_status.argtypes = [vp]
@@ -90,7 +91,8 @@ def lib() -> ctypes.CDLL:
     L.flint_version.restype = ctypes.c_char_p
     for name in ("flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_decode_units",
                  "flint_nvfp4_mma_scales", "flint_moe_decode", "flint_decode_tokens", "flint_decode_tokens_noalloc",
-                 "flint_moe_prefill", "flint_lm_head", "flint_last_device_status"):
+                 "flint_moe_prefill", "flint_lm_head", "flint_last_device_status",
+                 "flint_sample_logits"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -334,3 +336,17 @@ def status_string(status: int) -> str:
 
 def version() -> str:
     return lib().flint_version().decode()
+
+
+def sample_logits(logits: torch.Tensor, uniforms: torch.Tensor, temperature: float = 1.0,
+                  top_k: int = 20, top_p: float = 0.95, stream=None) -> torch.Tensor:
+    """One token per row of fp32 logits [B, V] (top-k, temperature, top-p; see flint.h),
+    drawn with the caller's uniforms fp32 [B] in [0, 1).  Returns int32 [B]."""
+    assert logits.dtype == torch.float32 and logits.is_cuda and logits.is_contiguous()
+    B, V = logits.shape
+    u = uniforms.to(device=logits.device, dtype=torch.float32).contiguous()
+    out = torch.empty(B, dtype=torch.int32, device=logits.device)
+    _check(lib().flint_sample_logits(_ptr(logits), B, V, float(temperature), int(top_k),
+                                     float(top_p), _ptr(u), _ptr(out), _stream(stream)),
+           "flint_sample_logits")
+    return out

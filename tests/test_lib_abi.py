@@ -167,3 +167,21 @@ def test_lm_head_argument_checks(L):
     assert h(ctypes.byref(W2), FAKE, FAKE, None, 1, FAKE, ws, None) == 3
     assert h(ctypes.byref(W), FAKE_MIS, FAKE, None, 1, FAKE, ws, None) == 2
     assert h(ctypes.byref(W), FAKE, FAKE, None, 1, FAKE, 16, None) == 4
+
+
+def test_sample_argument_checks(L):
+    s = L.flint_sample_logits
+    ok = dict(lg=FAKE, B=2, V=100, T=1.0, k=20, p=0.95, u=FAKE, out=FAKE)
+    call = lambda **kw: s(*(dict(ok, **kw)[n] for n in ("lg", "B", "V", "T", "k", "p", "u", "out")), None)
+    assert call(lg=None) == 1
+    assert call(u=None) == 1
+    assert call(out=None) == 1
+    assert call(B=0) == 1
+    assert call(V=0) == 1
+    assert call(k=0) == 1
+    assert call(k=33) == 8                                               # > FLINT_MAX_SAMPLE_TOP_K
+    assert call(T=0.0) == 1
+    assert call(T=float("inf")) == 1
+    assert call(p=0.0) == 1
+    assert call(p=1.5) == 1
+    assert call(lg=FAKE + 2) == 2
