@@ -3,14 +3,16 @@
 // perform on coding benchmarks?": temperature 1.0, top-p 0.95, top-k 20).
 //
 // One CTA per row of logits:
-//   1. the top_k-th largest order key, exactly, by a 4-pass radix select (8 bits per
-//      pass, shared-memory histograms); NaN reads as -inf;
-//   2. the candidates: every logit above that key, then the lowest-index logits equal
-//      to it (index order from a block-wide scan of per-thread counts over contiguous
-//      chunks), top_k in all;
-//   3. one warp sorts them (bitonic, by logit descending, lower index first) and
-//      computes p_i = exp((l_i - l_0) / T) over them, the shortest prefix whose p sum
-//      reaches top_p, and the draw from the renormalised prefix for the caller's u.
+//   1. every thread takes the largest order key of its strided share (NaN reads as
+//      -inf); the top_k-th largest of these maxima is at or below the top_k-th largest
+//      logit (at least top_k threads hold a logit at or above it);
+//   2. the logits at or above it (typically a few more than top_k) are ranked exactly
+//      by (logit descending, lower index first).  When ties leave more than kMaxCand of
+//      them, a radix select (four 8-bit histogram passes) finds the top_k-th largest
+//      key instead, and the lowest-index logits equal to it complete the set;
+//   3. one warp computes p_i = exp((l_i - l_0) / T) over the top_k, the shortest
+//      prefix whose p sum reaches top_p, and the draw from the renormalised prefix for
+//      the caller's u.
 #include "common.cuh"
 
 namespace flint {
@@ -27,26 +29,18 @@ __device__ __forceinline__ bool before(unsigned ka, int ia, unsigned kb, int ib)
   return ka > kb || (ka == kb && ia < ib);
 }
 
-__global__ void __launch_bounds__(kThreads) k_sample(const float* __restrict__ logits, int V, float temp,
-                                                    int K, float top_p, const float* __restrict__ uniforms,
-                                                    int32_t* __restrict__ out) {
-  __shared__ unsigned s_hist[256];
-  __shared__ unsigned s_sel, s_need;
-  __shared__ unsigned s_wsum[kThreads / 32];
-  __shared__ int s_nc;
-  __shared__ unsigned s_ck[32];
-  __shared__ int s_ci[32];
+// Candidates by radix select (any input): the K-th largest key exactly by four 8-bit
+// histogram passes, then every key above it and the lowest-index keys equal to it.
+// Leaves the K candidates, unordered, in s_ck / s_ci.
+__device__ void radix_candidates(const float* row, int V, int K, unsigned* s_hist, unsigned* s_wsum,
+                                 int* s_nc, unsigned* s_ck, int* s_ci, unsigned* s_sel, unsigned* s_need) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float* row = logits + (size_t)blockIdx.x * V;
-
-  // ---- 1. the K-th largest key: prefix/mask grow by 8 bits a pass; need = its rank
-  // among the keys that match the prefix so far
   unsigned prefix = 0u, mask = 0u, need = (unsigned)K;
 #pragma unroll 1
   for (int shift = 24; shift >= 0; shift -= 8) {
     if (tid < 256) s_hist[tid] = 0u;
     __syncthreads();
-#pragma unroll 1
+#pragma unroll 4
     for (int v = tid; v < V; v += kThreads) {
       const unsigned key = skey(row[v]);
       if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1u);
@@ -67,21 +61,19 @@ __global__ void __launch_bounds__(kThreads) k_sample(const float* __restrict__ l
       if (acc < need && suf >= need) {
 #pragma unroll 1
         for (int j = 7; j >= 0; --j) {
-          if (acc + c[j] >= need) { s_sel = 8u * lane + j; s_need = need - acc; break; }
+          if (acc + c[j] >= need) { *s_sel = 8u * lane + j; *s_need = need - acc; break; }
           acc += c[j];
         }
       }
     }
     __syncthreads();
-    prefix |= s_sel << shift;
+    prefix |= *s_sel << shift;
     mask |= 255u << shift;
-    need = s_need;
+    need = *s_need;
     __syncthreads();
   }
-  const unsigned thr = prefix;          // K - need logits lie above it
-
-  // ---- 2. candidates: those above thr, then the `need` lowest-index ones equal to it
-  if (tid == 0) s_nc = 0;
+  const unsigned thr = prefix;          // K - need keys lie above it
+  if (tid == 0) *s_nc = 0;
   __syncthreads();
   const int chunk = (V + kThreads - 1) / kThreads;
   const int v0 = min(V, tid * chunk), v1 = min(V, v0 + chunk);
@@ -90,7 +82,7 @@ __global__ void __launch_bounds__(kThreads) k_sample(const float* __restrict__ l
   for (int v = v0; v < v1; ++v) {
     const unsigned key = skey(row[v]);
     if (key > thr) {
-      const int slot = atomicAdd(&s_nc, 1);
+      const int slot = atomicAdd(s_nc, 1);
       s_ck[slot] = key;
       s_ci[slot] = v;
     } else if (key == thr) {
@@ -120,15 +112,74 @@ __global__ void __launch_bounds__(kThreads) k_sample(const float* __restrict__ l
 #pragma unroll 1
   for (int v = v0; v < v1 && rank < need; ++v) {
     if (skey(row[v]) == thr) {
-      const int slot = atomicAdd(&s_nc, 1);
+      const int slot = atomicAdd(s_nc, 1);
       s_ck[slot] = thr;
       s_ci[slot] = v;
       ++rank;
     }
   }
   __syncthreads();
+}
 
-  // ---- 3. sort, probabilities, top-p prefix, draw (warp 0)
+constexpr int kMaxCand = 2048;   // candidates the fast path ranks directly
+
+__global__ void __launch_bounds__(kThreads) k_sample(const float* __restrict__ logits, int V, float temp,
+                                                    int K, float top_p, const float* __restrict__ uniforms,
+                                                    int32_t* __restrict__ out) {
+  __shared__ unsigned s_hist[256];
+  __shared__ unsigned s_sel, s_need;
+  __shared__ unsigned s_wsum[kThreads / 32];
+  __shared__ int s_nc;
+  __shared__ unsigned s_ck[32];
+  __shared__ int s_ci[32];
+  __shared__ unsigned s_tmax[kThreads];
+  __shared__ unsigned s_fk[kMaxCand];
+  __shared__ int s_fi[kMaxCand];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* row = logits + (size_t)blockIdx.x * V;
+
+  // ---- 1. fast path: the K-th largest of the threads' maxima bounds the K-th largest
+  // logit from below (at least K threads hold a logit at or above it)
+  unsigned tmax = 0u;                    // 0: no logit (every key is >= 1)
+#pragma unroll 8
+  for (int v = tid; v < V; v += kThreads) tmax = max(tmax, skey(row[v]));
+  s_tmax[tid] = tmax;
+  __syncthreads();
+  int rk = 0;                            // rank of this thread's maximum among the maxima
+#pragma unroll 4
+  for (int j = 0; j < kThreads; ++j) rk += before(s_tmax[j], j, tmax, tid) ? 1 : 0;
+  if (rk == K - 1) s_sel = tmax;         // exactly one thread has rank K - 1 (K <= kThreads)
+  if (tid == 0) s_nc = 0;
+  __syncthreads();
+  const unsigned thr = s_sel;
+#pragma unroll 8
+  for (int v = tid; v < V; v += kThreads) {
+    const unsigned key = skey(row[v]);
+    if (key >= thr) {
+      const int slot = atomicAdd(&s_nc, 1);
+      if (slot < kMaxCand) { s_fk[slot] = key; s_fi[slot] = v; }
+    }
+  }
+  __syncthreads();
+  const int n = s_nc;
+  if (n <= kMaxCand) {
+    // exact ranks among the candidates; the K best go to s_ck / s_ci in rank order
+#pragma unroll 1
+    for (int j = tid; j < n; j += kThreads) {
+      const unsigned kj = s_fk[j];
+      const int ij = s_fi[j];
+      int r = 0;
+#pragma unroll 4
+      for (int i = 0; i < n; ++i) r += before(s_fk[i], s_fi[i], kj, ij) ? 1 : 0;
+      if (r < K) { s_ck[r] = kj; s_ci[r] = ij; }
+    }
+    __syncthreads();
+  } else {
+    __syncthreads();
+    radix_candidates(row, V, K, s_hist, s_wsum, &s_nc, s_ck, s_ci, &s_sel, &s_need);
+  }
+
+  // ---- 2. sort (a no-op after the fast path), probabilities, top-p prefix, draw (warp 0)
   if (warp != 0) return;
   unsigned key = lane < K ? s_ck[lane] : 0u;
   int idx = lane < K ? s_ci[lane] : 0x7FFFFFFF;
