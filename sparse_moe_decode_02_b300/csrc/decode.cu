@@ -278,16 +278,6 @@ __device__ __forceinline__ void lds_row(RowRegs<CPL>& r, const uint8_t* codes_ro
   }
 }
 
-template <int CPL>
-__device__ __forceinline__ void lds_row_bf16(RowBF16<CPL>& r, const uint16_t* row, int sl, int LPR) {
-#pragma unroll
-  for (int i = 0; i < CPL; ++i) {
-    const uint4* src = reinterpret_cast<const uint4*>(row + 32 * (sl + LPR * i));
-#pragma unroll
-    for (int j = 0; j < 4; ++j) r.q[i * 4 + j] = src[j];
-  }
-}
-
 // ---------------------------------------------------------------- units
 // A unit is kUnit = 8 consecutive SwiGLU outputs of one expert (routed or shared): 8
 // gate rows, 8 up rows, and the matching 8-column chunk of the down matrix (H rows x
@@ -552,16 +542,6 @@ __device__ __forceinline__ void topk_per(const float* logits, int E, int K, int*
   topk_exact<PER>(logits, E, K, s_sel, s_w);
 }
 
-__device__ __forceinline__ void topk_exact_dispatch(const float* logits, int E, int K, int* s_sel,
-                                                    float* s_w) {
-  const int per_lane = (E + 31) / 32;
-  if (per_lane <= 1) topk_exact<1>(logits, E, K, s_sel, s_w);
-  else if (per_lane <= 2) topk_exact<2>(logits, E, K, s_sel, s_w);
-  else if (per_lane <= 4) topk_exact<4>(logits, E, K, s_sel, s_w);
-  else if (per_lane <= 8) topk_exact<8>(logits, E, K, s_sel, s_w);
-  else topk_exact<16>(logits, E, K, s_sel, s_w);
-}
-
 __device__ __forceinline__ void topk_dispatch(const float* logits, int E, int K, int* s_sel,
                                               float* s_w) {
   const int per_lane = (E + 31) / 32;
@@ -570,30 +550,6 @@ __device__ __forceinline__ void topk_dispatch(const float* logits, int E, int K,
   else if (per_lane <= 4) topk_per<4>(logits, E, K, s_sel, s_w);
   else if (per_lane <= 8) topk_per<8>(logits, E, K, s_sel, s_w);
   else topk_per<16>(logits, E, K, s_sel, s_w);
-}
-
-// Packed 32-bit selection key: the order key's upper bits, then (2^ib - 1 - e) in the
-// low ib bits, so larger keys win and equal upper bits go to the lower index.
-__device__ __forceinline__ unsigned packed_key(float l, int e, int ib) {
-  l = (l == l) ? l : -INFINITY;
-  return ((order_key(l) >> ib) << ib) | ((1u << ib) - 1u - (unsigned)e);
-}
-
-// The n best of one key per lane (0 = none; keys are distinct): lane s < n gets the
-// s-th best.  tie: two consecutive winners agree above the index bits (so their
-// order, and possibly the selection, needs the exact path).
-__device__ __forceinline__ unsigned warp_select(unsigned key, int n, int ib, bool& tie) {
-  const int lane = threadIdx.x & 31;
-  unsigned mine = 0u, prev = 0u;
-  tie = false;
-  for (int s = 0; s < n; ++s) {
-    const unsigned w = __reduce_max_sync(0xffffffffu, key);
-    if (s > 0 && w != 0u && (w >> ib) == (prev >> ib)) tie = true;
-    prev = w;
-    if (key == w) key = 0u;
-    if (lane == s) mine = w;
-  }
-  return mine;
 }
 
 // ---------------------------------------------------------------- head

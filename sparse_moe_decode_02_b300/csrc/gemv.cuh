@@ -60,39 +60,6 @@ __device__ __forceinline__ void stage_bf16(XStage<CPL, 1>& xs, XRawBF16<CPL>* ra
   }
 }
 
-// Stage an fp32 vector as hi + lo f16 terms (about 22 significant bits).
-template <int CPL>
-__device__ __forceinline__ void stage_f32(XStage<CPL, 2>& xs, const float* __restrict__ x, int sl,
-                                          int LPR) {
-  float v[CPL * 32];
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < CPL; ++i) {
-    const float4* src = reinterpret_cast<const float4*>(x + 32 * (sl + LPR * i));
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float4 f = src[j];
-      v[i * 32 + j * 4 + 0] = f.x; v[i * 32 + j * 4 + 1] = f.y;
-      v[i * 32 + j * 4 + 2] = f.z; v[i * 32 + j * 4 + 3] = f.w;
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < CPL * 32; ++q) amax = fmaxf(amax, fabsf(v[q]));
-  amax = max_lanes_rt(amax, LPR);
-  const int k = f16_stage_exponent(amax);
-  const float s = exp2i(k);
-  xs.unscale = exp2i(-k);
-#pragma unroll
-  for (int q = 0; q < CPL * 16; ++q) {
-    const float a = v[2 * q] * s, b = v[2 * q + 1] * s;
-    const uint32_t hi = pack_f16x2_rn(a, b);
-    float ha, hb;
-    f16x2_to_f32x2(hi, ha, hb);
-    xs.p[0][q] = hi;
-    xs.p[1][q] = pack_f16x2_rn(a - ha, b - hb);
-  }
-}
-
 template <int CPL>
 struct RowRegs {
   uint4 q[CPL];
@@ -146,36 +113,6 @@ __device__ __forceinline__ float dot_row(const RowRegs<CPL>& r, const XStage<CPL
     acc = fmaf(b1, s1, acc);
   }
   return acc;
-}
-
-// bf16 row (router): lane's share of dot(row, x), both bf16, fp32 accumulation.
-template <int CPL>
-struct RowBF16 {
-  uint4 q[CPL * 4];
-};
-
-template <int CPL>
-__device__ __forceinline__ void load_row_bf16(RowBF16<CPL>& r, const uint16_t* __restrict__ row,
-                                              int sl, int LPR) {
-#pragma unroll
-  for (int i = 0; i < CPL; ++i) {
-    const uint4* src = reinterpret_cast<const uint4*>(row + 32 * (sl + LPR * i));
-#pragma unroll
-    for (int j = 0; j < 4; ++j) r.q[i * 4 + j] = ldg_stream(src + j);
-  }
-}
-
-template <int CPL>
-__device__ __forceinline__ float dot_row_bf16(const RowBF16<CPL>& r, const XRawBF16<CPL>& x) {
-  float a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int j = 0; j < CPL * 4; ++j) {
-    fma2_bf16(a[0], a[1], r.q[j].x, x.p[j * 4 + 0]);
-    fma2_bf16(a[2], a[3], r.q[j].y, x.p[j * 4 + 1]);
-    fma2_bf16(a[0], a[1], r.q[j].z, x.p[j * 4 + 2]);
-    fma2_bf16(a[2], a[3], r.q[j].w, x.p[j * 4 + 3]);
-  }
-  return (a[0] + a[1]) + (a[2] + a[3]);
 }
 
 }  // namespace flint
