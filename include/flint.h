@@ -177,10 +177,11 @@ flint_status flint_dequantize_nvfp4(const flint_nvfp4* m, float* out, flint_stre
  * flint_moe_decode -- one MoE layer for B <= FLINT_MAX_DECODE_TOKENS tokens
  * (flint_decode_tokens with one layer and no head; the tokens run one after
  * another).
- * Router: logits = Wr x + b (bf16 x bf16, fp32 accumulate); softmax over the E
- * experts; the top_k experts by logit (ties to the lower index) in descending
- * order; weights = p_i / sum of the selected p ("Recursive Releases Flint ...",
- * "How does Flint's architecture work?").  Experts are SwiGLU:
+ * Router: logits = Wr x + b (bf16 x bf16, fp32 accumulate); the top_k experts by
+ * logit (ties to the lower index) in descending order; weights = the selected
+ * scores renormalised, with softmax or sigmoid scores as layer->router_score says
+ * ("Recursive Releases Flint ...", "How does Flint's architecture work?").  Experts
+ * are SwiGLU:
  *   h_e = silu(Wg_e x) * (Wu_e x),  y_e = Wd_e h_e
  * and the shared expert is always added with weight 1:
  *   out = residual + sum_i w_i y_{e_i} + y_shared
@@ -212,8 +213,9 @@ flint_status flint_moe_decode(const flint_moe_layer* layer, const void* x_bf16,
  * [T, H] or NULL.  Outputs, each optional: out fp32 [T, H] = h_{n_layers};
  * x_out_bf16 [T, H] = x_{n_layers}; logits fp32 [T, V]; argmax int32 [T];
  * topk_idx int32 / topk_w fp32 [T, n_layers, k].
- * The kernel is cooperative: one CTA per SM, grid-wide barriers whose waits are
- * bounded (FLINT_ERR_TIMEOUT in the device status word if one expires).  Down
+ * The kernel is cooperative: one CTA per SM.  CTAs exchange the router logits and
+ * the residual sum through global memory each layer; every wait is bounded
+ * (FLINT_ERR_TIMEOUT in the device status word if one expires).  Down
  * projections are summed with fp32 atomics, so outputs may differ in the last
  * bits from run to run.  ws: flint_workspace_bytes(FLINT_OP_MOE_DECODE, ...).
  * -------------------------------------------------------------------------- */
