@@ -3,9 +3,9 @@
 // perform on coding benchmarks?": temperature 1.0, top-p 0.95, top-k 20).
 //
 // One CTA per row of logits:
-//   1. every thread takes the largest order key of its strided share (NaN reads as
-//      -inf); the top_k-th largest of these maxima is at or below the top_k-th largest
-//      logit (at least top_k threads hold a logit at or above it);
+//   1. every warp takes the largest order key of its strided share (NaN reads as
+//      -inf); the top_k-th largest of these 32 maxima is at or below the top_k-th
+//      largest logit (at least top_k warps hold a logit at or above it);
 //   2. the logits at or above it (typically a few more than top_k) are ranked exactly
 //      by (logit descending, lower index first).  When ties leave more than kMaxCand of
 //      them, a radix select (four 8-bit histogram passes) finds the top_k-th largest
@@ -132,32 +132,64 @@ __global__ void __launch_bounds__(kThreads) k_sample(const float* __restrict__ l
   __shared__ int s_nc;
   __shared__ unsigned s_ck[32];
   __shared__ int s_ci[32];
-  __shared__ unsigned s_tmax[kThreads];
+  __shared__ unsigned s_wm[kThreads / 32];
   __shared__ unsigned s_fk[kMaxCand];
   __shared__ int s_fi[kMaxCand];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* row = logits + (size_t)blockIdx.x * V;
 
-  // ---- 1. fast path: the K-th largest of the threads' maxima bounds the K-th largest
-  // logit from below (at least K threads hold a logit at or above it)
+  // ---- 1. fast path: the K-th largest of the warps' maxima bounds the K-th largest
+  // logit from below (at least K warps hold a logit at or above it).  Rows whose
+  // start and length are multiples of 4 floats are read as float4.
+  const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  const float4* row4 = reinterpret_cast<const float4*>(row);
   unsigned tmax = 0u;                    // 0: no logit (every key is >= 1)
-#pragma unroll 8
-  for (int v = tid; v < V; v += kThreads) tmax = max(tmax, skey(row[v]));
-  s_tmax[tid] = tmax;
-  __syncthreads();
-  int rk = 0;                            // rank of this thread's maximum among the maxima
+  if (vec) {
 #pragma unroll 4
-  for (int j = 0; j < kThreads; ++j) rk += before(s_tmax[j], j, tmax, tid) ? 1 : 0;
-  if (rk == K - 1) s_sel = tmax;         // exactly one thread has rank K - 1 (K <= kThreads)
+    for (int q = tid; q < V / 4; q += kThreads) {
+      const float4 f = row4[q];
+      tmax = max(tmax, max(max(skey(f.x), skey(f.y)), max(skey(f.z), skey(f.w))));
+    }
+  } else {
+#pragma unroll 8
+    for (int v = tid; v < V; v += kThreads) tmax = max(tmax, skey(row[v]));
+  }
+  const unsigned wmax = __reduce_max_sync(0xffffffffu, tmax);
+  if (lane == 0) s_wm[warp] = wmax;
   if (tid == 0) s_nc = 0;
   __syncthreads();
+  if (warp == 0) {
+    // rank of warp `lane`'s maximum among the 32 (ties to the lower warp); K <= 32
+    const unsigned m = s_wm[lane];
+    int rk = 0;
+#pragma unroll
+    for (int j = 0; j < kThreads / 32; ++j) rk += before(s_wm[j], j, m, lane) ? 1 : 0;
+    if (rk == K - 1) s_sel = m;
+  }
+  __syncthreads();
   const unsigned thr = s_sel;
+  if (vec) {
+#pragma unroll 4
+    for (int q = tid; q < V / 4; q += kThreads) {
+      const float4 f = row4[q];
+      const float e[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const unsigned key = skey(e[j]);
+        if (key >= thr) {
+          const int slot = atomicAdd(&s_nc, 1);
+          if (slot < kMaxCand) { s_fk[slot] = key; s_fi[slot] = 4 * q + j; }
+        }
+      }
+    }
+  } else {
 #pragma unroll 8
-  for (int v = tid; v < V; v += kThreads) {
-    const unsigned key = skey(row[v]);
-    if (key >= thr) {
-      const int slot = atomicAdd(&s_nc, 1);
-      if (slot < kMaxCand) { s_fk[slot] = key; s_fi[slot] = v; }
+    for (int v = tid; v < V; v += kThreads) {
+      const unsigned key = skey(row[v]);
+      if (key >= thr) {
+        const int slot = atomicAdd(&s_nc, 1);
+        if (slot < kMaxCand) { s_fk[slot] = key; s_fi[slot] = v; }
+      }
     }
   }
   __syncthreads();
