@@ -105,6 +105,25 @@ def _dist():
     return ws, rank, local
 
 
+def slowest_rank_ms(ms: float, world: int, device) -> float:
+    """The timed region's length on the slowest rank (ms): with world > 1 a MAX
+    all-reduce over the ranks (any backend), then a barrier."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def whole_job_rate(world: int, steps: int, tokens_per_step: int, ms: float) -> float:
+    """Tokens per second of the whole job: every rank decodes its own stream of
+    tokens_per_step tokens per step, timed by the slowest rank's `ms`."""
+    return world * steps * tokens_per_step / (ms / 1e3)
+
+
 # ------------------------------------------------------------------------------ flint arm
 def run_flint(args):
     import torch
@@ -153,12 +172,8 @@ def run_flint(args):
         torch.cuda.synchronize()
     per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     ms = ev[0].elapsed_time(ev[-1])
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-        dist.barrier()
-    tok_per_s = world * args.steps * T / (ms / 1e3)
+    ms = slowest_rank_ms(ms, world, dev)
+    tok_per_s = whole_job_rate(world, args.steps, T, ms)
     status = flint.last_device_status()
 
     layer_bytes = workload.layer_bytes_per_token(shape)
