@@ -295,7 +295,8 @@ flint_status flint_lm_head(const flint_nvfp4* W, const void* x_bf16, float* logi
  *   3. the shortest prefix i < m whose p sum reaches top_p (m >= 1);
  *   4. out[b] = the vocabulary index of the first i < m with
  *      uniforms[b] < (p_0 + ... + p_i) / (p_0 + ... + p_{m-1})
- *      (i = m - 1 if rounding leaves none); all candidates -inf: the first one.
+ *      (i = m - 1 if rounding leaves none); all candidates -inf, or a +inf logit
+ *      (all the probability; several: the lowest index): the first candidate.
  * The random numbers are the caller's: uniforms fp32 [B] in [0, 1).  Computed in
  * fp32, so a draw may differ from an exact one only where uniforms[b] or top_p lies
  * within float rounding of a cumulative sum.

@@ -439,7 +439,9 @@ int32_t orc_sample(const float* logits, int64_t V, double temperature, int top_k
   const double l0 = logit_or_ninf(logits[cand[0]]);
   int32_t pick = (int32_t)cand[0];
   int m = 1;
-  if (l0 != -INFINITY) {
+  /* A +inf logit takes all the probability (the softmax's limit); with several, the
+     lowest index (rank 0) is drawn, matching the top-k's tie order. */
+  if (l0 != -INFINITY && l0 != INFINITY) {
     double* p = (double*)malloc(sizeof(double) * top_k);
     /* 2. softmax with temperature over the candidates */
     double z = 0.0;

@@ -113,7 +113,8 @@ int orc_moe_forward(const orc_layer* L, const uint16_t* x, const double* residua
  *   4. q_i = p_i / (p_0 + ... + p_{m-1});
  *   5. the draw is the first i < m with u < q_0 + ... + q_i (i = m - 1 if rounding
  *      leaves none), for an input u in [0, 1).
- * If every candidate is -inf the first candidate is drawn.  Returns its vocabulary
+ * If every candidate is -inf, or the first is +inf (which then holds all the
+ * probability; ties among +inf go to the lower index), the first candidate is drawn.  Returns its vocabulary
  * index; *m_out (may be NULL) receives m.  top_k is clipped to V. */
 int32_t orc_sample(const float* logits, int64_t V, double temperature, int top_k, double top_p,
                    double u, int* m_out);

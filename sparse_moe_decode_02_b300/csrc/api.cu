@@ -190,7 +190,10 @@ static flint_status decode_tokens_impl(const flint_moe_layer* layers, int n_laye
       flint::decode_plan(L0.hidden, L0.n_experts, L0.top_k, L0.expert_width, L0.shared_width,
                          flint::decode_grid());
   if (!plan.ok) return FLINT_ERR_UNSUPPORTED;
-  static flint::PersistArgs a;   // large (layer table): keep it off the stack
+  // Large (layer table), so not on the stack; one per host thread, so concurrent calls
+  // from several threads never share it.  The launch copies it into the kernel's
+  // parameters, so it is free again as soon as launch_persistent returns.
+  thread_local flint::PersistArgs a;
   std::memset(&a, 0, sizeof(a));
   a.max_router_rows = plan.router_rows;
   a.max_shared_units = plan.shared_units;

@@ -38,6 +38,8 @@
 // CTA posts its best (logit, index) and CTA 0 reduces them.  Every wait is bounded by
 // %globaltimer: on expiry the kernel records FLINT_ERR_TIMEOUT, raises an abort flag
 // that releases all other waits, and runs to the end without hanging.
+#include <atomic>
+
 #include "common.cuh"
 #include "gemv.cuh"
 #include "launch.h"
@@ -1052,15 +1054,20 @@ void decode_carve(PersistArgs& a, void* ws) {
   a.best_i = reinterpret_cast<int*>(p);
 }
 
-static int g_sms = 0;
+// SM count of each device, looked up on the first launch from that device (the value
+// is the same for every thread that stores it, so a relaxed atomic is enough).
+constexpr int kMaxDevices = 64;
+static std::atomic<int> g_sms[kMaxDevices];
 int decode_grid() {
-  if (g_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_sms > kMaxCtas) g_sms = kMaxCtas;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int n = g_sms[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (n > kMaxCtas) n = kMaxCtas;
+    g_sms[dev].store(n, std::memory_order_relaxed);
   }
-  return g_sms;
+  return n;
 }
 
 DecodePlan decode_plan(int H, int E, int K, int F, int Fs, int G) {

@@ -230,8 +230,10 @@ __global__ void __launch_bounds__(kThreads) k_sample(const float* __restrict__ l
   }
   const float l = lane < K ? nan_to_ninf(row[idx]) : -INFINITY;
   const float l0 = __shfl_sync(0xffffffffu, l, 0);
+  // A +inf logit holds all the probability (the limit of the softmax); among several the
+  // lowest index, i.e. rank 0, is taken, as the top-k orders ties.  All -inf: rank 0 too.
   int pick_lane = 0;
-  if (l0 != -INFINITY) {
+  if (l0 != -INFINITY && l0 != INFINITY) {
     float p = lane < K ? expf((l - l0) / temp) : 0.f;
     float z = p;
 #pragma unroll

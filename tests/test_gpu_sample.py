@@ -18,7 +18,7 @@ def _near_boundary(row, T, k, top_p, u):
     r = np.where(np.isnan(row), -np.inf, row.astype(np.float64))
     k = min(k, r.size)
     order = np.argsort(-r, kind="stable")[:k]
-    if r[order[0]] == -np.inf:
+    if np.isinf(r[order[0]]):          # all -inf, or a +inf logit: no sums decide
         return False
     c = np.cumsum(softmax((r[order] - r[order[0]]) / T))
     # the last sum decides nothing: m = k whether or not it reaches top_p
@@ -61,7 +61,8 @@ def test_sample_ties_nan_and_small_vocab(orc):
              (np.full(500, 0.25, np.float32), 16, 0.4),
              ((rng.standard_normal(1000) * 2).astype(np.float32), 20, 0.95),
              (np.array([1.0, -2.0, 0.5, 3.0, 0.0], np.float32), 20, 0.95),       # V < top_k
-             (np.full(64, -np.inf, np.float32), 20, 0.95)]                        # all -inf
+             (np.full(64, -np.inf, np.float32), 20, 0.95),                        # all -inf
+             (np.array([0.5, np.inf, 3.0, np.inf, -1.0] * 40, np.float32), 20, 0.95)]  # +inf
     cases[3][0][rng.integers(0, 1000, 100)] = np.nan
     checked = skipped = 0
     for row, k, top_p in cases:

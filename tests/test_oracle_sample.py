@@ -74,3 +74,13 @@ def test_kept_prefix_is_the_shortest(orc, seed):
         want_m = min(k, int(np.searchsorted(cum, p) + 1))
         idx, m = orc.sample(lg, 1.0, k, p, 0.0)
         assert m == want_m and idx == order[0]
+
+
+def test_plus_infinity_takes_all_the_mass(orc):
+    # softmax's limit: a +inf logit has probability 1; with several, the lowest index
+    # (rank 0 in the top-k's tie order) is drawn, whatever the uniform
+    lg = np.array([0.5, np.inf, 3.0, np.inf, -1.0], np.float32)
+    for u in (0.0, 0.5, 0.999):
+        assert orc.sample(lg, 1.0, 4, 0.95, u) == (1, 1)
+    lg = np.array([2.0, np.nan, np.inf], np.float32)
+    assert orc.sample(lg, 0.7, 3, 0.5, 0.9) == (2, 1)
