@@ -75,32 +75,14 @@ typedef struct {
   int n_mat, rows, cols;
 } flint_nvfp4;
 
-/* Decode-unit copy of an expert's three matrices: the bytes a decode step needs for 8
- * consecutive SwiGLU outputs j = 8u .. 8u + 7 of expert m, packed into one block so
- * that one bulk copy fetches them.  Unit (m, u), FLINT_UNIT_BYTES(H) bytes, holds in
- * order:
- *   gate codes  rows 8u..8u+7 of gate[m]   8 x H/2 bytes   (row-major, as in the stack)
- *   gate scales the same rows              8 x H/16
- *   up codes, up scales                    likewise
- *   down codes  for each of the H rows r of down[m], the 4 code bytes of columns
- *               8u..8u+7                   H x 4
- *   down scales for each row r, the scale byte of the 16-column block holding
- *               columns 8u..8u+7           H
- * units: [n_mat][F/8][FLINT_UNIT_BYTES(H)] for gate, up [n_mat, F, H] and down
- * [n_mat, H, F].  Build it once with flint_decode_units; the tensor scales are those
- * of the row-major stacks. */
-#define FLINT_UNIT_BYTES(H) ((size_t)14 * (size_t)(H))
-
 /* One MoE layer.  Routed experts are stacks of n_experts matrices:
  *   gate, up : [E, F, H]      down : [E, H, F]
  *   sh_gate, sh_up : [1, Fs, H]   sh_down : [1, H, Fs]
  * router_w is bf16 [E, H]; router_bias fp32 [E] or NULL (added to the logits).
- * units / sh_units: decode-unit copies of (gate, up, down) / (sh_gate, sh_up,
- * sh_down), required by the decode entry points (flint_moe_decode,
- * flint_decode_tokens, flint_decode_tokens_noalloc), which read the experts' weights
- * only there (and their tensor scales from the stacks).
+ * The decode entry points read these row-major stacks directly (one copy of every
+ * weight serves decode).
  * mma_scales: MMA scale copies (flint_nvfp4_mma_scales) of gate, up, down, sh_gate,
- * sh_up, sh_down in that order, required by flint_moe_prefill, which reads the
+ * sh_up, sh_down in that order, required by flint_moe_prefill only, which reads the
  * row-major codes and these scales. */
 typedef struct {
   int hidden, n_experts, top_k, expert_width, shared_width;
@@ -108,8 +90,6 @@ typedef struct {
   const float* router_bias;
   flint_nvfp4 gate, up, down;
   flint_nvfp4 sh_gate, sh_up, sh_down;
-  const uint8_t* units;        /* [E][F/8][FLINT_UNIT_BYTES(H)] */
-  const uint8_t* sh_units;     /* [1][Fs/8][FLINT_UNIT_BYTES(H)] */
   const uint8_t* mma_scales[6];
   int router_score;            /* FLINT_ROUTER_SOFTMAX (0) or FLINT_ROUTER_SIGMOID (1) */
 } flint_moe_layer;
@@ -161,13 +141,22 @@ flint_status flint_quantize_nvfp4(const void* w_bf16, int n_mat, int rows, int c
 flint_status flint_nvfp4_mma_scales(const flint_nvfp4* m, uint8_t* scales_mma,
                                     flint_stream stream);
 
-/* Pack the decode-unit copy (see FLINT_UNIT_BYTES) of gate, up [n_mat, F, H] and
- * down [n_mat, H, F] (row-major NVFP4 stacks of one expert set).  units: device
- * output of n_mat * (F/8) * FLINT_UNIT_BYTES(H) bytes, 16-byte aligned.  Weight
- * preparation, like quantisation.  Errors: FLINT_ERR_SHAPE unless the three shapes
- * agree and F % 32 == 0, H % 32 == 0; FLINT_ERR_ALIGNMENT for a misaligned units. */
-flint_status flint_decode_units(const flint_nvfp4* gate, const flint_nvfp4* up,
-                                const flint_nvfp4* down, uint8_t* units, flint_stream stream);
+/* Block-scaled FP4 tensor-core microbenchmark (tcgen05.mma kind::mxf4nvf4, operands
+ * in shared memory and TMEM only), one CTA per launch slot, `ctas` CTAs:
+ *   mode 0: per iteration 8 MMAs of M = 128, N = 128, K = 64 (2 * 128 * 128 * 64 FLOP
+ *           each) issued back to back -- the peak of the block-scaled FP4 products
+ *           that the prompt path's grouped GEMM uses;
+ *   mode 1: per iteration one chain of 16 K-steps of M = 128, N = 32 with their scale
+ *           copies, a commit, its wait and the accumulator read -- the latency of the
+ *           decode kernel's per-tile products;
+ *   modes 2-4: mode 1's chain with the scales copied once before the loop (2), the
+ *           scale copies alone (3), two independent chains of 8 K-steps (4), and
+ *           modes 1 and 2 with the K-steps unrolled (5, 6).
+ * cycles (device, 16-byte aligned, `ctas` entries) receives each CTA's clock cycles
+ * over its loop.  Errors: FLINT_ERR_INVALID_ARG for another mode or a non-positive
+ * count. */
+flint_status flint_bench_fp4_mma(int mode, int iters, int ctas, unsigned long long* cycles,
+                                 flint_stream stream);
 
 /* Dequantise an NVFP4 stack to fp32 [n_mat, rows, cols] (the value formula above).
  * A check and debugging aid; no workspace. */
@@ -208,16 +197,25 @@ flint_status flint_moe_decode(const flint_moe_layer* layer, const void* x_bf16,
  * per token), and the CUDA counterpart of the single fused decode kernel of
  * "Flint-40B-A2B: AI-Built MoE Coding Model Hits 125 tok/s on MacBook Pro",
  * section "Custom Inference Kernels".
- * layers: host array of n_layers (<= FLINT_MAX_LAYERS) layers of equal shape.
+ * layers: host array of n_layers (<= FLINT_MAX_LAYERS) layers of the same hidden size.
  * head: one NVFP4 matrix [1, V, H], or NULL.  x_bf16: [T, H].  residual: fp32
  * [T, H] or NULL.  Outputs, each optional: out fp32 [T, H] = h_{n_layers};
  * x_out_bf16 [T, H] = x_{n_layers}; logits fp32 [T, V]; argmax int32 [T];
- * topk_idx int32 / topk_w fp32 [T, n_layers, k].
- * The kernel is cooperative: one CTA per SM.  CTAs exchange the router logits and
- * the residual sum through global memory each layer; every wait is bounded
- * (FLINT_ERR_TIMEOUT in the device status word if one expires).  Down
- * projections are summed with fp32 atomics, so outputs may differ in the last
- * bits from run to run.  ws: flint_workspace_bytes(FLINT_OP_MOE_DECODE, ...).
+ * topk_idx int32 / topk_w fp32 [T, n_layers, kmax] (kmax = the largest top_k; layer
+ * l fills its first top_k entries).
+ * How it runs: clusters of 16 CTAs, one CTA per SM, as many clusters as the device
+ * holds at once (at most 8; 7 on a 148-SM B300).  Each routed cluster computes all
+ * router logits itself and takes one selected expert; the remaining clusters take the
+ * shared expert; the only exchange between clusters is one tagged partial-sum board
+ * per layer.  Every sum has a fixed order, so runs repeat bit for bit.  Every wait
+ * is bounded (FLINT_ERR_TIMEOUT in the device status word if one expires; see
+ * flint_set_wait_limit_ns).
+ * Supported shapes: hidden a power of two in [256, 2048]; expert and shared widths
+ * powers of two >= 64 with the shared width a multiple of the expert width and the
+ * expert width at most 512 at hidden 2048 (1024 below); router rows per CTA
+ * (n_experts / 16, rounded up) times hidden times 2 at most 64 KiB; top_k at most
+ * FLINT_MAX_TOP_K.  Other shapes return FLINT_ERR_UNSUPPORTED.
+ * ws: flint_workspace_bytes(FLINT_OP_MOE_DECODE, ...).
  * -------------------------------------------------------------------------- */
 flint_status flint_decode_tokens(const flint_moe_layer* layers, int n_layers,
                                  const flint_nvfp4* head, const void* x_bf16,
@@ -225,6 +223,36 @@ flint_status flint_decode_tokens(const flint_moe_layer* layers, int n_layers,
                                  void* x_out_bf16, float* logits, int32_t* argmax,
                                  int32_t* topk_idx, float* topk_w, void* ws,
                                  size_t ws_bytes, flint_stream stream);
+
+/* flint_decode_tokens with a per-layer record of the chain, for checking it layer by
+ * layer against a reference:  x_trace_bf16 [T, n_layers, H] receives x_l (the bf16
+ * input of layer l as the kernel staged it) and h_trace fp32 [T, n_layers, H]
+ * receives h_l (the residual stream entering layer l).  Either may be NULL; both
+ * 16-byte aligned.  Everything else is flint_decode_tokens. */
+flint_status flint_decode_tokens_trace(const flint_moe_layer* layers, int n_layers,
+                                       const flint_nvfp4* head, const void* x_bf16,
+                                       const float* residual, int T, float rms_eps, float* out,
+                                       void* x_out_bf16, float* logits, int32_t* argmax,
+                                       int32_t* topk_idx, float* topk_w, void* x_trace_bf16,
+                                       float* h_trace, void* ws, size_t ws_bytes,
+                                       flint_stream stream);
+
+/* Bound, in nanoseconds of the GPU's global timer, of every wait the kernels make on
+ * another CTA or on a copy (default 2 s; 0 restores it).  A wait that runs out sets
+ * FLINT_ERR_TIMEOUT in the device status word and releases every other wait, and the
+ * kernel runs to its end without hanging (its outputs are then unspecified).  Applies
+ * to launches made after the call, from any host thread. */
+flint_status flint_set_wait_limit_ns(uint64_t ns);
+
+/* Fault-handling test aid: arms the next launch made by this host thread to withhold
+ * one hand-over, so that the waits on it run out:  what = 1, the next decode launch
+ * (flint_decode_tokens / flint_moe_decode / ...): CTA 0 never posts its first partial
+ * sums;  what = 2, the next prompt launch (flint_moe_prefill): the gate/up GEMM's copy
+ * issuer withholds its first pipeline stage;  what = 0 disarms.  Used with a short
+ * flint_set_wait_limit_ns to test that an expired wait is reported
+ * (FLINT_ERR_TIMEOUT) and that the next normal call succeeds.  FLINT_ERR_INVALID_ARG
+ * for other values. */
+flint_status flint_debug_hold_next_launch(int what);
 
 /* ----------------------------------------------------------------------------
  * flint_decode_tokens_noalloc -- flint_decode_tokens without a workspace argument.
@@ -241,14 +269,14 @@ flint_status flint_decode_tokens(const flint_moe_layer* layers, int n_layers,
  *  - All calls share the one array.  Calls whose kernels overlap on the GPU (other
  *    streams, other host threads) race on it and must be serialised by the caller.
  *    Each call clears what must start at zero; the rest is rewritten before use.
- *  - The array holds fewer copies of the router-logit board than a full workspace
- *    (each CTA polls one copy; fewer copies only mean more CTAs polling each), down
- *    to one.  A shape whose scratch exceeds FLINT_NOALLOC_SCRATCH_BYTES even with one
- *    copy is rejected with FLINT_ERR_UNSUPPORTED (every shape flint_decode_tokens
- *    supports fits).
+ *  - A hidden size whose scratch exceeds FLINT_NOALLOC_SCRATCH_BYTES is rejected with
+ *    FLINT_ERR_UNSUPPORTED; every hidden size flint_decode_tokens supports fits.
+ *  - The cached address belongs to the device's current context: after
+ *    cudaDeviceReset (or any teardown of the primary context) the library must be
+ *    reloaded before this entry point is called again on that device.
  * Arguments and results are those of flint_decode_tokens.
  * -------------------------------------------------------------------------- */
-#define FLINT_NOALLOC_SCRATCH_BYTES (64 * 1024)
+#define FLINT_NOALLOC_SCRATCH_BYTES (512 * 1024)
 flint_status flint_decode_tokens_noalloc(const flint_moe_layer* layers, int n_layers,
                                          const flint_nvfp4* head, const void* x_bf16,
                                          const float* residual, int T, float rms_eps,

@@ -1,5 +1,6 @@
 // api.cu -- the extern "C" entry points declared in include/flint.h: argument checks on
 // the host (nothing is enqueued when a check fails), workspace carving, launches.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -58,29 +59,23 @@ flint_status check_layer(const flint_moe_layer* L) {
 
 NVPtr nv(const flint_nvfp4& m) { return NVPtr{m.codes, m.scales, m.tensor_scale}; }
 
-// The decode path also reads the decode-unit copies of the experts.
-flint_status check_decode_layer(const flint_moe_layer* L) {
-  flint_status s = check_layer(L);
-  if (s != FLINT_OK) return s;
-  if (!L->units || !L->sh_units)
-    return FLINT_ERR_INVALID_ARG;
-  if (!aligned16(L->units) || !aligned16(L->sh_units))
-    return FLINT_ERR_ALIGNMENT;
-  return FLINT_OK;
+// The decode kernel's view of a layer (its pass plan is filled by decode_plan_layer).
+flint::DecLayer dec_layer(const flint_moe_layer& L) {
+  flint::DecLayer d;
+  std::memset(&d, 0, sizeof(d));
+  d.router_w = static_cast<const uint16_t*>(L.router_w);
+  d.router_bias = L.router_bias;
+  d.gate = nv(L.gate); d.up = nv(L.up); d.down = nv(L.down);
+  d.sh_gate = nv(L.sh_gate); d.sh_up = nv(L.sh_up); d.sh_down = nv(L.sh_down);
+  d.E = L.n_experts; d.K = L.top_k; d.F = L.expert_width; d.Fs = L.shared_width;
+  d.score = L.router_score;
+  return d;
 }
 
-flint::LayerPtrs layer_ptrs(const flint_moe_layer& L) {
-  flint::LayerPtrs p;
-  p.router_w = static_cast<const uint16_t*>(L.router_w);
-  p.router_bias = L.router_bias;
-  p.gate = nv(L.gate); p.up = nv(L.up); p.sh_gate = nv(L.sh_gate); p.sh_up = nv(L.sh_up);
-  p.units = L.units; p.sh_units = L.sh_units;
-  p.down_tsc = L.down.tensor_scale;
-  p.sh_down_tsc = L.sh_down.tensor_scale;
-  p.router_score = L.router_score;
-  p.pad_ = 0;
-  return p;
-}
+// Bound of every device-side wait (flint_set_wait_limit_ns) and the armed test aid of
+// flint_debug_hold_next_launch (per host thread, consumed by the next launch).
+std::atomic<unsigned long long> g_wait_ns{2000000000ull};
+thread_local int t_hold = 0;
 
 flint_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FLINT_OK : FLINT_ERR_CUDA; }
 
@@ -111,8 +106,8 @@ size_t flint_workspace_bytes(int op, int hidden, int n_experts, int top_k, int w
     case FLINT_OP_QUANTIZE:
       return ((size_t)(n_tokens > 0 ? n_tokens : 1) * sizeof(unsigned int) + 255) & ~(size_t)255;
     case FLINT_OP_MOE_DECODE:
-      (void)top_k; (void)width; (void)shared_width;
-      return flint::decode_workspace_bytes(hidden, n_experts, flint::decode_tag_copies(n_experts));
+      (void)n_experts; (void)top_k; (void)width; (void)shared_width;
+      return flint::decode_workspace_bytes(hidden);
     case FLINT_OP_LM_HEAD:
       return flint::lm_head_workspace_bytes(hidden, vocab, n_tokens);
     case FLINT_OP_MOE_PREFILL:
@@ -154,24 +149,21 @@ static flint_status decode_tokens_impl(const flint_moe_layer* layers, int n_laye
                                        const flint_nvfp4* head, const void* x_bf16,
                                        const float* residual, int T, float rms_eps, float* out,
                                        void* x_out_bf16, float* logits, int32_t* argmax,
-                                       int32_t* topk_idx, float* topk_w, void* ws,
-                                       size_t ws_bytes, flint_stream stream, int tag_copies = 0) {
+                                       int32_t* topk_idx, float* topk_w, void* x_trace_bf16,
+                                       float* h_trace, void* ws, size_t ws_bytes,
+                                       flint_stream stream) {
   if (!layers || !x_bf16 || !ws) return FLINT_ERR_INVALID_ARG;
   if (n_layers <= 0 || T <= 0) return FLINT_ERR_INVALID_ARG;
   if (n_layers > FLINT_MAX_LAYERS) return FLINT_ERR_UNSUPPORTED;
   if (!(rms_eps >= 0.f)) return FLINT_ERR_INVALID_ARG;
-  const flint_moe_layer& L0 = layers[0];
+  const int H = layers[0].hidden;
   for (int l = 0; l < n_layers; ++l) {
-    flint_status s = check_decode_layer(&layers[l]);
+    flint_status s = check_layer(&layers[l]);
     if (s != FLINT_OK) return s;
-    const flint_moe_layer& L = layers[l];
-    if (L.hidden != L0.hidden || L.n_experts != L0.n_experts || L.top_k != L0.top_k ||
-        L.expert_width != L0.expert_width || L.shared_width != L0.shared_width)
-      return FLINT_ERR_SHAPE;
+    if (layers[l].hidden != H) return FLINT_ERR_SHAPE;
   }
-  if (L0.hidden < 64 || L0.hidden > 2048) return FLINT_ERR_UNSUPPORTED;
   if (head) {
-    if (head->n_mat != 1 || head->cols != L0.hidden || head->rows <= 0) return FLINT_ERR_SHAPE;
+    if (head->n_mat != 1 || head->cols != H || head->rows <= 0) return FLINT_ERR_SHAPE;
     flint_status s = check_nvfp4(*head, 1, head->rows, head->cols);
     if (s != FLINT_OK) return s;
   } else if (logits || argmax) {
@@ -180,27 +172,32 @@ static flint_status decode_tokens_impl(const flint_moe_layer* layers, int n_laye
   if (!aligned16(x_bf16) || (residual && !aligned4(residual)) || (out && !aligned4(out)) ||
       (x_out_bf16 && !aligned16(x_out_bf16)) || (logits && !aligned4(logits)) ||
       (argmax && !aligned4(argmax)) || (topk_idx && !aligned4(topk_idx)) ||
-      (topk_w && !aligned4(topk_w)))
+      (topk_w && !aligned4(topk_w)) || (x_trace_bf16 && !aligned16(x_trace_bf16)) ||
+      (h_trace && !aligned16(h_trace)))
     return FLINT_ERR_ALIGNMENT;
-  if (tag_copies <= 0) tag_copies = flint::decode_tag_copies(L0.n_experts);
-  if (!aligned256(ws) ||
-      ws_bytes < flint::decode_workspace_bytes(L0.hidden, L0.n_experts, tag_copies))
-    return FLINT_ERR_WORKSPACE;
-  const flint::DecodePlan plan =
-      flint::decode_plan(L0.hidden, L0.n_experts, L0.top_k, L0.expert_width, L0.shared_width,
-                         flint::decode_grid());
-  if (!plan.ok) return FLINT_ERR_UNSUPPORTED;
+  if (!aligned256(ws) || ws_bytes < flint::decode_workspace_bytes(H)) return FLINT_ERR_WORKSPACE;
+  const int NC = flint::decode_clusters();
+  if (NC < 1) return FLINT_ERR_CUDA;
   // Large (layer table), so not on the stack; one per host thread, so concurrent calls
   // from several threads never share it.  The launch copies it into the kernel's
-  // parameters, so it is free again as soon as launch_persistent returns.
-  thread_local flint::PersistArgs a;
+  // parameters, so it is free again as soon as launch_decode returns.
+  thread_local flint::DecodeArgs a;
   std::memset(&a, 0, sizeof(a));
-  a.max_router_rows = plan.router_rows;
-  a.max_shared_units = plan.shared_units;
-  a.max_routed_units = plan.routed_units;
-  a.H = L0.hidden; a.E = L0.n_experts; a.K = L0.top_k; a.F = L0.expert_width;
-  a.Fs = L0.shared_width; a.L = n_layers; a.T = T; a.eps = rms_eps;
-  a.tag_copies = tag_copies;
+  int Emax = 0, Kmax = 0;
+  for (int l = 0; l < n_layers; ++l) {
+    a.layer[l] = dec_layer(layers[l]);
+    if (!flint::decode_plan_layer(a.layer[l], H, NC)) return FLINT_ERR_UNSUPPORTED;
+    Emax = layers[l].n_experts > Emax ? layers[l].n_experts : Emax;
+    Kmax = layers[l].top_k > Kmax ? layers[l].top_k : Kmax;
+  }
+  a.H = H; a.L = n_layers; a.T = T; a.NC = NC;
+  a.RR = flint::decode_router_rows(Emax);
+  a.Emax = flint::kDecCluster * a.RR;
+  a.Kmax = Kmax;
+  a.eps = rms_eps;
+  a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  a.hold = t_hold == 1 ? 1 : 0;
+  if (t_hold == 1) t_hold = 0;
   a.x = static_cast<const uint16_t*>(x_bf16);
   a.residual = residual;
   a.out = out;
@@ -213,9 +210,10 @@ static flint_status decode_tokens_impl(const flint_moe_layer* layers, int n_laye
   a.argmax = argmax;
   a.idx_out = topk_idx;
   a.w_out = topk_w;
-  for (int l = 0; l < n_layers; ++l) a.layer[l] = layer_ptrs(layers[l]);
+  a.x_trace = static_cast<uint16_t*>(x_trace_bf16);
+  a.h_trace = h_trace;
   flint::decode_carve(a, ws);
-  return from_cuda(flint::launch_persistent(a, static_cast<cudaStream_t>(stream)));
+  return from_cuda(flint::launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
 flint_status flint_decode_tokens(const flint_moe_layer* layers, int n_layers,
@@ -225,7 +223,31 @@ flint_status flint_decode_tokens(const flint_moe_layer* layers, int n_layers,
                                  int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
                                  flint_stream stream) {
   return decode_tokens_impl(layers, n_layers, head, x_bf16, residual, T, rms_eps, out,
-                            x_out_bf16, logits, argmax, topk_idx, topk_w, ws, ws_bytes, stream);
+                            x_out_bf16, logits, argmax, topk_idx, topk_w, nullptr, nullptr, ws,
+                            ws_bytes, stream);
+}
+
+flint_status flint_decode_tokens_trace(const flint_moe_layer* layers, int n_layers,
+                                       const flint_nvfp4* head, const void* x_bf16,
+                                       const float* residual, int T, float rms_eps, float* out,
+                                       void* x_out_bf16, float* logits, int32_t* argmax,
+                                       int32_t* topk_idx, float* topk_w, void* x_trace_bf16,
+                                       float* h_trace, void* ws, size_t ws_bytes,
+                                       flint_stream stream) {
+  return decode_tokens_impl(layers, n_layers, head, x_bf16, residual, T, rms_eps, out,
+                            x_out_bf16, logits, argmax, topk_idx, topk_w, x_trace_bf16, h_trace,
+                            ws, ws_bytes, stream);
+}
+
+flint_status flint_set_wait_limit_ns(uint64_t ns) {
+  g_wait_ns.store(ns ? (unsigned long long)ns : 2000000000ull, std::memory_order_relaxed);
+  return FLINT_OK;
+}
+
+flint_status flint_debug_hold_next_launch(int what) {
+  if (what < 0 || what > 2) return FLINT_ERR_INVALID_ARG;
+  t_hold = what;
+  return FLINT_OK;
 }
 
 flint_status flint_moe_decode(const flint_moe_layer* L, const void* x_bf16, const float* residual,
@@ -236,7 +258,8 @@ flint_status flint_moe_decode(const flint_moe_layer* L, const void* x_bf16, cons
   if (B <= 0) return FLINT_ERR_INVALID_ARG;
   if (B > FLINT_MAX_DECODE_TOKENS) return FLINT_ERR_UNSUPPORTED;
   return decode_tokens_impl(L, 1, nullptr, x_bf16, residual, B, rms_eps, out, x_next_bf16,
-                            nullptr, nullptr, topk_idx, topk_w, ws, ws_bytes, stream);
+                            nullptr, nullptr, topk_idx, topk_w, nullptr, nullptr, ws, ws_bytes,
+                            stream);
 }
 
 flint_status flint_nvfp4_mma_scales(const flint_nvfp4* m, uint8_t* scales_mma,
@@ -250,19 +273,11 @@ flint_status flint_nvfp4_mma_scales(const flint_nvfp4* m, uint8_t* scales_mma,
                                             static_cast<cudaStream_t>(stream)));
 }
 
-flint_status flint_decode_units(const flint_nvfp4* gate, const flint_nvfp4* up,
-                                const flint_nvfp4* down, uint8_t* units, flint_stream stream) {
-  if (!gate || !up || !down || !units) return FLINT_ERR_INVALID_ARG;
-  const int n = gate->n_mat, F = gate->rows, H = gate->cols;
-  if (n <= 0 || F <= 0 || H <= 0) return FLINT_ERR_INVALID_ARG;
-  if (F % 32 || H % 32) return FLINT_ERR_SHAPE;
-  flint_status s;
-  if ((s = check_nvfp4(*gate, n, F, H)) != FLINT_OK) return s;
-  if ((s = check_nvfp4(*up, n, F, H)) != FLINT_OK) return s;
-  if ((s = check_nvfp4(*down, n, H, F)) != FLINT_OK) return s;
-  if (!aligned16(units)) return FLINT_ERR_ALIGNMENT;
-  return from_cuda(flint::launch_unit_pack(nv(*gate), nv(*up), nv(*down), n, H, F, units,
-                                           static_cast<cudaStream_t>(stream)));
+flint_status flint_bench_fp4_mma(int mode, int iters, int ctas, unsigned long long* cycles,
+                                 flint_stream stream) {
+  if (mode < 0 || mode > 6 || iters <= 0 || ctas <= 0 || !cycles) return FLINT_ERR_INVALID_ARG;
+  if (!aligned16(cycles)) return FLINT_ERR_ALIGNMENT;
+  return from_cuda(flint::launch_fp4_mma_bench(mode, iters, ctas, cycles, static_cast<cudaStream_t>(stream)));
 }
 
 flint_status flint_lm_head(const flint_nvfp4* W, const void* x_bf16, float* logits,

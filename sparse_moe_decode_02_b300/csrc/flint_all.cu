@@ -4,6 +4,7 @@
 #include "decode.cu"
 #include "lm_head.cu"
 #include "prefill.cu"
+#include "mma_bench.cu"
 #include "sample.cu"
 #include "api.cu"
 #include "noalloc.cu"

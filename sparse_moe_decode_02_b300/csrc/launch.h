@@ -11,62 +11,71 @@ struct NVPtr {
   const float* tsc;
 };
 
-struct LayerPtrs {
-  const uint16_t* router_w;
-  const float* router_bias;
-  NVPtr gate, up, sh_gate, sh_up;  // the tensor scales are read from these stacks
-  const uint8_t* units;           // decode units of (gate, up, down) [E][F/8][14 H]
-  const uint8_t* sh_units;        // of (sh_gate, sh_up, sh_down) [1][Fs/8][14 H]
-  const float* down_tsc;          // [E]
-  const float* sh_down_tsc;       // [1]
-  int router_score;               // FLINT_ROUTER_SOFTMAX / FLINT_ROUTER_SIGMOID
-  int pad_;
-};
-
 constexpr int kMaxLayers = 64;
 
-struct PersistArgs {
-  int H, E, K, F, Fs, L, T, V;
+// ------------------------------------------------------------------ persistent decode
+// Clusters of kDecCluster CTAs.  In each layer a cluster runs up to kDecMaxGroups
+// groups: a group is one routed expert (one part of F outputs), or a contiguous run of
+// parts of the shared (or dense) expert.  The cluster's CTAs split each part's gate/up
+// rows, swap the SwiGLU values, and each CTA applies the group's down columns to its own
+// H/16 output rows.
+constexpr int kDecCluster = 16;
+constexpr int kDecMaxClusters = 8;
+constexpr int kDecMaxGroups = 2;
+constexpr int kDecThreads = 512;
+
+struct DecLayer {
+  const uint16_t* router_w;          // bf16 [E][H]; null for a dense layer
+  const float* router_bias;          // fp32 [E] or null
+  NVPtr gate, up, down;              // routed stacks [E][F][H], [E][F][H], [E][H][F]
+  NVPtr sh_gate, sh_up, sh_down;     // shared (or dense) expert [1][Fs][H], [1][Fs][H], [1][H][Fs]
+  int E, K, F, Fs;
+  int Wsh;                           // outputs of one shared part (a divisor of Fs)
+  int score;                         // FLINT_ROUTER_SOFTMAX / FLINT_ROUTER_SIGMOID
+  // group g of cluster c: rank[c][g] >= 0 is the routed expert of that rank (one part);
+  // -1 is parts [p0, p0 + np) of the shared expert
+  signed char rank[kDecMaxClusters][kDecMaxGroups];
+  unsigned char np[kDecMaxClusters][kDecMaxGroups];
+  unsigned char p0[kDecMaxClusters][kDecMaxGroups];
+  unsigned char n_grp[kDecMaxClusters];
+  unsigned char routed[kDecMaxClusters];   // cluster computes the router and top-k
+  int pad_[2];
+};
+
+struct DecodeArgs {
+  int H, L, T, V, NC, Kmax, Emax, RR;  // RR: router rows per CTA; Emax = 16 RR (logits per step)
   float eps;
-  const uint16_t* x;       // [T, H] bf16
-  const float* residual;   // [T, H] or null
-  float* out;              // [T, H] or null
-  uint16_t* x_out;         // [T, H] or null
-  NVPtr head;              // codes null: no head
-  float* logits;           // [T, V] or null
-  int32_t* argmax;         // [T] or null
-  int32_t* idx_out;        // [T, L, K] or null
-  float* w_out;            // [T, L, K] or null
-  // workspace
-  unsigned* bar;           // grid barrier {arrivals, generation, abort}
-  unsigned long long* logits_tag;   // [tag_copies][tag_stride] {logit bits, step + 1}
-  int tag_copies, tag_stride;
-  float* acc;              // [2][copies][H] residual ping-pong
-  float* best_v;           // [grid]
-  int* best_i;             // [grid]
-  int max_router_rows;     // per-CTA buffer sizes (decode_plan)
-  int max_shared_units;
-  int max_routed_units;
-  LayerPtrs layer[kMaxLayers];
+  int hold;                          // test aid: CTA 0 withholds its first partial
+  unsigned long long wait_ns;        // bound of every wait
+  const uint16_t* x;                 // [T][H] bf16
+  const float* residual;             // [T][H] or null
+  float* out;                        // [T][H] or null
+  uint16_t* x_out;                   // [T][H] or null
+  NVPtr head;                        // codes null: no head
+  float* logits;                     // [T][V] or null
+  int32_t* argmax;                   // [T] or null
+  int32_t* idx_out;                  // [T][L][Kmax] or null
+  float* w_out;                      // [T][L][Kmax] or null
+  uint16_t* x_trace;                 // [T][L][H] or null: x_l as staged
+  float* h_trace;                    // [T][L][H] or null: h_l
+  unsigned* sync;                    // [64]: [0] abort flag
+  unsigned long long* board;         // [2][kDecMaxClusters][H] tagged partial sums
+  unsigned long long* best;          // [2][kDecMaxClusters * kDecCluster][2] tagged head maxima
+  DecLayer layer[kMaxLayers];
 };
 
-// Per-CTA work bounds and shared memory of the persistent decode on G CTAs.
-struct DecodePlan {
-  int router_rows, shared_units, routed_units;
-  size_t smem;
-  bool ok;
+// Host-side plan of a decode launch.
+struct DecodeShape {
+  int H, E, K, F, Fs;                // E = K = 0: a dense layer (its width in Fs)
 };
-DecodePlan decode_plan(int H, int E, int K, int F, int Fs, int G);
-
-// Workspace of the persistent decode with `copies` copies of the logit board;
-// decode_tag_copies(E) is the number a full workspace holds.
-size_t decode_workspace_bytes(int H, int E, int copies);
-int decode_tag_copies(int E);
-int decode_grid();                                   // CTAs of the persistent kernel
-void decode_carve(PersistArgs& a, void* ws);          // a.H, a.E, a.tag_copies set
-cudaError_t launch_persistent(const PersistArgs& a, cudaStream_t st);
-cudaError_t launch_unit_pack(const NVPtr& gate, const NVPtr& up, const NVPtr& down, int n_mat, int H,
-                             int F, uint8_t* units, cudaStream_t st);
+int decode_clusters();                               // clusters the device co-schedules (0: none)
+int decode_router_rows(int E);
+size_t decode_workspace_bytes(int H);
+size_t decode_smem_bytes(int H, int Emax);
+// Checks a layer's shape and fills its pass plan; false when this build cannot run it.
+bool decode_plan_layer(DecLayer& d, int H, int NC);
+void decode_carve(DecodeArgs& a, void* ws);          // a.H set
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 
 struct PrefillArgs {
   int H, E, K, F, Fs, T;
@@ -86,6 +95,7 @@ struct PrefillArgs {
 size_t prefill_workspace_bytes(int H, int E, int K, int F, int Fs, int T);
 bool prefill_shape_ok(int H, int E, int K, int F, int Fs);
 cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st);
+cudaError_t launch_fp4_mma_bench(int mode, int iters, int ctas, unsigned long long* cycles, cudaStream_t st);
 cudaError_t launch_mma_scales(const uint8_t* scales, int n_mat, int rows, int cols, uint8_t* out,
                               cudaStream_t st);
 

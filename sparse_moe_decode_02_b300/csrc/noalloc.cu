@@ -4,8 +4,9 @@
 // Some callers cannot hand the library scratch memory: a host that reserves the whole
 // device up front and gives its extensions no allocator, or a serving loop that must
 // never call cudaMalloc (it can block, and it can synchronise the device).  For them
-// the decode's scratch (grid sync words, router logits, the residual ping-pong buffers
-// and the head's per-CTA argmax candidates) lives in the fixed device array below.
+// the decode's scratch (the abort word and the tagged boards through which the
+// clusters swap residual partial sums and the head's per-CTA maxima) lives in the fixed
+// device array below.
 // It is part of the loaded module, so every GPU that loads the library holds it until
 // the process exits.
 #include <mutex>
@@ -44,19 +45,13 @@ extern "C" flint_status flint_decode_tokens_noalloc(
     const float* residual, int T, float rms_eps, float* out, void* x_out_bf16, float* logits,
     int32_t* argmax, int32_t* topk_idx, float* topk_w, flint_stream stream) {
   if (!layers || n_layers <= 0) return FLINT_ERR_INVALID_ARG;
-  const flint_moe_layer& L0 = layers[0];
-  // as many copies of the logit board as the fixed array holds (at least one)
-  int copies = flint::decode_tag_copies(L0.n_experts);
-  while (copies > 1 && flint::decode_workspace_bytes(L0.hidden, L0.n_experts, copies) >
-                           flint::kNoAllocScratchBytes)
-    --copies;
-  if (flint::decode_workspace_bytes(L0.hidden, L0.n_experts, copies) > flint::kNoAllocScratchBytes)
+  if (flint::decode_workspace_bytes(layers[0].hidden) > flint::kNoAllocScratchBytes)
     return FLINT_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   if (flint::noalloc_scratch(&scratch) != cudaSuccess) return FLINT_ERR_CUDA;
-  // The sync words at the start of the scratch are cleared by every launch; the rest
-  // is written before it is read within one call.
+  // Every launch clears the scratch it uses (sync words and the tagged exchange
+  // boards) before the kernel starts, so what an earlier call left there is harmless.
   return decode_tokens_impl(layers, n_layers, head, x_bf16, residual, T, rms_eps, out,
-                            x_out_bf16, logits, argmax, topk_idx, topk_w, scratch,
-                            flint::kNoAllocScratchBytes, stream, copies);
+                            x_out_bf16, logits, argmax, topk_idx, topk_w, nullptr, nullptr,
+                            scratch, flint::kNoAllocScratchBytes, stream);
 }

@@ -449,6 +449,156 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
   }
 }
 
+// ---------------------------------------------------------------- warp top-k (k_topk)
+__device__ __forceinline__ unsigned order_key(float v) {
+  const unsigned u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+// (key, index) a comes before b: larger key, or equal key and lower index.
+__device__ __forceinline__ bool before(unsigned ka, int ia, unsigned kb, int ib) {
+  return ka > kb || (ka == kb && ia < ib);
+}
+
+// Bitonic network over N register pairs, leaving them in `before` order.
+template <int N>
+__device__ __forceinline__ void sort_pairs(unsigned (&k)[N], int (&ix)[N]) {
+#pragma unroll
+  for (int size = 2; size <= N; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool first_half = (i & size) == 0;
+          const bool swap = first_half ? before(k[j], ix[j], k[i], ix[i]) : before(k[i], ix[i], k[j], ix[j]);
+          const unsigned tk = swap ? k[j] : k[i];
+          const int ti = swap ? ix[j] : ix[i];
+          k[j] = swap ? k[i] : k[j];
+          ix[j] = swap ? ix[i] : ix[j];
+          k[i] = tk;
+          ix[i] = ti;
+        }
+      }
+    }
+  }
+}
+
+// Exact softmax top-k by one warp (see flint.h): the K largest logits, ties to the
+// lower index, in that order; weights exp(l_i - l_0) / sum over the selected.  Lane l
+// holds logits [PER*l, PER*l + PER) sorted; each round the warp takes the best head
+// (one max-reduction; a second reduction only when heads tie) and its lane pops it.
+template <int PER>
+__device__ __noinline__ void topk_exact(const float* logits, int E, int K, int* s_sel, float* s_w) {
+  const int lane = threadIdx.x & 31;
+  unsigned key[PER];
+  int idx[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane * PER + i;
+    float l = (e < E) ? logits[e] : -INFINITY;
+    l = (l == l) ? l : -INFINITY;
+    key[i] = (e < E) ? order_key(l) : 0u;      // every live key is >= 1
+    idx[i] = e;
+  }
+  if (PER > 1) sort_pairs<PER>(key, idx);
+  unsigned my_key = 0u;
+  int my_sel = 0;
+  for (int s = 0; s < K; ++s) {
+    const unsigned wk = __reduce_max_sync(0xffffffffu, key[0]);
+    unsigned tie = __ballot_sync(0xffffffffu, key[0] == wk);
+    if (tie & (tie - 1u)) {
+      const unsigned wi = __reduce_min_sync(0xffffffffu, key[0] == wk ? (unsigned)idx[0] : 0xFFFFFFFFu);
+      tie = __ballot_sync(0xffffffffu, key[0] == wk && (unsigned)idx[0] == wi);
+    }
+    const int wl = __ffs(tie) - 1;
+    const int we = __shfl_sync(0xffffffffu, idx[0], wl);
+    if (lane == s) { my_key = wk; my_sel = we; }
+    if (lane == wl) {
+#pragma unroll
+      for (int i = 0; i + 1 < PER; ++i) { key[i] = key[i + 1]; idx[i] = idx[i + 1]; }
+      key[PER - 1] = 0u;
+      idx[PER - 1] = 0x7FFFFFFF;
+    }
+  }
+  const float l = key_value(my_key);
+  const float l0 = __shfl_sync(0xffffffffu, l, 0);
+  const float p = lane < K ? expf(l - l0) : 0.f;
+  float z = p;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  if (lane < K) { s_sel[lane] = my_sel; s_w[lane] = p / z; }
+  __syncwarp();
+}
+
+// Fast path for E <= 256: one 32-bit key per logit = (upper 24 bits of the order key,
+// 255 - index), so a single max-reduction per round yields both the winner and its
+// index, and ties go to the lower index.  Dropping the low 8 bits of the order key can
+// only misorder logits that agree in their upper 24 bits; such a pair among the K + 1
+// best shows up as two consecutive winners with equal upper bits, and the exact path
+// then decides.  Returns false (warp-uniform) in that case.
+template <int PER>
+__device__ __forceinline__ bool topk_fast(const float* logits, int E, int K, int* s_sel, float* s_w) {
+  const int lane = threadIdx.x & 31;
+  unsigned pk[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane * PER + i;
+    float l = (e < E) ? logits[e] : -INFINITY;
+    l = (l == l) ? l : -INFINITY;
+    pk[i] = (e < E) ? ((order_key(l) & 0xFFFFFF00u) | (unsigned)(255 - e)) : 0u;
+  }
+  unsigned prev = 0u;
+  bool exact = true;
+  int my_sel = 0;
+  for (int s = 0; s <= K; ++s) {                    // round K only checks the boundary
+    unsigned m = pk[0];
+#pragma unroll
+    for (int i = 1; i < PER; ++i) m = max(m, pk[i]);
+    const unsigned w = __reduce_max_sync(0xffffffffu, m);
+    if (s > 0 && (w >> 8) == (prev >> 8) && w != 0u) exact = false;
+    prev = w;
+    if (s == K) break;
+    const int e = 255 - (int)(w & 255u);
+    if (lane == s) my_sel = e;
+    if (lane == e / PER) {
+#pragma unroll
+      for (int i = 0; i < PER; ++i)
+        if (i == e % PER) pk[i] = 0u;
+    }
+  }
+  if (!exact) return false;
+  float l = lane < K ? logits[my_sel] : 0.f;
+  l = (l == l) ? l : -INFINITY;
+  const float l0 = __shfl_sync(0xffffffffu, l, 0);
+  const float p = lane < K ? expf(l - l0) : 0.f;
+  float z = p;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  if (lane < K) { s_sel[lane] = my_sel; s_w[lane] = p / z; }
+  __syncwarp();
+  return true;
+}
+
+template <int PER>
+__device__ __forceinline__ void topk_per(const float* logits, int E, int K, int* s_sel, float* s_w) {
+  if (PER <= 8 && E <= 256 && topk_fast<PER>(logits, E, K, s_sel, s_w)) return;
+  topk_exact<PER>(logits, E, K, s_sel, s_w);
+}
+
+__device__ __forceinline__ void topk_dispatch(const float* logits, int E, int K, int* s_sel,
+                                              float* s_w) {
+  const int per_lane = (E + 31) / 32;
+  if (per_lane <= 1) topk_per<1>(logits, E, K, s_sel, s_w);
+  else if (per_lane <= 2) topk_per<2>(logits, E, K, s_sel, s_w);
+  else if (per_lane <= 4) topk_per<4>(logits, E, K, s_sel, s_w);
+  else if (per_lane <= 8) topk_per<8>(logits, E, K, s_sel, s_w);
+  else topk_per<16>(logits, E, K, s_sel, s_w);
+}
+
 // ---------------------------------------------------------------- router GEMM (bf16)
 // Partial logits over one K split: part[ks][t][e] = x[t, K_ks] . Wr[e, K_ks] for 128 tokens
 // and all E (<= 256) experts per CTA; A = x rows (TMA, 64 bf16 = 128 B per K-tile), B =

@@ -43,7 +43,6 @@ class _LayerC(ctypes.Structure):
                 ("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
                 ("gate", _NVFP4C), ("up", _NVFP4C), ("down", _NVFP4C),
                 ("sh_gate", _NVFP4C), ("sh_up", _NVFP4C), ("sh_down", _NVFP4C),
-                ("units", ctypes.c_void_p), ("sh_units", ctypes.c_void_p),
                 ("mma_scales", ctypes.c_void_p * 6), ("router_score", ctypes.c_int)]
 
 ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
@@ -51,11 +50,12 @@ ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
 
 _lib = None
 
-_SYMBOLS = ["flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_decode_units",
-            "flint_nvfp4_mma_scales", "flint_sample_logits",
-            "flint_moe_decode", "flint_decode_tokens", "flint_moe_prefill", "flint_lm_head",
-            "flint_workspace_bytes", "flint_last_device_status", "flint_status_string",
-            "flint_version"]
+_SYMBOLS = ["flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_nvfp4_mma_scales",
+            "flint_sample_logits", "flint_moe_decode", "flint_decode_tokens",
+            "flint_decode_tokens_trace", "flint_decode_tokens_noalloc", "flint_moe_prefill",
+            "flint_lm_head", "flint_workspace_bytes", "flint_last_device_status",
+            "flint_status_string", "flint_version", "flint_set_wait_limit_ns",
+            "flint_debug_hold_next_launch", "flint_bench_fp4_mma"]
 
 
 def lib() -> ctypes.CDLL:
@@ -70,10 +70,14 @@ def lib() -> ctypes.CDLL:
     vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     L.flint_quantize_nvfp4.argtypes = [vp, i, i, i, vp, vp, vp, vp, sz, vp]
     L.flint_dequantize_nvfp4.argtypes = [ctypes.POINTER(_NVFP4C), vp, vp]
-    L.flint_decode_units.argtypes = [ctypes.POINTER(_NVFP4C)] * 3 + [vp, vp]
     L.flint_nvfp4_mma_scales.argtypes = [ctypes.POINTER(_NVFP4C), vp, vp]
     L.flint_decode_tokens.argtypes = [ctypes.POINTER(_LayerC), i, ctypes.POINTER(_NVFP4C), vp, vp,
                                       i, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flint_decode_tokens_trace.argtypes = [ctypes.POINTER(_LayerC), i, ctypes.POINTER(_NVFP4C),
+                                            vp, vp, i, ctypes.c_float, vp, vp, vp, vp, vp, vp,
+                                            vp, vp, vp, sz, vp]
+    L.flint_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    L.flint_debug_hold_next_launch.argtypes = [i]
     L.flint_decode_tokens_noalloc.argtypes = [ctypes.POINTER(_LayerC), i, ctypes.POINTER(_NVFP4C),
                                               vp, vp, i, ctypes.c_float, vp, vp, vp, vp, vp, vp,
                                               vp]
@@ -83,16 +87,18 @@ def lib() -> ctypes.CDLL:
                                     vp]
     L.flint_lm_head.argtypes = [ctypes.POINTER(_NVFP4C), vp, vp, vp, i, vp, sz, vp]
     L.flint_sample_logits.argtypes = [vp, i, i, ctypes.c_float, i, ctypes.c_float, vp, vp, vp]
+    L.flint_bench_fp4_mma.argtypes = [i, i, i, vp, vp]
     L.flint_workspace_bytes.argtypes = [i] * 8
     L.flint_workspace_bytes.restype = sz
     L.flint_last_device_status.argtypes = [vp]
     L.flint_status_string.argtypes = [i]
     L.flint_status_string.restype = ctypes.c_char_p
     L.flint_version.restype = ctypes.c_char_p
-    for name in ("flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_decode_units",
-                 "flint_nvfp4_mma_scales", "flint_moe_decode", "flint_decode_tokens", "flint_decode_tokens_noalloc",
-                 "flint_moe_prefill", "flint_lm_head", "flint_last_device_status",
-                 "flint_sample_logits"):
+    for name in ("flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_nvfp4_mma_scales",
+                 "flint_moe_decode", "flint_decode_tokens", "flint_decode_tokens_trace",
+                 "flint_decode_tokens_noalloc", "flint_moe_prefill", "flint_lm_head",
+                 "flint_last_device_status", "flint_sample_logits", "flint_set_wait_limit_ns",
+                 "flint_debug_hold_next_launch", "flint_bench_fp4_mma"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -156,8 +162,6 @@ class MoELayer:
     sh_up: NVFP4
     sh_down: NVFP4
     top_k: int
-    units: torch.Tensor | None = None     # decode-unit copy of (gate, up, down)
-    sh_units: torch.Tensor | None = None  # decode-unit copy of (sh_gate, sh_up, sh_down)
     mma_scales: tuple | None = None   # MMA scale copies of gate, up, down, sh_gate, sh_up, sh_down
     router_score: int = 0             # ROUTER_SOFTMAX or ROUTER_SIGMOID
 
@@ -168,14 +172,12 @@ class MoELayer:
 
     def c(self) -> _LayerC:
         H, E, k, F, Fs = self.dims
-        ptr = lambda t: None if t is None else t.data_ptr()
         sf = (ctypes.c_void_p * 6)(*([None] * 6 if self.mma_scales is None else
                                      [m.data_ptr() for m in self.mma_scales]))
         return _LayerC(H, E, k, F, Fs, self.router_w.data_ptr(),
                        None if self.router_bias is None else self.router_bias.data_ptr(),
                        self.gate.c(), self.up.c(), self.down.c(), self.sh_gate.c(),
-                       self.sh_up.c(), self.sh_down.c(), ptr(self.units), ptr(self.sh_units), sf,
-                       self.router_score)
+                       self.sh_up.c(), self.sh_down.c(), sf, self.router_score)
 
     def nbytes(self) -> int:
         return (self.router_w.numel() * 2 + sum(m.nbytes() for m in (
@@ -201,21 +203,6 @@ def quantize_nvfp4(w: torch.Tensor, stream=None, ws=None) -> NVFP4:
     return q
 
 
-def decode_units(gate: NVFP4, up: NVFP4, down: NVFP4, stream=None) -> torch.Tensor:
-    """Decode-unit copy of (gate [n, F, H], up, down [n, H, F]) (see flint.h)."""
-    n, F, H = gate.shape
-    out = torch.empty(n, F // 8, unit_bytes(H), dtype=torch.uint8, device=gate.codes.device)
-    g, u, d = gate.c(), up.c(), down.c()
-    _check(lib().flint_decode_units(ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), _ptr(out),
-                                    _stream(stream)), "flint_decode_units")
-    return out
-
-
-def unit_bytes(hidden: int) -> int:
-    """Bytes of one decode unit (FLINT_UNIT_BYTES)."""
-    return 14 * hidden
-
-
 def nvfp4_mma_scales(m: NVFP4, stream=None) -> torch.Tensor:
     """MMA scale copy of an NVFP4 stack's block scales (see flint.h)."""
     out = torch.empty_like(m.scales)
@@ -223,6 +210,15 @@ def nvfp4_mma_scales(m: NVFP4, stream=None) -> torch.Tensor:
     _check(lib().flint_nvfp4_mma_scales(ctypes.byref(mc), _ptr(out), _stream(stream)),
            "flint_nvfp4_mma_scales")
     return out
+
+
+def bench_fp4_mma(mode: int, iters: int, ctas: int, stream=None) -> torch.Tensor:
+    """Launch the block-scaled FP4 MMA microbenchmark (see flint.h); returns the
+    per-CTA cycle counts (device int64 tensor, filled when the stream reaches it)."""
+    cyc = torch.zeros(ctas, dtype=torch.int64, device="cuda")
+    _check(lib().flint_bench_fp4_mma(mode, iters, ctas, _ptr(cyc), _stream(stream)),
+           "flint_bench_fp4_mma")
+    return cyc
 
 
 def dequantize_nvfp4(m: NVFP4, stream=None) -> torch.Tensor:
@@ -258,8 +254,9 @@ def moe_decode(layer: MoELayer, x: torch.Tensor, residual: torch.Tensor | None =
 def decode_tokens(layers, x: torch.Tensor, head: NVFP4 | None = None,
                   residual: torch.Tensor | None = None, rms_eps: float = 1e-6, out=None,
                   x_out=None, logits=None, argmax=None, topk_idx=None, topk_w=None, ws=None,
-                  stream=None):
-    """T tokens through len(layers) chained layers (+ head) in one launch."""
+                  stream=None, x_trace=None, h_trace=None):
+    """T tokens through len(layers) chained layers (+ head) in one launch.  With x_trace
+    (bf16 [T, L, H]) or h_trace (fp32 [T, L, H]) the call is flint_decode_tokens_trace."""
     if x.dim() == 1:
         x = x.unsqueeze(0)
     T = x.shape[0]
@@ -268,10 +265,27 @@ def decode_tokens(layers, x: torch.Tensor, head: NVFP4 | None = None,
     hc = head.c() if head is not None else None
     nb = workspace_bytes(OP_MOE_DECODE, H, E, k, F, Fs, 0, T)
     ws = _workspace(nb, x.device, ws)
-    _check(lib().flint_decode_tokens(arr, len(layers), ctypes.byref(hc) if hc else None, _ptr(x),
-                                     _ptr(residual), T, float(rms_eps), _ptr(out), _ptr(x_out),
-                                     _ptr(logits), _ptr(argmax), _ptr(topk_idx), _ptr(topk_w),
-                                     _ptr(ws), ws.numel(), _stream(stream)), "flint_decode_tokens")
+    common = (arr, len(layers), ctypes.byref(hc) if hc else None, _ptr(x), _ptr(residual), T,
+              float(rms_eps), _ptr(out), _ptr(x_out), _ptr(logits), _ptr(argmax),
+              _ptr(topk_idx), _ptr(topk_w))
+    if x_trace is None and h_trace is None:
+        _check(lib().flint_decode_tokens(*common, _ptr(ws), ws.numel(), _stream(stream)),
+               "flint_decode_tokens")
+    else:
+        _check(lib().flint_decode_tokens_trace(*common, _ptr(x_trace), _ptr(h_trace), _ptr(ws),
+                                               ws.numel(), _stream(stream)),
+               "flint_decode_tokens_trace")
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Bound of every device-side wait (0 restores the 2 s default)."""
+    _check(lib().flint_set_wait_limit_ns(int(ns)), "flint_set_wait_limit_ns")
+
+
+def debug_hold_next_launch(what: int) -> None:
+    """Arms the next decode (1) or prompt (2) launch of this thread to withhold one
+    hand-over, so that its waits run out (a fault-handling test aid; 0 disarms)."""
+    _check(lib().flint_debug_hold_next_launch(int(what)), "flint_debug_hold_next_launch")
 
 
 def decode_tokens_noalloc(layers, x: torch.Tensor, head: NVFP4 | None = None,

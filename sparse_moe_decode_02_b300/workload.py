@@ -31,8 +31,6 @@ def build_layer(spec: synth.LayerSpec, device="cuda", stream=None) -> flint.MoEL
     if all(m.shape[1] % 128 == 0 and m.shape[2] % 64 == 0 for m in stacks):
         mma = tuple(flint.nvfp4_mma_scales(m, stream=stream) for m in stacks)
     return flint.MoELayer(router, bias_t, gate, up, down, sh_gate, sh_up, sh_down, s.top_k,
-                          units=flint.decode_units(gate, up, down, stream=stream),
-                          sh_units=flint.decode_units(sh_gate, sh_up, sh_down, stream=stream),
                           mma_scales=mma, router_score=spec.router_score)
 
 

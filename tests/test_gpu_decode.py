@@ -168,8 +168,8 @@ def test_decode_out_aliases_residual(orc):
     want = flint.moe_decode(layer, x, residual=r.clone())
     flint.moe_decode(layer, x, residual=r, out=r)
     torch.cuda.synchronize()
-    # the split-K down sums use fp32 atomics: equal up to summation order
-    torch.testing.assert_close(r, want, rtol=1e-5, atol=1e-6)
+    # every sum has a fixed order: bit for bit the same
+    assert torch.equal(r, want)
 
 
 # ------------------------------------------------------------------ lm_head
@@ -230,27 +230,6 @@ def test_lm_head_argmax_only():
 
 
 # ------------------------------------------------------------------ persistent multi-layer decode
-def test_decode_units_bitexact():
-    # the decode-unit copy against the layout of FLINT_UNIT_BYTES, rebuilt with numpy
-    n, F, H = 3, 64, 256
-    key = synth.tensor_key(9)
-    g = flint.quantize_nvfp4(synth.normal_bf16(key, n * F * H, 0.02).view(n, F, H).to(DEV))
-    u = flint.quantize_nvfp4(synth.normal_bf16(key + 1, n * F * H, 0.02).view(n, F, H).to(DEV))
-    d = flint.quantize_nvfp4(synth.normal_bf16(key + 2, n * H * F, 0.02).view(n, H, F).to(DEV))
-    got = flint.decode_units(g, u, d).cpu().numpy()
-    assert got.shape == (n, F // 8, 14 * H)
-    gc, gs = g.codes.cpu().numpy(), g.scales.cpu().numpy()
-    uc, us = u.codes.cpu().numpy(), u.scales.cpu().numpy()
-    dc, ds = d.codes.cpu().numpy(), d.scales.cpu().numpy()
-    for m in range(n):
-        for j in range(F // 8):
-            rows = slice(8 * j, 8 * j + 8)
-            want = np.concatenate([gc[m, rows].ravel(), gs[m, rows].ravel(),
-                                   uc[m, rows].ravel(), us[m, rows].ravel(),
-                                   dc[m, :, 4 * j:4 * j + 4].ravel(), ds[m, :, j // 2]])
-            np.testing.assert_array_equal(got[m, j], want)
-
-
 def test_mma_scales_bitexact():
     w = synth.normal_bf16(synth.tensor_key(10), 2 * 256 * 512, 0.02).view(2, 256, 512).to(DEV)
     m = flint.quantize_nvfp4(w)

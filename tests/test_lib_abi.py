@@ -54,10 +54,10 @@ def _nv(n, r, c, codes=FAKE):
     return flint._NVFP4C(codes, FAKE, FAKE, n, r, c)
 
 
-def _layer(H=256, E=16, k=2, F=64, Fs=128, router=FAKE, gate_cols=None, units=FAKE, sf=FAKE, score=0):
+def _layer(H=256, E=16, k=2, F=64, Fs=128, router=FAKE, gate_cols=None, sf=FAKE, score=0):
     return flint._LayerC(H, E, k, F, Fs, router, None, _nv(E, F, gate_cols or H), _nv(E, F, H),
                          _nv(E, H, F), _nv(1, Fs, H), _nv(1, Fs, H), _nv(1, H, Fs),
-                         units, units, (ctypes.c_void_p * 6)(*[sf] * 6), score)
+                         (ctypes.c_void_p * 6)(*[sf] * 6), score)
 
 
 def test_quantize_argument_checks(L):
@@ -89,8 +89,6 @@ def test_decode_argument_checks(L):
     assert call(_layer(H=250), args()) == 3                             # not a multiple of 32
     assert call(_layer(gate_cols=512), args()) == 3                     # stack shape mismatch
     assert call(_layer(router=FAKE_MIS), args()) == 2
-    assert call(_layer(units=None), args()) == 1                        # no decode-unit copy
-    assert call(_layer(units=FAKE_MIS), args()) == 2
     assert call(_layer(score=2), args()) == 1                           # unknown router scoring
     assert call(_layer(score=-1), args()) == 1
 
@@ -112,23 +110,25 @@ def test_decode_tokens_argument_checks(L):
     assert call(ok(head=None)) == 1                                     # argmax without a head
     bad_head = _nv(1, 4096, 512)
     assert call(ok(head=ctypes.byref(bad_head))) == 3                   # head cols != hidden
-    mixed = (flint._LayerC * 2)(_layer(), _layer(F=128))
-    assert call(ok(layers=mixed, n=2)) == 3                             # layers of unequal shape
+    mixed = (flint._LayerC * 2)(_layer(), _layer(H=512))
+    assert call(ok(layers=mixed, n=2)) == 3                             # layers of unequal hidden
     assert call(ok(eps=-1.0)) == 1
     assert call(ok(wsb=16)) == 4
 
 
-def test_decode_units_argument_checks(L):
-    du = L.flint_decode_units
-    g, u, d = _nv(2, 64, 128), _nv(2, 64, 128), _nv(2, 128, 64)
-    r = ctypes.byref
-    assert du(r(g), r(u), r(d), None, None) == 1
-    assert du(None, r(u), r(d), FAKE, None) == 1
-    assert du(r(g), r(u), r(d), FAKE_MIS, None) == 2
-    g80, u80, d80 = _nv(2, 80, 128), _nv(2, 80, 128), _nv(2, 128, 80)
-    assert du(r(g80), r(u80), r(d80), FAKE, None) == 3                  # F % 32
-    assert du(r(g), r(u), r(_nv(2, 64, 128)), FAKE, None) == 3          # down not [n, H, F]
-    assert du(r(g), r(_nv(3, 64, 128)), r(d), FAKE, None) == 3          # up of another count
+def test_decode_trace_and_wait_controls(L):
+    tr = L.flint_decode_tokens_trace
+    ws = flint.workspace_bytes(flint.OP_MOE_DECODE, 256, 16, 2, 64, 128, 0, 4)
+    arr = (flint._LayerC * 1)(_layer())
+    call = lambda xt, ht: tr(arr, 1, None, FAKE, None, 2, 1e-6, FAKE, None, None, None, None,
+                             None, xt, ht, FAKE, ws, None)
+    assert call(FAKE_MIS, None) == 2                                   # trace rows 16-byte aligned
+    assert call(None, FAKE + 4) == 2
+    assert L.flint_set_wait_limit_ns(5_000_000) == 0
+    assert L.flint_set_wait_limit_ns(0) == 0                           # back to the default
+    assert L.flint_debug_hold_next_launch(3) == 1
+    assert L.flint_debug_hold_next_launch(-1) == 1
+    assert L.flint_debug_hold_next_launch(0) == 0
 
 
 def test_mma_scales_argument_checks(L):
