@@ -58,7 +58,6 @@ constexpr int kMaxE = 256;                // experts of a routed layer
 constexpr int kMaxRR = kMaxE / kDecCluster;   // router rows per CTA
 constexpr int kMaxN = 64;                 // SwiGLU outputs per CTA and part
 constexpr int kMaxG = kDecMaxClusters * kCS;
-constexpr int kChunkWords = 20;           // hi/lo table: 16 words per 32-value chunk, padded
 
 // ---------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -370,8 +369,8 @@ __device__ __noinline__ void topk(const float* s_lg, int E, int K, int score, in
     if (nw >= K) {
       const unsigned m = lane < nw ? s_wm[lane] : 0u;
       int ge = 0;
-#pragma unroll 1
-      for (int u = 0; u < nw; ++u) ge += s_wm[u] >= m ? 1 : 0;
+#pragma unroll
+      for (int u = 0; u < kMaxE / 32; ++u) ge += (u < nw && s_wm[u] >= m) ? 1 : 0;
       thr = __reduce_max_sync(0xffffffffu, (lane < nw && ge >= K) ? m : 0u);
     }
     const bool cand = key != 0u && key >= thr;
@@ -387,8 +386,8 @@ __device__ __noinline__ void topk(const float* s_lg, int E, int K, int score, in
     if (n <= 32) {
       const unsigned long long ck = lane < n ? s_cand[lane] : 0ull;
       int rank = 0;
-#pragma unroll 1
-      for (int m = 0; m < n; ++m) rank += __shfl_sync(0xffffffffu, ck, m) > ck ? 1 : 0;
+#pragma unroll
+      for (int m = 0; m < 32; ++m) rank += (m < n && s_cand[m] > ck) ? 1 : 0;   // broadcast reads
       if (lane < n && rank < K) {
         s_sel[rank] = (int)(~(unsigned)ck);
         s_key[rank] = (unsigned)(ck >> 32);
@@ -444,43 +443,53 @@ struct GroupOff {
   __host__ __device__ uint32_t down_slot(int np) const { return slot(np >= 2 ? (np - 2) % 2 : 1); }
 };
 
-// Part `part` of group g (thread 0): this CTA's n gate rows and n up rows into `dst` on
-// `bar` (part 0 also brings the group's three tensor scales into s_tsc).
-__device__ __noinline__ void issue_part(const DecLayer& D, int c, int g, int part, int e, int j, int H, uint8_t* dst,
-                                        float* s_tsc, uint64_t* bar) {
+// A group's contiguous copies, one per warp (lane 0 of warp w0 + k issues copy k: the
+// lanes of one warp issue bulk copies one after another, different warps side by side;
+// every thread calls this):
+//   what >= 0: part `what` -- this CTA's n gate rows and n up rows (codes, then scales)
+//              into `dst`; part 0 also brings the group's three tensor scales into tsc;
+//   what <  0: the group's down rows R_j (all its W columns: the group spans whole rows).
+// Copy 0's thread posts the byte count on `bar` (its one arrival); the copies land on it.
+__device__ __noinline__ void issue_copies(const DecLayer& D, int c, int g, int what, int e, int j, int H,
+                                          uint8_t* dst, float* tsc, uint64_t* bar, int w0) {
+  const int k = (threadIdx.x & 31) == 0 ? (int)(threadIdx.x >> 5) - w0 : -1;   // this thread's copy
+  if (k < 0 || k >= 7) return;
   const GroupDims d = group_dims(D, c, g);
-  const size_t row0 = d.rank >= 0 ? (size_t)e * D.F + (size_t)d.n * j
-                                   : (size_t)(D.p0[c][g] + part) * D.Wsh + (size_t)d.n * j;
-  const NVPtr& G = d.rank >= 0 ? D.gate : D.sh_gate;
-  const NVPtr& U = d.rank >= 0 ? D.up : D.sh_up;
-  const uint32_t cb = d.n * H / 2, sb = d.n * H / 16;
-  if (part == 0) {
-    const NVPtr& Dn = d.rank >= 0 ? D.down : D.sh_down;
-    const int ei = d.rank >= 0 ? e : 0;
-    cp_async4(s_tsc + 0, G.tsc + ei);
-    cp_async4(s_tsc + 1, U.tsc + ei);
-    cp_async4(s_tsc + 2, Dn.tsc + ei);
-    cp_async_arrive_hold(bar);
+  const bool routed = d.rank >= 0;
+  const uint8_t* src = nullptr;
+  uint32_t off = 0, bytes = 0, total = 0;
+  if (what >= 0) {
+    const size_t row0 = routed ? (size_t)e * D.F + (size_t)d.n * j
+                               : (size_t)(D.p0[c][g] + what) * D.Wsh + (size_t)d.n * j;
+    const NVPtr& P = (k & 1) ? (routed ? D.up : D.sh_up) : (routed ? D.gate : D.sh_gate);
+    const uint32_t cb = d.n * H / 2, sb = d.n * H / 16;
+    total = 2 * (cb + sb);
+    if (k < 2) {                                  // codes: gate, up
+      src = P.codes + row0 * (H / 2);
+      off = k * cb;
+      bytes = cb;
+    } else if (k < 4) {                           // scales: gate, up
+      src = P.scales + row0 * (H / 16);
+      off = a16(2 * cb) + (k - 2) * sb;
+      bytes = sb;
+    }
+    if (what == 0 && k >= 4 && k < 7) {        // tensor scales of gate, up, down
+      const NVPtr& T = k == 4 ? (routed ? D.gate : D.sh_gate) : k == 5 ? (routed ? D.up : D.sh_up)
+                                                                             : (routed ? D.down : D.sh_down);
+      cp_async4(tsc + (k - 4), T.tsc + (routed ? e : 0));
+      cp_async_arrive_hold(bar);
+    }
+  } else {
+    const int R16 = H / 16;
+    const size_t drow0 = (routed ? (size_t)e * H : 0) + (size_t)R16 * j;
+    const NVPtr& Dn = routed ? D.down : D.sh_down;
+    const uint32_t dcb = R16 * d.W / 2, dsb = R16 * d.W / 16;
+    total = dcb + dsb;
+    if (k == 0) { src = Dn.codes + drow0 * (d.W / 2); bytes = dcb; }
+    if (k == 1) { src = Dn.scales + drow0 * (d.W / 16); off = a16(dcb); bytes = dsb; }
   }
-  mbar_expect_tx(bar, 2 * (cb + sb));
-  bulk_g2s(dst, G.codes + row0 * (H / 2), cb, bar);
-  bulk_g2s(dst + cb, U.codes + row0 * (H / 2), cb, bar);
-  bulk_g2s(dst + a16(2 * cb), G.scales + row0 * (H / 16), sb, bar);
-  bulk_g2s(dst + a16(2 * cb) + sb, U.scales + row0 * (H / 16), sb, bar);
-}
-
-// The group's down rows R_j (all its W columns) into `dst`: one block (thread 0, on
-// bar_dn) when the group spans whole rows.
-__device__ __noinline__ void issue_down(const DecLayer& D, int c, int g, int e, int j, int H, uint8_t* dst,
-                                        uint64_t* bar) {
-  const GroupDims d = group_dims(D, c, g);
-  const int R16 = H / 16;
-  const size_t drow0 = (d.rank >= 0 ? (size_t)e * H : 0) + (size_t)R16 * j;
-  const NVPtr& Dn = d.rank >= 0 ? D.down : D.sh_down;
-  const uint32_t dcb = R16 * d.W / 2, dsb = R16 * d.W / 16;
-  mbar_expect_tx(bar, dcb + dsb);
-  bulk_g2s(dst, Dn.codes + drow0 * (d.W / 2), dcb, bar);
-  bulk_g2s(dst + a16(dcb), Dn.scales + drow0 * (d.W / 16), dsb, bar);
+  if (k == 0) mbar_expect_tx(bar, total);
+  if (bytes) bulk_g2s(dst + off, src, bytes, bar);
 }
 
 // ... strided down rows (a shared group spanning part of the columns): cp.async from every
@@ -508,93 +517,142 @@ __device__ __noinline__ void issue_down_strided(const DecLayer& D, int c, int g,
   cp_async_arrive_noinc(bar);
 }
 
-// Down columns of a group (this CTA's H/16 rows x W columns, W <= kMaxW) times the
-// group's W SwiGLU values hsw, added (times `scale`) into s_part.  The values are first
-// tabulated as hi/lo f16 pairs with one power-of-two scale per 32-value chunk (chunk c's
-// hi words at s_hhl[20 c + q], lo words 20 kMaxW/32 further, 2^-k at s_hk[c]; the 80-byte
-// chunk stride keeps eight lanes' 16-byte loads on different banks).  Lane sl of a row
-// slice then takes chunk sl.  Every thread calls this.
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// D (16 x 8, fp32) += A (16 x 16, f16, row) . B (16 x 8, f16, col)
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Down columns of a group: this CTA's R16 rows (codes [R16][W/2], scales [R16][W/16] in
+// shared memory) times the group's W SwiGLU values hsw, added (times `scale`) into
+// s_part.  Every thread calls this.
+//
+// hsw is split into two f16 terms under one power-of-two scale 2^k (max |hsw| 2^k in
+// [2^14, 2^15)): hi = f16(v 2^k), lo = f16(v 2^k - hi), about 22 bits of every value.
+// They are columns 0 and 1 of the B operand of mma.sync m16n8k16 (f16 x f16 products are
+// exact, accumulation fp32); the weights are decoded to f16 (cvt.rn.f16x2.e2m1x2) and
+// multiplied by their E4M3 block scale (exact in f16: |e2m1 x e4m3| lies in [2^-10,
+// 2688]).  A warp takes 16 rows and a range of 128-column chunk sets; lane (g, t) of the
+// mma fragments holds rows g and g + 8 and reads 32-column chunk 4 c + t of each, so the
+// order of the columns within an mma is a fixed permutation that the B operand (read by
+// the same lane from the same chunk) follows.
 __device__ __noinline__ void group_down(const uint8_t* dcodes, const uint8_t* dscales, int W, int R16,
-                                        const float* hsw, uint32_t* s_hhl, float* s_hk, float scale, float* s_part) {
+                                        const float* hsw, uint32_t* s_hh, uint32_t* s_hl, float* s_red, float* s_acc,
+                                        float scale, float* s_part) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // 1. one scale for the group: max |hsw| over the CTA (non-negative floats order as
+  // their bit patterns)
+  float am = 0.f;
 #pragma unroll 1
-  for (int t = threadIdx.x; t < W / 2; t += kThreads) {
-    const float2 v = *reinterpret_cast<const float2*>(hsw + 2 * t);
-    float am = fmaxf(fabsf(v.x), fabsf(v.y));
-#pragma unroll
-    for (int o = 8; o; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));   // 16 pairs: a chunk
-    const int k = f16_stage_exponent(am);
-    const float s = exp2i(k);
-    const float a = v.x * s, b = v.y * s;
+  for (int i = threadIdx.x; i < W; i += kThreads) am = fmaxf(am, fabsf(hsw[i]));
+  const unsigned wm = __reduce_max_sync(0xffffffffu, __float_as_uint(am));
+  if (lane == 0) s_red[warp] = __uint_as_float(wm);
+  __syncthreads();
+  am = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(s_red[lane & (kWarps - 1)])));
+  const int k = f16_stage_exponent(am);
+  const float s2k = exp2i(k);
+  // 2. the hi / lo terms, f16 pairs in column order
+#pragma unroll 1
+  for (int i = threadIdx.x; i < W / 2; i += kThreads) {
+    const float2 v = *reinterpret_cast<const float2*>(hsw + 2 * i);
+    const float a = v.x * s2k, b = v.y * s2k;
     const uint32_t hi = pack_f16x2_rn(a, b);
     float ha, hb;
     f16x2_to_f32x2(hi, ha, hb);
-    const int c = t >> 4, q = t & 15;
-    s_hhl[kChunkWords * c + q] = hi;
-    s_hhl[kChunkWords * (kMaxW / 32) + kChunkWords * c + q] = pack_f16x2_rn(a - ha, b - hb);
-    if (q == 0) s_hk[c] = exp2i(-k);
+    s_hh[i] = hi;
+    s_hl[i] = pack_f16x2_rn(a - ha, b - hb);
   }
   __syncthreads();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int LPR = W / 32, RPP = 32 / LPR;
-  const int slice = lane / LPR, sl = lane % LPR;
-  if (warp * RPP >= R16) return;
-  uint32_t hh[16], hl[16];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 u = *reinterpret_cast<const uint4*>(s_hhl + kChunkWords * sl + 4 * q);
-    const uint4 v = *reinterpret_cast<const uint4*>(s_hhl + kChunkWords * (kMaxW / 32) + kChunkWords * sl + 4 * q);
-    hh[4 * q] = u.x; hh[4 * q + 1] = u.y; hh[4 * q + 2] = u.z; hh[4 * q + 3] = u.w;
-    hl[4 * q] = v.x; hl[4 * q + 1] = v.y; hl[4 * q + 2] = v.z; hl[4 * q + 3] = v.w;
-  }
-  const float unscale = s_hk[sl] * scale;
+  // 3. 16-row tiles x chunk-set ranges over the warps
+  const int g = lane >> 2, t = lane & 3;
+  const int tiles = R16 / 16, csets = (W + 127) / 128, qmax = W / 32;
+  int ksegs = kWarps / tiles;
+  ksegs = ksegs < 1 ? 1 : (ksegs > csets ? csets : ksegs);
+  const int per = (csets + ksegs - 1) / ksegs;
+  const uint32_t* bsrc = g == 1 ? s_hl : s_hh;         // B column 1 (lanes 4-7) = lo, column 0 = hi
 #pragma unroll 1
-  for (int r0 = warp * RPP; r0 < R16; r0 += kWarps * RPP) {
-    const int r = r0 + slice;
-    const int rc = r < R16 ? r : 0;
-    const uint4 cw = *reinterpret_cast<const uint4*>(dcodes + (size_t)rc * (W / 2) + 16 * sl);
-    const uint32_t sw = *reinterpret_cast<const uint16_t*>(dscales + (size_t)rc * (W / 16) + 2 * sl);
-    const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
-    float blk[2];
+  for (int item = warp; item < tiles * ksegs; item += kWarps) {
+    const int tile = item % tiles, ks = item / tiles;
+    const uint8_t* ra = dcodes + (size_t)(16 * tile + g) * (W / 2);
+    const uint8_t* rb = ra + (size_t)8 * (W / 2);
+    const uint8_t* sa = dscales + (size_t)(16 * tile + g) * (W / 16);
+    const uint8_t* sb = sa + (size_t)8 * (W / 16);
+    float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    const int c1 = min(csets, (ks + 1) * per);
+#pragma unroll 1
+    for (int c = ks * per; c < c1; ++c) {
+      const int q = 4 * c + t;
+      uint4 wa = make_uint4(0u, 0u, 0u, 0u), wb = wa, x0 = wa, x1 = wa, x2 = wa, x3 = wa;
+      uint32_t fa = 0u, fb = 0u;
+      if (q < qmax) {
+        wa = *reinterpret_cast<const uint4*>(ra + 16 * q);
+        wb = *reinterpret_cast<const uint4*>(rb + 16 * q);
+        fa = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sa + 2 * q));
+        fb = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sb + 2 * q));
+        const uint4* xp = reinterpret_cast<const uint4*>(bsrc + 16 * q);
+        x0 = xp[0]; x1 = xp[1]; x2 = xp[2]; x3 = xp[3];
+      }
+      const uint32_t SA[2] = {__byte_perm(fa, 0, 0x1010), __byte_perm(fa, 0, 0x3232)};
+      const uint32_t SB[2] = {__byte_perm(fb, 0, 0x1010), __byte_perm(fb, 0, 0x3232)};
+      const uint32_t xv[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
+                               x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+      const uint32_t wav[4] = {wa.x, wa.y, wa.z, wa.w}, wbv[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
+      for (int h = 0; h < 4; ++h) {                    // word h of the chunk: mmas 2h, 2h + 1
+        uint32_t a[4], b[4];
+        e2m1x8_to_f16x2x4(wav[h], a[0], a[1], a[2], a[3]);
+        e2m1x8_to_f16x2x4(wbv[h], b[0], b[1], b[2], b[3]);
+        const uint32_t S_a = SA[h >> 1], S_b = SB[h >> 1];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t f[4];
-        e2m1x8_to_f16x2x4(wv[2 * b + h], f[0], f[1], f[2], f[3]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          fma2_f16(a0, a1, f[i], hh[8 * b + 4 * h + i]);
-          fma2_f16(c0, c1, f[i], hl[8 * b + 4 * h + i]);
+        for (int m = 0; m < 2; ++m) {
+          const int j = 2 * h + m;
+          mma16816(d[m], hmul2(a[2 * m], S_a), hmul2(b[2 * m], S_b), hmul2(a[2 * m + 1], S_a),
+                   hmul2(b[2 * m + 1], S_b), xv[2 * j], xv[2 * j + 1]);
         }
       }
-      blk[b] = (a0 + a1) + (c0 + c1);
     }
-    float s0, s1;
-    f16x2_to_f32x2(e4m3x2_to_f16x2(sw), s0, s1);
-    float acc = fmaf(blk[0], s0, blk[1] * s1) * unscale;
+    if (t == 0) {
+      s_acc[ks * R16 + 16 * tile + g] = (d[0][0] + d[0][1]) + (d[1][0] + d[1][1]);
+      s_acc[ks * R16 + 16 * tile + g + 8] = (d[0][2] + d[0][3]) + (d[1][2] + d[1][3]);
+    }
+  }
+  __syncthreads();
+  const float unscale = exp2i(-k) * scale;
 #pragma unroll 1
-    for (int m = LPR / 2; m; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-    if (sl == 0 && r < R16) s_part[r] += acc;
+  for (int r = threadIdx.x; r < R16; r += kThreads) {
+    float v = 0.f;
+#pragma unroll 1
+    for (int ks = 0; ks < ksegs; ++ks) v += s_acc[ks * R16 + r];
+    s_part[r] += v * unscale;
   }
 }
 
 // ---------------------------------------------------------------- residual exchange
-// Posts this CTA's rows (unless `post` is false) and waits (bounded) until every word it
+// post_rows posts this CTA's partial rows.  exchange waits (bounded) until every word it
 // reads carries `tag`: word i = c' * H/16 + r is row r of R_j from cluster c'; two per
 // thread, both in flight at once.  Then h_{l+1}[R_j] = h_l[R_j] + the clusters' partials
 // in cluster order, into s_hn, which goes to every CTA of the cluster (h_nxt) and, when
 // `out` is given, to out.  Thread 0 also refreshes *s_abort (its load completes during
 // the poll).  Every thread calls this.
-__device__ __noinline__ void exchange(unsigned long long* bd, int NC, int c, int H, int j, unsigned tag, bool post,
-                                      const float* s_part, float* s_pp, const float* h_cur, float* s_hn, float* h_nxt,
+__device__ __forceinline__ void post_rows(unsigned long long* bd, int c, int H, int j, unsigned tag,
+                                          const float* s_part) {
+  const int R16 = H / 16;
+#pragma unroll 1
+  for (int r = threadIdx.x; r < R16; r += kThreads)
+    st_tagged(bd + (size_t)c * H + (size_t)R16 * j + r, ((unsigned long long)tag << 32) | __float_as_uint(s_part[r]));
+}
+__device__ __noinline__ void exchange(const unsigned long long* bd, int NC, int H, int j, unsigned tag,
+                                      float* s_pp, const float* h_cur, float* s_hn, float* h_nxt,
                                       float* out, unsigned* sync, unsigned long long limit, int* s_abort) {
   const int R16 = H / 16;
   const unsigned ab = threadIdx.x == 0 ? ld_abort(sync) : 0u;
-  if (post)
-#pragma unroll 1
-    for (int r = threadIdx.x; r < R16; r += kThreads)
-      st_tagged(bd + (size_t)c * H + (size_t)R16 * j + r, ((unsigned long long)tag << 32) | __float_as_uint(s_part[r]));
   const int N = NC * R16;
   const int i0 = threadIdx.x, i1 = threadIdx.x + kThreads;
   bool n0 = i0 < N, n1 = i1 < N;
@@ -682,7 +740,7 @@ static_assert(sizeof(DecLayer) % 8 == 0 && kLayerWords <= 32, "layer table: at m
 
 // Shared-memory carve (bytes), the same on the host and the device.
 struct Smem {
-  uint32_t h, xb, xl, lg, hsw, tmp, part, pp, gu, hn, hv, hhl, hk, cand, big, total;
+  uint32_t h, xb, xl, lg, hsw, tmp, part, pp, gu, hn, hv, hh, hl, acc, cand, big, total;
   __host__ __device__ static Smem of(int H, int Emax) {
     Smem s;
     const int R16 = H / 16;
@@ -697,9 +755,10 @@ struct Smem {
     s.gu = s.pp + 4 * kDecMaxClusters * R16;   // [2 kMaxN] gate/up values
     s.hn = s.gu + 8 * kMaxN;                   // [H/16] fp32 h_{l+1} rows of this CTA
     s.hv = s.hn + 4 * R16;                     // [256] fp32 head chunk values
-    s.hhl = s.hv + 4 * 256;                    // [2][kMaxW/32][kChunkWords] u32 hi/lo table
-    s.hk = s.hhl + 8 * kChunkWords * (kMaxW / 32);   // [kMaxW/32] fp32 chunk scales
-    s.cand = s.hk + 4 * (kMaxW / 32);          // [kMaxE] u64 top-k candidates
+    s.hh = s.hv + 4 * 256;                     // [kMaxW/2] f16 pairs: hi terms of the SwiGLU values
+    s.hl = s.hh + 2 * kMaxW;                   // [kMaxW/2] f16 pairs: lo terms
+    s.acc = s.hl + 2 * kMaxW;                  // [256] fp32 down partials (chunk-set range x row)
+    s.cand = s.acc + 4 * 256;                  // [kMaxE] u64 top-k candidates
     s.big = (s.cand + 8 * kMaxE + 127) & ~127u;      // router rows + group buffer, or the head ring
     s.total = s.big + kBigBytes;
     return s;
@@ -775,11 +834,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
   __shared__ unsigned s_key[FLINT_MAX_TOP_K];
   __shared__ unsigned s_wm[8];
   __shared__ int s_n;
-  __shared__ __align__(16) float s_tsc[4];           // tensor scales of the group in flight
+  __shared__ __align__(16) float s_tsc[2][4];        // tensor scales of the shared / routed group in flight
   __shared__ float s_red[2 * kWarps];
   __shared__ float s_bv[kWarps];
   __shared__ int s_bi[kWarps];
-  __shared__ __align__(8) uint64_t bar_rt, bar_gu[2], bar_dn, bar_dna, bar_hd[2];
+  // copy barriers: router rows, shared parts (two slots), shared down rows (bulk or
+  // cp.async), routed part, routed down rows; head ring
+  __shared__ __align__(8) uint64_t bars[7], bar_hd[2];
   __shared__ int s_abort;                            // this CTA saw the abort flag (refreshed per step)
 
   const int H = a.H, R16 = H / 16;
@@ -796,8 +857,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
   float* s_gu = reinterpret_cast<float*>(s_dyn + S.gu);
   float* s_hn = reinterpret_cast<float*>(s_dyn + S.hn);
   float* s_hv = reinterpret_cast<float*>(s_dyn + S.hv);
-  uint32_t* s_hhl = reinterpret_cast<uint32_t*>(s_dyn + S.hhl);
-  float* s_hk = reinterpret_cast<float*>(s_dyn + S.hk);
+  uint32_t* s_hh = reinterpret_cast<uint32_t*>(s_dyn + S.hh);
+  uint32_t* s_hl = reinterpret_cast<uint32_t*>(s_dyn + S.hl);
+  float* s_acc = reinterpret_cast<float*>(s_dyn + S.acc);
   unsigned long long* s_cand = reinterpret_cast<unsigned long long*>(s_dyn + S.cand);
   uint8_t* s_big = s_dyn + S.big;
   uint16_t* s_router = reinterpret_cast<uint16_t*>(s_big);
@@ -809,13 +871,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
   unsigned* sync = a.sync;
   const unsigned long long lim = a.wait_ns;
   const int n_steps = a.T * a.L;
-  uint32_t ph_rt = 0, ph_gu = 0, ph_dn = 0, ph_dna = 0, ph_hd = 0;   // mbarrier parities (ph_gu, ph_hd: a bit per slot)
-  // copies in flight on each barrier: a wait happens only for an issued copy, and after an
-  // abort no new copy is issued, so the kernel ends with nothing in flight
-  bool pend_rt = false, pend_dn = false, pend_dna = false;
-  unsigned pend_gu = 0u, pend_hd = 0u;               // bit per slot
+  enum { B_RT, B_GU0, B_GU1, B_DN, B_DNA, B_RGU, B_RDN };
+  // per barrier (a bit each): the parity of its current phase, and whether a copy is in
+  // flight on it.  A wait happens only for an issued copy, and after an abort no new copy
+  // is issued, so the kernel ends with nothing in flight.
+  uint32_t ph = 0, pend = 0, ph_hd = 0, pend_hd = 0;
   unsigned grp_seq = 0;                              // groups run by this cluster
-  bool pre_issued = false;                           // this step's first group already in flight
+  unsigned pre = 0;                                  // this step's groups already in flight (a bit each)
+  auto wait_bar = [&](int i) {
+    if (pend & (1u << i)) {
+      mbar_wait(&bars[i], (ph >> i) & 1u, sync, lim);
+      ph ^= 1u << i;
+      pend &= ~(1u << i);
+    }
+  };
 
   // warp 15: the layer table of step `st` and this CTA's router bias entries (the
   // parameter's table sits in the constant bank, where each layer's first use would
@@ -839,29 +908,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     const int r0 = j * a.RR;
     const int nr = min(a.RR, D.E - r0);
     if (nr <= 0) return;
-    pend_rt = true;
+    pend |= 1u << B_RT;
     if (threadIdx.x != 0) return;
-    mbar_expect_tx(&bar_rt, (uint32_t)nr * H * 2);
-    bulk_g2s(s_router, D.router_w + (size_t)r0 * H, (uint32_t)nr * H * 2, &bar_rt);
+    mbar_expect_tx(&bars[B_RT], (uint32_t)nr * H * 2);
+    bulk_g2s(s_router, D.router_w + (size_t)r0 * H, (uint32_t)nr * H * 2, &bars[B_RT]);
   };
-  // the group buffer: after the router rows in a routed cluster
-  auto group_buf = [&](const DecLayer& D) { return s_big + (D.routed[c] ? kRouterBytes : 0); };
+  // a group's buffer: routed groups at the start of the big region (over the router
+  // rows, which are consumed before a routed group is issued), shared groups after the
+  // routed buffer in a routed cluster
+  auto group_buf = [&](const DecLayer& D, int g) {
+    return s_big + (D.rank[c][g] >= 0 ? 0u : (D.routed[c] ? D.sh_off : 0u));
+  };
   // a group's copies: what >= 0 a part (into slot what % 2), what < 0 the down rows
   auto issue = [&](const DecLayer& D, int g, int what) {
     const GroupDims d = group_dims(D, c, g);
     const GroupOff o = GroupOff::of(d.n, d.W, d.np, H);
-    const int e = d.rank >= 0 ? s_sel[d.rank] : 0;
-    uint8_t* buf = group_buf(D);
-    if (what >= 0) {
-      if (threadIdx.x == 0) issue_part(D, c, g, what, e, j, H, buf + o.slot(what & 1), s_tsc, &bar_gu[what & 1]);
-      pend_gu |= 1u << (what & 1);
-    } else if (d.contiguous) {
-      if (threadIdx.x == 0) issue_down(D, c, g, e, j, H, buf + o.down_slot(d.np), &bar_dn);
-      pend_dn = true;
-    } else {
-      issue_down_strided(D, c, g, j, H, buf + o.down_slot(d.np), &bar_dna);
-      pend_dna = true;
+    const bool routed = d.rank >= 0;
+    uint8_t* buf = group_buf(D, g);
+    if (what < 0 && !d.contiguous) {
+      issue_down_strided(D, c, g, j, H, buf + o.down_slot(d.np), &bars[B_DNA]);
+      pend |= 1u << B_DNA;
+      return;
     }
+    const int b = what >= 0 ? (routed ? B_RGU : B_GU0 + (what & 1)) : (routed ? B_RDN : B_DN);
+    issue_copies(D, c, g, what, routed ? s_sel[d.rank] : 0, j, H, buf + (what >= 0 ? o.slot(what & 1) : o.down_slot(d.np)),
+                   s_tsc[routed], &bars[b], what >= 0 ? 0 : 8);
+    pend |= 1u << b;
   };
   // a group's first copies: part 0, and part 1 or else the down rows
   auto issue_start = [&](const DecLayer& D, int g) {
@@ -875,11 +947,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
   store_layer(1);
   if (threadIdx.x == 0) {
     s_abort = 0;
-    mbar_init(&bar_rt, 1);
-    mbar_init(&bar_gu[0], 1);
-    mbar_init(&bar_gu[1], 1);
-    mbar_init(&bar_dn, 1);
-    mbar_init(&bar_dna, kThreads);
+#pragma unroll 1
+    for (int i = 0; i < 7; ++i) mbar_init(&bars[i], i == B_DNA ? kThreads : 1);
     mbar_init(&bar_hd[0], 1);
     mbar_init(&bar_hd[1], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -902,10 +971,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
       // ---- a token's first step: the copies that were not made a step ahead (the
       // head used the buffers), and a router this cluster had no step ahead to fetch
       if (!s_abort) {
-        if (D.routed[c] && !pend_rt) issue_router(D);
+        if (D.routed[c] && !(pend & (1u << B_RT))) issue_router(D);
         if (l == 0 && D.n_grp[c] > 0 && D.rank[c][0] < 0) {
           issue_start(D, 0);
-          pre_issued = true;
+          pre = 1u;
         }
       }
       // ---- 1. stage x_l (and h_0 at a token's first layer)
@@ -927,15 +996,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
       // ---- 2. router and top-k (routed clusters)
       if (D.routed[c]) {
         const int r0 = j * a.RR, nr = min(a.RR, D.E - r0);
-        if (pend_rt) {
-          mbar_wait(&bar_rt, ph_rt, sync, lim);
-          ph_rt ^= 1;
-          pend_rt = false;
-        }
+        wait_bar(B_RT);
         if (nr > 0) router_rows(s_router, s_xb, H, r0, nr, s_bias[step % 3], s_tmp, lg);
         cluster_sync();                              // all E logits in every CTA
-        if (next_in_token && !s_abort && DN.routed[c]) issue_router(DN);
         topk(lg, D.E, D.K, D.score, s_sel, s_w, s_wm, &s_n, s_cand, s_key);
+        // the first routed group's copies at once: the groups ahead of it (shared parts,
+        // in flight already) run while they land
+#pragma unroll 1
+        for (int g = 0; g < D.n_grp[c]; ++g)
+          if (D.rank[c][g] >= 0) {
+            if (!s_abort) {
+              issue_start(D, g);
+              pre |= 1u << g;
+            }
+            break;
+          }
         if (c == 0 && j == 0 && threadIdx.x < D.K) {
           const size_t o = ((size_t)t * a.L + l) * a.Kmax + threadIdx.x;
           if (a.idx_out) a.idx_out[o] = s_sel[threadIdx.x];
@@ -944,23 +1019,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
       }
       // ---- 3. the cluster's groups
       const int ng = D.n_grp[c];
-      uint8_t* buf = group_buf(D);
 #pragma unroll 1
       for (int g = 0; g < ng; ++g, ++grp_seq) {
         const GroupDims d = group_dims(D, c, g);
         const GroupOff o = GroupOff::of(d.n, d.W, d.np, H);
+        const bool routed = d.rank >= 0;
+        const uint8_t* buf = group_buf(D, g);
+        const float* tsc = s_tsc[routed];
         float* hsw = s_hsw + (grp_seq & 1) * kMaxW;
-        if (!(g == 0 && pre_issued) && !s_abort) issue_start(D, g);
+        if (!(pre & (1u << g)) && !s_abort) issue_start(D, g);
 #pragma unroll 1
         for (int part = 0; part < d.np; ++part) {
           const int sl = part & 1;
-          if (pend_gu & (1u << sl)) {
-            mbar_wait(&bar_gu[sl], (ph_gu >> sl) & 1u, sync, lim);
-            ph_gu ^= 1u << sl;
-            pend_gu &= ~(1u << sl);
-          }
+          wait_bar(routed ? B_RGU : B_GU0 + sl);
           const uint8_t* pb = buf + o.slot(sl);
-          rows_dot<CPL>(pb, pb + a16(d.n * H), 2 * d.n, d.n, s_tsc[0] * unscale, s_tsc[1] * unscale, H, s_xl, s_gu);
+          rows_dot<CPL>(pb, pb + a16(d.n * H), 2 * d.n, d.n, tsc[0] * unscale, tsc[1] * unscale, H, s_xl, s_gu);
           __syncthreads();
           if (threadIdx.x < d.n) s_tmp[threadIdx.x] = silu(s_gu[threadIdx.x]) * s_gu[d.n + threadIdx.x];
           __syncthreads();                           // s_tmp; this part's slot is free
@@ -971,35 +1044,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
           to_cluster(hsw + part * d.Wp + d.n * j, s_tmp, d.n / 4);
         }
         cluster_sync();                              // the group's W SwiGLU values everywhere
-        if (pend_dn) {
-          mbar_wait(&bar_dn, ph_dn, sync, lim);
-          ph_dn ^= 1;
-          pend_dn = false;
-        }
-        if (pend_dna) {
-          mbar_wait(&bar_dna, ph_dna, sync, lim);
-          ph_dna ^= 1;
-          pend_dna = false;
-        }
+        wait_bar(routed ? B_RDN : B_DN);
+        wait_bar(B_DNA);
         const uint8_t* db = buf + o.down_slot(d.np);
-        group_down(db, db + a16(R16 * d.W / 2), d.W, R16, hsw, s_hhl, s_hk,
-                   s_tsc[2] * (d.rank >= 0 ? s_w[d.rank] : 1.0f), s_part);
+        group_down(db, db + a16(R16 * d.W / 2), d.W, R16, hsw, s_hh, s_hl, s_red, s_acc,
+                   tsc[2] * (routed ? s_w[d.rank] : 1.0f), s_part);
         __syncthreads();                             // the group buffer is free again
-      }
-      // the next step's first group, when it does not depend on the data (within a token;
-      // at a token's end the head uses the buffers)
-      pre_issued = false;
-      if (next_in_token && !s_abort && DN.n_grp[c] > 0 && DN.rank[c][0] < 0) {
-        issue_start(DN, 0);
-        pre_issued = true;
       }
       store_layer(step + 2);                         // read from the next step on
       // ---- 4. residual exchange.  A cluster that met no cluster barrier in this step
       // meets one here: then every one of its CTAs has staged its inputs before any of
       // them posts (out may alias residual).
       if (ng == 0 && !D.routed[c]) cluster_sync();
-      exchange(a.board + (size_t)par * kDecMaxClusters * H, a.NC, c, H, j, step + 1,
-               !(a.hold && step == 0 && blockIdx.x == 0), s_part, s_pp, h_cur, s_hn, s_h + (par ^ 1) * H,
+      unsigned long long* bd = a.board + (size_t)par * kDecMaxClusters * H;
+      if (!(a.hold && step == 0 && blockIdx.x == 0)) post_rows(bd, c, H, j, step + 1, s_part);
+      // copies for the next step that do not depend on its data, issued while the other
+      // clusters' rows arrive (within a token; at a token's end the head uses the
+      // buffers): the router rows, and the first group when it is a shared one
+      pre = 0u;
+      if (next_in_token && !s_abort) {
+        if (DN.routed[c]) issue_router(DN);
+        if (DN.n_grp[c] > 0 && DN.rank[c][0] < 0) {
+          issue_start(DN, 0);
+          pre = 1u;
+        }
+      }
+      exchange(bd, a.NC, H, j, step + 1, s_pp, h_cur, s_hn, s_h + (par ^ 1) * H,
                (!next_in_token && c == 0 && a.out) ? a.out + (size_t)t * H : nullptr, sync, lim, &s_abort);
       cluster_sync();                                // h_{l+1} complete in every CTA
     }
@@ -1037,14 +1107,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
   // serve, so normally nothing is in flight here; after an abort, what a skipped wait
   // left in flight is drained (bounded) before the CTA exits.  The last remote writes
   // precede the last cluster barrier.
-  if (pend_rt) mbar_wait(&bar_rt, ph_rt, sync, lim);
 #pragma unroll 1
-  for (int k = 0; k < 2; ++k) {
-    if (pend_gu & (1u << k)) mbar_wait(&bar_gu[k], (ph_gu >> k) & 1u, sync, lim);
+  for (int i = 0; i < 7; ++i) wait_bar(i);
+#pragma unroll 1
+  for (int k = 0; k < 2; ++k)
     if (pend_hd & (1u << k)) mbar_wait(&bar_hd[k], (ph_hd >> k) & 1u, sync, lim);
-  }
-  if (pend_dn) mbar_wait(&bar_dn, ph_dn, sync, lim);
-  if (pend_dna) mbar_wait(&bar_dna, ph_dna, sync, lim);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1117,51 +1184,64 @@ bool decode_plan_layer(DecLayer& d, int H, int NC) {
   std::memset(d.n_grp, 0, sizeof(d.n_grp));
   std::memset(d.routed, 0, sizeof(d.routed));
   if (d.Fs < 0 || d.K < 0 || d.E < 0) return false;
-  // a group of down width W with parts of n outputs per CTA fits its buffer
-  auto fits = [&](int n, int W, int np, bool routed) {
-    if (n < 4 || n > dc::kMaxN || (n & 3) || W > dc::kMaxW || W < 64) return false;
-    return dc::GroupOff::of(n, W, np, H).bytes <= (uint32_t)(dc::kBigBytes - (routed ? dc::kRouterBytes : 0));
-  };
   if (d.K > 0) {
     const int RR = decode_router_rows(d.E);
     if (d.E > dc::kMaxE || d.K > d.E || d.K > FLINT_MAX_TOP_K) return false;
     if (RR > dc::kMaxRR || (size_t)2 * RR * H > (size_t)dc::kRouterBytes) return false;
-    if (d.F < 64 || (d.F & (d.F - 1)) || !fits(d.F / dc::kCS, d.F, 1, true)) return false;
+    const int n = d.F / dc::kCS;
+    if (d.F < 64 || (d.F & (d.F - 1)) || n > dc::kMaxN || d.F > dc::kMaxW) return false;
   }
-  int S = 0;                                         // shared parts
-  if (d.Fs > 0) {
-    if (d.Fs < 64 || (d.Fs & (d.Fs - 1))) return false;
-    d.Wsh = d.K > 0 ? (d.F < d.Fs ? d.F : d.Fs) : (d.Fs < 512 ? d.Fs : 512);
-    S = d.Fs / d.Wsh;
-  } else {
-    d.Wsh = 0;
-  }
-  if (d.K + S == 0) return false;
   // Routed experts on clusters [0, NR), one cluster per selected expert when there are
-  // enough (a cluster takes a second one otherwise); the shared parts, as contiguous
-  // runs, on the other clusters, or with none left ahead of the routed groups (they do
-  // not depend on the router).
+  // enough (a cluster takes a second one otherwise).
   int NR = 0;
   if (d.K > 0) {
-    NR = d.K < (S > 0 ? NC - 1 : NC) ? d.K : (S > 0 ? NC - 1 : NC);
+    NR = d.K < (d.Fs > 0 ? NC - 1 : NC) ? d.K : (d.Fs > 0 ? NC - 1 : NC);
     if (NR < 1) NR = 1;
   }
   const int NS = NC - NR;
-  if (S > 0) {
-    const int nc = NS > 0 ? NS : NC;                 // clusters sharing the parts
-    const int base = NS > 0 ? NR : 0;
-    const int used = S < nc ? S : nc;
-    int p = 0;
-    for (int i = 0; i < used; ++i) {
-      const int cnt = S / used + (i < S % used ? 1 : 0);
-      const int cc = base + i;
-      if (d.n_grp[cc] >= kDecMaxGroups) return false;
-      if (!fits(d.Wsh / dc::kCS, cnt * d.Wsh, cnt, NS == 0 && d.K > 0)) return false;
+  int n_routed[kDecMaxClusters] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int s = 0; s < d.K; ++s) ++n_routed[s % NR];
+  for (int cc = 0; cc < NC; ++cc)
+    if (n_routed[cc] > kDecMaxGroups) return false;
+  // The shared expert in parts of Wsh outputs, as contiguous runs on the clusters
+  // without a routed expert (a group costs a few microseconds of fixed latency, so few
+  // large groups beat many small ones); with no such cluster, on the routed clusters
+  // with a free group, ahead of their routed groups.
+  int sh_np[kDecMaxClusters] = {0, 0, 0, 0, 0, 0, 0, 0};
+  d.Wsh = 0;
+  if (d.Fs > 0) {
+    if (d.Fs < 64 || (d.Fs & (d.Fs - 1))) return false;
+    int hosts[kDecMaxClusters], nh = 0;
+    for (int cc = NR; cc < NC; ++cc) hosts[nh++] = cc;
+    if (nh == 0)
+      for (int cc = 0; cc < NR; ++cc)
+        if (n_routed[cc] < kDecMaxGroups) hosts[nh++] = cc;
+    if (nh == 0) return false;
+    // parts of at most 512 outputs (and of the routed width when there is one); at most
+    // one run per host
+    int w = d.K > 0 ? (d.F < d.Fs ? d.F : d.Fs) : (d.Fs < 512 ? d.Fs : 512);
+    if (w > 512) w = 512;
+    d.Wsh = w;
+    const int S = d.Fs / d.Wsh;
+    const int used = S < nh ? S : nh;
+    for (int i = 0; i < used; ++i) sh_np[hosts[i]] = S / used + (i < S % used ? 1 : 0);
+  }
+  if (d.K == 0 && d.Fs == 0) return false;
+  const uint32_t routed_bytes = d.K > 0 ? dc::GroupOff::of(d.F / dc::kCS, d.F, 1, H).bytes : 0u;
+  d.sh_off = (uint32_t)((dc::kRouterBytes > routed_bytes ? dc::kRouterBytes : routed_bytes) + 127) & ~127u;
+  if (d.K > 0 && routed_bytes > (uint32_t)dc::kBigBytes) return false;
+  int p = 0;
+  for (int cc = 0; cc < NC; ++cc) {
+    if (sh_np[cc] > 0) {
+      const int n = d.Wsh / dc::kCS, W = sh_np[cc] * d.Wsh;
+      if (n < 4 || n > dc::kMaxN || (n & 3) || W > dc::kMaxW) return false;
+      const uint32_t base = n_routed[cc] > 0 ? d.sh_off : 0u;
+      if (base + dc::GroupOff::of(n, W, sh_np[cc], H).bytes > (uint32_t)dc::kBigBytes) return false;
       const int g = d.n_grp[cc]++;
       d.rank[cc][g] = -1;
-      d.np[cc][g] = (unsigned char)cnt;
+      d.np[cc][g] = (unsigned char)sh_np[cc];
       d.p0[cc][g] = (unsigned char)p;
-      p += cnt;
+      p += sh_np[cc];
     }
   }
   for (int s = 0; s < d.K; ++s) {

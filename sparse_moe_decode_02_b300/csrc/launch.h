@@ -39,7 +39,8 @@ struct DecLayer {
   unsigned char p0[kDecMaxClusters][kDecMaxGroups];
   unsigned char n_grp[kDecMaxClusters];
   unsigned char routed[kDecMaxClusters];   // cluster computes the router and top-k
-  int pad_[2];
+  unsigned sh_off;                   // shared groups' buffer offset in a routed cluster
+  int pad_;
 };
 
 struct DecodeArgs {
