@@ -354,6 +354,9 @@ flint_status flint_moe_prefill(const flint_moe_layer* L, const void* x_bf16, flo
   a.idx_out = topk_idx; a.w_out = topk_w;
   a.counts_out = expert_counts; a.order_out = pair_order;
   for (int i = 0; i < 6; ++i) a.sf[i] = L->mma_scales[i];
+  a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  a.hold = t_hold == 2 ? 1 : 0;
+  if (t_hold == 2) t_hold = 0;
   return from_cuda(flint::launch_prefill(a, ws, static_cast<cudaStream_t>(stream)));
 }
 

@@ -24,7 +24,8 @@ __device__ __forceinline__ void raise_status(unsigned int code) {
   atomicCAS(&g_status, 0u, code);
 }
 
-// Bounded wait budget for any spin on a flag/counter/mbarrier: ~2 s of %globaltimer.
+// Default bound of any spin on a flag/counter/mbarrier: 2 s of %globaltimer (the library's
+// decode and prompt kernels take the runtime bound of flint_set_wait_limit_ns instead).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ unsigned long long globaltimer() {

@@ -91,6 +91,8 @@ struct PrefillArgs {
   int32_t* order_out;
   const uint8_t* sf[6];    // MMA scale copies: gate, up, down, sh_gate, sh_up, sh_down
   int router_score;        // FLINT_ROUTER_SOFTMAX / FLINT_ROUTER_SIGMOID
+  unsigned long long wait_ns;   // bound of every device-side wait
+  int hold;                     // test aid: withhold the gate/up GEMM's first stage in CTA 0
 };
 
 size_t prefill_workspace_bytes(int H, int E, int K, int F, int Fs, int T);

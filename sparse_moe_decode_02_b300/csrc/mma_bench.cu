@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fp4_mma_bench(int mode, int ite
     }
     __syncwarp();
     int abort_flag = 0;
-    pf::mb_wait(&done, 0, &abort_flag);
+    pf::mb_wait(&done, 0, &abort_flag, kWaitLimitNs);
   } else {
     // D = columns [0, 32) (mode 4: [32 c, 32 c + 32) for chain c); A scales at 64 + 4 s,
     // B scales at 128 + 4 s (s = K step)
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fp4_mma_bench(int mode, int ite
       }
       __syncwarp();
       int abort_flag = 0;
-      pf::mb_wait(&done, phase, &abort_flag);
+      pf::mb_wait(&done, phase, &abort_flag, kWaitLimitNs);
       phase ^= 1u;
       pf::tc_fence_after();
       uint32_t r[16];

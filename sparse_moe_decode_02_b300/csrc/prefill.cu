@@ -98,6 +98,8 @@ struct GemmArgs {
   const int32_t* order;         // padded routed row -> pair id
   const float* wpair;           // [T*K]
   int H, K;
+  unsigned long long wait_ns;   // bound of every wait
+  int hold;                     // test aid: CTA 0's copy issuer withholds its first stage
 };
 
 // ---------------------------------------------------------------- primitives
@@ -130,8 +132,10 @@ __device__ __forceinline__ void mb_arrive(uint64_t* b) {
 __device__ __forceinline__ void mb_expect(uint64_t* b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(sh(b)), "r"(bytes) : "memory");
 }
-// Bounded parity wait; false on expiry (FLINT_ERR_TIMEOUT recorded, *abort set).
-__device__ __forceinline__ bool mb_wait(uint64_t* b, uint32_t parity, volatile int* abort) {
+// Bounded parity wait (limit in ns of %globaltimer); false on expiry (FLINT_ERR_TIMEOUT
+// recorded, *abort set) or once *abort is set.
+__device__ __forceinline__ bool mb_wait(uint64_t* b, uint32_t parity, volatile int* abort,
+                                        unsigned long long limit) {
   unsigned long long t0 = 0;
   for (unsigned i = 0;; ++i) {
     uint32_t ok;
@@ -142,7 +146,7 @@ __device__ __forceinline__ bool mb_wait(uint64_t* b, uint32_t parity, volatile i
       if (*abort) return false;
       const unsigned long long now = globaltimer();
       if (t0 == 0) t0 = now;
-      else if (now - t0 > kWaitLimitNs) {
+      else if (now - t0 > limit) {
         raise_status(FLINT_ERR_TIMEOUT);
         *abort = 1;
         return false;
@@ -269,6 +273,9 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
 
   if (warp == kWarpTMA && lane == 0) {
     uint32_t it = 0;
+    int last[S];                                  // per stage slot: the last issued iteration
+#pragma unroll
+    for (int s = 0; s < S; ++s) last[s] = -1;
     Item nxt = blockIdx.x < n_items ? load_item(g.items + blockIdx.x) : Item{0, 0, 0, 0};
     for (int i = blockIdx.x; i < n_items && !abort_flag; i += gridDim.x) {
       const Item item = nxt;
@@ -278,7 +285,9 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
       const uint8_t* sfa = g.sfA[item.kind()] + (size_t)(item.row0 >> 7) * ksteps * 512;
       for (int kt = 0; kt < K / 256; ++kt, ++it) {
         const int s = it % S;
-        if (it >= S && !mb_wait(&empty[s], ((it / S) - 1) & 1, &abort_flag)) break;
+        if (it >= S && !mb_wait(&empty[s], ((it / S) - 1) & 1, &abort_flag, g.wait_ns)) break;
+        if (g.hold && blockIdx.x == 0 && it == 0) continue;   // withheld: its phase never completes
+        last[s] = (int)it;
         uint8_t* st = smem + s * C::stride;
         mb_expect(&full[s], C::bytes);
         tma2d(st + C::a, &g.mapA[item.kind()], kt * 128, item.row0, &full[s]);
@@ -291,6 +300,13 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
         }
       }
     }
+    // after an expired wait: the stages issued but not consumed land before the CTA exits
+    if (abort_flag) {
+      volatile int no_abort = 0;
+#pragma unroll
+      for (int s = 0; s < S; ++s)
+        if (last[s] >= 0) mb_wait(&full[s], (last[s] / S) & 1, &no_abort, g.wait_ns);
+    }
   } else if (warp == kWarpMMA && lane == 0) {
     const uint64_t dA0 = umma_desc_sw128(sh(smem + C::a)), dB0 = umma_desc_sw128(sh(smem + C::b));
     const uint64_t dSA0 = sf_desc(sh(smem + C::sfa)), dSB0 = sf_desc(sh(smem + C::sfb));
@@ -300,12 +316,12 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
       const Item item = nxt;
       if (i + (int)gridDim.x < n_items) nxt = load_item(g.items + i + gridDim.x);
       const int kt_n = g.Kel[item.kind()] / 256;
-      if (done > 0 && !mb_wait(&acce, (done - 1) & 1, &abort_flag)) break;
+      if (done > 0 && !mb_wait(&acce, (done - 1) & 1, &abort_flag, g.wait_ns)) break;
       tc_fence_after();
       bool ok = true;
       for (int kt = 0; kt < kt_n; ++kt, ++it) {
         const int s = it % S;
-        if (!mb_wait(&full[s], (it / S) & 1, &abort_flag)) { ok = false; break; }
+        if (!mb_wait(&full[s], (it / S) & 1, &abort_flag, g.wait_ns)) { ok = false; break; }
         tc_fence_after();
         // descriptors of stage s: the stage-0 ones plus the stage offset (address field)
         const uint64_t so = (uint64_t)(s * (C::stride >> 4));
@@ -341,7 +357,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
     for (int i = blockIdx.x; i < n_items && !abort_flag; i += gridDim.x, ++done) {
       const Item item = nxt;
       if (i + (int)gridDim.x < n_items) nxt = load_item(g.items + i + gridDim.x);
-      if (!mb_wait(&accf, done & 1, &abort_flag)) break;
+      if (!mb_wait(&accf, done & 1, &abort_flag, g.wait_ns)) break;
       tc_fence_after();
       const bool valid = r < item.rows;
       const int arow = item.row0 + r;
@@ -441,7 +457,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       tc_commit(&drain);
       volatile int no_abort = 0;
-      mb_wait(&drain, 0, &no_abort);
+      mb_wait(&drain, 0, &no_abort, g.wait_ns);
     }
     __syncwarp();
     tc_fence_after();
@@ -613,6 +629,7 @@ struct RouterArgs {
   CUtensorMap mapW;
   float* part;             // [kRSplit][T][E]
   int T, E, H;
+  unsigned long long wait_ns;
 };
 
 __global__ void __launch_bounds__(kRThreads, 1) k_router_gemm(const __grid_constant__ RouterArgs g) {
@@ -645,7 +662,7 @@ __global__ void __launch_bounds__(kRThreads, 1) k_router_gemm(const __grid_const
   if (warp == kWarpTMA && lane == 0) {
     for (int kt = 0; kt < kt_n; ++kt) {
       const int s = kt % kRStages;
-      if (kt >= kRStages && !mb_wait(&empty[s], ((kt / kRStages) - 1) & 1, &abort_flag)) break;
+      if (kt >= kRStages && !mb_wait(&empty[s], ((kt / kRStages) - 1) & 1, &abort_flag, g.wait_ns)) break;
       uint8_t* st = smem + s * kStageBytes;
       mb_expect(&full[s], stage_bytes);
       tma2d(st, &g.mapX, (kt0 + kt) * 128, row0, &full[s]);
@@ -656,7 +673,7 @@ __global__ void __launch_bounds__(kRThreads, 1) k_router_gemm(const __grid_const
     bool ok = true;
     for (int kt = 0; kt < kt_n; ++kt) {
       const int s = kt % kRStages;
-      if (!mb_wait(&full[s], (kt / kRStages) & 1, &abort_flag)) { ok = false; break; }
+      if (!mb_wait(&full[s], (kt / kRStages) & 1, &abort_flag, g.wait_ns)) { ok = false; break; }
       tc_fence_after();
       const uint64_t so = (uint64_t)(s * (kStageBytes >> 4));
 #pragma unroll
@@ -668,7 +685,7 @@ __global__ void __launch_bounds__(kRThreads, 1) k_router_gemm(const __grid_const
   } else if (warp >= 4) {
     const int q = warp & 3;
     const int t = row0 + q * 32 + lane;
-    if (mb_wait(&accf, 0, &abort_flag)) {
+    if (mb_wait(&accf, 0, &abort_flag, g.wait_ns)) {
       tc_fence_after();
       float* dst = g.part + ((size_t)ks * g.T + t) * g.E;
       for (int c0 = 0; c0 < g.E; c0 += 16) {
@@ -692,7 +709,7 @@ __global__ void __launch_bounds__(kRThreads, 1) k_router_gemm(const __grid_const
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       tc_commit(&drain);
       volatile int no_abort = 0;
-      mb_wait(&drain, 0, &no_abort);
+      mb_wait(&drain, 0, &no_abort, g.wait_ns);
     }
     __syncwarp();
     tc_fence_after();
@@ -1113,6 +1130,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st) {
   RouterArgs ra;
   memset(&ra, 0, sizeof(ra));
   ra.part = reinterpret_cast<float*>(at(L.logits)); ra.T = T; ra.E = E; ra.H = H;
+  ra.wait_ns = a.wait_ns;
   if (!make_map(&ra.mapX, a.x, T, (uint64_t)H * 2, kBM) || !make_map(&ra.mapW, a.router_w, E, (uint64_t)H * 2, E))
     return cudaErrorInvalidValue;
   const int smem_r = kRStages * (16384 + 256 * 128) + 1024;
@@ -1162,6 +1180,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st) {
   gu.hcodes[1] = reinterpret_cast<uint8_t*>(at(L.hq_c)); gu.hsf[1] = reinterpret_cast<uint8_t*>(at(L.hq_s));
   gu.Fout[0] = Fs; gu.Fout[1] = F;
   gu.H = H; gu.K = K;
+  gu.wait_ns = a.wait_ns;
+  gu.hold = a.hold;
   e = cudaFuncSetAttribute(k_gemm_fp4<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kGateUp>::smem);
   if (e != cudaSuccess) return e;
   k_gemm_fp4<kGateUp><<<sms, kGThreads, Cfg<kGateUp>::smem, st>>>(gu);
@@ -1182,6 +1202,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st) {
   dn.out = a.out; dn.x = a.x; dn.yp = reinterpret_cast<uint16_t*>(at(L.yp));
   dn.order = sa.order_pad; dn.wpair = r.w;
   dn.H = H; dn.K = K;
+  dn.wait_ns = a.wait_ns;
   e = cudaFuncSetAttribute(k_gemm_fp4<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kDown>::smem);
   if (e != cudaSuccess) return e;
   k_gemm_fp4<kDown><<<sms, kGThreads, Cfg<kDown>::smem, st>>>(dn);

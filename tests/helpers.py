@@ -17,26 +17,28 @@ def bits16(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def oracle_stack(orc, spec: synth.LayerSpec, kind: int, experts):
-    """NVFP4 stack for one matrix kind; only `experts` are generated (others zero)."""
+def oracle_stack(orc, spec: synth.LayerSpec, kind: int, experts, gen_device="cpu"):
+    """NVFP4 stack for one matrix kind; only `experts` are generated (others zero).  The
+    seeded generator gives the same bits on any device (`gen_device` only sets where the
+    bf16 draws are made); the oracle quantises them itself."""
     n, r, c = spec.dims(kind)
     codes = np.zeros((n, r, c // 2), np.uint8)
     scales = np.zeros((n, r, c // 16), np.uint8)
     tsc = np.ones(n, np.float32)
     for e in sorted(set(int(e) for e in experts)):
-        q, st = orc.quantize_nvfp4(spec.weights_bf16(kind, experts=[e]))
+        q, st = orc.quantize_nvfp4(spec.weights_bf16(kind, device=gen_device, experts=[e]).cpu())
         assert st == 0
         codes[e], scales[e], tsc[e] = q.codes[0], q.scales[0], q.tsc[0]
     return orc.NVFP4(codes, scales, tsc)
 
 
-def oracle_layer(orc, spec: synth.LayerSpec, experts=None):
+def oracle_layer(orc, spec: synth.LayerSpec, experts=None, gen_device="cpu"):
     """Oracle-side layer built from the same seeded bf16 tensors as the device layer."""
     s = spec.shape
     E = s.n_experts
     experts = range(E) if experts is None else experts
-    router = bits16(spec.weights_bf16(synth.KIND_ROUTER)[0])
-    mk = lambda kind, ex: oracle_stack(orc, spec, kind, ex)
+    router = bits16(spec.weights_bf16(synth.KIND_ROUTER, device=gen_device)[0])
+    mk = lambda kind, ex: oracle_stack(orc, spec, kind, ex, gen_device)
     return orc.Layer(router, spec.bias(), mk(synth.KIND_GATE, experts),
                      mk(synth.KIND_UP, experts), mk(synth.KIND_DOWN, experts),
                      mk(synth.KIND_SH_GATE, [0]), mk(synth.KIND_SH_UP, [0]),

@@ -69,23 +69,37 @@ def test_prefill_mid_all_tokens(orc, T, zipf, score):
 def test_prefill_flint_config(orc):
     """The Flint prompt-processing layer: 4096 tokens, 256 experts top-6 with a Zipf(1.1)
     router bias, shared expert 1024.  Routing, counts and order on every token; the
-    outputs of a sample of tokens against the oracle."""
+    outputs of the first and the last token of every 128-row tile of every expert's
+    token list (where the grouped GEMM masks a partial tile) and of every tile of the
+    shared expert, against the oracle."""
     shape = synth.FLINT
-    T = 4096
+    T, E, k = 4096, shape.n_experts, shape.top_k
     spec = synth.LayerSpec(shape, seed=0, zipf=1.1)
     layer = workload.build_layer(spec, DEV)
     x = synth.tokens_bf16(0, shape.hidden, T, stream=9)
-    out, gidx, gw, counts, order = _prefill(layer, x.to(DEV), shape.n_experts, shape.top_k)
+    out, gidx, gw, counts, order = _prefill(layer, x.to(DEV), E, k)
     xb = bits16(x)
     logits, oidx, ow = oracle_routes(orc, spec, xb)
-    ok = check_routing(gidx, gw, logits, oidx, ow, shape.top_k)
-    _check_bookkeeping(orc, gidx, counts, order, shape.n_experts)
-    sample = np.array([0, 1, 127, 128, 2047, 4000, 4094, 4095])
+    ok = check_routing(gidx, gw, logits, oidx, ow, k)
+    _check_bookkeeping(orc, gidx, counts, order, E)
+    offs = np.concatenate([[0], np.cumsum(counts)[:-1]])
+    pick = set()
+    for e in range(E):
+        for r0 in range(0, int(counts[e]), 128):
+            r1 = min(r0 + 127, int(counts[e]) - 1)
+            pick.add(int(order[offs[e] + r0]) // k)
+            pick.add(int(order[offs[e] + r1]) // k)
+    for r0 in range(0, T, 128):
+        pick.update((r0, min(r0 + 127, T - 1)))
+    sample = np.array(sorted(pick))
+    tiles = sum((int(c) + 127) // 128 for c in counts)
     sample = sample[ok[sample]]
-    L = oracle_layer(orc, spec, experts=np.unique(oidx[sample]))
+    assert len(sample) >= tiles // 2
+    L = oracle_layer(orc, spec, experts=np.unique(oidx[sample]), gen_device=DEV)
     oout, _, _ = orc.moe_forward(L, xb[sample], quantize_acts=True)
     xd = x.double().numpy()[sample]
-    assert_close(out[sample] - xd, oout - xd, "prefill MoE delta (sampled)")
+    for i, t in enumerate(sample):
+        assert_close(out[t] - xd[i], oout[i] - xd[i], "prefill MoE delta, token %d" % t)
     # and close to the unquantised layer (the activation quantisation error only)
     plain, _, _ = orc.moe_forward(L, xb[sample])
     rel = np.linalg.norm((out[sample] - xd) - (plain - xd)) / np.linalg.norm(plain - xd)
