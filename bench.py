@@ -35,12 +35,44 @@ ZIPF = 1.1
 PREFILL_TOKENS = 4096
 
 
+NOMINAL_FP4_TFLOPS = 13500.0     # dense NVFP4 per GPU, NVIDIA's figure (without 2:4 sparsity)
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
         return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"), "src": "measured"}
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "src": "fallback"}
+
+
+def _sha1(path):
+    import hashlib
+    return hashlib.sha1(open(path, "rb").read()).hexdigest()
+
+
+def decode_traffic(tokens: int, layers: int):
+    """DRAM bytes (read + write) of one decode launch from the committed ncu capture
+    (profiles/k_decode_dram.md: a smaller launch of the same kernel, scaled by the
+    token-layers and head passes it processes), or None when the kernel source changed
+    since the capture."""
+    p = os.path.join(ROOT, "profiles", "k_decode_dram.md")
+    if not os.path.exists(p):
+        return None
+    fields = {}
+    for ln in open(p):
+        if ln.startswith("- ") and ":" in ln:
+            k, v = ln[2:].split(":", 1)
+            fields[k.strip()] = v.strip().split()[0]
+    src = os.path.join(ROOT, "sparse_moe_decode_02_b300", "csrc", "decode.cu")
+    if fields.get("decode.cu sha1") != _sha1(src):
+        return None
+    try:
+        per_tl = float(fields["dram bytes per token-layer"])
+        per_head = float(fields["dram bytes per head pass"])
+    except (KeyError, ValueError):
+        return None
+    return tokens * (layers * per_tl + per_head)
 
 
 class ClockSampler:
@@ -222,14 +254,17 @@ def run_flint(args):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "k_decode_persistent (flint_decode_tokens: %d tokens x %d layers + head)"
+            "kernel": "k_decode<2> (flint_decode_tokens: %d tokens x %d layers + head)"
                       % (T, args.layers),
             "achieved": round(achieved, 1),
             "peak": peaks["hbm_gbs"],
             "peak_src": peaks["src"],
             "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "traffic": None,
+            "traffic": decode_traffic(T, args.layers),
+            "traffic_src": "profiles/k_decode_dram.md (ncu dram__bytes_read.sum + "
+                           "dram__bytes_write.sum of a smaller launch, scaled per token-layer "
+                           "and head pass; null if decode.cu changed since)",
             "algorithmic_bytes_per_launch": launch_bytes,
             "algorithmic_bytes_per_token": token_bytes,
             "launch_ms": round(launch_ms, 4),
@@ -242,17 +277,119 @@ def run_flint(args):
         "clocks": clk.summary(),
         "device_status": status,
         "prefill": None,
-        "sampling": measure_sampling(dev),
     }
-    if not args.no_prefill:
-        del layers, head
-        torch.cuda.empty_cache()
-        result["prefill"] = measure_prefill(dev)
-    if rank == 0 and not args.no_cpu_baseline:
+    if not args.decode_only:
+        result["sampling"] = measure_sampling(dev)
+        result["config3_lm_head"] = measure_lm_head(dev, head)
+    del layers, head
+    torch.cuda.empty_cache()
+    if not args.decode_only:
+        result["config2_layer"] = measure_layer(dev)
+        fp4 = measure_fp4_peak(dev)
+        result["fp4_peak"] = fp4
+        if not args.no_prefill:
+            result["prefill"] = measure_prefill(dev, fp4_tflops=fp4["tflops"])
+    if rank == 0 and not args.no_cpu_baseline and not args.decode_only:
         result["cpu_baseline"] = cpu_baseline(args)
     if world > 1:
         dist.destroy_process_group()
     return result if rank == 0 else None
+
+
+def _time_ms(fn, reps, stream=None, inner=1):
+    """Median ms of one `fn` call over `reps` timed runs of `inner` back-to-back calls
+    (CUDA events on the current stream)."""
+    import torch
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(inner):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / inner)
+    return statistics.median(times)
+
+
+def measure_lm_head(dev, head, reps: int = 10):
+    """The standalone NVFP4 lm_head (flint_lm_head): 150,144 x 2048 weights, batch 1 and
+    batch 8, fp32 logits plus argmax; ten calls back to back per timed run.  The 173 MB of
+    weights exceed L2, so every call streams them from HBM."""
+    import torch
+
+    from sparse_moe_decode_02_b300 import flint, synth, workload
+
+    shape = synth.FLINT
+    H, V = shape.hidden, shape.vocab
+    peaks = _peaks()
+    wbytes = workload.head_bytes(V, H)
+    res = {"workload": "NVFP4 lm_head %d x %d, fp32 logits + argmax" % (V, H)}
+    for B in (1, 8):
+        x = synth.tokens_bf16(SEED, H, B, stream=21, device=dev)
+        lg = torch.empty(B, V, dtype=torch.float32, device=dev)
+        am = torch.empty(B, dtype=torch.int32, device=dev)
+        for _ in range(3):
+            flint.lm_head(head, x, logits=lg, argmax=am)
+        torch.cuda.synchronize()
+        ws = torch.empty(flint.workspace_bytes(flint.OP_LM_HEAD, H, 0, 0, 0, 0, V, B),
+                         dtype=torch.uint8, device=dev)
+        ms = _time_ms(lambda: flint.lm_head(head, x, logits=lg, argmax=am, ws=ws), reps, inner=10)
+        moved = wbytes + B * (H * 2 + V * 4 + 4)
+        gbs = moved / (ms * 1e-3) / 1e9
+        res["B%d" % B] = {"value": round(B / (ms * 1e-3), 1), "unit": "tok/s",
+                          "us": round(ms * 1e3, 2), "bytes": moved, "GBs": round(gbs, 1),
+                          "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+    res["kernel"] = "k_lm_head (profiles/k_lm_head_dram.md)"
+    return res
+
+
+def measure_layer(dev, reps: int = 5):
+    """One Flint MoE layer (no router bias), batch 1, 1000 seeded tokens one after another
+    in one flint_decode_tokens launch: tokens/s and bytes per token (router 1 MB + 6
+    routed experts + shared expert = 15,204,352 B)."""
+    import torch
+
+    from sparse_moe_decode_02_b300 import flint, synth, workload
+
+    shape = synth.FLINT
+    H, T = shape.hidden, 1000
+    layer = workload.build_layer(synth.LayerSpec(shape, seed=SEED, layer=0), dev)
+    x = synth.tokens_bf16(SEED, H, T, stream=2, device=dev)
+    out = torch.empty(T, H, dtype=torch.float32, device=dev)
+    for _ in range(2):
+        flint.decode_tokens([layer], x, out=out)
+    torch.cuda.synchronize()
+    ms = _time_ms(lambda: flint.decode_tokens([layer], x, out=out), reps)
+    per_tok = workload.layer_bytes_per_token(shape)
+    gbs = per_tok * T / (ms * 1e-3) / 1e9
+    peaks = _peaks()
+    del layer
+    return {"workload": "one Flint MoE layer (H=2048, E=256 top-6, F=512, shared 1024), "
+                        "batch 1, %d tokens per launch" % T,
+            "value": round(T / (ms * 1e-3), 1), "unit": "tok/s", "ms": round(ms, 4),
+            "us_per_token": round(ms * 1e3 / T, 3), "bytes_per_token": per_tok,
+            "GBs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "note": "consecutive tokens of one layer reuse experts already in L2 (453 MB of "
+                    "routed weights, 126 MB L2): DRAM traffic is below the algorithmic bytes"}
+
+
+def measure_fp4_peak(dev, iters: int = 20000):
+    """Block-scaled FP4 tensor-core throughput (flint_bench_fp4_mma mode 0: M = 128,
+    N = 128, K = 64 tcgen05.mma kind::mxf4nvf4 back to back, operands in shared memory
+    and TMEM) on every SM, timed with CUDA events."""
+    import torch
+
+    from sparse_moe_decode_02_b300 import flint
+
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    flint.bench_fp4_mma(0, 200, sms)
+    torch.cuda.synchronize()
+    ms = _time_ms(lambda: flint.bench_fp4_mma(0, iters, sms), 3)
+    flop = sms * iters * 8 * 2.0 * 128 * 128 * 64
+    return {"tflops": round(flop / (ms * 1e-3) / 1e12, 1), "ctas": sms, "iters": iters,
+            "ms": round(ms, 3), "nominal_tflops": NOMINAL_FP4_TFLOPS,
+            "shape": "tcgen05.mma kind::mxf4nvf4 block16, M=128 N=128 K=64, 8 per iteration"}
 
 
 def measure_sampling(dev, reps: int = 20):
@@ -286,7 +423,7 @@ def measure_sampling(dev, reps: int = 20):
     return res
 
 
-def measure_prefill(dev, reps: int = 10):
+def measure_prefill(dev, reps: int = 10, fp4_tflops: float | None = None):
     """Prompt processing on one Flint layer: 4096 tokens, Zipf(1.1) router bias."""
     import torch
 
@@ -327,7 +464,8 @@ def measure_prefill(dev, reps: int = 10):
     weight_bytes = touched * 3 * nv(H * F) + 3 * nv(H * Fs) + shape.n_experts * H * 2
     bytes_ = weight_bytes + T * H * 2 + T * H * 4
     peaks = _peaks()
-    fp4_peak = peaks["bf16_tflops"] * 6.0                              # nominal fp4/bf16 = 6
+    # the larger of the measured tcgen05 FP4 peak and NVIDIA's dense figure
+    fp4_peak = max(fp4_tflops or 0.0, NOMINAL_FP4_TFLOPS)
     tflops = flops / (ms * 1e-3) / 1e12
     del layer, ws, flush
     return {
@@ -335,7 +473,8 @@ def measure_prefill(dev, reps: int = 10):
         "value": round(T / (ms * 1e-3), 1), "unit": "tok/s", "ms": round(ms, 4),
         "fp4_gflop": round(flops / 1e9, 1), "router_gflop": round(router_flops / 1e9, 2),
         "tflops": round(tflops, 1), "fp4_peak_tflops": round(fp4_peak, 1),
-        "fp4_peak_src": "measured bf16 %s x 6 (nominal FP4/BF16 dense ratio)" % peaks["src"],
+        "fp4_peak_src": "max(measured tcgen05 mxf4nvf4 %s TF/s, NVIDIA dense %s TF/s)" % (
+            fp4_tflops, NOMINAL_FP4_TFLOPS),
         "frac_fp4_peak": round(tflops / fp4_peak, 4),
         "experts_touched": touched, "bytes": bytes_,
         "frac_hbm": round(bytes_ / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
@@ -344,62 +483,124 @@ def measure_prefill(dev, reps: int = 10):
 
 
 # ------------------------------------------------------------------------------ oracle arm
-def oracle_decode_sample(n_tokens: int, n_layers: int):
-    """Times the CPU oracle on `n_tokens` tokens (processed together: the oracle threads
-    over tokens) through the first `n_layers` chained layers and the head.  Returns
-    (seconds of oracle compute per token through all 47 layers + head, threads used,
-    description).  Weight generation is excluded from the timing."""
+def _gen_device():
+    """Where the seeded bf16 draws are made for the oracle (the same bits on any device;
+    only the oracle's own arithmetic is timed)."""
+    try:
+        import torch
+        return "cuda" if torch.cuda.is_available() else "cpu"
+    except ImportError:
+        return "cpu"
+
+
+class OracleDecode:
+    """The CPU oracle decoding `n_tokens` tokens (processed together: the oracle threads
+    over tokens) through the 47 chained Flint layers and the 150,144-row head.  The
+    weights each token's route needs are generated and quantised once (one untimed pass
+    over the chain finds the routes); run() times the oracle's arithmetic only."""
+
+    def __init__(self, n_tokens: int, n_layers: int = N_LAYERS):
+        import numpy as np
+
+        import oracle
+        from oracle import seeded
+        from sparse_moe_decode_02_b300 import synth
+
+        self.np, self.oracle = np, oracle
+        shape = synth.FLINT
+        gen = _gen_device()
+        self.n_tokens, self.n_layers = n_tokens, n_layers
+        self.x = seeded.bits16(synth.tokens_bf16(SEED, shape.hidden, n_tokens, stream=1))
+        self.layers = []
+        xb, h = self.x, None
+        for l in range(n_layers):
+            spec = synth.LayerSpec(shape, seed=SEED, layer=l, zipf=ZIPF)
+            _, idx, _ = seeded.routes(spec, xb)
+            L = seeded.layer(spec, experts=np.unique(idx), gen_device=gen)
+            h, _, _ = oracle.moe_forward(L, xb, residual=h)
+            xb = np.stack([oracle.rmsnorm_bf16(h[t], EPS) for t in range(n_tokens)])
+            self.layers.append(L)
+        self.head = seeded.head(SEED, shape.vocab, shape.hidden, gen)
+        self.threads = min(oracle.get_threads(), n_tokens)
+
+    def run(self) -> float:
+        """Seconds of oracle compute for the tokens through every layer and the head."""
+        np, oracle = self.np, self.oracle
+        t0 = time.perf_counter()
+        xb, h = self.x, None
+        for L in self.layers:
+            h, _, _ = oracle.moe_forward(L, xb, residual=h)
+            xb = np.stack([oracle.rmsnorm_bf16(h[t], EPS) for t in range(self.n_tokens)])
+        oracle.lm_head(self.head, xb)
+        return time.perf_counter() - t0
+
+    def sample(self) -> str:
+        return ("%d tokens (batched) x %d chained Flint layers (oracle-selected experts) + the "
+                "150144-row head, fp64; weight generation and quantisation not timed"
+                % (self.n_tokens, self.n_layers))
+
+
+def oracle_units(dec: OracleDecode, n_tokens: int = 16):
+    """CPU oracle rates of the other benchmarked configurations on bounded samples:
+    config 2 (one Flint layer, no bias), config 3 (the head, batch 1 and 8; reuses the
+    decode's head) and config 5 (the prompt layer with activation quantisation)."""
     import numpy as np
 
     import oracle
+    from oracle import seeded
     from sparse_moe_decode_02_b300 import synth
 
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from helpers import bits16, oracle_layer, oracle_routes
-
+    gen = _gen_device()
     shape = synth.FLINT
     H = shape.hidden
-    threads = min(oracle.get_threads(), n_tokens)
-    xb = bits16(synth.tokens_bf16(SEED, H, n_tokens, stream=1))
-    hres = None
-    layer_s = 0.0
-    for l in range(n_layers):
-        spec = synth.LayerSpec(shape, seed=SEED, layer=l, zipf=ZIPF)
-        _, idx, _ = oracle_routes(oracle, spec, xb)
-        L = oracle_layer(oracle, spec, experts=np.unique(idx))
-        t0 = time.perf_counter()
-        out, _, _ = oracle.moe_forward(L, xb, residual=hres)
-        xb = np.stack([oracle.rmsnorm_bf16(out[t], EPS) for t in range(n_tokens)])
-        layer_s += time.perf_counter() - t0
-        hres = out
-    hq, _ = oracle.quantize_nvfp4(synth.head_bf16(SEED, shape.vocab, H))
+    res = {}
+    x = seeded.bits16(synth.tokens_bf16(SEED, H, n_tokens, stream=2))
+    spec = synth.LayerSpec(shape, seed=SEED, layer=0)
+    _, idx, _ = seeded.routes(spec, x)
+    L = seeded.layer(spec, experts=np.unique(idx), gen_device=gen)
     t0 = time.perf_counter()
-    oracle.lm_head(hq, xb)
-    head_s = time.perf_counter() - t0
-    per_token = (layer_s / n_layers * N_LAYERS + head_s) / n_tokens
-    desc = ("%d tokens together x the first %d of 47 layers (oracle-selected experts), then "
-            "the full 150144-row head; per-token time = (mean layer time x 47 + head time) / "
-            "%d" % (n_tokens, n_layers, n_tokens))
-    return per_token, threads, desc
+    oracle.moe_forward(L, x)
+    s2 = time.perf_counter() - t0
+    res["config2_layer"] = {"value": round(n_tokens / s2, 3), "unit": "tok/s",
+                            "sample": "%d tokens of one Flint layer" % n_tokens}
+    for B in (1, 8):
+        xb = seeded.bits16(synth.tokens_bf16(SEED, H, B, stream=21))
+        t0 = time.perf_counter()
+        oracle.lm_head(dec.head, xb)
+        s3 = time.perf_counter() - t0
+        res["config3_lm_head_B%d" % B] = {"value": round(B / s3, 3), "unit": "tok/s",
+                                          "sample": "the full head, %d row(s) of x" % B}
+    spec5 = synth.LayerSpec(shape, seed=SEED, layer=0, zipf=ZIPF)
+    x5 = seeded.bits16(synth.tokens_bf16(SEED, H, n_tokens, stream=11))
+    _, idx5, _ = seeded.routes(spec5, x5)
+    L5 = seeded.layer(spec5, experts=np.unique(idx5), gen_device=gen)
+    t0 = time.perf_counter()
+    oracle.moe_forward(L5, x5, quantize_acts=True)
+    s5 = time.perf_counter() - t0
+    res["config5_prefill"] = {"value": round(n_tokens / s5, 3), "unit": "tok/s",
+                              "sample": "%d of the 4096 prompt tokens (activations quantised "
+                                        "to NVFP4 as the prompt path does)" % n_tokens}
+    return res
 
 
 def cpu_baseline(args):
-    per_tok, threads, desc = oracle_decode_sample(args.cpu_tokens, args.cpu_layers)
-    return {"value": round(1.0 / per_tok, 4), "unit": "tok/s", "cores": threads,
-            "kind": "oracle", "sample": desc}
+    dec = OracleDecode(args.cpu_tokens)
+    secs = dec.run()
+    out = {"value": round(dec.n_tokens / secs, 4), "unit": "tok/s", "cores": dec.threads,
+           "kind": "oracle", "sample": dec.sample(), "seconds": round(secs, 2)}
+    out["units"] = oracle_units(dec)
+    return out
 
 
 def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
         return None
-    times = []
-    threads, desc = None, None
-    for _ in range(args.warmup + args.steps):
-        per_tok, threads, desc = oracle_decode_sample(args.cpu_tokens, args.cpu_layers)
-        times.append(per_tok)
+    dec = OracleDecode(args.cpu_tokens)
+    times = [dec.run() for _ in range(args.warmup + args.steps)]
     timed = times[args.warmup:]
-    tok_s = 1.0 / statistics.mean(timed)
+    secs = statistics.mean(timed)
+    tok_s = dec.n_tokens / secs
     return {
         "impl": "reference",
         "metric": METRIC,
@@ -408,7 +609,7 @@ def run_reference(args):
         "n_gpus": 0,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(statistics.mean(timed) * 1e3, 2),
+        "ms_per_step": round(secs * 1e3, 2),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -416,8 +617,8 @@ def run_reference(args):
         "data": "synthetic (seeded, same generator as the flint arm)",
         "config": {"workload": "Flint FFN weight stream (47 layers + NVFP4 head), B=1 decode; "
                                "each step is a bounded sample, see cpu_baseline.sample"},
-        "cpu_baseline": {"value": round(tok_s, 4), "unit": "tok/s", "cores": threads,
-                         "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": round(tok_s, 4), "unit": "tok/s", "cores": dec.threads,
+                         "kind": "oracle", "sample": dec.sample()},
         "e2e": {"value": round(tok_s, 4), "unit": "tok/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -431,19 +632,33 @@ def main():
     ap.add_argument("--impl", default="flint", choices=["flint", "reference"])
     ap.add_argument("--tokens", type=int, default=N_TOKENS)
     ap.add_argument("--layers", type=int, default=N_LAYERS)
-    ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--cpu-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
-    ap.add_argument("--prefill-only", action="store_true",
-                    help="time only the prompt-processing layer (prints its object)")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="the decode line alone (no other measurements, no CPU baseline)")
+    ap.add_argument("--case", default=None, choices=["prefill", "layer", "lm_head", "fp4"],
+                    help="time one other configuration alone (prints its object)")
+    ap.add_argument("--prefill-only", action="store_true", help="same as --case prefill")
     args = ap.parse_args()
-    if args.prefill_only and args.impl == "flint":
+    if args.prefill_only:
+        args.case = "prefill"
+    if args.case and args.impl == "flint":
         import torch
         torch.cuda.set_device(0)
-        from sparse_moe_decode_02_b300 import flint
+        from sparse_moe_decode_02_b300 import flint, synth, workload
         flint.lib()
-        print(json.dumps(measure_prefill(torch.device("cuda", 0), reps=args.steps)), flush=True)
+        dev = torch.device("cuda", 0)
+        if args.case == "prefill":
+            res = measure_prefill(dev, reps=args.steps)
+        elif args.case == "layer":
+            res = measure_layer(dev, reps=args.steps)
+        elif args.case == "lm_head":
+            head = workload.build_head(SEED, synth.FLINT.vocab, synth.FLINT.hidden, dev)
+            res = measure_lm_head(dev, head, reps=args.steps)
+        else:
+            res = measure_fp4_peak(dev)
+        print(json.dumps(res), flush=True)
         return
     res = run_reference(args) if args.impl == "reference" else run_flint(args)
     if res is not None:

@@ -290,7 +290,9 @@ flint_status flint_decode_tokens_noalloc(const flint_moe_layer* layers, int n_la
  * products are NVFP4: x rows and the SwiGLU outputs h are quantised with the
  * recipe above and a unit tensor scale before their products.
  *   out[t] = x[t] + sum_j w_tj * y_{e_tj}(t) + y_shared(t)      (fp32 [T, H])
- * topk_idx / topk_w: optional [T, k] outputs.  expert_counts: optional int32 [E]
+ * The terms are added into out with fp32 reductions in no fixed order, so out may
+ * differ from run to run in its last bits (the decode entry points are bit-exact run
+ * to run).  topk_idx / topk_w: optional [T, k] outputs.  expert_counts: optional int32 [E]
  * output (tokens routed to each expert); pair_order: optional int32 [T*k] output,
  * the (t*k + j) pair ids in expert-major order, ascending t within an expert.
  * ws: flint_workspace_bytes(FLINT_OP_MOE_PREFILL, ...).
@@ -305,7 +307,9 @@ flint_status flint_moe_prefill(const flint_moe_layer* layer, const void* x_bf16,
  * "The shape, read from the headers" and "Why active parameters set the speed").
  * logits[b, v] = sum_k value(W[v, k]) x[b, k]  (fp32 [B, V]); argmax[b] = the
  * largest logit's index, ties to the lower index (int32 [B]).  Either output may
- * be NULL.  W: one matrix [1, V, H].  B <= FLINT_MAX_DECODE_TOKENS.
+ * be NULL.  W: one matrix [1, V, H], H a multiple of 128 (else FLINT_ERR_SHAPE).
+ * B <= FLINT_MAX_DECODE_TOKENS; the B tokens share one pass over W (products on
+ * mma.sync tensor cores with fp32 accumulation), so B = 8 reads the weights once.
  * ws: flint_workspace_bytes(FLINT_OP_LM_HEAD, ...).
  * -------------------------------------------------------------------------- */
 flint_status flint_lm_head(const flint_nvfp4* W, const void* x_bf16, float* logits,

@@ -290,7 +290,7 @@ flint_status flint_lm_head(const flint_nvfp4* W, const void* x_bf16, float* logi
   if (W->n_mat != 1 || W->rows <= 0 || W->cols <= 0) return FLINT_ERR_SHAPE;
   flint_status s = check_nvfp4(*W, 1, W->rows, W->cols);
   if (s != FLINT_OK) return s;
-  if (W->cols % 32) return FLINT_ERR_SHAPE;
+  if (W->cols % 128) return FLINT_ERR_SHAPE;
   if (!gemv_width_ok(W->cols)) return FLINT_ERR_UNSUPPORTED;
   if (!aligned16(x_bf16) || (logits && !aligned4(logits)) || (argmax && !aligned4(argmax)))
     return FLINT_ERR_ALIGNMENT;

@@ -11,15 +11,17 @@
 //                 device-side item lists
 //   4 scatter     per token: x quantised to NVFP4 once (unit tensor scale) and written
 //                 to the shared expert's operand Xq and to the K expert-major rows of Xp
-//                 (each expert's rows start on a 128-row tile); out[t] = x[t]
+//                 (each expert's rows start on a 128-row tile); out[t] = x[t] (fp32)
 //   5 gate/up     grouped GEMM, tcgen05 kind::mxf4nvf4 (E2M1 x E2M1, E4M3 scale per
 //                 16): per 128-row tile of one expert, the gate and up tiles accumulate
 //                 in TMEM; the epilogue applies the tensor scales, SwiGLU, and
 //                 quantises h to NVFP4 (unit tensor scale)
-//   6 down        grouped GEMM as 5 over the shared and the routed tiles; the shared
-//                 tiles write out = x + y, the routed tiles write w_pair * y as f16 rows
-//   7 combine     per token, out[t] += its K routed rows (slot order): the
-//                 un-permuting combine
+//   6 down        grouped GEMM as 5 over the shared and the routed tiles; the epilogue
+//                 adds y (shared rows) and w_pair * y (routed rows, at their token: the
+//                 un-permuting combine) into out with fp32 reductions (red.global.add),
+//                 so the routed rows never go to memory.  The adds into one element
+//                 commute but their order is not fixed: out may differ from run to run
+//                 in its last bits
 //
 // Every FP4 operand's block scales are kept in the MMA scale layout (512 bytes per
 // 128-row tile and 64 columns, see flint.h), so one pipeline stage of a GEMM is four
@@ -92,9 +94,7 @@ struct GemmArgs {
   uint8_t* hcodes[2];           // gate/up output codes: [0] shared h [Tp][Fs/2], [1] routed h
   uint8_t* hsf[2];              // gate/up output scales, MMA scale layout
   int Fout[2];
-  float* out;                   // [T][H]: shared-expert tiles write x + y here
-  const uint16_t* x;            // [T][H] bf16
-  uint16_t* yp;                 // [Pp][H] f16: routed rows, w_pair * y
+  float* out;                   // [T][H]: x (from the scatter), the down tiles add into it
   const int32_t* order;         // padded routed row -> pair id
   const float* wpair;           // [T*K]
   int H, K;
@@ -410,40 +410,20 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
         if (valid) {
           const float td = g.tscA[item.kind()][item.kind() ? item.expert() : 0];
           const int col = item.n0 + 64 * hf;
-          if (item.kind() == 0) {
-            // shared expert: out[t] = x[t] + y (the only write of these elements)
-            const uint16_t* xr = g.x + (size_t)arow * g.H + col;
-            float* o = g.out + (size_t)arow * g.H + col;
-#pragma unroll
-            for (int j = 0; j < 64; j += 8) {
-              const uint4 xb = *reinterpret_cast<const uint4*>(xr + j);
-              const uint32_t xw[4] = {xb.x, xb.y, xb.z, xb.w};
-              float4 lo, hi;
-              lo.x = bf16_bits_to_f32(xw[0] & 0xFFFFu) + y[j] * td;
-              lo.y = bf16_bits_to_f32(xw[0] >> 16) + y[j + 1] * td;
-              lo.z = bf16_bits_to_f32(xw[1] & 0xFFFFu) + y[j + 2] * td;
-              lo.w = bf16_bits_to_f32(xw[1] >> 16) + y[j + 3] * td;
-              hi.x = bf16_bits_to_f32(xw[2] & 0xFFFFu) + y[j + 4] * td;
-              hi.y = bf16_bits_to_f32(xw[2] >> 16) + y[j + 5] * td;
-              hi.z = bf16_bits_to_f32(xw[3] & 0xFFFFu) + y[j + 6] * td;
-              hi.w = bf16_bits_to_f32(xw[3] >> 16) + y[j + 7] * td;
-              *reinterpret_cast<float4*>(o + j) = lo;
-              *reinterpret_cast<float4*>(o + j + 4) = hi;
-            }
-          } else {
-            // routed row: w_pair * y as f16, summed per token by the combine kernel
-            const float scale = td * g.wpair[g.order[arow]];
-            uint16_t* yr = g.yp + (size_t)arow * g.H + col;
-#pragma unroll
-            for (int j = 0; j < 64; j += 8) {
-              uint4 pk;
-              pk.x = pack_f16x2_rn(y[j] * scale, y[j + 1] * scale);
-              pk.y = pack_f16x2_rn(y[j + 2] * scale, y[j + 3] * scale);
-              pk.z = pack_f16x2_rn(y[j + 4] * scale, y[j + 5] * scale);
-              pk.w = pack_f16x2_rn(y[j + 6] * scale, y[j + 7] * scale);
-              *reinterpret_cast<uint4*>(yr + j) = pk;
-            }
+          // shared rows: token arow, weight 1; routed rows: the pair's token and weight
+          int tok = arow;
+          float scale = td;
+          if (item.kind() != 0) {
+            const int pair = g.order[arow];
+            tok = pair / g.K;
+            scale = td * g.wpair[pair];
           }
+          float* o = g.out + (size_t)tok * g.H + col;
+#pragma unroll
+          for (int j = 0; j < 64; j += 4)
+            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                         :: "l"(o + j), "f"(y[j] * scale), "f"(y[j + 1] * scale), "f"(y[j + 2] * scale),
+                            "f"(y[j + 3] * scale) : "memory");
         }
       }
     }
@@ -888,8 +868,8 @@ __global__ void __launch_bounds__(1024) k_scan(ScanArgs s) {
 }
 
 // One warp per token: x[t] quantised to NVFP4 once (unit tensor scale), written to the
-// shared expert's operand row t and to the token's K expert-major rows; the pair order
-// (plain and padded positions).
+// shared expert's operand row t and to the token's K expert-major rows; out[t] = x[t];
+// the pair order (plain and padded positions).
 struct ScatterArgs {
   RouteArgs r;
   const uint16_t* x;
@@ -897,6 +877,7 @@ struct ScatterArgs {
   int32_t* pos_of_pair;    // pair -> padded row
   int32_t* order_pad;      // padded row -> pair
   int32_t* order_out;      // plain position -> pair (optional)
+  float* out;              // [T][H]: x, to which the down GEMM adds
   uint8_t* xq_codes;  uint8_t* xq_sf;   // [Tp][H/2], MMA scale layout
   uint8_t* xp_codes;  uint8_t* xp_sf;   // [Pp][H/2], MMA scale layout
 };
@@ -932,6 +913,9 @@ __global__ void __launch_bounds__(256) k_scatter_quant(ScatterArgs s) {
         f[8 * p + 2 * q + 1] = bf16_bits_to_f32(u[q] >> 16);
       }
     }
+    float4* o = reinterpret_cast<float4*>(s.out + (size_t)t * H + 64 * gk);
+#pragma unroll
+    for (int p = 0; p < 16; ++p) o[p] = make_float4(f[4 * p], f[4 * p + 1], f[4 * p + 2], f[4 * p + 3]);
     uint2 cw[4];
     uint32_t sw = 0;
 #pragma unroll
@@ -956,44 +940,6 @@ __global__ void __launch_bounds__(256) k_scatter_quant(ScatterArgs s) {
   }
 }
 
-// One warp per token: out[t] += sum over the token's K routed rows of Yp (f16, already
-// scaled by the routing weights), slots in order.  out[t] holds x[t] + shared y[t].
-struct CombineArgs {
-  const uint16_t* yp;
-  const int32_t* pos_of_pair;
-  float* out;
-  int T, H, K;
-};
-
-__global__ void __launch_bounds__(256) k_combine(CombineArgs c) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= c.T) return;
-  const int pos_l = lane < c.K ? c.pos_of_pair[t * c.K + lane] : 0;
-  float* o = c.out + (size_t)t * c.H;
-  for (int n0 = 8 * lane; n0 < c.H; n0 += 8 * 32) {
-    float acc[8];
-    const float4 a = *reinterpret_cast<const float4*>(o + n0);
-    const float4 b = *reinterpret_cast<const float4*>(o + n0 + 4);
-    acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
-    acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
-    for (int j = 0; j < c.K; ++j) {
-      const int pos = __shfl_sync(0xffffffffu, pos_l, j);
-      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(c.yp + (size_t)pos * c.H + n0));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float lo, hi;
-        f16x2_to_f32x2(w[q], lo, hi);
-        acc[2 * q] += lo;
-        acc[2 * q + 1] += hi;
-      }
-    }
-    *reinterpret_cast<float4*>(o + n0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    *reinterpret_cast<float4*>(o + n0 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-  }
-}
-
 // ---------------------------------------------------------------- MMA scale copies
 // scales [m][rows][cols/16] -> [m][rows/128][cols/64][512] (see flint.h)
 __global__ void k_mma_scales(const uint8_t* __restrict__ scales, int rows, int cols,
@@ -1013,7 +959,7 @@ __global__ void k_mma_scales(const uint8_t* __restrict__ scales, int rows, int c
 // ---------------------------------------------------------------- host side
 struct WsLayout {
   size_t logits, idx, w, bits, wordpre, counts, offsets, offp, order, pos, xq_c, xq_s, xp_c, xp_s, hs_c,
-      hs_s, hq_c, hq_s, yp, items_gu, items_dn, nitems, total;
+      hs_s, hq_c, hq_s, items_gu, items_dn, nitems, total;
 };
 
 static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -1049,7 +995,6 @@ static WsLayout ws_layout(int H, int E, int K, int F, int Fs, int T) {
   L.hs_s = o;     o += a256(Tp * Fs / 16);
   L.hq_c = o;     o += a256(Pp * F / 2);
   L.hq_s = o;     o += a256(Pp * F / 16);
-  L.yp = o;       o += a256(Pp * H * 2);
   L.items_gu = o; o += a256(sizeof(Item) * (mt_sh * (Fs / kBN) + mt_rt * (F / kBN)));
   L.items_dn = o; o += a256(sizeof(Item) * (mt_sh + mt_rt) * (H / kBN));
   L.nitems = o;   o += 256;
@@ -1150,7 +1095,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st) {
   k_expert_prefix<<<(E + 7) / 8, 256, 0, st>>>(r);
   k_scan<<<1, 1024, 0, st>>>(sc);
   ScatterArgs sa;
-  sa.r = r; sa.x = a.x; sa.H = H;
+  sa.r = r; sa.x = a.x; sa.H = H; sa.out = a.out;
   sa.order_pad = reinterpret_cast<int32_t*>(at(L.order));
   sa.pos_of_pair = reinterpret_cast<int32_t*>(at(L.pos));
   sa.order_out = a.order_out;
@@ -1199,7 +1144,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st) {
   dn.rowsB[0] = H; dn.rowsB[1] = H;
   dn.items = sc.items_dn; dn.n_items = sc.n_items_dn;
   dn.tscA[0] = a.sh_down.tsc; dn.tscA[1] = a.down.tsc;
-  dn.out = a.out; dn.x = a.x; dn.yp = reinterpret_cast<uint16_t*>(at(L.yp));
+  dn.out = a.out;
   dn.order = sa.order_pad; dn.wpair = r.w;
   dn.H = H; dn.K = K;
   dn.wait_ns = a.wait_ns;
@@ -1207,10 +1152,6 @@ cudaError_t launch_prefill(const PrefillArgs& a, void* ws, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   k_gemm_fp4<kDown><<<sms, kGThreads, Cfg<kDown>::smem, st>>>(dn);
 
-  // 7 combine: out[t] += routed rows
-  CombineArgs cb;
-  cb.yp = dn.yp; cb.pos_of_pair = sa.pos_of_pair; cb.out = a.out; cb.T = T; cb.H = H; cb.K = K;
-  k_combine<<<(T + 7) / 8, 256, 0, st>>>(cb);
   return cudaGetLastError();
 }
 

@@ -6,6 +6,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
+from oracle import seeded
 from sparse_moe_decode_02_b300 import synth
 
 REL_L2 = 2e-3          # relative L2 bound on floating outputs
@@ -14,54 +15,27 @@ TIE_GAP = 1e-4         # routing / argmax decisions closer than this are exempt
 
 
 def bits16(t: torch.Tensor) -> np.ndarray:
-    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    return seeded.bits16(t)
 
 
 def oracle_stack(orc, spec: synth.LayerSpec, kind: int, experts, gen_device="cpu"):
-    """NVFP4 stack for one matrix kind; only `experts` are generated (others zero).  The
-    seeded generator gives the same bits on any device (`gen_device` only sets where the
-    bf16 draws are made); the oracle quantises them itself."""
-    n, r, c = spec.dims(kind)
-    codes = np.zeros((n, r, c // 2), np.uint8)
-    scales = np.zeros((n, r, c // 16), np.uint8)
-    tsc = np.ones(n, np.float32)
-    for e in sorted(set(int(e) for e in experts)):
-        q, st = orc.quantize_nvfp4(spec.weights_bf16(kind, device=gen_device, experts=[e]).cpu())
-        assert st == 0
-        codes[e], scales[e], tsc[e] = q.codes[0], q.scales[0], q.tsc[0]
-    return orc.NVFP4(codes, scales, tsc)
+    """NVFP4 stack for one matrix kind; only `experts` are generated (others zero)."""
+    return seeded.stack(spec, kind, experts, gen_device)
 
 
 def oracle_layer(orc, spec: synth.LayerSpec, experts=None, gen_device="cpu"):
     """Oracle-side layer built from the same seeded bf16 tensors as the device layer."""
-    s = spec.shape
-    E = s.n_experts
-    experts = range(E) if experts is None else experts
-    router = bits16(spec.weights_bf16(synth.KIND_ROUTER, device=gen_device)[0])
-    mk = lambda kind, ex: oracle_stack(orc, spec, kind, ex, gen_device)
-    return orc.Layer(router, spec.bias(), mk(synth.KIND_GATE, experts),
-                     mk(synth.KIND_UP, experts), mk(synth.KIND_DOWN, experts),
-                     mk(synth.KIND_SH_GATE, [0]), mk(synth.KIND_SH_UP, [0]),
-                     mk(synth.KIND_SH_DOWN, [0]), s.top_k, router_score=spec.router_score)
+    return seeded.layer(spec, experts, gen_device)
 
 
 def router_only_layer(orc, spec: synth.LayerSpec):
     """A layer whose expert stacks are empty placeholders: enough for orc.router."""
-    s = spec.shape
-    z = lambda n, r, c: orc.NVFP4(np.zeros((n, r, c // 2), np.uint8),
-                                  np.zeros((n, r, c // 16), np.uint8), np.ones(n, np.float32))
-    H, E, F, Fs = s.hidden, s.n_experts, s.expert_width, s.shared_width
-    return orc.Layer(bits16(spec.weights_bf16(synth.KIND_ROUTER)[0]), spec.bias(),
-                     z(1, F, H), z(1, F, H), z(1, H, F), z(1, Fs, H), z(1, Fs, H), z(1, H, Fs),
-                     s.top_k, router_score=spec.router_score)
+    return seeded.router_only_layer(spec)
 
 
 def oracle_routes(orc, spec, x_bits: np.ndarray):
     """(logits [T, E], idx [T, k], w [T, k]) from the oracle router."""
-    L = router_only_layer(orc, spec)
-    out = [orc.router(L, x_bits[t]) for t in range(x_bits.shape[0])]
-    return (np.stack([o[0] for o in out]), np.stack([o[1] for o in out]),
-            np.stack([o[2] for o in out]))
+    return seeded.routes(spec, x_bits)
 
 
 def float_errors(got, ref):
