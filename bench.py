@@ -280,6 +280,18 @@ def run_flint(args):
     }
     if not args.decode_only:
         result["sampling"] = measure_sampling(dev)
+        # the same step with the token drawn in the launch (top-k 20, top-p 0.95, T = 1)
+        u = torch.rand(T, device=dev, generator=torch.Generator(device=dev).manual_seed(SEED))
+        toks = torch.empty(T, dtype=torch.int32, device=dev)
+        fused = lambda: flint.decode_tokens_sample(layers, x_tok, head, u, tokens=toks, rms_eps=EPS,
+                                                   ws=ws, stream=stream)
+        fused()
+        torch.cuda.synchronize()
+        ms_f = _time_ms(fused, 2, stream)
+        result["sampling"]["fused_decode"] = {
+            "value": round(T / (ms_f * 1e-3), 1), "unit": "tok/s", "ms_per_step": round(ms_f, 3),
+            "workload": "the decode step with each token drawn inside the launch "
+                        "(flint_decode_tokens_sample: top-k 20, top-p 0.95, temperature 1)"}
         result["config3_lm_head"] = measure_lm_head(dev, head)
     del layers, head
     torch.cuda.empty_cache()

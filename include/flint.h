@@ -224,6 +224,29 @@ flint_status flint_decode_tokens(const flint_moe_layer* layers, int n_layers,
                                  int32_t* topk_idx, float* topk_w, void* ws,
                                  size_t ws_bytes, flint_stream stream);
 
+/* flint_decode_tokens with the head's token drawn instead of taken greedily ("Recursive
+ * Releases Flint, a 40B MoE Coding Model That Runs Locally at 125 Tokens per Second",
+ * section "How does Flint perform on coding benchmarks?": temperature 1.0, top-p 0.95,
+ * top-k 20), fused into the same launch: the logits never need to leave the GPU.
+ * tokens[t] (int32 [T]) is the draw of flint_sample_logits from token t's logits with
+ * uniforms[t] (fp32 [T], the caller's numbers in [0, 1)): the top_k logits (ties to the
+ * lower index), p_i = exp((l_i - l_0) / temperature) over them, the shortest prefix
+ * whose p sum reaches top_p, the first i of it with uniforms[t] < (p_0 + ... + p_i) /
+ * (prefix sum); a +inf or all -inf leading logit gives the first candidate.  argmax
+ * (optional) is the first candidate.  top_k is clipped to the vocabulary.  Errors:
+ * those of flint_decode_tokens; FLINT_ERR_INVALID_ARG for a null head, uniforms or
+ * tokens, temperature not > 0 and finite, top_p outside (0, 1], top_k < 1;
+ * FLINT_ERR_UNSUPPORTED for top_k > FLINT_MAX_SAMPLE_TOP_K or more than 2048
+ * vocabulary rows per CTA (a vocabulary above ~229k at 112 CTAs). */
+flint_status flint_decode_tokens_sample(const flint_moe_layer* layers, int n_layers,
+                                        const flint_nvfp4* head, const void* x_bf16,
+                                        const float* residual, int T, float rms_eps,
+                                        float temperature, int top_k, float top_p,
+                                        const float* uniforms, int32_t* tokens, float* out,
+                                        void* x_out_bf16, float* logits, int32_t* argmax,
+                                        int32_t* topk_idx, float* topk_w, void* ws,
+                                        size_t ws_bytes, flint_stream stream);
+
 /* flint_decode_tokens with a per-layer record of the chain, for checking it layer by
  * layer against a reference:  x_trace_bf16 [T, n_layers, H] receives x_l (the bf16
  * input of layer l as the kernel staged it) and h_trace fp32 [T, n_layers, H]

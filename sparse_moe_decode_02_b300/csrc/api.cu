@@ -145,13 +145,21 @@ flint_status flint_dequantize_nvfp4(const flint_nvfp4* m, float* out, flint_stre
                                             static_cast<cudaStream_t>(stream)));
 }
 
+// Sampling options of flint_decode_tokens_sample (checked by the caller).
+struct SampleOpts {
+  float temp, top_p;
+  int top_k;
+  const float* uniforms;
+  int32_t* tokens;
+};
+
 static flint_status decode_tokens_impl(const flint_moe_layer* layers, int n_layers,
                                        const flint_nvfp4* head, const void* x_bf16,
                                        const float* residual, int T, float rms_eps, float* out,
                                        void* x_out_bf16, float* logits, int32_t* argmax,
                                        int32_t* topk_idx, float* topk_w, void* x_trace_bf16,
                                        float* h_trace, void* ws, size_t ws_bytes,
-                                       flint_stream stream) {
+                                       flint_stream stream, const SampleOpts* smp = nullptr) {
   if (!layers || !x_bf16 || !ws) return FLINT_ERR_INVALID_ARG;
   if (n_layers <= 0 || T <= 0) return FLINT_ERR_INVALID_ARG;
   if (n_layers > FLINT_MAX_LAYERS) return FLINT_ERR_UNSUPPORTED;
@@ -166,7 +174,7 @@ static flint_status decode_tokens_impl(const flint_moe_layer* layers, int n_laye
     if (head->n_mat != 1 || head->cols != H || head->rows <= 0) return FLINT_ERR_SHAPE;
     flint_status s = check_nvfp4(*head, 1, head->rows, head->cols);
     if (s != FLINT_OK) return s;
-  } else if (logits || argmax) {
+  } else if (logits || argmax || smp) {
     return FLINT_ERR_INVALID_ARG;
   }
   if (!aligned16(x_bf16) || (residual && !aligned4(residual)) || (out && !aligned4(out)) ||
@@ -212,6 +220,16 @@ static flint_status decode_tokens_impl(const flint_moe_layer* layers, int n_laye
   a.w_out = topk_w;
   a.x_trace = static_cast<uint16_t*>(x_trace_bf16);
   a.h_trace = h_trace;
+  if (smp) {
+    // each CTA keeps its rows' logits in shared memory: at most 2048 rows per CTA
+    if ((head->rows + NC * flint::kDecCluster - 1) / (NC * flint::kDecCluster) > 2048)
+      return FLINT_ERR_UNSUPPORTED;
+    a.temp = smp->temp;
+    a.top_p = smp->top_p;
+    a.top_k = smp->top_k < head->rows ? smp->top_k : head->rows;
+    a.uniforms = smp->uniforms;
+    a.tokens = smp->tokens;
+  }
   flint::decode_carve(a, ws);
   return from_cuda(flint::launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
@@ -225,6 +243,25 @@ flint_status flint_decode_tokens(const flint_moe_layer* layers, int n_layers,
   return decode_tokens_impl(layers, n_layers, head, x_bf16, residual, T, rms_eps, out,
                             x_out_bf16, logits, argmax, topk_idx, topk_w, nullptr, nullptr, ws,
                             ws_bytes, stream);
+}
+
+flint_status flint_decode_tokens_sample(const flint_moe_layer* layers, int n_layers,
+                                        const flint_nvfp4* head, const void* x_bf16,
+                                        const float* residual, int T, float rms_eps,
+                                        float temperature, int top_k, float top_p,
+                                        const float* uniforms, int32_t* tokens, float* out,
+                                        void* x_out_bf16, float* logits, int32_t* argmax,
+                                        int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
+                                        flint_stream stream) {
+  if (!head || !uniforms || !tokens) return FLINT_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || !(temperature < INFINITY)) return FLINT_ERR_INVALID_ARG;
+  if (!(top_p > 0.f && top_p <= 1.f) || top_k < 1) return FLINT_ERR_INVALID_ARG;
+  if (top_k > FLINT_MAX_SAMPLE_TOP_K) return FLINT_ERR_UNSUPPORTED;
+  if (!aligned4(uniforms) || !aligned4(tokens)) return FLINT_ERR_ALIGNMENT;
+  const SampleOpts smp{temperature, top_p, top_k, uniforms, tokens};
+  return decode_tokens_impl(layers, n_layers, head, x_bf16, residual, T, rms_eps, out,
+                            x_out_bf16, logits, argmax, topk_idx, topk_w, nullptr, nullptr, ws,
+                            ws_bytes, stream, &smp);
 }
 
 flint_status flint_decode_tokens_trace(const flint_moe_layer* layers, int n_layers,

@@ -734,6 +734,135 @@ __device__ __noinline__ void head_argmax(const unsigned long long* best, int G, 
   if (lane == 0 && out) *out = (i >= 0 && i < V) ? i : 0;
 }
 
+// ---------------------------------------------------------------- fused sampling
+// ("Recursive Releases Flint, a 40B MoE Coding Model That Runs Locally at 125 Tokens per
+// Second", section "How does Flint perform on coding benchmarks?": temperature 1.0,
+// top-p 0.95, top-k 20.)  The K largest logits of the token are found in two levels --
+// each CTA its own rows, then the last CTA over the CTAs' lists -- and the draw follows
+// flint_sample_logits exactly.
+
+// K rounds of warp-wide maxima over the warp's candidates (S per lane; key 0 = empty):
+// the K largest keys, ties to the lower index, in rank order into out_key / out_idx.
+template <int S>
+__device__ __forceinline__ void warp_topk(unsigned (&key)[S], int (&idx)[S], int K, unsigned* out_key, int* out_idx) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int s = 0; s < K; ++s) {
+    unsigned lb = 0u;
+    int li = 0x7FFFFFFF;
+#pragma unroll
+    for (int q = 0; q < S; ++q)
+      if (key[q] > lb || (key[q] == lb && idx[q] < li)) { lb = key[q]; li = idx[q]; }
+    const unsigned wk = __reduce_max_sync(0xffffffffu, lb);
+    const int wi = (int)__reduce_min_sync(0xffffffffu, lb == wk ? (unsigned)li : 0xFFFFFFFFu);
+    if (lane == 0) { out_key[s] = wk; out_idx[s] = wi; }
+#pragma unroll
+    for (int q = 0; q < S; ++q)
+      if (key[q] == wk && idx[q] == wi) { key[q] = 0u; idx[q] = 0x7FFFFFFF; }
+  }
+}
+
+// The K (<= 32) largest of n <= kThreads * 8 candidates (order keys s_key, 0 = empty;
+// indices s_idx, or base + i when s_idx is null), ties to the lower index, in rank
+// order into out_key / out_idx.  Each warp takes its slice (<= 256), then warp 0 the
+// warps' K-lists (<= 512).  Every thread calls this.
+__device__ __noinline__ void block_topk(const unsigned* s_key, const int* s_idx, int n, int K, int base,
+                                        unsigned* s_wk, int* s_wi, unsigned* out_key, int* out_idx) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = (n + kWarps - 1) / kWarps;
+  const int b0 = warp * per, b1 = min(n, b0 + per);
+  {
+    unsigned key[8];
+    int idx[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int i = b0 + lane + 32 * q;
+      key[q] = i < b1 ? s_key[i] : 0u;
+      idx[q] = i < b1 ? (s_idx ? s_idx[i] : base + i) : 0x7FFFFFFF;
+    }
+    warp_topk<8>(key, idx, K, s_wk + warp * K, s_wi + warp * K);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    unsigned key[16];
+    int idx[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int c = lane + 32 * q;
+      key[q] = c < kWarps * K ? s_wk[c] : 0u;
+      idx[q] = c < kWarps * K ? s_wi[c] : 0x7FFFFFFF;
+    }
+    warp_topk<16>(key, idx, K, out_key, out_idx);
+  }
+  __syncthreads();
+}
+
+// The last CTA: every CTA's K candidates of token t (tagged words {tag, key},
+// {tag, index}, waited for with a bound), their K best, and the draw with the caller's
+// uniform u: p_i = exp((l_i - l_0) / temp) over the K, the shortest prefix whose p sum
+// reaches top_p, the first i of it with u < (p_0 + ... + p_i) / (sum of the prefix).
+// +inf / all -inf: rank 0.  Writes the token and the argmax (rank 0).  Every thread of
+// the CTA calls this.
+__device__ __noinline__ void head_sample(const unsigned long long* cand, int G, int K, unsigned tag, float temp,
+                                         float top_p, float u, int V, int32_t* token, int32_t* amax,
+                                         unsigned* s_ck, int* s_ci, unsigned* s_wk, int* s_wi, unsigned* s_fk,
+                                         int* s_fi, unsigned* sync, unsigned long long lim) {
+  const int n = G * K;
+#pragma unroll 1
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    const unsigned long long* w = cand + 2 * ((size_t)(i / K) * 32 + i % K);
+    unsigned long long wk = ld_relaxed(w), wi = ld_relaxed(w + 1);
+    unsigned long long t0 = 0;
+    for (unsigned polls = 1; (unsigned)(wk >> 32) != tag || (unsigned)(wi >> 32) != tag; ++polls) {
+      if ((polls & 15u) == 0) {
+        if (ld_abort(sync)) break;
+        const unsigned long long now = globaltimer();
+        if (t0 == 0) {
+          t0 = now;
+        } else if (now - t0 > lim) {
+          give_up(sync);
+          break;
+        }
+      }
+      wk = ld_relaxed(w);
+      wi = ld_relaxed(w + 1);
+    }
+    s_ck[i] = (unsigned)wk;
+    s_ci[i] = (int)(unsigned)wi;
+  }
+  __syncthreads();
+  block_topk(s_ck, s_ci, n, K, 0, s_wk, s_wi, s_fk, s_fi);
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  const int idx = lane < K ? s_fi[lane] : 0;
+  const float l = lane < K ? key_value(s_fk[lane]) : -INFINITY;
+  const float l0 = __shfl_sync(0xffffffffu, l, 0);
+  int pick_lane = 0;
+  if (l0 != -INFINITY && l0 != INFINITY) {
+    float p = lane < K ? expf((l - l0) / temp) : 0.f;
+    float z = p;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    p /= z;
+    float c = p;                                       // inclusive prefix sums in rank order
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float x = __shfl_up_sync(0xffffffffu, c, o);
+      if (lane >= o) c += x;
+    }
+    const unsigned reach = __ballot_sync(0xffffffffu, lane < K && c >= top_p);
+    const int m = reach ? __ffs(reach) : K;
+    const float zm = __shfl_sync(0xffffffffu, c, m - 1);
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < m && u < c / zm);
+    pick_lane = hit ? __ffs(hit) - 1 : m - 1;
+  }
+  const int pick = __shfl_sync(0xffffffffu, idx, pick_lane);
+  if (lane == 0) {
+    *token = (pick >= 0 && pick < V) ? pick : 0;
+    if (amax) *amax = (idx >= 0 && idx < V) ? idx : 0;
+  }
+}
+
 // ---------------------------------------------------------------- the kernel
 constexpr int kLayerWords = (int)(sizeof(DecLayer) / 8);
 static_assert(sizeof(DecLayer) % 8 == 0 && kLayerWords <= 32, "layer table: at most 32 words");
@@ -768,17 +897,18 @@ struct Smem {
 // Head rows per ring slot at hidden H: a multiple of 64, at most 256, two slots in the
 // big region.
 __host__ __device__ __forceinline__ int head_chunk_rows(int H) {
-  int r = (kBigBytes / 2) / (H / 2 + H / 16);
+  int r = ((kBigBytes - 8192) / 2) / (H / 2 + H / 16);    // the last 8 KB: sampled logits
   r = r > 256 ? 256 : r;
   return r & ~63;
 }
 
 // The head for one token: this CTA's rows [v0, v1) stream through a two-slot ring of TMA
-// bulk copies in s_big and are dotted with x (s_xl).  Writes the logits (optional) and
-// leaves this thread's running best in (bv, bi).  Every thread calls this.
+// bulk copies in s_big and are dotted with x (s_xl).  Writes the logits (optional; also
+// into s_lv[v - v0] when s_lv is given) and leaves this thread's running best in
+// (bv, bi).  Every thread calls this.
 template <int CPL>
 __device__ __noinline__ void head_phase(const DecodeArgs& a, int t, int v0, int v1, const uint4* s_xl,
-                                        float unscale, uint8_t* s_big, float* s_hv, uint64_t* bar_hd,
+                                        float unscale, uint8_t* s_big, float* s_hv, float* s_lv, uint64_t* bar_hd,
                                         uint32_t& ph_hd, unsigned& pend_hd, bool abort, float& bv, int& bi) {
   const int H = a.H;
   const int HR = head_chunk_rows(H);
@@ -804,6 +934,7 @@ __device__ __noinline__ void head_phase(const DecodeArgs& a, int t, int v0, int 
       for (int r = threadIdx.x; r < nr; r += kThreads) {
         const float v = s_hv[r];
         if (a.logits) a.logits[(size_t)t * a.V + r0 + r] = v;
+        if (s_lv) s_lv[r0 - v0 + r] = v;
         const float vv = (v == v) ? v : -INFINITY;
         if (vv > bv || (vv == bv && r0 + r < bi)) { bv = vv; bi = r0 + r; }
       }
@@ -1086,21 +1217,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     const int v0 = min(a.V, blockIdx.x * chunk), v1 = min(a.V, v0 + chunk);
     float bv = -INFINITY;
     int bi = 0x7FFFFFFF;
-    head_phase<CPL>(a, t, v0, v1, s_xl, unscale, s_big, s_hv, bar_hd, ph_hd, pend_hd, s_abort != 0, bv, bi);
-    best_reduce_warp(bv, bi);
-    if (lane == 0) { s_bv[warp] = bv; s_bi[warp] = bi; }
-    __syncthreads();
-    unsigned long long* best = a.best + (size_t)(t & 1) * kMaxG * 2;
+    // the CTA's logits: the last 8 KB of the big region, past the head's ring (two slots
+    // of at most kBigBytes / 2 - 8 KB each; peers never write the big region)
+    float* s_lv = a.tokens ? reinterpret_cast<float*>(s_big + kBigBytes - 8192) : nullptr;
+    head_phase<CPL>(a, t, v0, v1, s_xl, unscale, s_big, s_hv, s_lv, bar_hd, ph_hd, pend_hd, s_abort != 0, bv, bi);
     const unsigned ttag = (unsigned)t + 1;
-    if (threadIdx.x == 0) {
+    if (a.tokens) {
+      // the CTA's K best logits, posted as tagged words; the last CTA draws the token
+      unsigned* s_key = reinterpret_cast<unsigned*>(s_lv);
 #pragma unroll 1
-      for (int w = 1; w < kWarps; ++w)
-        if (s_bv[w] > bv || (s_bv[w] == bv && s_bi[w] < bi)) { bv = s_bv[w]; bi = s_bi[w]; }
-      st_tagged(best + 2 * blockIdx.x, ((unsigned long long)ttag << 32) | __float_as_uint(bv));
-      st_tagged(best + 2 * blockIdx.x + 1, ((unsigned long long)ttag << 32) | (unsigned)bi);
+      for (int i = threadIdx.x; i < v1 - v0; i += kThreads) s_key[i] = order_key(s_lv[i]);
+      __syncthreads();
+      unsigned* s_wk = reinterpret_cast<unsigned*>(s_big);          // the head ring is drained
+      int* s_wi = reinterpret_cast<int*>(s_big + 4 * kWarps * 32);
+      unsigned* s_fk = reinterpret_cast<unsigned*>(s_big + 8 * kWarps * 32);
+      int* s_fi = reinterpret_cast<int*>(s_big + 8 * kWarps * 32 + 128);
+      block_topk(s_key, nullptr, v1 - v0, a.top_k, v0, s_wk, s_wi, s_fk, s_fi);
+      unsigned long long* cand = a.cand + (size_t)(t & 1) * kMaxG * 64;
+      if (threadIdx.x < a.top_k) {
+        unsigned long long* w = cand + 2 * ((size_t)blockIdx.x * 32 + threadIdx.x);
+        st_tagged(w, ((unsigned long long)ttag << 32) | s_fk[threadIdx.x]);
+        st_tagged(w + 1, ((unsigned long long)ttag << 32) | (unsigned)s_fi[threadIdx.x]);
+      }
+      if (blockIdx.x == G - 1) {
+        __syncthreads();
+        unsigned* s_ck = reinterpret_cast<unsigned*>(s_big + 8 * kWarps * 32 + 256);
+        int* s_ci = reinterpret_cast<int*>(s_big + 8 * kWarps * 32 + 256 + 4 * kMaxG * 32);
+        head_sample(cand, G, a.top_k, ttag, a.temp, a.top_p, __ldg(a.uniforms + t), a.V, a.tokens + t,
+                    a.argmax ? a.argmax + t : nullptr, s_ck, s_ci, s_wk, s_wi, s_fk, s_fi, sync, lim);
+      }
+    } else {
+      best_reduce_warp(bv, bi);
+      if (lane == 0) { s_bv[warp] = bv; s_bi[warp] = bi; }
+      __syncthreads();
+      unsigned long long* best = a.best + (size_t)(t & 1) * kMaxG * 2;
+      if (threadIdx.x == 0) {
+#pragma unroll 1
+        for (int w = 1; w < kWarps; ++w)
+          if (s_bv[w] > bv || (s_bv[w] == bv && s_bi[w] < bi)) { bv = s_bv[w]; bi = s_bi[w]; }
+        st_tagged(best + 2 * blockIdx.x, ((unsigned long long)ttag << 32) | __float_as_uint(bv));
+        st_tagged(best + 2 * blockIdx.x + 1, ((unsigned long long)ttag << 32) | (unsigned)bi);
+      }
+      // the last CTA (in the cluster with the most slack) reduces the CTAs' maxima
+      if (blockIdx.x == G - 1 && warp == 0)
+        head_argmax(best, G, ttag, a.V, a.argmax ? a.argmax + t : nullptr, sync, lim);
     }
-    // the last CTA (in the cluster with the most slack) reduces the CTAs' maxima
-    if (blockIdx.x == G - 1 && warp == 0) head_argmax(best, G, ttag, a.V, a.argmax ? a.argmax + t : nullptr, sync, lim);
     __syncthreads();                                 // s_xb / s_xl are restaged next
   }
   // Copies are issued only for a step that follows and waited for in the step they
@@ -1161,7 +1322,8 @@ int decode_clusters() {
 int decode_router_rows(int E) { return (((E + dc::kCS - 1) / dc::kCS) + 3) & ~3; }
 
 size_t decode_workspace_bytes(int H) {
-  return 256 + (size_t)2 * kDecMaxClusters * H * 8 + (size_t)2 * dc::kMaxG * 2 * 8;
+  return 256 + (size_t)2 * kDecMaxClusters * H * 8 + (size_t)2 * dc::kMaxG * 2 * 8 +
+         (size_t)2 * dc::kMaxG * 64 * 8;
 }
 
 size_t decode_smem_bytes(int H, int Emax) { return dc::Smem::of(H, Emax).total; }
@@ -1173,6 +1335,8 @@ void decode_carve(DecodeArgs& a, void* ws) {
   a.board = reinterpret_cast<unsigned long long*>(p);
   p += (size_t)2 * kDecMaxClusters * a.H * 8;
   a.best = reinterpret_cast<unsigned long long*>(p);
+  p += (size_t)2 * dc::kMaxG * 2 * 8;
+  a.cand = reinterpret_cast<unsigned long long*>(p);
 }
 
 bool decode_plan_layer(DecLayer& d, int H, int NC) {

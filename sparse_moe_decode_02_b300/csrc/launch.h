@@ -62,6 +62,13 @@ struct DecodeArgs {
   unsigned* sync;                    // [64]: [0] abort flag
   unsigned long long* board;         // [2][kDecMaxClusters][H] tagged partial sums
   unsigned long long* best;          // [2][kDecMaxClusters * kDecCluster][2] tagged head maxima
+  // fused sampling of the head (tokens non-null): temperature, top-k (<= 32), top-p, one
+  // uniform per token; board of the CTAs' candidates [2][kDecMaxClusters * kDecCluster][32][2]
+  float temp, top_p;
+  int top_k;
+  const float* uniforms;
+  int32_t* tokens;
+  unsigned long long* cand;
   DecLayer layer[kMaxLayers];
 };
 

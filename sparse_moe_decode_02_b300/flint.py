@@ -55,7 +55,7 @@ _SYMBOLS = ["flint_quantize_nvfp4", "flint_dequantize_nvfp4", "flint_nvfp4_mma_s
             "flint_decode_tokens_trace", "flint_decode_tokens_noalloc", "flint_moe_prefill",
             "flint_lm_head", "flint_workspace_bytes", "flint_last_device_status",
             "flint_status_string", "flint_version", "flint_set_wait_limit_ns",
-            "flint_debug_hold_next_launch", "flint_bench_fp4_mma"]
+            "flint_debug_hold_next_launch", "flint_bench_fp4_mma", "flint_decode_tokens_sample"]
 
 
 def lib() -> ctypes.CDLL:
@@ -76,6 +76,10 @@ def lib() -> ctypes.CDLL:
     L.flint_decode_tokens_trace.argtypes = [ctypes.POINTER(_LayerC), i, ctypes.POINTER(_NVFP4C),
                                             vp, vp, i, ctypes.c_float, vp, vp, vp, vp, vp, vp,
                                             vp, vp, vp, sz, vp]
+    L.flint_decode_tokens_sample.argtypes = [ctypes.POINTER(_LayerC), i, ctypes.POINTER(_NVFP4C),
+                                             vp, vp, i, ctypes.c_float, ctypes.c_float, i,
+                                             ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                             sz, vp]
     L.flint_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.flint_debug_hold_next_launch.argtypes = [i]
     L.flint_decode_tokens_noalloc.argtypes = [ctypes.POINTER(_LayerC), i, ctypes.POINTER(_NVFP4C),
@@ -98,7 +102,8 @@ def lib() -> ctypes.CDLL:
                  "flint_moe_decode", "flint_decode_tokens", "flint_decode_tokens_trace",
                  "flint_decode_tokens_noalloc", "flint_moe_prefill", "flint_lm_head",
                  "flint_last_device_status", "flint_sample_logits", "flint_set_wait_limit_ns",
-                 "flint_debug_hold_next_launch", "flint_bench_fp4_mma"):
+                 "flint_debug_hold_next_launch", "flint_bench_fp4_mma",
+                 "flint_decode_tokens_sample"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -275,6 +280,32 @@ def decode_tokens(layers, x: torch.Tensor, head: NVFP4 | None = None,
         _check(lib().flint_decode_tokens_trace(*common, _ptr(x_trace), _ptr(h_trace), _ptr(ws),
                                                ws.numel(), _stream(stream)),
                "flint_decode_tokens_trace")
+
+
+def decode_tokens_sample(layers, x: torch.Tensor, head: NVFP4, uniforms: torch.Tensor,
+                         temperature: float = 1.0, top_k: int = 20, top_p: float = 0.95,
+                         tokens=None, residual=None, rms_eps: float = 1e-6, out=None, x_out=None,
+                         logits=None, argmax=None, topk_idx=None, topk_w=None, ws=None,
+                         stream=None) -> torch.Tensor:
+    """decode_tokens with each token drawn from the head's logits inside the launch
+    (flint_decode_tokens_sample); returns tokens (int32 [T])."""
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    T = x.shape[0]
+    H, E, k, F, Fs = layers[0].dims
+    if tokens is None:
+        tokens = torch.empty(T, dtype=torch.int32, device=x.device)
+    arr = (_LayerC * len(layers))(*[l.c() for l in layers])
+    hc = head.c()
+    nb = workspace_bytes(OP_MOE_DECODE, H, E, k, F, Fs, 0, T)
+    ws = _workspace(nb, x.device, ws)
+    _check(lib().flint_decode_tokens_sample(arr, len(layers), ctypes.byref(hc), _ptr(x),
+                                            _ptr(residual), T, float(rms_eps), float(temperature),
+                                            int(top_k), float(top_p), _ptr(uniforms), _ptr(tokens),
+                                            _ptr(out), _ptr(x_out), _ptr(logits), _ptr(argmax),
+                                            _ptr(topk_idx), _ptr(topk_w), _ptr(ws), ws.numel(),
+                                            _stream(stream)), "flint_decode_tokens_sample")
+    return tokens
 
 
 def set_wait_limit_ns(ns: int) -> None:

@@ -70,3 +70,43 @@ def test_sample_ties_nan_and_small_vocab(orc):
             skipped += _check(orc, row[None].copy(), np.array([u], np.float32), 1.0, k, top_p)
             checked += 1
     assert skipped <= checked // 4
+
+
+@pytest.mark.parametrize("shape_name,L,T,temp,k,top_p", [("FLINT", 2, 6, 1.0, 20, 0.95),
+                                                          ("FLINT", 1, 4, 0.6, 32, 0.8),
+                                                          ("TINY", 3, 8, 1.0, 20, 0.95),
+                                                          ("TINY", 2, 5, 1.5, 1, 0.95)])
+def test_decode_fused_sampling(orc, shape_name, L, T, temp, k, top_p):
+    """flint_decode_tokens_sample: the token drawn inside the decode launch equals the
+    oracle's draw from the same logits (the launch also writes them), the argmax is the
+    first candidate, and the rest of the launch matches flint_decode_tokens."""
+    from sparse_moe_decode_02_b300 import synth, workload
+    shape = getattr(synth, shape_name)
+    layers = [workload.build_layer(synth.LayerSpec(shape, seed=51, layer=l, zipf=1.1), DEV)
+              for l in range(L)]
+    head = workload.build_head(51, shape.vocab, shape.hidden, DEV)
+    x = synth.tokens_bf16(51, shape.hidden, T, stream=6).to(DEV)
+    rng = np.random.default_rng(T + k)
+    u = torch.from_numpy(rng.random(T).astype(np.float32)).to(DEV)
+    lg = torch.empty(T, shape.vocab, dtype=torch.float32, device=DEV)
+    am = torch.empty(T, dtype=torch.int32, device=DEV)
+    out = torch.empty(T, shape.hidden, dtype=torch.float32, device=DEV)
+    tok = flint.decode_tokens_sample(layers, x, head, u, temperature=temp, top_k=k, top_p=top_p,
+                                     logits=lg, argmax=am, out=out)
+    torch.cuda.synchronize()
+    assert flint.last_device_status() == 0
+    lg2 = torch.empty_like(lg)
+    out2 = torch.empty_like(out)
+    flint.decode_tokens(layers, x, head=head, logits=lg2, out=out2)
+    torch.cuda.synchronize()
+    assert torch.equal(lg, lg2) and torch.equal(out, out2)
+    logits, tok, am, u = lg.cpu().numpy(), tok.cpu().numpy(), am.cpu().numpy(), u.cpu().numpy()
+    skipped = 0
+    for t in range(T):
+        assert am[t] == int(np.argmax(logits[t]))
+        if _near_boundary(logits[t], temp, k, top_p, float(u[t])):
+            skipped += 1
+            continue
+        want, _ = orc.sample(logits[t], temp, k, top_p, float(u[t]))
+        assert tok[t] == want, (t, tok[t], want)
+    assert skipped <= T // 2

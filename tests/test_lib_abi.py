@@ -185,3 +185,24 @@ def test_sample_argument_checks(L):
     assert call(p=0.0) == 1
     assert call(p=1.5) == 1
     assert call(lg=FAKE + 2) == 2
+
+
+def test_decode_tokens_sample_argument_checks(L):
+    ds = L.flint_decode_tokens_sample
+    ws = flint.workspace_bytes(flint.OP_MOE_DECODE, 256, 16, 2, 64, 128, 0, 4)
+    arr = (flint._LayerC * 1)(_layer())
+    head = _nv(1, 4096, 256)
+    ok = dict(head=ctypes.byref(head), temp=1.0, k=20, p=0.95, u=FAKE, tok=FAKE)
+    call = lambda **kw: ds(arr, 1, dict(ok, **kw)["head"], FAKE, None, 2, 1e-6, dict(ok, **kw)["temp"],
+                           dict(ok, **kw)["k"], dict(ok, **kw)["p"], dict(ok, **kw)["u"],
+                           dict(ok, **kw)["tok"], None, None, None, None, None, None, FAKE, ws, None)
+    assert call(head=None) == 1
+    assert call(u=None) == 1
+    assert call(tok=None) == 1
+    assert call(temp=0.0) == 1
+    assert call(temp=float("inf")) == 1
+    assert call(p=0.0) == 1
+    assert call(p=1.5) == 1
+    assert call(k=0) == 1
+    assert call(k=33) == 8                                               # > FLINT_MAX_SAMPLE_TOP_K
+    assert call(tok=FAKE + 2) == 2
