@@ -297,6 +297,7 @@ def run_flint(args):
     torch.cuda.empty_cache()
     if not args.decode_only:
         result["config2_layer"] = measure_layer(dev)
+        result["dense_layers"] = measure_dense(dev)
         fp4 = measure_fp4_peak(dev)
         result["fp4_peak"] = fp4
         if not args.no_prefill:
@@ -384,6 +385,34 @@ def measure_layer(dev, reps: int = 5):
             "GBs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
             "note": "consecutive tokens of one layer reuse experts already in L2 (453 MB of "
                     "routed weights, 126 MB L2): DRAM traffic is below the algorithmic bytes"}
+
+
+def measure_dense(dev, reps: int = 3, T: int = 256):
+    """The model's two dense SwiGLU layers (width 6,144, no router) decoded in one launch,
+    batch 1, T tokens one after another: tokens/s and bytes per token."""
+    import torch
+
+    from sparse_moe_decode_02_b300 import flint, synth, workload
+
+    shape = synth.FLINT_DENSE
+    H = shape.hidden
+    layers = [workload.build_layer(synth.LayerSpec(shape, seed=SEED, layer=100 + l), dev)
+              for l in range(2)]
+    x = synth.tokens_bf16(SEED, H, T, stream=12, device=dev)
+    out = torch.empty(T, H, dtype=torch.float32, device=dev)
+    for _ in range(2):
+        flint.decode_tokens(layers, x, out=out)
+    torch.cuda.synchronize()
+    ms = _time_ms(lambda: flint.decode_tokens(layers, x, out=out), reps)
+    per_tok = 2 * workload.layer_bytes_per_token(shape)
+    gbs = per_tok * T / (ms * 1e-3) / 1e9
+    peaks = _peaks()
+    del layers
+    return {"workload": "2 dense SwiGLU layers (H=2048, width 6144, no router), batch 1, "
+                        "%d tokens per launch" % T,
+            "value": round(T / (ms * 1e-3), 1), "unit": "tok/s", "ms": round(ms, 4),
+            "us_per_token": round(ms * 1e3 / T, 3), "bytes_per_token": per_tok,
+            "GBs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
 
 
 def measure_fp4_peak(dev, iters: int = 20000):
@@ -649,7 +678,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--decode-only", action="store_true",
                     help="the decode line alone (no other measurements, no CPU baseline)")
-    ap.add_argument("--case", default=None, choices=["prefill", "layer", "lm_head", "fp4"],
+    ap.add_argument("--case", default=None, choices=["prefill", "layer", "lm_head", "fp4", "dense"],
                     help="time one other configuration alone (prints its object)")
     ap.add_argument("--prefill-only", action="store_true", help="same as --case prefill")
     args = ap.parse_args()
@@ -665,6 +694,8 @@ def main():
             res = measure_prefill(dev, reps=args.steps)
         elif args.case == "layer":
             res = measure_layer(dev, reps=args.steps)
+        elif args.case == "dense":
+            res = measure_dense(dev, reps=args.steps)
         elif args.case == "lm_head":
             head = workload.build_head(SEED, synth.FLINT.vocab, synth.FLINT.hidden, dev)
             res = measure_lm_head(dev, head, reps=args.steps)

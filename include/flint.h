@@ -81,6 +81,13 @@ typedef struct {
  * router_w is bf16 [E, H]; router_bias fp32 [E] or NULL (added to the logits).
  * The decode entry points read these row-major stacks directly (one copy of every
  * weight serves decode).
+ * A dense SwiGLU layer (the model's two dense MLP layers, width 6,144: "Flint: 125
+ * tokens a second ...", section "Built from scratch?") is a layer with n_experts =
+ * top_k = expert_width = 0: router_w, router_bias and the routed stacks are ignored
+ * (may be NULL), its block is sh_gate / sh_up / sh_down (shared_width a multiple of
+ * 64) and it is added with weight 1:  out = res + Wd (silu(Wg x) * (Wu x)).  The decode
+ * entry points take dense layers, alone or between MoE layers; flint_moe_prefill
+ * returns FLINT_ERR_UNSUPPORTED for them.
  * mma_scales: MMA scale copies (flint_nvfp4_mma_scales) of gate, up, down, sh_gate,
  * sh_up, sh_down in that order, required by flint_moe_prefill only, which reads the
  * row-major codes and these scales. */

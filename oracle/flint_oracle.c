@@ -333,7 +333,7 @@ static void forward_tokens_fn(void* p, int64_t lo, int64_t hi) {
   for (int64_t t = lo; t < hi; ++t) {
     const uint16_t* xt = c->x + t * H;
     double* ot = c->out + t * H;
-    orc_router(L, xt, NULL, ti, tw);
+    if (k > 0) orc_router(L, xt, NULL, ti, tw);    /* k = 0: a dense layer, no router */
     for (int64_t h = 0; h < H; ++h) xin[h] = orc_bf16_value(xt[h]);
     if (c->quantize_acts) requantize_unit(xin, H);
     for (int64_t h = 0; h < H; ++h)
@@ -352,7 +352,8 @@ static void forward_tokens_fn(void* p, int64_t lo, int64_t hi) {
 
 int orc_moe_forward(const orc_layer* L, const uint16_t* x, const double* residual,
                     int64_t n_tok, int quantize_acts, double* out, int32_t* idx, double* w) {
-  if (!L || L->top_k < 1 || L->top_k > L->n_experts || L->hidden % 16 ||
+  const int dense = L && L->top_k == 0 && L->n_experts == 0 && L->expert_width == 0;
+  if (!L || (!dense && (L->top_k < 1 || L->top_k > L->n_experts)) || L->hidden % 16 ||
       L->expert_width % 16 || L->shared_width % 16 ||
       (L->router_score != ORC_ROUTER_SOFTMAX && L->router_score != ORC_ROUTER_SIGMOID))
     return ORC_ERR_ARG;

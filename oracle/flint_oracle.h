@@ -99,7 +99,13 @@ void orc_router(const orc_layer* L, const uint16_t* x, double* logits, int32_t* 
  * residual: fp64 [n_tok, H] or NULL (then the bf16 input itself).
  * quantize_acts = 1 mirrors the prompt-processing path: x rows and the SwiGLU
  * outputs are NVFP4-quantised with unit tensor scale before each product.
- * idx/w: [n_tok, k] outputs (may be NULL).  Threads over tokens/rows. */
+ * idx/w: [n_tok, k] outputs (may be NULL).  Threads over tokens/rows.
+ * A dense SwiGLU layer -- the model's two dense MLP layers, width 6,144 ("Flint: 125
+ * tokens a second is what 2.5B active parameters buy at 273 GB/s", section "Built from
+ * scratch?") -- is a layer with n_experts = top_k = expert_width = 0: no router, no
+ * routed experts, out = residual + shared(x) with its matrices in sh_gate / sh_up /
+ * sh_down.  (Reading: the pages give the dense layers' width only; they are taken as
+ * the same SwiGLU block as an expert, without a router, added with weight 1.) */
 int orc_moe_forward(const orc_layer* L, const uint16_t* x, const double* residual,
                     int64_t n_tok, int quantize_acts, double* out, int32_t* idx, double* w);
 

@@ -30,8 +30,26 @@ flint_status check_nvfp4(const flint_nvfp4& m, int n_mat, int rows, int cols) {
   return FLINT_OK;
 }
 
+// A dense SwiGLU layer: no router and no routed experts, the block in sh_* (flint.h).
+inline bool is_dense(const flint_moe_layer* L) {
+  return L->n_experts == 0 && L->top_k == 0 && L->expert_width == 0;
+}
+
 flint_status check_layer(const flint_moe_layer* L) {
   if (!L) return FLINT_ERR_INVALID_ARG;
+  if (L->router_score != FLINT_ROUTER_SOFTMAX && L->router_score != FLINT_ROUTER_SIGMOID)
+    return FLINT_ERR_INVALID_ARG;
+  if (is_dense(L)) {
+    if (L->hidden <= 0 || L->shared_width <= 0) return FLINT_ERR_INVALID_ARG;
+    if (L->hidden % 32 || L->shared_width % 64) return FLINT_ERR_SHAPE;
+    if (!gemv_width_ok(L->hidden) || L->shared_width > 8 * FLINT_MAX_HIDDEN) return FLINT_ERR_UNSUPPORTED;
+    const int H = L->hidden, Fs = L->shared_width;
+    flint_status s;
+    if ((s = check_nvfp4(L->sh_gate, 1, Fs, H)) != FLINT_OK) return s;
+    if ((s = check_nvfp4(L->sh_up, 1, Fs, H)) != FLINT_OK) return s;
+    if ((s = check_nvfp4(L->sh_down, 1, H, Fs)) != FLINT_OK) return s;
+    return FLINT_OK;
+  }
   if (L->hidden <= 0 || L->n_experts <= 0 || L->top_k <= 0 || L->expert_width <= 0 ||
       L->shared_width <= 0)
     return FLINT_ERR_INVALID_ARG;
@@ -359,6 +377,7 @@ flint_status flint_moe_prefill(const flint_moe_layer* L, const void* x_bf16, flo
                                int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
                                int32_t* pair_order, int T, void* ws, size_t ws_bytes,
                                flint_stream stream) {
+  if (L && is_dense(L)) return FLINT_ERR_UNSUPPORTED;     // prompt path: MoE layers only
   flint_status s = check_layer(L);
   if (s != FLINT_OK) return s;
   if (!x_bf16 || !out || !ws) return FLINT_ERR_INVALID_ARG;

@@ -1374,7 +1374,7 @@ bool decode_plan_layer(DecLayer& d, int H, int NC) {
   int sh_np[kDecMaxClusters] = {0, 0, 0, 0, 0, 0, 0, 0};
   d.Wsh = 0;
   if (d.Fs > 0) {
-    if (d.Fs < 64 || (d.Fs & (d.Fs - 1))) return false;
+    if (d.Fs < 64 || d.Fs % 64) return false;
     int hosts[kDecMaxClusters], nh = 0;
     for (int cc = NR; cc < NC; ++cc) hosts[nh++] = cc;
     if (nh == 0)
@@ -1385,6 +1385,8 @@ bool decode_plan_layer(DecLayer& d, int H, int NC) {
     // one run per host
     int w = d.K > 0 ? (d.F < d.Fs ? d.F : d.Fs) : (d.Fs < 512 ? d.Fs : 512);
     if (w > 512) w = 512;
+    while (w > 64 && (d.Fs % w || (w / dc::kCS) % 4)) w -= 64;   // a divisor of Fs, n % 4 == 0
+    if (d.Fs % w || (w / dc::kCS) % 4) return false;
     d.Wsh = w;
     const int S = d.Fs / d.Wsh;
     const int used = S < nh ? S : nh;

@@ -133,6 +133,12 @@ TINY = MoeShape(hidden=256, n_experts=16, top_k=2, expert_width=64, shared_width
 FLINT = MoeShape(hidden=2048, n_experts=256, top_k=6, expert_width=512, shared_width=1024,
                  vocab=150144)
 
+# One of the model's dense SwiGLU layers ("Flint: 125 tokens a second is what 2.5B active
+# parameters buy at 273 GB/s", section "Built from scratch?": width 6,144): no router,
+# no routed experts; the block is the layer's shared matrices.
+FLINT_DENSE = MoeShape(hidden=2048, n_experts=0, top_k=0, expert_width=0, shared_width=6144,
+                       vocab=150144)
+
 W_SIGMA = 0.02
 X_SIGMA = 1.0
 

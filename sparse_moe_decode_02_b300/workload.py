@@ -21,8 +21,17 @@ def build_layer(spec: synth.LayerSpec, device="cuda", stream=None) -> flint.MoEL
         return m
 
     router = spec.weights_bf16(synth.KIND_ROUTER, device=device)[0].contiguous()
-    bias = spec.bias()
+    bias = spec.bias() if s.n_experts > 0 else None
     bias_t = None if bias is None else torch.from_numpy(bias).to(device)
+    if s.n_experts == 0:
+        # a dense layer: no routed stacks (empty placeholders; the library ignores them)
+        empty = lambda: flint.NVFP4(torch.empty(0, 0, s.hidden // 2, dtype=torch.uint8, device=device),
+                                    torch.empty(0, 0, s.hidden // 16, dtype=torch.uint8, device=device),
+                                    torch.empty(0, dtype=torch.float32, device=device))
+        gate, up, down = empty(), empty(), empty()
+        sh_gate, sh_up, sh_down = q(synth.KIND_SH_GATE), q(synth.KIND_SH_UP), q(synth.KIND_SH_DOWN)
+        return flint.MoELayer(router, None, gate, up, down, sh_gate, sh_up, sh_down, 0,
+                              mma_scales=None, router_score=spec.router_score)
     gate, up, down = q(synth.KIND_GATE), q(synth.KIND_UP), q(synth.KIND_DOWN)
     sh_gate, sh_up, sh_down = q(synth.KIND_SH_GATE), q(synth.KIND_SH_UP), q(synth.KIND_SH_DOWN)
     stacks = (gate, up, down, sh_gate, sh_up, sh_down)
@@ -44,7 +53,7 @@ def build_head(seed: int, vocab: int, hidden: int, device="cuda", stream=None) -
 def layer_bytes_per_token(shape: synth.MoeShape) -> int:
     """Algorithmic weight bytes one decode token reads from one layer: the bf16 router,
     top_k routed experts and the shared expert (gate, up, down) in NVFP4 (0.5 B codes +
-    1/16 B scales per weight), plus the per-matrix tensor scales."""
+    1/16 B scales per weight).  A dense layer (no experts) reads its block only."""
     H, F, Fs, k, E = (shape.hidden, shape.expert_width, shape.shared_width, shape.top_k,
                       shape.n_experts)
     nv = lambda n: n // 2 + n // 16

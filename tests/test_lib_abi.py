@@ -206,3 +206,20 @@ def test_decode_tokens_sample_argument_checks(L):
     assert call(k=0) == 1
     assert call(k=33) == 8                                               # > FLINT_MAX_SAMPLE_TOP_K
     assert call(tok=FAKE + 2) == 2
+
+
+def test_dense_layer_checks(L):
+    # a dense SwiGLU layer: n_experts = top_k = expert_width = 0, the block in sh_*
+    dense = flint._LayerC(256, 0, 0, 0, 384, None, None, _nv(0, 0, 256), _nv(0, 0, 256),
+                          _nv(0, 256, 0), _nv(1, 384, 256), _nv(1, 384, 256), _nv(1, 256, 384),
+                          (ctypes.c_void_p * 6)(*[None] * 6), 0)
+    ws = flint.workspace_bytes(flint.OP_MOE_DECODE, 256, 0, 0, 0, 384, 0, 1)
+    d = L.flint_moe_decode
+    # the checks accept it; with no GPU here the call then stops at the device query
+    assert d(ctypes.byref(dense), FAKE, None, FAKE, None, 1e-6, None, None, 1, FAKE, ws, None) == 7
+    bad = flint._LayerC(256, 0, 0, 0, 200, None, None, _nv(0, 0, 256), _nv(0, 0, 256),
+                        _nv(0, 256, 0), _nv(1, 200, 256), _nv(1, 200, 256), _nv(1, 256, 200),
+                        (ctypes.c_void_p * 6)(*[None] * 6), 0)
+    assert d(ctypes.byref(bad), FAKE, None, FAKE, None, 1e-6, None, None, 1, FAKE, ws, None) == 3
+    p = L.flint_moe_prefill
+    assert p(ctypes.byref(dense), FAKE, FAKE, None, None, None, None, 4, FAKE, 1 << 30, None) == 8

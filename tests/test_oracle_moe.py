@@ -293,3 +293,39 @@ def test_page_byte_accounting():
     assert abs(per_tok * bpw / 1e6 - g["routed_mb_per_token_4p5bpw"]["value"]) <= 0.5
     assert abs(head * bpw / 1e6 - g["head_mb_per_token_4p5bpw"]["value"]) <= 0.5
     assert s.hidden * 4 // 8 == g["head_bytes_per_row_4bit"]["value"]
+
+
+def _dense_layer(orc, seed=5, H=64, Fs=384, scale=0.02):
+    """A dense SwiGLU layer (no router, no routed experts; the block in sh_*)."""
+    g = torch.Generator().manual_seed(seed)
+    mk = lambda *s: (torch.randn(*s, generator=g) * scale).to(torch.bfloat16)
+    empty = lambda r, c: orc.NVFP4(np.zeros((0, r, c // 2), np.uint8), np.zeros((0, r, c // 16), np.uint8),
+                                   np.zeros(0, np.float32))
+    sg, _ = orc.quantize_nvfp4(mk(1, Fs, H))
+    su, _ = orc.quantize_nvfp4(mk(1, Fs, H))
+    sd, _ = orc.quantize_nvfp4(mk(1, H, Fs))
+    return orc.Layer(np.zeros((0, H), np.uint16), None, empty(0, H), empty(0, H), empty(H, 0), sg, su, sd, 0)
+
+
+def test_dense_layer_matches_numpy_restatement(orc):
+    # out = residual + Wd (silu(Wg x) * (Wu x)): the block alone, no router (width 384 is
+    # not a power of two, as the model's 6,144 is not)
+    L = _dense_layer(orc)
+    xb = orc._bits16(_x(5, 64, seed=9))
+    res = np.random.default_rng(3).standard_normal((5, 64))
+    out, idx, w = orc.moe_forward(L, xb, residual=res)
+    deq = lambda m: indep.dequantize_np(m.codes, m.scales, m.tsc).astype(np.float64)[0]
+    Sg, Su, Sd = deq(L.sh_gate), deq(L.sh_up), deq(L.sh_down)
+    xs = indep.bf16_to_f64(xb)
+    want = res + np.stack([Sd @ (indep.silu(Sg @ x) * (Su @ x)) for x in xs])
+    np.testing.assert_allclose(out, want, rtol=1e-12, atol=1e-12)
+    assert idx.shape == (5, 0) and w.shape == (5, 0)
+
+
+def test_dense_layer_zero_down_is_identity(orc):
+    L = _dense_layer(orc, seed=6)
+    zero, _ = orc.quantize_nvfp4(torch.zeros(1, 64, 384, dtype=torch.bfloat16))
+    L.sh_down = zero
+    xb = orc._bits16(_x(3, 64, seed=10))
+    out, _, _ = orc.moe_forward(L, xb)
+    np.testing.assert_array_equal(out, indep.bf16_to_f64(xb))
