@@ -116,8 +116,9 @@ __device__ __forceinline__ float exp2i(int k) { return __uint_as_float((uint32_t
 // every activation at full precision down to amax * 2^-29.  0 when amax == 0.
 __device__ __forceinline__ int f16_stage_exponent(float amax) {
   if (!(amax > 0.f)) return 0;
-  int e;
-  frexpf(amax, &e);             // amax in [2^(e-1), 2^e)
+  const uint32_t b = __float_as_uint(amax);
+  int e = (int)(b >> 23) - 126;  // amax in [2^(e-1), 2^e) for a normal amax
+  if ((b >> 23) == 0) frexpf(amax, &e);
   int k = 15 - e;
   return k > 126 ? 126 : (k < -126 ? -126 : k);
 }

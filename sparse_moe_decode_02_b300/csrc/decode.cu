@@ -24,7 +24,7 @@
 //   * The only exchange between clusters is the residual: CTA (c, j) posts its partial
 //     sums of rows R_j = [j H/16, (j+1) H/16) as tagged 64-bit words {value, step + 1}
 //     (no fence, no counter, no atomics); CTA j of every cluster reads all clusters'
-//     words of R_j and adds them in cluster order, so every cluster computes
+//     words of R_j and adds them in one fixed order, so every cluster computes
 //     bit-identical h rows, which the cluster then gathers through distributed shared
 //     memory.  Every sum has a fixed order: runs repeat bit for bit.
 //   * The head: after a token's last layer every CTA streams its share of the head rows
@@ -51,12 +51,15 @@ namespace dc {
 constexpr int kCS = kDecCluster;
 constexpr int kThreads = kDecThreads;
 constexpr int kWarps = kThreads / 32;
+static_assert(kWarps >= 8 && (kWarps & (kWarps - 1)) == 0, "warps per CTA: a power of two, at least 8");
 constexpr int kRouterBytes = 64 * 1024;   // router rows of one CTA
 constexpr int kBigBytes = 172 * 1024;     // router rows + group buffer, or the head ring
 constexpr int kMaxW = 1024;               // down columns of a group (one 32-column chunk per lane)
 constexpr int kMaxE = 256;                // experts of a routed layer
 constexpr int kMaxRR = kMaxE / kDecCluster;   // router rows per CTA
 constexpr int kMaxN = 64;                 // SwiGLU outputs per CTA and part
+constexpr int kMaxParts = 16;             // parts of a group (at least 4 SwiGLU values per CTA and part)
+static_assert(kMaxParts * 4 * kDecCluster >= kMaxW, "parts of a group");
 constexpr int kMaxG = kDecMaxClusters * kCS;
 
 // ---------------------------------------------------------------- PTX helpers
@@ -71,6 +74,14 @@ __device__ __forceinline__ unsigned cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// The two halves of cluster_sync, for work in between that touches no shared data of
+// the barrier's (the CTA's own copy descriptors, say).
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __device__ __forceinline__ uint32_t peer_addr(const void* local, int rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(local)), "r"(rank));
@@ -79,6 +90,27 @@ __device__ __forceinline__ uint32_t peer_addr(const void* local, int rank) {
 __device__ __forceinline__ void st_peer4(uint32_t addr, float4 v) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
                "f"(v.w) : "memory");
+}
+__device__ __forceinline__ void st_peer1(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
+}
+// One float to `dst` in CTA `peer`, completing 4 bytes on that CTA's barrier `bar`.
+__device__ __forceinline__ void st_async1(float* dst, float v, uint64_t* bar, int peer) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+               :: "r"(peer_addr(dst, peer)), "r"(__float_as_uint(v)), "r"(peer_addr(bar, peer)) : "memory");
+}
+// n 16-byte pieces of `src` (local shared memory) to `dst` in every CTA of the cluster,
+// each completing its bytes on that CTA's barrier `bar` (st.async: the receiver waits on
+// bar instead of a cluster barrier).
+__device__ __forceinline__ void to_cluster_async(float* dst, const float* src, int n, uint64_t* bar) {
+#pragma unroll 1
+  for (int i = threadIdx.x; i < kCS * n; i += kThreads) {
+    const int peer = i / n, k = i - peer * n;
+    const float4 v = *reinterpret_cast<const float4*>(src + 4 * k);
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+                 :: "r"(peer_addr(dst + 4 * k, peer)), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w),
+                    "r"(peer_addr(bar, peer)) : "memory");
+  }
 }
 // n 16-byte pieces of `src` (local shared memory) to `dst` in every CTA of the cluster.
 __device__ __forceinline__ void to_cluster(float* dst, const float* src, int n) {
@@ -119,6 +151,27 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for a copy phase (every thread that reads the data waits itself).
+// ... a phase completed by other CTAs' st.async (acquire at cluster scope).
+__device__ __forceinline__ bool mbar_try_cluster(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+               : "=r"(ok) : "r"(smem_addr(b)), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __noinline__ void mbar_wait_cluster(uint64_t* b, uint32_t parity, unsigned* sync, unsigned long long limit) {
+  unsigned long long t0 = 0;
+  for (unsigned polls = 1; !mbar_try_cluster(b, parity); ++polls) {
+    if ((polls & 63u) == 0) {
+      const unsigned long long now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > limit) {
+        give_up(sync);
+        return;
+      }
+    }
+  }
+}
 __device__ __noinline__ void mbar_wait(uint64_t* b, uint32_t parity, unsigned* sync, unsigned long long limit) {
   unsigned long long t0 = 0;
   for (unsigned polls = 1; !mbar_try(b, parity); ++polls) {
@@ -168,7 +221,7 @@ __device__ __forceinline__ int xl_index(int e, int LPR) {
 //   else:  x = bf16(h / sqrt(mean(h^2) + eps)), gain 1        (later layers, the head)
 // s_xb = x; s_xl = f16(x * 2^k) as above, 2^k putting max|x| in [2^14, 2^15) (max|bf16(h
 // r)| = bf16(max|h| r): rounding is monotone).  Returns 2^-k.
-__device__ __noinline__ float stage(const uint16_t* xg, const float* rg, bool input, int H, int LPR, float eps,
+__device__ __forceinline__ float stage(const uint16_t* xg, const float* rg, bool input, int H, int LPR, float eps,
                                     float* s_h, uint16_t* s_xb, uint32_t* s_xl, float* s_red) {
   const int n = 4 * threadIdx.x;
   float v[4] = {0.f, 0.f, 0.f, 0.f};
@@ -197,12 +250,26 @@ __device__ __noinline__ float stage(const uint16_t* xg, const float* rg, bool in
   const int warp = threadIdx.x >> 5;
   if ((threadIdx.x & 31) == 0) { s_red[warp] = ss; s_red[kWarps + warp] = am; }
   __syncthreads();
-  float tot = 0.f, amax = 0.f;
-#pragma unroll 1
-  for (int w = 0; w < kWarps; ++w) { tot += s_red[w]; amax = fmaxf(amax, s_red[kWarps + w]); }
+  // the kWarps partials in 16-byte loads, summed in one fixed order
+  const float4* r4 = reinterpret_cast<const float4*>(s_red);
+  float4 q[kWarps / 2];
+#pragma unroll
+  for (int i = 0; i < kWarps / 2; ++i) q[i] = r4[i];
+  float ps[kWarps / 4], pm[kWarps / 4];
+#pragma unroll
+  for (int i = 0; i < kWarps / 4; ++i) {
+    ps[i] = (q[i].x + q[i].y) + (q[i].z + q[i].w);
+    const float4 m = q[kWarps / 4 + i];
+    pm[i] = fmaxf(fmaxf(m.x, m.y), fmaxf(m.z, m.w));
+  }
+#pragma unroll
+  for (int w = kWarps / 8; w; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) { ps[i] += ps[i + w]; pm[i] = fmaxf(pm[i], pm[i + w]); }
+  const float tot = ps[0], amax = pm[0];
   float xmax = amax;
   if (!input) {
-    const float r = 1.0f / sqrtf(tot / (float)H + eps);
+    const float r = rsqrtf(__fdividef(tot, (float)H) + eps);
 #pragma unroll
     for (int q = 0; q < 4; ++q) b[q] = f32_to_bf16_rn(v[q] * r);
     xmax = bf16_bits_to_f32(f32_to_bf16_rn(amax * r));
@@ -283,31 +350,64 @@ __device__ __noinline__ void rows_dot(const uint8_t* codes, const uint8_t* scale
 }
 
 // ---------------------------------------------------------------- router and top-k
-// Router rows [r0, r0 + nr) from shared memory (warp w: rows w, w + 16, ...), bf16 x bf16
-// with fp32 accumulation, plus the bias, into s_tmp[r]; then every CTA of the cluster
-// receives them as 16-byte pieces (r0 is a multiple of 4; what a last piece carries past
-// row E lands past the logits the top-k reads).
-__device__ __noinline__ void router_rows(const uint16_t* s_router, const uint16_t* s_xb, int H, int r0, int nr,
-                                         const float* bias, float* s_tmp, float* s_lg) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll 1
-  for (int r = warp; r < nr; r += kWarps) {
-    const uint16_t* row = s_router + (size_t)r * H;
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 1
-    for (int e = 8 * lane; e < H; e += 256) {
-      const uint4 w = *reinterpret_cast<const uint4*>(row + e);
-      const uint4 x = *reinterpret_cast<const uint4*>(s_xb + e);
-      fma2_bf16(a0, a1, w.x, x.x);
-      fma2_bf16(a2, a3, w.y, x.y);
-      fma2_bf16(a0, a1, w.z, x.z);
-      fma2_bf16(a2, a3, w.w, x.w);
-    }
-    const float v = sum_lanes<32>((a0 + a1) + (a2 + a3)) + bias[r];
-    if (lane == 0) s_tmp[r] = v;
+// Router rows [r0, r0 + nr) (nr <= kMaxRR) from shared memory, bf16 x bf16 with fp32
+// accumulation, plus the bias; every CTA of the cluster receives them (4 bytes each on
+// its bar_lg).  Thread t takes
+// columns [4 q, 4 q + 4), q = t, t + kThreads, ..., of every row (x read once per CTA);
+// a warp reduces its sixteen row partials by halving exchanges (lane pair 2 m, 2 m + 1
+// ends with row m), the warps' partials meet in s_rp in a fixed order.
+// One halving exchange: lanes with bit O set keep rows [Hh, 2 Hh) of their current 2 Hh,
+// the others rows [0, Hh); each adds its partner's copy of the rows it keeps.
+template <int O, int Hh>
+__device__ __forceinline__ void halve_rows(float (&p)[kMaxRR], int lane) {
+  const bool up = (lane & O) != 0;
+#pragma unroll
+  for (int i = 0; i < Hh; ++i) {
+    const float send = up ? p[i] : p[i + Hh];
+    const float keep = up ? p[i + Hh] : p[i];
+    p[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
   }
+}
+__device__ __noinline__ void router_rows(const uint16_t* s_router, const uint16_t* s_xb, int H, int r0, int nr,
+                                         const float* bias, float* s_rp, float* s_lg, uint64_t* bar_lg) {
+  static_assert(kMaxRR == 16 && kWarps * kMaxRR <= 256, "router partials");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float p[kMaxRR], ph[kMaxRR];
+#pragma unroll
+  for (int r = 0; r < kMaxRR; ++r) { p[r] = 0.f; ph[r] = 0.f; }
+#pragma unroll 1
+  for (int q = threadIdx.x; q < H / 4; q += kThreads) {
+    const uint2 x = *reinterpret_cast<const uint2*>(s_xb + 4 * q);
+#pragma unroll
+    for (int r = 0; r < kMaxRR; ++r)
+      if (r < nr) {
+        const uint2 w = *reinterpret_cast<const uint2*>(s_router + (size_t)r * H + 4 * q);
+        fma2_bf16(p[r], ph[r], w.x, x.x);
+        fma2_bf16(p[r], ph[r], w.y, x.y);
+      }
+  }
+#pragma unroll
+  for (int r = 0; r < kMaxRR; ++r) p[r] += ph[r];
+  halve_rows<16, 8>(p, lane);
+  halve_rows<8, 4>(p, lane);
+  halve_rows<4, 2>(p, lane);
+  halve_rows<2, 1>(p, lane);
+  p[0] += __shfl_xor_sync(0xffffffffu, p[0], 1);
+  if ((lane & 1) == 0) s_rp[warp * kMaxRR + (lane >> 1)] = p[0];
   __syncthreads();
-  to_cluster(s_lg + r0, s_tmp, (nr + 3) / 4);
+  if (threadIdx.x < kMaxRR * kCS) {
+    const int r = threadIdx.x % kMaxRR, peer = threadIdx.x / kMaxRR;
+    if (r < nr) {
+      float v[kWarps];
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) v[w] = s_rp[w * kMaxRR + r];
+#pragma unroll
+      for (int h = kWarps / 2; h; h >>= 1)
+#pragma unroll
+        for (int i = 0; i < h; ++i) v[i] += v[i + h];
+      st_async1(s_lg + r0 + r, v[0] + bias[r], bar_lg, peer);
+    }
+  }
 }
 
 __device__ __forceinline__ unsigned order_key(float v) {
@@ -319,91 +419,64 @@ __device__ __forceinline__ float key_value(unsigned k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Exact top-k by one warp when the threshold step leaves too many candidates (ties):
-// lane l holds logits l + 32 i; each of K rounds takes the largest key, lowest index
-// among equals.  Selected (index, key) into s_sel / s_key.
-__device__ __noinline__ void topk_rounds(const float* s_lg, int E, int K, int* s_sel, unsigned* s_key) {
-  const int lane = threadIdx.x & 31;
-  unsigned key[kMaxE / 32];
-#pragma unroll
-  for (int i = 0; i < kMaxE / 32; ++i) {
-    const int e = lane + 32 * i;
-    key[i] = e < E ? order_key(s_lg[e]) : 0u;  // every live key is >= 1
-  }
-#pragma unroll 1
-  for (int s = 0; s < K; ++s) {
-    unsigned lb = 0u;
-    int li = 0x7FFFFFFF;
-#pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i)
-      if (key[i] > lb) { lb = key[i]; li = lane + 32 * i; }
-    const unsigned wk = __reduce_max_sync(0xffffffffu, lb);
-    const int wi = (int)__reduce_min_sync(0xffffffffu, lb == wk ? (unsigned)li : 0xFFFFFFFFu);
-    if (lane == 0) { s_sel[s] = wi; s_key[s] = wk; }
-#pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i)
-      if (lane + 32 * i == wi) key[i] = 0u;
-  }
-}
-
 // Softmax (or sigmoid) top-k of the E <= kMaxE logits, ties to the lower index, exact.
-// Warps w < ceil(E/32) hold logits 32 w + lane.  The K-th largest warp maximum is a
-// threshold the K best all reach (at least K warps hold a logit at or above it); the
-// logits at or above it are ranked by (key, lower index) in one warp.  If more than 32
-// reach it (ties), topk_rounds decides.  Weights: the selected scores over their sum.
-// Every thread calls this.
-__device__ __noinline__ void topk(const float* s_lg, int E, int K, int score, int* s_sel, float* s_w,
-                                  unsigned* s_wm, int* s_n, unsigned long long* s_cand, unsigned* s_key) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nw = (E + 31) / 32;
-  const int e = 32 * warp + lane;
-  const unsigned key = (warp < nw && e < E) ? order_key(s_lg[e]) : 0u;
-  if (warp < nw) {
-    const unsigned wm = __reduce_max_sync(0xffffffffu, key);
-    if (lane == 0) s_wm[warp] = wm;
-  }
-  if (threadIdx.x == 0) *s_n = 0;
-  __syncthreads();
-  if (warp < nw) {
-    unsigned thr = 0u;                           // K > nw: every logit is a candidate
-    if (nw >= K) {
-      const unsigned m = lane < nw ? s_wm[lane] : 0u;
-      int ge = 0;
+// Warp 0 alone: lane l holds the keys of logits l + 32 i; each of K rounds takes the
+// largest key by one warp max-reduction, the lowest index holding it by one
+// min-reduction, and retires it.  Weights: the selected scores over their sum.  Every
+// thread calls this (one barrier at the end).
+__device__ __forceinline__ void best_of_lane(const unsigned (&key)[kMaxE / 32], unsigned& b, int& bi) {
+  unsigned k2[kMaxE / 64];
+  int i2[kMaxE / 64];
 #pragma unroll
-      for (int u = 0; u < kMaxE / 32; ++u) ge += (u < nw && s_wm[u] >= m) ? 1 : 0;
-      thr = __reduce_max_sync(0xffffffffu, (lane < nw && ge >= K) ? m : 0u);
-    }
-    const bool cand = key != 0u && key >= thr;
-    const unsigned bal = __ballot_sync(0xffffffffu, cand);
-    int base = 0;
-    if (lane == 0 && bal) base = atomicAdd(s_n, __popc(bal));
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (cand) s_cand[base + __popc(bal & ((1u << lane) - 1u))] = ((unsigned long long)key << 32) | (unsigned)(~e);
+  for (int i = 0; i < kMaxE / 64; ++i) {           // pairs, then a tree: ties keep the lower i
+    const bool hi = key[2 * i + 1] > key[2 * i];
+    k2[i] = hi ? key[2 * i + 1] : key[2 * i];
+    i2[i] = hi ? 2 * i + 1 : 2 * i;
   }
-  __syncthreads();
-  if (warp == 0) {
-    const int n = *s_n;
-    if (n <= 32) {
-      const unsigned long long ck = lane < n ? s_cand[lane] : 0ull;
-      int rank = 0;
 #pragma unroll
-      for (int m = 0; m < 32; ++m) rank += (m < n && s_cand[m] > ck) ? 1 : 0;   // broadcast reads
-      if (lane < n && rank < K) {
-        s_sel[rank] = (int)(~(unsigned)ck);
-        s_key[rank] = (unsigned)(ck >> 32);
-      }
-      __syncwarp();
-    } else {
-      topk_rounds(s_lg, E, K, s_sel, s_key);
-      __syncwarp();
+  for (int w = kMaxE / 128; w; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const bool hi = k2[i + w] > k2[i];
+      k2[i] = hi ? k2[i + w] : k2[i];
+      i2[i] = hi ? i2[i + w] : i2[i];
     }
-    const float l = lane < K ? key_value(s_key[lane]) : 0.f;
+  b = k2[0];
+  bi = i2[0];
+}
+__device__ __noinline__ void topk(const float* s_lg, int E, int K, int score, int* s_sel, float* s_w) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    unsigned key[kMaxE / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) {
+      const int e = lane + 32 * i;
+      key[i] = e < E ? order_key(s_lg[e]) : 0u;  // every live key is >= 1
+    }
+    unsigned mine = 0u;                           // lane r < K: round r's key and index
+    int mine_e = 0;
+#pragma unroll 1
+    for (int r = 0; r < K; ++r) {
+      unsigned b;
+      int bi;
+      best_of_lane(key, b, bi);
+      const unsigned wk = __reduce_max_sync(0xffffffffu, b);
+      const int wi = (int)__reduce_min_sync(0xffffffffu, b == wk ? (unsigned)(lane + 32 * bi) : 0xFFFFFFFFu);
+      if (lane == r) { mine = wk; mine_e = wi; }
+#pragma unroll
+      for (int i = 0; i < kMaxE / 32; ++i)
+        if (lane + 32 * i == wi) key[i] = 0u;
+    }
+    const float l = lane < K ? key_value(mine) : 0.f;
     const float l0 = __shfl_sync(0xffffffffu, l, 0);
     const float p = lane >= K ? 0.f : score == FLINT_ROUTER_SIGMOID ? 1.0f / (1.0f + expf(-l)) : expf(l - l0);
     float z = p;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    if (lane < K) s_w[lane] = p / z;
+    for (int o = FLINT_MAX_TOP_K / 2; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    if (lane < K) {
+      s_sel[lane] = mine_e;
+      s_w[lane] = __fdividef(p, z);
+    }
   }
   __syncthreads();
 }
@@ -443,53 +516,171 @@ struct GroupOff {
   __host__ __device__ uint32_t down_slot(int np) const { return slot(np >= 2 ? (np - 2) % 2 : 1); }
 };
 
-// A group's contiguous copies, one per warp (lane 0 of warp w0 + k issues copy k: the
-// lanes of one warp issue bulk copies one after another, different warps side by side;
-// every thread calls this):
+// A group's contiguous copies, one per warp (lane 0 of warp w0 + k makes copy k: the
+// lanes of one warp issue bulk copies one after another, different warps side by side):
 //   what >= 0: part `what` -- this CTA's n gate rows and n up rows (codes, then scales)
 //              into `dst`; part 0 also brings the group's three tensor scales into tsc;
 //   what <  0: the group's down rows R_j (all its W columns: the group spans whole rows).
 // Copy 0's thread posts the byte count on `bar` (its one arrival); the copies land on it.
-__device__ __noinline__ void issue_copies(const DecLayer& D, int c, int g, int what, int e, int j, int H,
-                                          uint8_t* dst, float* tsc, uint64_t* bar, int w0) {
-  const int k = (threadIdx.x & 31) == 0 ? (int)(threadIdx.x >> 5) - w0 : -1;   // this thread's copy
-  if (k < 0 || k >= 7) return;
+// A copy is described before the expert is known: source base + e * stride (e the routed
+// expert, 0 for a shared group), `bytes` (0: none) to dst, a bulk copy (kind 0) or a
+// 4-byte cp.async that holds bar's phase open until it lands (kind 1).
+struct CopyDesc {
+  const uint8_t* base;
+  unsigned long long stride;
+  uint32_t dst, bar, bytes, kind;
+};
+constexpr int kCopyWarps = 7;                 // copies of one call: warps w0 .. w0 + 6
+constexpr int kDownW0 = 8;                    // first warp of the down-row copies
+static_assert(kDownW0 >= kCopyWarps && kDownW0 + kCopyWarps <= kWarps, "copy warps");
+
+// Copy k (0 <= k < kCopyWarps) of a group; *expect: the byte count copy 0 posts.
+__device__ __forceinline__ CopyDesc copy_desc(const DecLayer& D, int c, int g, int what, int k, int j, int H,
+                                              uint8_t* dst, float* tsc, uint64_t* bar, uint32_t* expect) {
+  CopyDesc cd;
+  cd.base = nullptr;
+  cd.stride = 0;
+  cd.dst = smem_addr(dst);
+  cd.bar = smem_addr(bar);
+  cd.bytes = 0;
+  cd.kind = 0;
   const GroupDims d = group_dims(D, c, g);
   const bool routed = d.rank >= 0;
-  const uint8_t* src = nullptr;
-  uint32_t off = 0, bytes = 0, total = 0;
   if (what >= 0) {
-    const size_t row0 = routed ? (size_t)e * D.F + (size_t)d.n * j
-                               : (size_t)(D.p0[c][g] + what) * D.Wsh + (size_t)d.n * j;
+    const size_t row0 = routed ? (size_t)d.n * j : (size_t)(D.p0[c][g] + what) * D.Wsh + (size_t)d.n * j;
+    const size_t rows_e = routed ? (size_t)D.F : 0;          // rows per expert
     const NVPtr& P = (k & 1) ? (routed ? D.up : D.sh_up) : (routed ? D.gate : D.sh_gate);
     const uint32_t cb = d.n * H / 2, sb = d.n * H / 16;
-    total = 2 * (cb + sb);
+    *expect = 2 * (cb + sb);
     if (k < 2) {                                  // codes: gate, up
-      src = P.codes + row0 * (H / 2);
-      off = k * cb;
-      bytes = cb;
+      cd.base = P.codes + row0 * (H / 2);
+      cd.stride = rows_e * (H / 2);
+      cd.dst += k * cb;
+      cd.bytes = cb;
     } else if (k < 4) {                           // scales: gate, up
-      src = P.scales + row0 * (H / 16);
-      off = a16(2 * cb) + (k - 2) * sb;
-      bytes = sb;
-    }
-    if (what == 0 && k >= 4 && k < 7) {        // tensor scales of gate, up, down
+      cd.base = P.scales + row0 * (H / 16);
+      cd.stride = rows_e * (H / 16);
+      cd.dst += a16(2 * cb) + (k - 2) * sb;
+      cd.bytes = sb;
+    } else if (what == 0 && k < 7) {              // tensor scales of gate, up, down
       const NVPtr& T = k == 4 ? (routed ? D.gate : D.sh_gate) : k == 5 ? (routed ? D.up : D.sh_up)
-                                                                             : (routed ? D.down : D.sh_down);
-      cp_async4(tsc + (k - 4), T.tsc + (routed ? e : 0));
-      cp_async_arrive_hold(bar);
+                                                                       : (routed ? D.down : D.sh_down);
+      cd.base = reinterpret_cast<const uint8_t*>(T.tsc);
+      cd.stride = routed ? 4 : 0;
+      cd.dst = smem_addr(tsc + (k - 4));
+      cd.bytes = 4;
+      cd.kind = 1;
     }
   } else {
     const int R16 = H / 16;
-    const size_t drow0 = (routed ? (size_t)e * H : 0) + (size_t)R16 * j;
+    const size_t drow0 = (size_t)R16 * j;
+    const size_t rows_e = routed ? (size_t)H : 0;
     const NVPtr& Dn = routed ? D.down : D.sh_down;
     const uint32_t dcb = R16 * d.W / 2, dsb = R16 * d.W / 16;
-    total = dcb + dsb;
-    if (k == 0) { src = Dn.codes + drow0 * (d.W / 2); bytes = dcb; }
-    if (k == 1) { src = Dn.scales + drow0 * (d.W / 16); off = a16(dcb); bytes = dsb; }
+    *expect = dcb + dsb;
+    if (k == 0) {
+      cd.base = Dn.codes + drow0 * (d.W / 2);
+      cd.stride = rows_e * (d.W / 2);
+      cd.bytes = dcb;
+    } else if (k == 1) {
+      cd.base = Dn.scales + drow0 * (d.W / 16);
+      cd.stride = rows_e * (d.W / 16);
+      cd.dst += a16(dcb);
+      cd.bytes = dsb;
+    }
   }
-  if (k == 0) mbar_expect_tx(bar, total);
-  if (bytes) bulk_g2s(dst + off, src, bytes, bar);
+  return cd;
+}
+__device__ __forceinline__ void copy_go(const CopyDesc& cd, int e) {
+  if (!cd.bytes) return;
+  const uint8_t* src = cd.base + (size_t)e * cd.stride;
+  if (cd.kind == 0) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(cd.dst), "l"(src), "r"(cd.bytes), "r"(cd.bar) : "memory");
+  } else {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(cd.dst), "l"(src) : "memory");
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" :: "r"(cd.bar) : "memory");
+  }
+}
+// The copies of a group issued now (e: the routed expert); every thread calls this.
+__device__ __noinline__ void issue_copies(const DecLayer& D, int c, int g, int what, int e, int j, int H,
+                                          uint8_t* dst, float* tsc, uint64_t* bar, int w0) {
+  const int k = (threadIdx.x & 31) == 0 ? (int)(threadIdx.x >> 5) - w0 : -1;   // this thread's copy
+  if (k < 0 || k >= kCopyWarps) return;
+  uint32_t expect = 0;
+  const CopyDesc cd = copy_desc(D, c, g, what, k, j, H, dst, tsc, bar, &expect);
+  if (k == 0) mbar_expect_tx(bar, expect);
+  copy_go(cd, e);
+}
+// ... described now, issued later by prepared_go (a shared group: e = 0); copy 0 posts
+// the byte count at once.  Every thread calls this.
+__device__ __noinline__ void prepare_copies(const DecLayer& D, int c, int g, int what, int j, int H, uint8_t* dst,
+                                            float* tsc, uint64_t* bar, int w0, CopyDesc* s_cp) {
+  const int k = (threadIdx.x & 31) == 0 ? (int)(threadIdx.x >> 5) - w0 : -1;
+  if (k < 0 || k >= kCopyWarps) return;
+  uint32_t expect = 0;
+  s_cp[threadIdx.x >> 5] = copy_desc(D, c, g, what, k, j, H, dst, tsc, bar, &expect);
+  if (k == 0) mbar_expect_tx(bar, expect);
+}
+// A routed group's first copies described before its expert is known, for expert 0
+// (prepared_go adds e * stride): part 0 (copies 0..6, warps 0..6) into buf, the down rows
+// (copies 0..1, warps kDownW0..) into slot 1.  The routed buffer sits at the start of the
+// big region and holds one part, so none of this depends on which group it is.  Copy 0
+// of each posts its byte count at once (the phase then waits for the copies).  Every
+// thread calls this.
+__device__ __noinline__ void prepare_routed_copies(const DecLayer& D, int j, int H, uint8_t* buf, float* tsc,
+                                                   uint64_t* bar_gu, uint64_t* bar_dn, CopyDesc* s_cp) {
+  if (threadIdx.x & 31) return;
+  const int w = threadIdx.x >> 5;
+  const bool part = w < kCopyWarps, down = w >= kDownW0 && w < kDownW0 + kCopyWarps;
+  if (!part && !down) return;
+  const int F = D.F, n = F / kCS, R16 = H / 16;
+  const uint32_t cb = n * H / 2, sb = n * H / 16;
+  CopyDesc cd;
+  cd.base = nullptr;
+  cd.stride = 0;
+  cd.bytes = 0;
+  cd.kind = 0;
+  if (part) {
+    const int k = w;
+    cd.bar = smem_addr(bar_gu);
+    cd.dst = smem_addr(buf);
+    if (k < 4) {                                  // codes gate, up; scales gate, up
+      const NVPtr& P = (k & 1) ? D.up : D.gate;
+      const bool sc = k >= 2;
+      const uint32_t row = sc ? H / 16 : H / 2;
+      cd.base = (sc ? P.scales : P.codes) + (size_t)n * j * row;
+      cd.stride = (unsigned long long)F * row;
+      cd.dst += sc ? a16(2 * cb) + (k - 2) * sb : k * cb;
+      cd.bytes = sc ? sb : cb;
+    } else {                                      // tensor scales of gate, up, down
+      const NVPtr& T = k == 4 ? D.gate : k == 5 ? D.up : D.down;
+      cd.base = reinterpret_cast<const uint8_t*>(T.tsc);
+      cd.stride = 4;
+      cd.dst = smem_addr(tsc + (k - 4));
+      cd.bytes = 4;
+      cd.kind = 1;
+    }
+    if (k == 0) mbar_expect_tx(bar_gu, 2 * (cb + sb));
+  } else {
+    const int k = w - kDownW0;
+    const uint32_t dcb = R16 * F / 2, dsb = R16 * F / 16;
+    cd.bar = smem_addr(bar_dn);
+    cd.dst = smem_addr(buf) + a16(2 * cb) + a16(2 * sb);   // slot 1 of a one-part group
+    if (k < 2) {                                  // codes, scales
+      const uint32_t row = k ? F / 16 : F / 2;
+      cd.base = (k ? D.down.scales : D.down.codes) + (size_t)R16 * j * row;
+      cd.stride = (unsigned long long)H * row;
+      cd.dst += k ? a16(dcb) : 0u;
+      cd.bytes = k ? dsb : dcb;
+    }
+    if (k == 0) mbar_expect_tx(bar_dn, dcb + dsb);
+  }
+  s_cp[w] = cd;
+}
+__device__ __forceinline__ void prepared_go(const CopyDesc* s_cp, int e, int w0) {
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0 && w >= w0 && w < w0 + kCopyWarps) copy_go(s_cp[w], e);
 }
 
 // ... strided down rows (a shared group spanning part of the columns): cp.async from every
@@ -531,8 +722,8 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 // Down columns of a group: this CTA's R16 rows (codes [R16][W/2], scales [R16][W/16] in
-// shared memory) times the group's W SwiGLU values hsw, added (times `scale`) into
-// s_part.  Every thread calls this.
+// shared memory) times the group's W SwiGLU values hsw (whose producers' maxima are in
+// hmax), added (times `scale`) into s_part.  Every thread calls this.
 //
 // hsw is split into two f16 terms under one power-of-two scale 2^k (max |hsw| 2^k in
 // [2^14, 2^15)): hi = f16(v 2^k), lo = f16(v 2^k - hi), about 22 bits of every value.
@@ -544,18 +735,16 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 // order of the columns within an mma is a fixed permutation that the B operand (read by
 // the same lane from the same chunk) follows.
 __device__ __noinline__ void group_down(const uint8_t* dcodes, const uint8_t* dscales, int W, int R16,
-                                        const float* hsw, uint32_t* s_hh, uint32_t* s_hl, float* s_red, float* s_acc,
-                                        float scale, float* s_part) {
+                                        const float* hsw, const float* hmax, int nmax, uint32_t* s_hh,
+                                        uint32_t* s_hl, float* s_acc, float scale, float* s_part) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // 1. one scale for the group: max |hsw| over the CTA (non-negative floats order as
+  // 1. one scale for the group: the max of the producers' maxima (hmax[i], i < nmax:
+  // every part's CTAs sent theirs with their values; non-negative floats order as
   // their bit patterns)
   float am = 0.f;
 #pragma unroll 1
-  for (int i = threadIdx.x; i < W; i += kThreads) am = fmaxf(am, fabsf(hsw[i]));
-  const unsigned wm = __reduce_max_sync(0xffffffffu, __float_as_uint(am));
-  if (lane == 0) s_red[warp] = __uint_as_float(wm);
-  __syncthreads();
-  am = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(s_red[lane & (kWarps - 1)])));
+  for (int i = lane; i < nmax; i += 32) am = fmaxf(am, hmax[i]);
+  am = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(am)));
   const int k = f16_stage_exponent(am);
   const float s2k = exp2i(k);
   // 2. the hi / lo terms, f16 pairs in column order
@@ -637,10 +826,11 @@ __device__ __noinline__ void group_down(const uint8_t* dcodes, const uint8_t* ds
 // ---------------------------------------------------------------- residual exchange
 // post_rows posts this CTA's partial rows.  exchange waits (bounded) until every word it
 // reads carries `tag`: word i = c' * H/16 + r is row r of R_j from cluster c'; two per
-// thread, both in flight at once.  Then h_{l+1}[R_j] = h_l[R_j] + the clusters' partials
-// in cluster order, into s_hn, which goes to every CTA of the cluster (h_nxt) and, when
-// `out` is given, to out.  Thread 0 also refreshes *s_abort (its load completes during
-// the poll).  Every thread calls this.
+// thread, both in flight at once.  Then h_{l+1}[R_j] = h_l[R_j] + the
+// clusters' partials summed pairwise in a fixed order, into s_hn, which goes to every
+// CTA of the cluster (h_nxt, completing on each one's bar_nxt) and, when `out` is given,
+// to out.  Thread 0 also refreshes *s_abort (its load completes during the poll).  Every
+// thread calls this.
 __device__ __forceinline__ void post_rows(unsigned long long* bd, int c, int H, int j, unsigned tag,
                                           const float* s_part) {
   const int R16 = H / 16;
@@ -649,7 +839,7 @@ __device__ __forceinline__ void post_rows(unsigned long long* bd, int c, int H, 
     st_tagged(bd + (size_t)c * H + (size_t)R16 * j + r, ((unsigned long long)tag << 32) | __float_as_uint(s_part[r]));
 }
 __device__ __noinline__ void exchange(const unsigned long long* bd, int NC, int H, int j, unsigned tag,
-                                      float* s_pp, const float* h_cur, float* s_hn, float* h_nxt,
+                                      float* s_pp, const float* h_cur, float* s_hn, float* h_nxt, uint64_t* bar_nxt,
                                       float* out, unsigned* sync, unsigned long long limit, int* s_abort) {
   const int R16 = H / 16;
   const unsigned ab = threadIdx.x == 0 ? ld_abort(sync) : 0u;
@@ -682,14 +872,19 @@ __device__ __noinline__ void exchange(const unsigned long long* bd, int NC, int 
   __syncthreads();
 #pragma unroll 1
   for (int r = threadIdx.x; r < R16; r += kThreads) {
-    float h = h_cur[R16 * j + r];
-#pragma unroll 1
-    for (int k = 0; k < NC; ++k) h += s_pp[k * R16 + r];
+    float v[kDecMaxClusters];
+#pragma unroll
+    for (int k = 0; k < kDecMaxClusters; ++k) v[k] = k < NC ? s_pp[k * R16 + r] : 0.f;
+#pragma unroll
+    for (int w = kDecMaxClusters / 2; w; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) v[i] += v[i + w];
+    const float h = h_cur[R16 * j + r] + v[0];
     s_hn[r] = h;
     if (out) out[R16 * j + r] = h;
   }
   __syncthreads();
-  to_cluster(h_nxt + R16 * j, s_hn, R16 / 4);
+  to_cluster_async(h_nxt + R16 * j, s_hn, R16 / 4, bar_nxt);
 }
 
 // ---------------------------------------------------------------- head
@@ -869,7 +1064,7 @@ static_assert(sizeof(DecLayer) % 8 == 0 && kLayerWords <= 32, "layer table: at m
 
 // Shared-memory carve (bytes), the same on the host and the device.
 struct Smem {
-  uint32_t h, xb, xl, lg, hsw, tmp, part, pp, gu, hn, hv, hh, hl, acc, cand, big, total;
+  uint32_t h, xb, xl, lg, hsw, hmax, tmp, part, pp, gu, hn, hv, hh, hl, acc, big, total;
   __host__ __device__ static Smem of(int H, int Emax) {
     Smem s;
     const int R16 = H / 16;
@@ -878,7 +1073,8 @@ struct Smem {
     s.xl = s.xb + 2 * H;                       // [H/8] uint4 x operand, lane-major
     s.lg = s.xl + 2 * H;                       // [2][Emax] fp32 logits (by step parity)
     s.hsw = s.lg + a16(8 * Emax);              // [2][kMaxW] fp32 SwiGLU values (by group parity)
-    s.tmp = s.hsw + 8 * kMaxW;                 // [kMaxN] fp32 this CTA's SwiGLU values / logits
+    s.hmax = s.hsw + 8 * kMaxW;                // [2][kMaxParts][kCS] fp32 the producers' max |value|
+    s.tmp = s.hmax + 2 * 4 * kCS * kMaxParts;  // [kMaxN] fp32 this CTA's SwiGLU values / logits
     s.part = s.tmp + 4 * kMaxN;                // [H/16] fp32 partial sums of this CTA's rows
     s.pp = s.part + 4 * R16;                   // [kDecMaxClusters][H/16] polled partials
     s.gu = s.pp + 4 * kDecMaxClusters * R16;   // [2 kMaxN] gate/up values
@@ -887,8 +1083,7 @@ struct Smem {
     s.hh = s.hv + 4 * 256;                     // [kMaxW/2] f16 pairs: hi terms of the SwiGLU values
     s.hl = s.hh + 2 * kMaxW;                   // [kMaxW/2] f16 pairs: lo terms
     s.acc = s.hl + 2 * kMaxW;                  // [256] fp32 down partials (chunk-set range x row)
-    s.cand = s.acc + 4 * 256;                  // [kMaxE] u64 top-k candidates
-    s.big = (s.cand + 8 * kMaxE + 127) & ~127u;      // router rows + group buffer, or the head ring
+    s.big = (s.acc + 4 * 256 + 127) & ~127u;   // router rows + group buffer, or the head ring
     s.total = s.big + kBigBytes;
     return s;
   }
@@ -962,16 +1157,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
   __shared__ float s_bias[3][kMaxRR];
   __shared__ int s_sel[FLINT_MAX_TOP_K];
   __shared__ float s_w[FLINT_MAX_TOP_K];
-  __shared__ unsigned s_key[FLINT_MAX_TOP_K];
-  __shared__ unsigned s_wm[8];
-  __shared__ int s_n;
   __shared__ __align__(16) float s_tsc[2][4];        // tensor scales of the shared / routed group in flight
-  __shared__ float s_red[2 * kWarps];
+  __shared__ __align__(16) CopyDesc s_cp[kWarps];      // prepared copies, by issuing warp
+  __shared__ __align__(16) float s_red[2 * kWarps];
   __shared__ float s_bv[kWarps];
   __shared__ int s_bi[kWarps];
   // copy barriers: router rows, shared parts (two slots), shared down rows (bulk or
   // cp.async), routed part, routed down rows; head ring
-  __shared__ __align__(8) uint64_t bars[7], bar_hd[2];
+  __shared__ __align__(8) uint64_t bars[7], bar_hd[2], bar_h[2];   // bar_h: h_{l+1} landed (by parity)
+  // the peers' logits (by step parity) and SwiGLU values (by group parity) landed
+  __shared__ __align__(8) uint64_t bar_c[4];
+  uint64_t* bar_lg = bar_c;
   __shared__ int s_abort;                            // this CTA saw the abort flag (refreshed per step)
 
   const int H = a.H, R16 = H / 16;
@@ -983,6 +1179,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
   float* s_lg = reinterpret_cast<float*>(s_dyn + S.lg);
   float* s_hsw = reinterpret_cast<float*>(s_dyn + S.hsw);
   float* s_tmp = reinterpret_cast<float*>(s_dyn + S.tmp);
+  float* s_hmax = reinterpret_cast<float*>(s_dyn + S.hmax);
   float* s_part = reinterpret_cast<float*>(s_dyn + S.part);
   float* s_pp = reinterpret_cast<float*>(s_dyn + S.pp);
   float* s_gu = reinterpret_cast<float*>(s_dyn + S.gu);
@@ -991,7 +1188,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
   uint32_t* s_hh = reinterpret_cast<uint32_t*>(s_dyn + S.hh);
   uint32_t* s_hl = reinterpret_cast<uint32_t*>(s_dyn + S.hl);
   float* s_acc = reinterpret_cast<float*>(s_dyn + S.acc);
-  unsigned long long* s_cand = reinterpret_cast<unsigned long long*>(s_dyn + S.cand);
   uint8_t* s_big = s_dyn + S.big;
   uint16_t* s_router = reinterpret_cast<uint16_t*>(s_big);
 
@@ -1006,7 +1202,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
   // per barrier (a bit each): the parity of its current phase, and whether a copy is in
   // flight on it.  A wait happens only for an issued copy, and after an abort no new copy
   // is issued, so the kernel ends with nothing in flight.
-  uint32_t ph = 0, pend = 0, ph_hd = 0, pend_hd = 0;
+  uint32_t ph = 0, pend = 0, ph_hd = 0, pend_hd = 0, ph_h = 0, ph_c = 0;
   unsigned grp_seq = 0;                              // groups run by this cluster
   unsigned pre = 0;                                  // this step's groups already in flight (a bit each)
   auto wait_bar = [&](int i) {
@@ -1017,9 +1213,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     }
   };
 
-  // warp 15: the layer table of step `st` and this CTA's router bias entries (the
+  // the last warp: the layer table of step `st` and this CTA's router bias entries (the
   // parameter's table sits in the constant bank, where each layer's first use would
-  // miss).  The loads are issued at a step's start and stored at its end.
+  // miss).  The loads are issued at a step's start and stored at its end; the staging
+  // between them is inlined, so the first call that needs them settled comes late.
   unsigned long long ly_word = 0;
   float ly_bias = 0.f;
   auto load_layer = [&](int st) {
@@ -1063,7 +1260,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     }
     const int b = what >= 0 ? (routed ? B_RGU : B_GU0 + (what & 1)) : (routed ? B_RDN : B_DN);
     issue_copies(D, c, g, what, routed ? s_sel[d.rank] : 0, j, H, buf + (what >= 0 ? o.slot(what & 1) : o.down_slot(d.np)),
-                   s_tsc[routed], &bars[b], what >= 0 ? 0 : 8);
+                   s_tsc[routed], &bars[b], what >= 0 ? 0 : kDownW0);
     pend |= 1u << b;
   };
   // a group's first copies: part 0, and part 1 or else the down rows
@@ -1071,17 +1268,53 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     issue(D, g, 0);
     issue(D, g, D.rank[c][g] < 0 && D.np[c][g] >= 2 ? 1 : -1);
   };
+  // While this step's last group waits for its SwiGLU values, the next step's copies
+  // that have room already: its router rows over this routed group's consumed part, and
+  // for a next group like this one (shared, an even number >= 2 of parts, same buffer and
+  // slots: this group's down rows sit in slot 0) its part 1 into the free slot 1, with
+  // part 0 described for prepared_go once this group's down rows are used.  Returns
+  // whether part 0 was described (bit 0) and the router rows issued (bit 1).
+  auto issue_early = [&](const DecLayer& D, const DecLayer& DN, int g, const GroupDims& d, const GroupOff& o,
+                         const uint8_t* buf) -> unsigned {
+    unsigned r = 0;
+    if (DN.routed[c] && d.rank >= 0 && (uint32_t)2 * a.RR * H <= o.slot0) {
+      issue_router(DN);
+      r |= 2u;
+    }
+    if (d.rank < 0 && d.np >= 2 && (d.np & 1) == 0 && DN.n_grp[c] > 0 && DN.rank[c][0] < 0 && group_buf(DN, 0) == buf) {
+      const GroupDims dn = group_dims(DN, c, 0);
+      const GroupOff on = GroupOff::of(dn.n, dn.W, dn.np, H);
+      if (dn.np >= 2 && on.slot0 == o.slot0) {
+        issue(DN, 0, 1);
+        prepare_copies(DN, c, 0, 0, j, H, group_buf(DN, 0), s_tsc[0], &bars[B_GU0], 0, s_cp);
+        pend |= 1u << B_GU0;
+        r |= 1u;
+      }
+    }
+    return r;
+  };
+  // a routed group's first copies (part 0 and the down rows), described before its
+  // expert is known; prepared_go(s_cp, e) issues them
+  auto prepare_routed = [&](const DecLayer& D) {
+    prepare_routed_copies(D, j, H, s_big, s_tsc[1], &bars[B_RGU], &bars[B_RDN], s_cp);
+    pend |= (1u << B_RGU) | (1u << B_RDN);
+  };
 
   load_layer(0);
   store_layer(0);
   load_layer(1);
   store_layer(1);
+  if (threadIdx.x < kWarps) s_cp[threadIdx.x].bytes = 0;
   if (threadIdx.x == 0) {
     s_abort = 0;
 #pragma unroll 1
     for (int i = 0; i < 7; ++i) mbar_init(&bars[i], i == B_DNA ? kThreads : 1);
     mbar_init(&bar_hd[0], 1);
     mbar_init(&bar_hd[1], 1);
+    mbar_init(&bar_h[0], 1);
+    mbar_init(&bar_h[1], 1);
+#pragma unroll 1
+    for (int i = 0; i < 4; ++i) mbar_init(&bar_c[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -1125,23 +1358,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
 #pragma unroll 1
       for (int r = threadIdx.x; r < R16; r += kThreads) s_part[r] = 0.f;
       // ---- 2. router and top-k (routed clusters)
+      int g_r = -1;                                  // the routed group issued after the top-k
+      unsigned early = 0u;                           // the next step's copies made early (issue_early)
       if (D.routed[c]) {
         const int r0 = j * a.RR, nr = min(a.RR, D.E - r0);
         wait_bar(B_RT);
-        if (nr > 0) router_rows(s_router, s_xb, H, r0, nr, s_bias[step % 3], s_tmp, lg);
-        cluster_sync();                              // all E logits in every CTA
-        topk(lg, D.E, D.K, D.score, s_sel, s_w, s_wm, &s_n, s_cand, s_key);
-        // the first routed group's copies at once: the groups ahead of it (shared parts,
-        // in flight already) run while they land
+        if (nr > 0) router_rows(s_router, s_xb, H, r0, nr, s_bias[step % 3], s_acc, lg, &bar_lg[par]);
+        // the first routed group's copies are described while the logits travel
 #pragma unroll 1
         for (int g = 0; g < D.n_grp[c]; ++g)
-          if (D.rank[c][g] >= 0) {
-            if (!s_abort) {
-              issue_start(D, g);
-              pre |= 1u << g;
-            }
-            break;
-          }
+          if (D.rank[c][g] >= 0) { g_r = g; break; }
+        if (g_r >= 0 && s_abort) g_r = -1;
+        if (g_r >= 0) prepare_routed(D);
+        // all E logits in every CTA: E * 4 bytes on bar_lg
+        if (threadIdx.x == 0) mbar_expect_tx(&bar_lg[par], (uint32_t)D.E * 4);
+        mbar_wait_cluster(&bar_lg[par], (ph_c >> par) & 1u, sync, lim);
+        ph_c ^= 1u << par;
+        topk(lg, D.E, D.K, D.score, s_sel, s_w);
+        // the first routed group's copies at once: the groups ahead of it (shared parts,
+        // in flight already) run while they land
+        if (g_r >= 0) {                              // its down rows once its part has landed
+          prepared_go(s_cp, s_sel[D.rank[c][g_r]], 0);
+          pre |= 1u << g_r;
+        }
         if (c == 0 && j == 0 && threadIdx.x < D.K) {
           const size_t o = ((size_t)t * a.L + l) * a.Kmax + threadIdx.x;
           if (a.idx_out) a.idx_out[o] = s_sel[threadIdx.x];
@@ -1158,27 +1397,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         const uint8_t* buf = group_buf(D, g);
         const float* tsc = s_tsc[routed];
         float* hsw = s_hsw + (grp_seq & 1) * kMaxW;
+        float* hmax = s_hmax + (grp_seq & 1) * (kCS * kMaxParts);
+        uint64_t* bar_sw = &bar_c[2 + (grp_seq & 1)];
         if (!(pre & (1u << g)) && !s_abort) issue_start(D, g);
 #pragma unroll 1
         for (int part = 0; part < d.np; ++part) {
           const int sl = part & 1;
           wait_bar(routed ? B_RGU : B_GU0 + sl);
+          if (g == g_r && part == 0) prepared_go(s_cp, s_sel[d.rank], kDownW0);
           const uint8_t* pb = buf + o.slot(sl);
           rows_dot<CPL>(pb, pb + a16(d.n * H), 2 * d.n, d.n, tsc[0] * unscale, tsc[1] * unscale, H, s_xl, s_gu);
           __syncthreads();
           if (threadIdx.x < d.n) s_tmp[threadIdx.x] = silu(s_gu[threadIdx.x]) * s_gu[d.n + threadIdx.x];
           __syncthreads();                           // s_tmp; this part's slot is free
+          if (warp == 0) {
+            // this CTA's max |value| of the part goes to every CTA with the values
+            float m = 0.f;
+#pragma unroll 1
+            for (int i = lane; i < d.n; i += 32) m = fmaxf(m, fabsf(s_tmp[i]));
+            m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
+            if (lane < kCS) st_async1(hmax + part * kCS + j, m, bar_sw, lane);
+          }
           if (!s_abort) {
             if (part + 2 < d.np) issue(D, g, part + 2);
             else if (d.np >= 2 && part == d.np - 2) issue(D, g, -1);
           }
-          to_cluster(hsw + part * d.Wp + d.n * j, s_tmp, d.n / 4);
+          to_cluster_async(hsw + part * d.Wp + d.n * j, s_tmp, d.n / 4, bar_sw);
         }
-        cluster_sync();                              // the group's W SwiGLU values everywhere
+        if (g == ng - 1 && next_in_token && !s_abort) early = issue_early(D, DN, g, d, o, buf);
+        // the group's W SwiGLU values and the producers' maxima everywhere
+        if (threadIdx.x == 0) mbar_expect_tx(bar_sw, (uint32_t)d.np * kCS * (4 * d.n + 4));
+        mbar_wait_cluster(bar_sw, (ph_c >> (2 + (grp_seq & 1))) & 1u, sync, lim);
+        ph_c ^= 1u << (2 + (grp_seq & 1));
         wait_bar(routed ? B_RDN : B_DN);
         wait_bar(B_DNA);
         const uint8_t* db = buf + o.down_slot(d.np);
-        group_down(db, db + a16(R16 * d.W / 2), d.W, R16, hsw, s_hh, s_hl, s_red, s_acc,
+        group_down(db, db + a16(R16 * d.W / 2), d.W, R16, hsw, hmax, d.np * kCS, s_hh, s_hl, s_acc,
                    tsc[2] * (routed ? s_w[d.rank] : 1.0f), s_part);
         __syncthreads();                             // the group buffer is free again
       }
@@ -1189,20 +1443,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
       if (ng == 0 && !D.routed[c]) cluster_sync();
       unsigned long long* bd = a.board + (size_t)par * kDecMaxClusters * H;
       if (!(a.hold && step == 0 && blockIdx.x == 0)) post_rows(bd, c, H, j, step + 1, s_part);
-      // copies for the next step that do not depend on its data, issued while the other
-      // clusters' rows arrive (within a token; at a token's end the head uses the
-      // buffers): the router rows, and the first group when it is a shared one
+      exchange(bd, a.NC, H, j, step + 1, s_pp, h_cur, s_hn, s_h + (par ^ 1) * H, &bar_h[par ^ 1],
+               (!next_in_token && c == 0 && a.out) ? a.out + (size_t)t * H : nullptr, sync, lim, &s_abort);
+      // the rest of the next step's copies that do not depend on its data (within a token;
+      // at a token's end the head uses the buffers): the router rows, and the first group
+      // when it is a shared one.  Issued after the exchange has read the clusters' words:
+      // data streaming into the SM delays those reads.
       pre = 0u;
+      if (early & 1u) {                              // part 1 is in flight already
+        prepared_go(s_cp, 0, 0);
+        pre = 1u;
+      }
       if (next_in_token && !s_abort) {
-        if (DN.routed[c]) issue_router(DN);
-        if (DN.n_grp[c] > 0 && DN.rank[c][0] < 0) {
+        if (DN.routed[c] && !(early & 2u)) issue_router(DN);
+        if (!(early & 1u) && DN.n_grp[c] > 0 && DN.rank[c][0] < 0) {
           issue_start(DN, 0);
           pre = 1u;
         }
       }
-      exchange(bd, a.NC, H, j, step + 1, s_pp, h_cur, s_hn, s_h + (par ^ 1) * H,
-               (!next_in_token && c == 0 && a.out) ? a.out + (size_t)t * H : nullptr, sync, lim, &s_abort);
-      cluster_sync();                                // h_{l+1} complete in every CTA
+      // h_{l+1} complete here: the H * 4 bytes of the cluster's CTAs on bar_h (the barrier
+      // each step meets earlier keeps a CTA from writing a buffer a peer still reads)
+      if (threadIdx.x == 0) mbar_expect_tx(&bar_h[par ^ 1], (uint32_t)H * 4);
+      mbar_wait_cluster(&bar_h[par ^ 1], (ph_h >> (par ^ 1)) & 1u, sync, lim);
+      ph_h ^= 1u << (par ^ 1);
     }
     // ---------------- token t's outputs: x_L and the head
     if (!a.x_out && !a.head.codes) continue;
@@ -1267,7 +1530,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
   // Copies are issued only for a step that follows and waited for in the step they
   // serve, so normally nothing is in flight here; after an abort, what a skipped wait
   // left in flight is drained (bounded) before the CTA exits.  The last remote writes
-  // precede the last cluster barrier.
+  // (the last step's h rows) have landed: each CTA waited for them on bar_h.
 #pragma unroll 1
   for (int i = 0; i < 7; ++i) wait_bar(i);
 #pragma unroll 1
@@ -1362,7 +1625,6 @@ bool decode_plan_layer(DecLayer& d, int H, int NC) {
     NR = d.K < (d.Fs > 0 ? NC - 1 : NC) ? d.K : (d.Fs > 0 ? NC - 1 : NC);
     if (NR < 1) NR = 1;
   }
-  const int NS = NC - NR;
   int n_routed[kDecMaxClusters] = {0, 0, 0, 0, 0, 0, 0, 0};
   for (int s = 0; s < d.K; ++s) ++n_routed[s % NR];
   for (int cc = 0; cc < NC; ++cc)
