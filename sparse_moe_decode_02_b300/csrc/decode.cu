@@ -308,7 +308,7 @@ __device__ __noinline__ void rows_dot(const uint8_t* codes, const uint8_t* scale
       row[k] = r < nrows ? r : 0;
     }
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
+#pragma unroll
     for (int i = 0; i < CPL; ++i) {
       const int cidx = sl + LPR * i;
       uint32_t xp[16];
