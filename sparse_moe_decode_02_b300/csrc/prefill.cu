@@ -353,17 +353,43 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
     const int r = q * 32 + lane;                            // tile row of this thread
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t done = 0;
+    // What an item's epilogue reads from global memory (its tensor scales; for a routed
+    // down tile this row's token and pair weight, two dependent loads) is loaded one item
+    // ahead, so that its latency passes while the tensor cores work.
+    auto item_vals = [&](const Item& it, float& v0, float& v1, int& tok) {
+      const int kd = it.kind(), ex = kd ? it.expert() : 0;
+      v0 = g.tscA[kd][ex];
+      tok = it.row0 + r;
+      if (MODE == kGateUp) {
+        v1 = g.tscB[kd][ex];
+      } else {
+        v1 = 1.0f;
+        if (kd != 0 && r < it.rows) {
+          const int pair = g.order[it.row0 + r];
+          tok = pair / g.K;
+          v1 = g.wpair[pair];
+        }
+      }
+    };
     Item nxt = blockIdx.x < n_items ? load_item(g.items + blockIdx.x) : Item{0, 0, 0, 0};
+    float nv0 = 0.f, nv1 = 0.f;
+    int ntok = 0;
+    if (blockIdx.x < n_items) item_vals(nxt, nv0, nv1, ntok);
     for (int i = blockIdx.x; i < n_items && !abort_flag; i += gridDim.x, ++done) {
       const Item item = nxt;
-      if (i + (int)gridDim.x < n_items) nxt = load_item(g.items + i + gridDim.x);
+      const float v0 = nv0, v1 = nv1;
+      const int vtok = ntok;
+      if (i + (int)gridDim.x < n_items) {
+        nxt = load_item(g.items + i + gridDim.x);
+        item_vals(nxt, nv0, nv1, ntok);
+      }
       if (!mb_wait(&accf, done & 1, &abort_flag, g.wait_ns)) break;
       tc_fence_after();
       const bool valid = r < item.rows;
       const int arow = item.row0 + r;
       if (MODE == kGateUp) {
-        const float tg = g.tscA[item.kind()][item.kind() ? item.expert() : 0];
-        const float tu = g.tscB[item.kind()][item.kind() ? item.expert() : 0];
+        const float tg = v0;
+        const float tu = v1;
         float h[64];
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 16) {
@@ -408,16 +434,10 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_fp4(const __grid_constant
         __syncwarp();
         if (lane == 0) mb_arrive(&acce);
         if (valid) {
-          const float td = g.tscA[item.kind()][item.kind() ? item.expert() : 0];
           const int col = item.n0 + 64 * hf;
           // shared rows: token arow, weight 1; routed rows: the pair's token and weight
-          int tok = arow;
-          float scale = td;
-          if (item.kind() != 0) {
-            const int pair = g.order[arow];
-            tok = pair / g.K;
-            scale = td * g.wpair[pair];
-          }
+          const int tok = vtok;
+          const float scale = v0 * v1;
           float* o = g.out + (size_t)tok * g.H + col;
 #pragma unroll
           for (int j = 0; j < 64; j += 4)
