@@ -919,43 +919,51 @@ __global__ void __launch_bounds__(256) k_scatter_quant(ScatterArgs s) {
     s.pos_of_pair[pair] = mypos;
     if (s.order_out) s.order_out[a.offsets[e] + rank] = pair;
   }
+  // lane l takes elements [256 i + 8 l, + 8): loads, the fp32 copy and the codes of a
+  // warp are contiguous; a 16-element block is a lane pair (its amax by one shuffle), the
+  // four block scales of a 64-element group meet in the group's first lane.  Each block
+  // is quantised by the same recipe as quant_block_unit.
   const int H = s.H, ks = H / 64;
   const uint16_t* xr = s.x + (size_t)t * H;
-  for (int gk = lane; gk < ks; gk += 32) {
-    float f[64];
+  int pos[FLINT_MAX_TOP_K];
+#pragma unroll 1
+  for (int j = 0; j < a.K; ++j) pos[j] = __shfl_sync(0xffffffffu, mypos, j);
+#pragma unroll 1
+  for (int e0 = 8 * lane; e0 < H; e0 += 256) {
+    float f[8];
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + e0));
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + 64 * gk + 8 * p));
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        f[8 * p + 2 * q] = bf16_bits_to_f32(u[q] & 0xFFFFu);
-        f[8 * p + 2 * q + 1] = bf16_bits_to_f32(u[q] >> 16);
-      }
+    for (int q = 0; q < 4; ++q) {
+      f[2 * q] = bf16_bits_to_f32(u[q] & 0xFFFFu);
+      f[2 * q + 1] = bf16_bits_to_f32(u[q] >> 16);
     }
-    float4* o = reinterpret_cast<float4*>(s.out + (size_t)t * H + 64 * gk);
+    float4* o = reinterpret_cast<float4*>(s.out + (size_t)t * H + e0);
+    o[0] = make_float4(f[0], f[1], f[2], f[3]);
+    o[1] = make_float4(f[4], f[5], f[6], f[7]);
+    float amax = 0.f;
 #pragma unroll
-    for (int p = 0; p < 16; ++p) o[p] = make_float4(f[4 * p], f[4 * p + 1], f[4 * p + 2], f[4 * p + 3]);
-    uint2 cw[4];
-    uint32_t sw = 0;
+    for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(f[q]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    const uint32_t sc = to_e4m3(__fdiv_rn(__fdiv_rn(amax, 6.0f), 1.0f));
+    const float eff = e4m3_value(sc);
+    uint32_t cw = 0u;
+    if (eff != 0.f) {
 #pragma unroll
-    for (int b4 = 0; b4 < 4; ++b4) {
-      uint32_t sc;
-      quant_block_unit(f + 16 * b4, cw[b4], sc);
-      sw |= sc << (8 * b4);
+      for (int q = 0; q < 4; ++q)
+        cw |= to_e2m1x2(__fdiv_rn(f[2 * q], eff), __fdiv_rn(f[2 * q + 1], eff)) << (8 * q);
     }
-    const uint4 c0 = make_uint4(cw[0].x, cw[0].y, cw[1].x, cw[1].y);
-    const uint4 c1 = make_uint4(cw[2].x, cw[2].y, cw[3].x, cw[3].y);
-    uint8_t* q = s.xq_codes + (size_t)t * (H / 2) + 32 * gk;
-    *reinterpret_cast<uint4*>(q) = c0;
-    *reinterpret_cast<uint4*>(q + 16) = c1;
-    *reinterpret_cast<uint32_t*>(s.xq_sf + sf_word_offset(t, gk, ks)) = sw;
+    // the group's scale word: blocks 0..3 from lanes 8m, 8m + 2, 8m + 4, 8m + 6
+    uint32_t sw = 0u;
+#pragma unroll
+    for (int b4 = 0; b4 < 4; ++b4) sw |= __shfl_sync(0xffffffffu, sc, (lane & ~7) + 2 * b4) << (8 * b4);
+    const int gk = e0 >> 6;
+    *reinterpret_cast<uint32_t*>(s.xq_codes + (size_t)t * (H / 2) + (e0 >> 1)) = cw;
+    if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(s.xq_sf + sf_word_offset(t, gk, ks)) = sw;
+#pragma unroll 1
     for (int j = 0; j < a.K; ++j) {
-      const int pos = __shfl_sync(0xffffffffu, mypos, j);
-      uint8_t* p = s.xp_codes + (size_t)pos * (H / 2) + 32 * gk;
-      *reinterpret_cast<uint4*>(p) = c0;
-      *reinterpret_cast<uint4*>(p + 16) = c1;
-      *reinterpret_cast<uint32_t*>(s.xp_sf + sf_word_offset(pos, gk, ks)) = sw;
+      *reinterpret_cast<uint32_t*>(s.xp_codes + (size_t)pos[j] * (H / 2) + (e0 >> 1)) = cw;
+      if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(s.xp_sf + sf_word_offset(pos[j], gk, ks)) = sw;
     }
   }
 }
