@@ -31,10 +31,11 @@
 //     through a two-slot ring of TMA bulk copies; each posts its best (value, index) and
 //     the last CTA reduces them.
 //
-// At batch 1 every phase of a step runs once, so a step's time follows the bytes of code
-// it executes (instruction fetch from L2 runs at a few bytes per cycle): the phases are
-// small out-of-line functions with rolled loops, each called from one place, and remote
-// writes are 16-byte stores of values computed locally first.  Every wait on another
+// Within a cluster every hand-off (logits, SwiGLU values, h) is st.async into the
+// receivers' shared memory, completing bytes on their mbarriers: a CTA waits for the
+// data it needs, not for the cluster, and no cluster barrier remains in a step.  The
+// copies of the next step that do not depend on its data go out a step ahead, and a
+// routed expert's copies are described before the top-k ends.  Every wait on another
 // CTA or on a copy is bounded by %globaltimer: on expiry the kernel records
 // FLINT_ERR_TIMEOUT, raises an abort flag that releases every other wait, stops issuing
 // copies and runs to its end.
@@ -74,25 +75,10 @@ __device__ __forceinline__ unsigned cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// The two halves of cluster_sync, for work in between that touches no shared data of
-// the barrier's (the CTA's own copy descriptors, say).
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 __device__ __forceinline__ uint32_t peer_addr(const void* local, int rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(local)), "r"(rank));
   return r;
-}
-__device__ __forceinline__ void st_peer4(uint32_t addr, float4 v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
-               "f"(v.w) : "memory");
-}
-__device__ __forceinline__ void st_peer1(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
 }
 // One float to `dst` in CTA `peer`, completing 4 bytes on that CTA's barrier `bar`.
 __device__ __forceinline__ void st_async1(float* dst, float v, uint64_t* bar, int peer) {
@@ -110,14 +96,6 @@ __device__ __forceinline__ void to_cluster_async(float* dst, const float* src, i
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
                  :: "r"(peer_addr(dst + 4 * k, peer)), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w),
                     "r"(peer_addr(bar, peer)) : "memory");
-  }
-}
-// n 16-byte pieces of `src` (local shared memory) to `dst` in every CTA of the cluster.
-__device__ __forceinline__ void to_cluster(float* dst, const float* src, int n) {
-#pragma unroll 1
-  for (int i = threadIdx.x; i < kCS * n; i += kThreads) {
-    const int peer = i / n, k = i - peer * n;
-    st_peer4(peer_addr(dst + 4 * k, peer), *reinterpret_cast<const float4*>(src + 4 * k));
   }
 }
 __device__ __forceinline__ void st_tagged(unsigned long long* p, unsigned long long v) {
