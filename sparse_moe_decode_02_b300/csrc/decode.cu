@@ -914,34 +914,88 @@ __device__ __noinline__ void head_argmax(const unsigned long long* best, int G, 
 // each CTA its own rows, then the last CTA over the CTAs' lists -- and the draw follows
 // flint_sample_logits exactly.
 
-// K rounds of warp-wide maxima over the warp's candidates (S per lane; key 0 = empty):
-// the K largest keys, ties to the lower index, in rank order into out_key / out_idx.
-template <int S>
-__device__ __forceinline__ void warp_topk(unsigned (&key)[S], int (&idx)[S], int K, unsigned* out_key, int* out_idx) {
+// Candidates are (order key, index) pairs ranked by key, ties to the lower index; key 0
+// is empty (index 0x7FFFFFFF).  prec(a, b): a ranks before b.
+__device__ __forceinline__ bool prec(unsigned ka, int ia, unsigned kb, int ib) {
+  return ka > kb || (ka == kb && ia < ib);
+}
+__device__ __forceinline__ void cas(unsigned (&k)[8], int (&x)[8], int i, int j) {
+  const bool sw = prec(k[j], x[j], k[i], x[i]);
+  const unsigned ki = k[i], kj = k[j];
+  const int xi = x[i], xj = x[j];
+  k[i] = sw ? kj : ki; k[j] = sw ? ki : kj;
+  x[i] = sw ? xj : xi; x[j] = sw ? xi : xj;
+}
+// This lane's eight candidates in rank order (Batcher's odd-even merge network).
+__device__ __forceinline__ void lane_sort8(unsigned (&k)[8], int (&x)[8]) {
+  cas(k, x, 0, 1); cas(k, x, 2, 3); cas(k, x, 4, 5); cas(k, x, 6, 7);
+  cas(k, x, 0, 2); cas(k, x, 1, 3); cas(k, x, 4, 6); cas(k, x, 5, 7);
+  cas(k, x, 1, 2); cas(k, x, 5, 6);
+  cas(k, x, 0, 4); cas(k, x, 1, 5); cas(k, x, 2, 6); cas(k, x, 3, 7);
+  cas(k, x, 2, 4); cas(k, x, 3, 5);
+  cas(k, x, 1, 2); cas(k, x, 3, 4); cas(k, x, 5, 6);
+}
+// The K best of the warp's candidates (eight per lane, each lane's in rank order), in
+// rank order into out_key / out_idx: each round takes the best lane head by two warp
+// reductions (largest key, then lowest index holding it) and that lane moves on.
+__device__ __forceinline__ void warp_topk8(unsigned (&k)[8], int (&x)[8], int K, unsigned* out_key, int* out_idx) {
   const int lane = threadIdx.x & 31;
 #pragma unroll 1
   for (int s = 0; s < K; ++s) {
-    unsigned lb = 0u;
-    int li = 0x7FFFFFFF;
-#pragma unroll
-    for (int q = 0; q < S; ++q)
-      if (key[q] > lb || (key[q] == lb && idx[q] < li)) { lb = key[q]; li = idx[q]; }
-    const unsigned wk = __reduce_max_sync(0xffffffffu, lb);
-    const int wi = (int)__reduce_min_sync(0xffffffffu, lb == wk ? (unsigned)li : 0xFFFFFFFFu);
+    const unsigned wk = __reduce_max_sync(0xffffffffu, k[0]);
+    const int wi = (int)__reduce_min_sync(0xffffffffu, k[0] == wk ? (unsigned)x[0] : 0xFFFFFFFFu);
     if (lane == 0) { out_key[s] = wk; out_idx[s] = wi; }
+    if (k[0] == wk && x[0] == wi) {
 #pragma unroll
-    for (int q = 0; q < S; ++q)
-      if (key[q] == wk && idx[q] == wi) { key[q] = 0u; idx[q] = 0x7FFFFFFF; }
+      for (int q = 0; q < 7; ++q) { k[q] = k[q + 1]; x[q] = x[q + 1]; }
+      k[7] = 0u;
+      x[7] = 0x7FFFFFFF;
+    }
+  }
+}
+// The K best of M <= 128 lists in rank order (list m: keys[m * ld + r], r < len), in
+// rank order into out_key / out_idx; one warp (lane l holds lists l, l + 32, ...).
+__device__ __noinline__ void merge_lists(const unsigned* keys, const int* idx, int M, int ld, int len, int K,
+                                         unsigned* out_key, int* out_idx) {
+  const int lane = threadIdx.x & 31;
+  unsigned hk[4];
+  int hx[4], hp[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int m = lane + 32 * q;
+    hp[q] = 0;
+    hk[q] = m < M && len > 0 ? keys[m * ld] : 0u;
+    hx[q] = m < M && len > 0 ? (hk[q] ? idx[m * ld] : 0x7FFFFFFF) : 0x7FFFFFFF;
+  }
+#pragma unroll 1
+  for (int s = 0; s < K; ++s) {
+    unsigned bk = hk[0];
+    int bx = hx[0], bq = 0;
+#pragma unroll
+    for (int q = 1; q < 4; ++q)
+      if (prec(hk[q], hx[q], bk, bx)) { bk = hk[q]; bx = hx[q]; bq = q; }
+    const unsigned wk = __reduce_max_sync(0xffffffffu, bk);
+    const int wi = (int)__reduce_min_sync(0xffffffffu, bk == wk ? (unsigned)bx : 0xFFFFFFFFu);
+    if (lane == 0) { out_key[s] = wk; out_idx[s] = wi; }
+    if (bk == wk && bx == wi && (wk != 0u || wi != 0x7FFFFFFF)) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (q == bq) {
+          const int m = lane + 32 * q, r = ++hp[q];
+          hk[q] = r < len ? keys[m * ld + r] : 0u;
+          hx[q] = r < len && hk[q] ? idx[m * ld + r] : 0x7FFFFFFF;
+        }
+    }
   }
 }
 
 // The K (<= 32) largest of n <= kThreads * 8 candidates (order keys s_key, 0 = empty;
 // indices s_idx, or base + i when s_idx is null), ties to the lower index, in rank
-// order into out_key / out_idx.  Each warp takes its slice (<= 256), then warp 0 the
-// warps' K-lists (<= 512).  Every thread calls this.
+// order into out_key / out_idx.  Each warp ranks its slice (<= 256, eight per lane),
+// then warp 0 merges the warps' K-lists.  Every thread calls this.
 __device__ __noinline__ void block_topk(const unsigned* s_key, const int* s_idx, int n, int K, int base,
                                         unsigned* s_wk, int* s_wi, unsigned* out_key, int* out_idx) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int per = (n + kWarps - 1) / kWarps;
   const int b0 = warp * per, b1 = min(n, b0 + per);
   {
@@ -951,22 +1005,13 @@ __device__ __noinline__ void block_topk(const unsigned* s_key, const int* s_idx,
     for (int q = 0; q < 8; ++q) {
       const int i = b0 + lane + 32 * q;
       key[q] = i < b1 ? s_key[i] : 0u;
-      idx[q] = i < b1 ? (s_idx ? s_idx[i] : base + i) : 0x7FFFFFFF;
+      idx[q] = i < b1 && key[q] ? (s_idx ? s_idx[i] : base + i) : 0x7FFFFFFF;
     }
-    warp_topk<8>(key, idx, K, s_wk + warp * K, s_wi + warp * K);
+    lane_sort8(key, idx);
+    warp_topk8(key, idx, K, s_wk + warp * K, s_wi + warp * K);
   }
   __syncthreads();
-  if (warp == 0) {
-    unsigned key[16];
-    int idx[16];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const int c = lane + 32 * q;
-      key[q] = c < kWarps * K ? s_wk[c] : 0u;
-      idx[q] = c < kWarps * K ? s_wi[c] : 0x7FFFFFFF;
-    }
-    warp_topk<16>(key, idx, K, out_key, out_idx);
-  }
+  if (warp == 0) merge_lists(s_wk, s_wi, kWarps, K, K, K, out_key, out_idx);
   __syncthreads();
 }
 
@@ -1004,7 +1049,9 @@ __device__ __noinline__ void head_sample(const unsigned long long* cand, int G, 
     s_ci[i] = (int)(unsigned)wi;
   }
   __syncthreads();
-  block_topk(s_ck, s_ci, n, K, 0, s_wk, s_wi, s_fk, s_fi);
+  // each CTA's K candidates are in rank order: one warp merges the G lists
+  if (threadIdx.x < 32) merge_lists(s_ck, s_ci, G, K, K, K, s_fk, s_fi);
+  __syncwarp();
   if (threadIdx.x >= 32) return;
   const int lane = threadIdx.x;
   const int idx = lane < K ? s_fi[lane] : 0;
